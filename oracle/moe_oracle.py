@@ -1,0 +1,287 @@
+"""CPU oracle for the sparsely-gated Mixture-of-Experts FFN layer (test infrastructure).
+
+This is a plain, slow, fp64 restatement of what the layer computes. Only the
+tests, the package's smoke check and the benchmark's CPU-baseline leg may use
+it; the CUDA library never calls it and shares no code with it.
+
+Pages followed (cited by title and section/equation):
+
+* [Switch] "Mixture of Experts (MoE) を1から解説 — Switch Transformerのルーティング
+  と負荷分散": eq. (1) softmax router, eq. (2) gated sum over the selected
+  experts, eq. (3) expert capacity and the dropped-token rule (section
+  エキスパートには「定員」がある), eq. (4) load-balancing loss and its numpy
+  sketch (section 負荷分散損失), fp32 router (section 学習を安定させる3つの工夫).
+* [LRMoE] "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE Training on
+  Memory-Constrained Nodes" (section この記事のポイント): kept token-expert
+  pairs are physically compacted into variable-size groups per expert.
+* [Wiki] "Mixture-of-Experts" (notes.yuuk.io): top-k lineage beyond k = 1,
+  SwiGLU experts, importance/load statistics.
+
+Readings taken where the pages are silent (the same list is kept in the
+project's design notes):
+
+* W_r is stored [E, d]; h = W_r x (+ a fixed logit bias b when given).
+* Top-k is chosen on h: descending value, ties to the lower expert index.
+* Gates are the raw p_i of the selected experts (eq. (2)); with
+  renormalisation g_i = p_i / sum_{j in T} p_j over all k selected experts
+  (dropped ones stay in the denominator and contribute nothing).
+* Capacity C = floor(n * cf / E), n = k*T assignments by default (keeps the
+  "cf = 1.0 fits a perfectly balanced batch" meaning for k > 1), n = T when
+  count_assignments is off; no limit when cf is None.
+* Within an expert, assignments are ranked in ascending token order; rank < C
+  is kept (slot = rank), the rest are dropped (slot = -1).
+* out = x + sum over kept selected experts of g * E_i(x); a token whose
+  assignments are all dropped returns x unchanged.
+* f_e = load_e / (T*k) counted before capacity, P_e = importance_e / T,
+  aux = alpha * E * sum_e f_e P_e.
+* Experts have no biases. ReLU: W2 relu(W1 z). SwiGLU: W2 (silu(Wg z) * (Wu z)),
+  W1 = [Wg; Wu] stacked by rows, silu(u) = u / (1 + exp(-u)).
+* Backward of L = <dY, out> + aux with top-k sets, capacity masks and f held
+  constant.
+
+Parity status: every function here is pinned by the oracle tests (invariants,
+closed forms, brute force on tiny inputs, finite differences); none is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+from typing import Callable, Optional, Sequence, Tuple, Union
+
+import numpy as np
+
+ExpertSource = Union[Tuple[np.ndarray, np.ndarray], Callable[[int], Tuple[np.ndarray, np.ndarray]]]
+
+
+def _f64(a):
+    return None if a is None else np.asarray(a, dtype=np.float64)
+
+
+def _expert(experts: ExpertSource, e: int) -> Tuple[np.ndarray, np.ndarray]:
+    if callable(experts):
+        w1, w2 = experts(e)
+    else:
+        w1, w2 = experts[0][e], experts[1][e]
+    return _f64(w1), _f64(w2)
+
+
+# ------------------------------------------------------------------ router
+def router_logits(x, w_r, bias=None) -> np.ndarray:
+    """h = W_r . x per token ([Switch] section 仕組み(1)), plus the fixed bias."""
+    h = _f64(x) @ _f64(w_r).T
+    if bias is not None:
+        h = h + _f64(bias)[None, :]
+    return h
+
+
+def softmax(h: np.ndarray) -> np.ndarray:
+    """p_i = exp(h_i) / sum_j exp(h_j) over all N experts ([Switch] eq. (1)).
+
+    The row maximum is subtracted first; the quotient is unchanged by it.
+    """
+    z = np.exp(h - h.max(axis=1, keepdims=True))
+    return z / z.sum(axis=1, keepdims=True)
+
+
+def top_k(h: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest logits per token, largest first, ties to the
+    lower index ([Switch] section 仕組み(1): "上位k個を選び"; k = 1 is the
+    argmax of the numpy sketch in section 負荷分散損失)."""
+    order = np.argsort(-h, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def route(x, w_r, bias, k: int, renormalize: bool, alpha: float) -> dict:
+    """Router, gates and balance statistics for one batch of T tokens.
+
+    [Switch] eqs. (1), (2), (4) and the numpy sketch of section 負荷分散損失:
+    probs -> expert choice -> gate -> f (fraction of assignments per expert)
+    -> P (mean probability) -> aux = alpha * N * sum f_i P_i.
+    """
+    h = router_logits(x, w_r, bias)
+    T, E = h.shape
+    p = softmax(h)
+    idx = top_k(h, k)
+    gate = np.take_along_axis(p, idx, axis=1)
+    if renormalize:
+        gate = gate / gate.sum(axis=1, keepdims=True)
+    load = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    importance = p.sum(axis=0)
+    f = load / float(T * k)
+    P = importance / float(T)
+    aux = alpha * E * float(np.sum(f * P))
+    return dict(h=h, p=p, idx=idx, gate=gate, load=load, importance=importance,
+                f=f, P=P, aux=aux)
+
+
+# ------------------------------------------------------------------ capacity
+def capacity(T: int, E: int, k: int, cf: Optional[Tuple[int, int]],
+             count_assignments: bool = True) -> Optional[int]:
+    """expert capacity = tokens per batch / number of experts * capacity factor
+    ([Switch] eq. (3)), floored, in integer arithmetic. None = no limit."""
+    if cf is None:
+        return None
+    num, den = cf
+    n = (k * T) if count_assignments else T
+    return (n * num) // (E * den)
+
+
+def assign_slots(idx: np.ndarray, E: int, C: Optional[int]) -> dict:
+    """Token-order capacity slots ([Switch] eq. (3) and the dropped-token rule).
+
+    Each expert takes the tokens that chose it in ascending token order; the
+    first C are kept (slot = their rank), later ones are dropped (slot = -1)
+    and skip the expert. Kept pairs are compacted per expert into contiguous
+    row groups ([LRMoE] physical compaction -> variable-size groups):
+    row(t, j) = offsets[e] + slot.
+    """
+    T, k = idx.shape
+    count = np.zeros(E, dtype=np.int64)
+    slot = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            r = count[e]
+            count[e] += 1
+            if C is None or r < C:
+                slot[t, j] = r
+    kept = count.copy() if C is None else np.minimum(count, C)
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(kept)
+    row_token = np.full(int(offsets[-1]), -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            if slot[t, j] >= 0:
+                row_token[offsets[idx[t, j]] + slot[t, j]] = t
+    return dict(slot=slot, kept=kept, offsets=offsets, row_token=row_token)
+
+
+# ------------------------------------------------------------------ experts
+def silu(u):
+    return u / (1.0 + np.exp(-u))
+
+
+def expert_ffn(z: np.ndarray, w1: np.ndarray, w2: np.ndarray, act: str) -> dict:
+    """One expert FFN on rows z [n, d] ([Switch] section 直感: the experts are
+    copies of the Transformer FFN; SwiGLU from [Wiki])."""
+    if act == "relu":
+        a = z @ w1.T
+        hid = np.maximum(a, 0.0)
+        return dict(a=a, hid=hid, y=hid @ w2.T)
+    F = w2.shape[1]
+    g = z @ w1[:F].T
+    u = z @ w1[F:].T
+    hid = silu(g) * u
+    return dict(g=g, u=u, hid=hid, y=hid @ w2.T)
+
+
+# ------------------------------------------------------------------ layer
+def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
+            cf: Optional[Tuple[int, int]], count_assignments: bool = True,
+            renormalize: bool = False, alpha: float = 0.01,
+            tokens: Optional[Sequence[int]] = None) -> dict:
+    """out = x + sum_{i in T, kept} g_i E_i(x) ([Switch] eq. (2) with the
+    residual passthrough of dropped tokens).
+
+    `tokens` restricts the expert evaluation (and `out`) to a subset of
+    tokens; routing, slots and statistics always cover the whole batch,
+    because capacity depends on every token before a given one.
+    """
+    x64 = _f64(x)
+    T, d = x64.shape
+    E = np.asarray(w_r).shape[0]
+    r = route(x64, w_r, bias, k, renormalize, alpha)
+    C = capacity(T, E, k, cf, count_assignments)
+    s = assign_slots(r["idx"], E, C)
+    sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    out = x64[sel].copy()
+    where = {int(t): i for i, t in enumerate(sel)}
+    for e in range(E):
+        tt, jj = np.nonzero((r["idx"] == e) & (s["slot"] >= 0))
+        keep = [n for n, t in enumerate(tt) if int(t) in where]
+        if not keep:
+            continue
+        tt, jj = tt[keep], jj[keep]
+        w1, w2 = _expert(experts, e)
+        y = expert_ffn(x64[tt], w1, w2, act)["y"]
+        for n in range(len(tt)):
+            out[where[int(tt[n])]] += r["gate"][tt[n], jj[n]] * y[n]
+    res = dict(r)
+    res.update(s)
+    res.update(C=C, out=out, tokens=sel)
+    return res
+
+
+def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
+             cf: Optional[Tuple[int, int]], count_assignments: bool = True,
+             renormalize: bool = False, alpha: float = 0.01,
+             experts_needed: Optional[Sequence[int]] = None) -> dict:
+    """Gradients of L = <dY, out> + aux (chain rule through eqs. (1), (2), (4)).
+
+    Top-k sets, capacity masks and f are constants ([Switch] section
+    負荷分散損失: f comes from an argmax and has no gradient; P does).
+    Returns dx [T, d], dw_r [E, d], dg [T, k] and, for every expert in
+    `experts_needed` (all by default), dw1[e] and dw2[e].
+    """
+    x64, dy64 = _f64(x), _f64(dy)
+    T, d = x64.shape
+    wr64 = _f64(w_r)
+    E = wr64.shape[0]
+    r = route(x64, wr64, bias, k, renormalize, alpha)
+    C = capacity(T, E, k, cf, count_assignments)
+    s = assign_slots(r["idx"], E, C)
+    dx = dy64.copy()                       # residual path
+    dg = np.zeros((T, k))
+    dw1, dw2 = {}, {}
+    need = set(range(E)) if experts_needed is None else set(int(e) for e in experts_needed)
+    for e in range(E):
+        tt, jj = np.nonzero((r["idx"] == e) & (s["slot"] >= 0))
+        w1, w2 = _expert(experts, e)
+        if len(tt) == 0:
+            if e in need:
+                dw1[e], dw2[e] = np.zeros_like(w1), np.zeros_like(w2)
+            continue
+        z = x64[tt]
+        fw = expert_ffn(z, w1, w2, act)
+        g = r["gate"][tt, jj][:, None]
+        dg[tt, jj] = np.sum(dy64[tt] * fw["y"], axis=1)
+        dyp = g * dy64[tt]                 # d(out)/d(y_e) = g
+        dhid = dyp @ w2
+        if e in need:
+            dw2[e] = dyp.T @ fw["hid"]
+        if act == "relu":
+            da = dhid * (fw["a"] > 0)
+            dz = da @ w1
+            if e in need:
+                dw1[e] = da.T @ z
+        else:
+            sg = 1.0 / (1.0 + np.exp(-fw["g"]))
+            dgate = dhid * fw["u"] * (sg * (1.0 + fw["g"] * (1.0 - sg)))
+            dup = dhid * silu(fw["g"])
+            da = np.concatenate([dgate, dup], axis=1)
+            dz = da @ w1
+            if e in need:
+                dw1[e] = da.T @ z
+        dx[tt] += dz
+    # gates -> probabilities
+    p, idx = r["p"], r["idx"]
+    dp = np.zeros((T, E))
+    if renormalize:
+        psel = np.take_along_axis(p, idx, axis=1)
+        S = psel.sum(axis=1, keepdims=True)
+        corr = np.sum(dg * r["gate"], axis=1, keepdims=True)
+        np.put_along_axis(dp, idx, (dg - corr) / S, axis=1)
+    else:
+        np.put_along_axis(dp, idx, dg, axis=1)
+    # eq. (4): d aux / d p_{t,e} = alpha * E * f_e / T
+    dp += alpha * E * r["f"][None, :] / float(T)
+    # eq. (1): softmax Jacobian
+    dh = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    dw_r = dh.T @ x64
+    dx += dh @ wr64
+    return dict(dx=dx, dw_r=dw_r, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r, slots=s)
+
+
+def loss(x, w_r, bias, experts: ExpertSource, dy, **kw) -> float:
+    """L = <dY, out> + aux, the scalar whose gradient `backward` returns."""
+    f = forward(x, w_r, bias, experts, **kw)
+    return float(np.sum(_f64(dy) * f["out"])) + f["aux"]

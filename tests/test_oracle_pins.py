@@ -1,0 +1,335 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Closed forms from the pages' equations, invariants the pages state, brute
+force on tiny inputs, textbook loops, a library routine the oracle does not
+use, and central finite differences for the backward pass.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import moe_synth as syn
+from oracle import moe_oracle as O
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+# ------------------------------------------------------------------ eq. (1)
+def test_softmax_closed_form():
+    g = GOLD["softmax"]
+    p = O.softmax(np.array([g["h"]]))
+    np.testing.assert_allclose(p[0], g["p"], rtol=0, atol=1e-15)
+
+
+def test_softmax_rows_sum_to_one_and_match_library():
+    rng = np.random.default_rng(1)
+    h = rng.standard_normal((300, 17)) * 8.0
+    p = O.softmax(h)
+    assert np.max(np.abs(p.sum(axis=1) - 1.0)) <= 1e-12
+    np.testing.assert_allclose(p, scipy.special.softmax(h, axis=1), rtol=1e-13, atol=1e-300)
+    # a shift of one row by a constant leaves it unchanged
+    np.testing.assert_allclose(O.softmax(h + 123.0), p, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ top-k
+def _brute_topk(h, k):
+    """Rank by counting: rank(e) = #{e' beating e}; beating = larger, or equal with lower index."""
+    T, E = h.shape
+    out = np.empty((T, k), dtype=np.int64)
+    for t in range(T):
+        for e in range(E):
+            rank = sum(1 for f in range(E) if h[t, f] > h[t, e] or (h[t, f] == h[t, e] and f < e))
+            if rank < k:
+                out[t, rank] = e
+    return out
+
+
+@pytest.mark.parametrize("k", [1, 2, 3, 8])
+def test_topk_brute_force(k):
+    rng = np.random.default_rng(k)
+    h = rng.standard_normal((40, 8))
+    h[0, :] = 0.5                     # all tied: order must be 0, 1, 2, ...
+    h[1, 3] = h[1, 5] = h[1].max() + 1
+    np.testing.assert_array_equal(O.top_k(h, k), _brute_topk(h, k))
+    assert list(O.top_k(h, k)[0]) == list(range(k))
+    if k >= 2:
+        assert list(O.top_k(h, k)[1][:2]) == [3, 5]
+
+
+# ------------------------------------------------------------------ eq. (4)
+def test_aux_uniform_is_alpha():
+    g = GOLD["aux_uniform"]
+    E, m = 8, 5
+    T = E * m
+    x = np.zeros((T, E))
+    x[np.arange(T), np.arange(T) % E] = 1.0
+    w_r = 3.0 * np.eye(E)                      # h_t = 3 * onehot(t mod E)
+    r = O.route(x, w_r, None, 1, False, g["alpha"])
+    np.testing.assert_allclose(r["f"], 1.0 / E, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(r["P"], 1.0 / E, rtol=1e-14)
+    assert abs(r["aux"] - g["loss"]) <= 1e-15
+
+
+def test_aux_collapsed_limit():
+    g = GOLD["aux_collapsed"]
+    E = g["N"]
+    x = np.ones((16, 1))
+    w_r = np.zeros((E, 1))
+    w_r[0, 0] = 60.0                           # p_0 = 1 - O(e^-60)
+    r = O.route(x, w_r, None, 1, False, g["alpha"])
+    assert np.all(r["idx"] == 0) and r["f"][0] == 1.0
+    assert abs(r["aux"] - g["loss_limit"]) <= 1e-15
+
+
+def test_route_statistics_brute_force():
+    rng = np.random.default_rng(3)
+    T, E, d, k = 50, 6, 5, 2
+    x = rng.standard_normal((T, d))
+    w_r = rng.standard_normal((E, d))
+    r = O.route(x, w_r, None, k, False, 0.01)
+    load = np.zeros(E, int)
+    imp = np.zeros(E)
+    for t in range(T):
+        hs = [sum(w_r[e, i] * x[t, i] for i in range(d)) for e in range(E)]
+        zs = [math.exp(v) for v in hs]
+        for e in range(E):
+            imp[e] += zs[e] / sum(zs)
+        for e in _brute_topk(np.array([hs]), k)[0]:
+            load[e] += 1
+    np.testing.assert_array_equal(r["load"], load)
+    np.testing.assert_allclose(r["importance"], imp, rtol=1e-12)
+    assert abs(r["f"].sum() - 1.0) < 1e-15 and abs(r["P"].sum() - 1.0) < 1e-12
+    np.testing.assert_allclose(np.take_along_axis(r["p"], r["idx"], 1), r["gate"], rtol=0)
+
+
+def test_renormalized_gates_sum_to_one():
+    rng = np.random.default_rng(4)
+    r = O.route(rng.standard_normal((30, 4)), rng.standard_normal((7, 4)), None, 3, True, 0.01)
+    np.testing.assert_allclose(r["gate"].sum(axis=1), 1.0, rtol=1e-14)
+
+
+# ------------------------------------------------------------------ eq. (3)
+def test_capacity_closed_forms():
+    for c in GOLD["capacity"]["cases"]:
+        cf = tuple(c["cf"])
+        assert O.capacity(c["T"], c["E"], c["k"], cf, True) == c["assignments"], c
+        assert O.capacity(c["T"], c["E"], c["k"], cf, False) == c["tokens"], c
+    assert O.capacity(100, 8, 1, None) is None
+
+
+def _brute_slots(idx, E, C):
+    T, k = idx.shape
+    slot = np.full((T, k), -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            rank = sum(1 for u in range(t) if e in idx[u])
+            if C is None or rank < C:
+                slot[t, j] = rank
+    return slot
+
+
+@pytest.mark.parametrize("k,C", [(1, 3), (2, 5), (3, 0), (2, None), (1, 64)])
+def test_slots_brute_force_and_invariants(k, C):
+    rng = np.random.default_rng(10 + k)
+    T, E = 48, 6
+    idx = np.stack([rng.permutation(E)[:k] for _ in range(T)])
+    s = O.assign_slots(idx, E, C)
+    np.testing.assert_array_equal(s["slot"], _brute_slots(idx, E, C))
+    load = np.bincount(idx.ravel(), minlength=E)
+    kept = load if C is None else np.minimum(load, C)
+    np.testing.assert_array_equal(s["kept"], kept)
+    assert s["offsets"][-1] == (s["slot"] >= 0).sum()
+    if C is not None:
+        assert np.all(s["kept"] <= C)
+    # every kept pair owns exactly one row, inside its expert's group
+    for t in range(T):
+        for j in range(k):
+            if s["slot"][t, j] >= 0:
+                e = idx[t, j]
+                row = s["offsets"][e] + s["slot"][t, j]
+                assert s["offsets"][e] <= row < s["offsets"][e + 1]
+                assert s["row_token"][row] == t
+
+
+# ------------------------------------------------------------------ experts
+def _ffn_loops(z, w1, w2, act):
+    n, d = z.shape
+    F = w2.shape[1]
+    y = np.zeros((n, w2.shape[0]))
+    for r in range(n):
+        hid = []
+        for f in range(F):
+            a = sum(w1[f, i] * z[r, i] for i in range(d))
+            if act == "relu":
+                hid.append(max(a, 0.0))
+            else:
+                u = sum(w1[F + f, i] * z[r, i] for i in range(d))
+                hid.append(a / (1.0 + math.exp(-a)) * u)
+        for o in range(w2.shape[0]):
+            y[r, o] = sum(w2[o, f] * hid[f] for f in range(F))
+    return y
+
+
+@pytest.mark.parametrize("act", ["relu", "swiglu"])
+def test_expert_ffn_textbook_loops(act):
+    rng = np.random.default_rng(5)
+    d, F = 6, 5
+    z = rng.standard_normal((4, d))
+    w1 = rng.standard_normal(((2 if act == "swiglu" else 1) * F, d))
+    w2 = rng.standard_normal((d, F))
+    np.testing.assert_allclose(O.expert_ffn(z, w1, w2, act)["y"], _ffn_loops(z, w1, w2, act), rtol=1e-12, atol=1e-13)
+
+
+def test_silu_closed_forms():
+    assert O.silu(np.array(0.0)) == 0.0
+    assert abs(O.silu(np.array(math.log(3.0))) - 0.75 * math.log(3.0)) < 1e-15   # sigma(ln 3) = 3/4
+    assert abs(O.silu(np.array(-60.0))) < 1e-24
+
+
+# ------------------------------------------------------------------ eq. (2)
+@pytest.mark.parametrize("act,k,renorm", [("relu", 1, False), ("relu", 2, False), ("swiglu", 3, True)])
+def test_infinite_capacity_equals_dense_masked(act, k, renorm):
+    """With no drops, out = x + sum over top-k of g_i E_i(x), using every expert
+    evaluated densely on every token and a brute-force top-k mask."""
+    w = syn.Workload("pin", T=24, d=8, E=5, k=k, F=6, act=act, dtype="f32", cf=None,
+                     renormalize=renorm, router_std=0.5)
+    inp = syn.make_inputs(w)
+    f = O.forward(inp["x"], inp["w_r"], None, (inp["w1"], inp["w2"]), k=k, act=act, cf=None,
+                  renormalize=renorm)
+    x = inp["x"].astype(np.float64)
+    h = x @ inp["w_r"].astype(np.float64).T
+    p = scipy.special.softmax(h, axis=1)
+    top = _brute_topk(h, k)
+    ref = x.copy()
+    for t in range(w.T):
+        ys = [_ffn_loops(x[t:t + 1], inp["w1"][e].astype(np.float64), inp["w2"][e].astype(np.float64), act)[0]
+              for e in range(w.E)]
+        mask = np.zeros(w.E)
+        mask[top[t]] = 1.0
+        gates = p[t] * mask
+        if renorm:
+            gates = gates / gates.sum()
+        ref[t] += sum(gates[e] * ys[e] for e in range(w.E))
+    np.testing.assert_allclose(f["out"], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_single_expert_is_plain_ffn():
+    """E = 1, k = 1: p = 1, so the layer is x + FFN(x)."""
+    rng = np.random.default_rng(6)
+    T, d, F = 7, 5, 4
+    x = rng.standard_normal((T, d))
+    w1 = rng.standard_normal((1, F, d))
+    w2 = rng.standard_normal((1, d, F))
+    f = O.forward(x, rng.standard_normal((1, d)), None, (w1, w2), k=1, act="relu", cf=None)
+    np.testing.assert_allclose(f["out"], x + _ffn_loops(x, w1[0], w2[0], "relu"), rtol=1e-12, atol=1e-13)
+    assert f["aux"] == pytest.approx(0.01)   # N = 1: f = P = 1
+
+
+def test_dropped_tokens_return_x_bitwise():
+    w = syn.WORKLOADS["tiny-top1-f32"].with_(T=96)
+    inp = syn.make_inputs(w)
+    for C in (0, 3):
+        cf = (C * w.E, w.T)      # gives capacity floor(T*cf/E) = C
+        f = O.forward(inp["x"], inp["w_r"], None, (inp["w1"], inp["w2"]), k=1, act="relu", cf=cf)
+        assert f["C"] == C
+        dropped = np.all(f["slot"] < 0, axis=1)
+        assert dropped.sum() >= (w.T - w.E * C)
+        assert np.array_equal(f["out"][dropped], inp["x"][dropped].astype(np.float64))
+
+
+# ------------------------------------------------------------------ backward
+def _relu_pattern(pp, base, w):
+    """Signs of every kept row's ReLU pre-activations (empty for SwiGLU)."""
+    if w.act != "relu":
+        return ()
+    out = []
+    for e in range(w.E):
+        tt = np.nonzero(((base["idx"] == e) & (base["slot"] >= 0)).any(axis=1))[0]
+        out.append((pp["x"][tt] @ pp["w1"][e].T) > 0)
+    return out
+
+
+def _fd_check(w, n_coords=60, eps=1e-4, seed=0):
+    """Central differences of L = <dY, out> + aux against the oracle's backward.
+
+    eps = 1e-4: at 1e-6 the fp64 rounding of L divided by 2 eps already
+    exceeds the 1e-6 relative bound on single coordinates. Samples where +-eps
+    changes a routing decision or crosses a ReLU kink are skipped and counted.
+    """
+    inp = syn.make_inputs(w, dy=True)
+    kw = dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments,
+              renormalize=w.renormalize, alpha=w.alpha)
+    x = inp["x"].astype(np.float64)
+    w_r = inp["w_r"].astype(np.float64)
+    w1 = inp["w1"].astype(np.float64)
+    w2 = inp["w2"].astype(np.float64)
+    bias = inp["bias"]
+    dy = inp["dy"].astype(np.float64)
+    g = O.backward(x, w_r, bias, (w1, w2), dy, **kw)
+    grads = {"x": g["dx"], "w_r": g["dw_r"],
+             "w1": np.stack([g["dw1"][e] for e in range(w.E)]),
+             "w2": np.stack([g["dw2"][e] for e in range(w.E)])}
+    base = O.forward(x, w_r, bias, (w1, w2), **kw)
+    params = {"x": x, "w_r": w_r, "w1": w1, "w2": w2}
+    pattern0 = _relu_pattern(params, base, w)
+
+    def L(pp):
+        f = O.forward(pp["x"], pp["w_r"], bias, (pp["w1"], pp["w2"]), **kw)
+        same = np.array_equal(f["idx"], base["idx"]) and np.array_equal(f["slot"], base["slot"])
+        same = same and all(np.array_equal(a, b) for a, b in zip(_relu_pattern(pp, base, w), pattern0))
+        return float(np.sum(dy * f["out"])) + f["aux"], same
+
+    rng = np.random.default_rng(seed)
+    checked = skipped = 0
+    for name, arr in params.items():
+        dirs = [rng.standard_normal(arr.shape)]                       # one random direction
+        for _ in range(n_coords):                                      # and single coordinates
+            v = np.zeros(arr.shape)
+            v[tuple(rng.integers(0, s) for s in arr.shape)] = 1.0
+            dirs.append(v)
+        for v in dirs:
+            plus = dict(params); plus[name] = arr + eps * v
+            minus = dict(params); minus[name] = arr - eps * v
+            lp, sp = L(plus)
+            lm, sm = L(minus)
+            if not (sp and sm):
+                skipped += 1
+                continue
+            fd = (lp - lm) / (2 * eps)
+            an = float(np.sum(grads[name] * v))
+            scale = max(1.0, abs(an)) if np.count_nonzero(v) > 1 else max(1e-3, abs(an))
+            assert abs(fd - an) <= 1e-6 * scale, f"{name}: fd {fd!r} vs analytic {an!r}"
+            checked += 1
+    return checked, skipped
+
+
+def test_gradients_finite_differences_tiny():
+    w = syn.WORKLOADS["tiny-top1-f32"].with_(T=128)
+    checked, skipped = _fd_check(w)
+    assert checked >= 200 and skipped <= checked // 10
+
+
+def test_gradients_finite_differences_swiglu_renorm_capacity():
+    w = syn.Workload("fd-swiglu", T=48, d=12, E=6, k=3, F=10, act="swiglu", dtype="f32", cf=(3, 4),
+                     renormalize=True, router_std=0.4, zipf_s=1.2, backward=True)
+    checked, skipped = _fd_check(w, n_coords=40)
+    assert checked >= 150 and skipped <= checked // 10
+
+
+def test_gradient_of_aux_term_alone():
+    """With dY = 0 only eq. (4) contributes: d aux / d h = p * (c - <p, c>), c_e = alpha E f_e / T."""
+    rng = np.random.default_rng(8)
+    T, E, d = 20, 5, 3
+    x, w_r = rng.standard_normal((T, d)), rng.standard_normal((E, d))
+    w1, w2 = rng.standard_normal((E, 4, d)), rng.standard_normal((E, d, 4))
+    g = O.backward(x, w_r, None, (w1, w2), np.zeros((T, d)), k=1, act="relu", cf=None, alpha=0.5)
+    r = O.route(x, w_r, None, 1, False, 0.5)
+    c = 0.5 * E * r["f"] / T
+    dh = r["p"] * (c[None, :] - (r["p"] * c[None, :]).sum(axis=1, keepdims=True))
+    np.testing.assert_allclose(g["dh"], dh, rtol=1e-12, atol=1e-16)
+    np.testing.assert_allclose(g["dw_r"], dh.T @ x, rtol=1e-12, atol=1e-16)
