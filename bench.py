@@ -1,0 +1,332 @@
+"""Benchmark of the MoE FFN layer on B300.
+
+One step = one forward pass of the whole layer (router -> dispatch -> expert
+grouped GEMM -> combine) over one batch of the Switch-Base-like top-1
+workload: T = 8192 tokens (16 x 512), d_model 768, 128 experts, ReLU FFN
+768 -> 3072 -> 768, capacity factor 1.25, bf16 activations and experts with
+an fp32 router. Inputs are seeded synthetic data of that shape, resident in
+HBM before timing. The L2 cache is flushed (a 256 MiB write) before every
+timed step, outside the step's CUDA events.
+
+Prints one JSON line. `--impl reference` times the CPU oracle instead (the
+reference arm of this build: a plain fp64 restatement of the layer).
+Under torchrun (N > 1) every rank runs its own independent batch (data-
+parallel replicas, no collective on the data path); time = max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import moe_synth as syn  # noqa: E402
+
+WORKLOAD = "switch-base-top1"
+METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; dispatch % HBM BW"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6400.0, 1800.0, 1400.0, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Largest `value` across ranks (identity for one rank)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if "Active" in r[5 + i]
+                          and "Not" not in r[5 + i]})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- algorithmic traffic and flops
+def algorithmic(w, K_a: int):
+    """Bytes / FLOPs each step must move or do (kept assignments only, weights read once)."""
+    s = 2  # bf16
+    d, F, E, T, k = w.d, w.F, w.E, w.T, w.k
+    router_b = T * d * s + E * d * 4 + T * k * 8 + T * E * 4   # x, W_r, idx+gate, probs
+    dispatch_b = T * d * s + K_a * d * s + T * k * 4 * 3 + K_a * 4
+    gemm_b = w.nm * E * F * d * s + K_a * d * s * 2 + K_a * F * s * 2   # weights, x_perm in, y out, h out+in
+    combine_b = T * d * s * 2 + K_a * d * s + T * k * 12
+    gemm_flops = 2 * K_a * d * F * w.nm
+    return dict(router=router_b, dispatch=dispatch_b, gemm=gemm_b, combine=combine_b, gemm_flops=gemm_flops)
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    import sparse_mixture_experts_49_b300 as moe
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    w = syn.WORKLOADS[WORKLOAD]
+    inp = syn.make_inputs(w, dy=False)
+    cap = moe.moe_capacity(w.T, w.E, w.k, w.cf[0], w.cf[1], w.count_assignments)
+    cfg = moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=w.k, d_ff=w.F, act=w.act, dtype=w.dtype,
+                          renormalize=w.renormalize, capacity=cap, aux_alpha=w.alpha)
+    stream = torch.cuda.current_stream()
+    L = moe.MoELayer(cfg)
+    bf = torch.bfloat16
+    x = torch.from_numpy(inp["x"]).cuda().to(bf)
+    w_r = torch.from_numpy(inp["w_r"]).cuda()
+    w1 = torch.from_numpy(inp["w1"]).cuda().to(bf)
+    w2 = torch.from_numpy(inp["w2"]).cuda().to(bf)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    calls = ["router", "dispatch", "gemm", "combine"]
+
+    def step(marks=None):
+        if marks: marks[0].record(stream)
+        moe.moe_router(cfg, x, w_r, None, L.probs, L.topk_idx, L.topk_gate, L.importance, L.load, L.aux, L.ws)
+        if marks: marks[1].record(stream)
+        moe.moe_dispatch(cfg, x, L.topk_idx, L.slot, L.kept, L.offsets, L.row_token, L.x_perm, L.ws)
+        if marks: marks[2].record(stream)
+        moe.moe_expert_gemm(cfg, L.x_perm, L.offsets, w1, w2, None, L.h, L.y_perm, L.ws)
+        if marks: marks[3].record(stream)
+        moe.moe_combine(cfg, x, L.y_perm, L.topk_idx, L.topk_gate, L.slot, L.offsets, L.out)
+        if marks: marks[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if L.device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    K_a = int(L.offsets[-1].item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    marks = [[ev() for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        step(marks[i])
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    clk = clocks.stop()
+    per_step = [m[0].elapsed_time(m[4]) for m in marks]
+    per_call = {c: [m[j].elapsed_time(m[j + 1]) for m in marks] for j, c in enumerate(calls)}
+    ms_step = statistics.mean(per_step)
+    total_ms = max_over_ranks(sum(per_step), world)
+    value = world * w.T * args.steps / (total_ms / 1e3)
+
+    # end to end: pinned host x in, host out back, through the same C-ABI calls
+    x_host = torch.from_numpy(inp["x"]).to(bf).pin_memory()
+    out_host = torch.empty(w.T, w.d, dtype=bf).pin_memory()
+    e2e_steps = max(10, args.steps // 4)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        x.copy_(x_host, non_blocking=True)
+        step()
+        out_host.copy_(L.out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * w.T * e2e_steps / (e2e_ms / 1e3)
+
+    hbm, tflops, tflops_sus, peak_src = load_peaks()
+    alg = algorithmic(w, K_a)
+    mean_call = {c: statistics.mean(v) for c, v in per_call.items()}
+    kernels = {}
+    for c in ["router", "dispatch", "combine", "gemm"]:
+        gbs = alg[c] / (mean_call[c] * 1e-3) / 1e9
+        kernels[c] = {"ms": round(mean_call[c], 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+    gemm_tf = alg["gemm_flops"] / (mean_call["gemm"] * 1e-3) / 1e12
+    kernels["gemm"].update({"TFLOP/s": round(gemm_tf, 1), "frac_bf16_peak": round(gemm_tf / tflops, 4)})
+    gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        try:
+            traffic = json.load(open(tpath)).get(WORKLOAD, {}).get("gemm_bytes_per_call")
+        except Exception:
+            traffic = None
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "pass": "fwd", "T": w.T, "d_model": w.d, "experts": w.E, "top_k": w.k,
+                   "d_ff": w.F, "act": w.act, "capacity_factor": "1.25", "capacity": cap,
+                   "capacity_reading": "floor(k*T*cf/E)", "kept_assignments": K_a,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "flushed before every timed step (256 MiB write, outside the step's events)"},
+        "roofline": {"kernel": "moe_expert_gemm (grouped GEMM, 2 launches: W1+ReLU, W2)", "bound": "hbm",
+                     "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(gemm_gbs / hbm, 4), "traffic": traffic, "peak_source": peak_src,
+                     "algorithmic_bytes_per_call": alg["gemm"]},
+        "kernels": kernels,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
+                "d2h_bytes_per_step": w.T * w.d * 2},
+        "gpu_launches": 9 * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- the oracle, timed on the host cores
+def _oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def _oracle_step(w, x, w_r, bias, w1_64, w2_64):
+    from oracle import moe_oracle as O
+    O.forward(x, w_r, bias, (w1_64, w2_64), k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments,
+              renormalize=w.renormalize, alpha=w.alpha)
+
+
+def cpu_baseline(w, inp):
+    w1_64 = inp["w1"].astype(np.float64)
+    w2_64 = inp["w2"].astype(np.float64)
+    t0 = time.perf_counter()
+    _oracle_step(w, inp["x"], inp["w_r"], inp["bias"], w1_64, w2_64)
+    dt = time.perf_counter() - t0
+    return {"value": round(w.T / dt, 1), "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
+            "sample": f"one full forward of the {WORKLOAD} batch (T={w.T}), fp64 numpy, weights widened to fp64 "
+                      f"before timing; {dt:.2f} s"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    w = syn.WORKLOADS[WORKLOAD]
+    inp = syn.make_inputs(w, dy=False)
+    w1_64 = inp["w1"].astype(np.float64)
+    w2_64 = inp["w2"].astype(np.float64)
+    budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    # calibrate a sub-batch size whose step fits the per-step budget
+    Ts = w.T
+    while Ts > 64:
+        ws = w.with_(T=Ts)
+        t0 = time.perf_counter()
+        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
+        if time.perf_counter() - t0 <= budget:
+            break
+        Ts //= 2
+    ws = w.with_(T=Ts)
+    for _ in range(args.warmup):
+        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
+    dt = time.perf_counter() - t0
+    value = Ts * args.steps / dt
+    sample = (f"each step: the first {Ts} of the {w.T} tokens as one batch (same capacity factor), "
+              f"fp64 numpy oracle, weights widened to fp64 before timing")
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "pass": "fwd", "T_sample": Ts},
+           "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": _oracle_threads(),
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

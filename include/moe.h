@@ -1,0 +1,243 @@
+/*
+ * moe.h — C ABI of the sparsely-gated Mixture-of-Experts FFN layer on one
+ * NVIDIA B300 (sm_103a): router -> top-k -> capacity/dispatch -> expert FFNs
+ * as a grouped GEMM -> combine, and the matching backward pass.
+ *
+ * Pages the operations follow (cited by title and section/equation):
+ *   [Switch] "Mixture of Experts (MoE) を1から解説 — Switch Transformerの
+ *            ルーティングと負荷分散": eq. (1) softmax router, eq. (2) gated sum,
+ *            eq. (3) expert capacity and dropped tokens, eq. (4) load-balancing
+ *            loss, the fp32 router of section 学習を安定させる3つの工夫, and the
+ *            parameter vocabulary of section 現場ではこう使う
+ *            (num_experts, capacity_factor, expert_capacity, alpha).
+ *   [LRMoE]  "LRMoE: Demand-Side Load Re-Calibration for Efficient MoE
+ *            Training on Memory-Constrained Nodes", section この記事のポイント:
+ *            kept token-expert pairs compacted into variable-size groups that
+ *            feed a grouped GEMM.
+ *   [Wiki]   "Mixture-of-Experts" (notes.yuuk.io): top-k routing with k > 1,
+ *            SwiGLU experts, importance/load statistics, replay of recorded
+ *            routing.
+ *
+ * Conventions for every call:
+ *   - All array pointers are caller-owned DEVICE memory, row-major, at least
+ *     16-byte aligned (MOE_ERR_ALIGNMENT otherwise). The library never
+ *     allocates device memory: scratch lives in the caller's workspace.
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream). Nothing on the path synchronises the host;
+ *     moe_get_device_error is the one call that does.
+ *   - Arguments are validated on the host before any launch. On an error
+ *     status nothing was launched and no output was touched.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - "x dtype" below is cfg->dtype: MOE_BF16 (bf16 x, expert weights,
+ *     activations; fp32 accumulation) or MOE_F32 (fp32 throughout, no TF32).
+ *     Router weights, probabilities and gates are always fp32 ([Switch]
+ *     section 学習を安定させる3つの工夫: the router stays in float32).
+ *   - Sizes: T tokens, d = d_model, E experts, k = top_k, F = d_ff,
+ *     R1 = F (ReLU) or 2F (SwiGLU: gate rows then up rows),
+ *     rows = moe_max_rows(cfg) = min(T*k, E*C) (T*k without a capacity).
+ *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 1; d and F are
+ *     multiples of 64 for MOE_BF16 and of 4 for MOE_F32 (MOE_ERR_ALIGNMENT
+ *     otherwise).
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, k > E, ... */
+  MOE_ERR_UNSUPPORTED = 2, /* outside the limits above */
+  MOE_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned, or d/F not a multiple of 64 for bf16 */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed (see moe_last_cuda_error) */
+  MOE_ERR_DEVICE = 5       /* a kernel recorded an error (see moe_get_device_error) */
+} moe_status;
+
+enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
+enum { MOE_F32 = 0, MOE_BF16 = 1 };
+
+/* Codes a kernel can record in the workspace's error word. */
+enum {
+  MOE_DEVERR_NONE = 0,
+  MOE_DEVERR_BAD_EXPERT = 1, /* a top-k index outside [0, E) */
+  MOE_DEVERR_DUP_EXPERT = 2, /* the same expert twice in one token's top-k */
+  MOE_DEVERR_TIMEOUT = 3     /* a bounded on-chip wait gave up; outputs are invalid */
+};
+
+/* Problem description ([Switch] section 現場ではこう使う: num_experts,
+ * expert_capacity, the aux-loss coefficient alpha). */
+typedef struct moe_config {
+  int32_t T;           /* tokens in this call ("tokens per batch" of eq. (3)) */
+  int32_t d_model;     /* d */
+  int32_t n_experts;   /* E, the N of eqs. (1)-(4) */
+  int32_t top_k;       /* k (Switch: 1) */
+  int32_t d_ff;        /* F, hidden width of one expert */
+  int32_t act;         /* MOE_ACT_RELU: W2 relu(W1 z); MOE_ACT_SWIGLU: W2 (silu(Wg z) * Wu z) */
+  int32_t dtype;       /* MOE_BF16 or MOE_F32 */
+  int32_t renormalize; /* 1: gates renormalised over the k selected experts */
+  int64_t capacity;    /* expert capacity C per expert; < 0: no limit (dropless) */
+  float aux_alpha;     /* alpha of eq. (4) */
+  int32_t reserved;    /* must be 0 */
+} moe_config;
+
+/* Expert capacity, [Switch] eq. (3): floor(n * cf_num / (E * cf_den)) with
+ * n = k*T assignments (count_assignments != 0) or n = T tokens. Integer
+ * arithmetic only. Returns -1 on invalid arguments (E, cf_den <= 0, ...). */
+int64_t moe_capacity(int64_t T, int32_t E, int32_t k, int32_t cf_num, int32_t cf_den,
+                     int32_t count_assignments);
+
+/* Rows of the permuted buffers x_perm / h / y_perm / pre_act: min(T*k, E*C),
+ * or T*k without a capacity. -1 if cfg is invalid. */
+int64_t moe_max_rows(const moe_config *cfg);
+
+/* Bytes of the workspace every call below takes (forward and backward
+ * scratch, and the device error word). */
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes);
+
+/* Clears the workspace's error word. Call once after allocating it. */
+moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stream);
+
+/*
+ * Router: h = W_r x (+ b), p = softmax(h) over all E experts ([Switch]
+ * eq. (1)), the k largest logits per token (descending, ties to the lower
+ * index), gates g = p of the chosen experts ([Switch] eq. (2); divided by
+ * their sum when cfg->renormalize), and the balance statistics of eq. (4).
+ *
+ *   x          [T, d]  x dtype
+ *   w_r        [E, d]  fp32 (h = W_r x)
+ *   logit_bias [E]     fp32 constant added to h before the softmax, or NULL
+ *   probs      [T, E]  fp32 out, or NULL (the backward pass needs it)
+ *   topk_idx   [T, k]  int32 out
+ *   topk_gate  [T, k]  fp32 out
+ *   importance [E]     fp32 out: sum_t p[t, e]
+ *   load       [E]     int32 out: number of tokens with e in their top-k
+ *   aux_loss   [1]     fp32 out or NULL: alpha * E * sum_e f_e P_e with
+ *                      f_e = load_e / (T k), P_e = importance_e / T
+ * Reductions are in a fixed order: results are bitwise reproducible.
+ */
+moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r,
+                      const float *logit_bias, float *probs, int32_t *topk_idx,
+                      float *topk_gate, float *importance, int32_t *load, float *aux_loss,
+                      void *ws, moe_stream_t stream);
+
+/*
+ * Dispatch ([Switch] eq. (3) and its dropped-token rule; [LRMoE] compaction
+ * into variable-size groups). Every expert takes the tokens that chose it in
+ * ascending token order and keeps the first C: slot = rank, or -1 when the
+ * assignment is dropped. Kept pairs are packed expert by expert:
+ * row(t, j) = expert_offsets[e] + slot[t, j], and x_perm[row] = x[t].
+ * topk_idx may come from moe_router or from the caller (replay of a recorded
+ * routing). An index outside [0, E) or a repeated expert within one token
+ * records MOE_DEVERR_BAD_EXPERT / MOE_DEVERR_DUP_EXPERT and the pair is
+ * treated as dropped.
+ *
+ *   x              [T, d]    x dtype
+ *   topk_idx       [T, k]    int32
+ *   slot           [T, k]    int32 out
+ *   kept           [E]       int32 out: min(load_e, C)
+ *   expert_offsets [E + 1]   int32 out: exclusive prefix sum of kept
+ *   row_token      [rows]    int32 out: token of each packed row (rows past
+ *                            expert_offsets[E] are left untouched)
+ *   x_perm         [rows, d] x dtype out
+ */
+moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                        int32_t *slot, int32_t *kept, int32_t *expert_offsets,
+                        int32_t *row_token, void *x_perm, void *ws, moe_stream_t stream);
+
+/*
+ * Expert FFNs over the packed groups ([Switch] section 直感: each expert is a
+ * copy of the FFN; [LRMoE] variable-size grouped GEMM). For the rows of
+ * expert e (expert_offsets[e] .. expert_offsets[e+1]):
+ *   ReLU:   h = relu(x_perm W1_e^T),                 y_perm = h W2_e^T
+ *   SwiGLU: h = silu(x_perm Wg_e^T) * (x_perm Wu_e^T), y_perm = h W2_e^T
+ * fp32 accumulation; h and y_perm rounded to the x dtype.
+ *
+ *   x_perm  [rows, d]      x dtype
+ *   w1      [E, R1, d]     x dtype (SwiGLU: rows 0..F-1 gate, F..2F-1 up)
+ *   w2      [E, d, F]      x dtype
+ *   pre_act [rows, 2F]     x dtype out (SwiGLU only: gate | up pre-activations,
+ *                          kept for the backward pass); NULL = not stored
+ *                          (must be NULL for ReLU: h itself carries the mask)
+ *   h       [rows, F]      x dtype out
+ *   y_perm  [rows, d]      x dtype out
+ * Rows past expert_offsets[E] are not written.
+ */
+moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm,
+                           const int32_t *expert_offsets, const void *w1, const void *w2,
+                           void *pre_act, void *h, void *y_perm, void *ws,
+                           moe_stream_t stream);
+
+/*
+ * Combine ([Switch] eq. (2) plus the residual passthrough of dropped tokens):
+ *   out[t] = x[t] + sum over j with slot[t, j] >= 0 of
+ *            topk_gate[t, j] * y_perm[expert_offsets[e] + slot[t, j]]
+ * summed in fp32 and rounded once. A token with every assignment dropped
+ * gets x[t] bit for bit.
+ *
+ *   out [T, d] x dtype out (may not alias x or y_perm)
+ */
+moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
+                       const int32_t *topk_idx, const float *topk_gate, const int32_t *slot,
+                       const int32_t *expert_offsets, void *out, moe_stream_t stream);
+
+/* Everything the forward pass produced that the backward pass reads. */
+typedef struct moe_saved {
+  const void *x;                  /* [T, d] */
+  const float *w_r;               /* [E, d] */
+  const void *w1;                 /* [E, R1, d] */
+  const void *w2;                 /* [E, d, F] */
+  const float *probs;             /* [T, E] */
+  const int32_t *topk_idx;        /* [T, k] */
+  const float *topk_gate;         /* [T, k] */
+  const int32_t *slot;            /* [T, k] */
+  const int32_t *expert_offsets;  /* [E + 1] */
+  const int32_t *load;            /* [E] */
+  const void *x_perm;             /* [rows, d] */
+  const void *pre_act;            /* [rows, 2F] (SwiGLU) or NULL (ReLU) */
+  const void *h;                  /* [rows, F] */
+  const void *y_perm;             /* [rows, d] */
+} moe_saved;
+
+/*
+ * Backward of L = <dY, out> + aux, with the top-k sets, capacity masks and
+ * f_e held constant ([Switch] section 負荷分散損失: f comes from an argmax and
+ * carries no gradient; P does, through eq. (1)).
+ *
+ *   dy   [T, d]      x dtype
+ *   dx   [T, d]      x dtype out: dY (residual) + expert path + router path
+ *   dw_r [E, d]      fp32 out
+ *   dw1  [E, R1, d]  x dtype out
+ *   dw2  [E, d, F]   x dtype out
+ * The fixed logit bias gets no gradient.
+ */
+moe_status moe_backward(const moe_config *cfg, const moe_saved *saved, const void *dy, void *dx,
+                        float *dw_r, void *dw1, void *dw2, void *ws, moe_stream_t stream);
+
+/* Device pointers, inside `ws`, of the backward pass's intermediates, valid
+ * after moe_backward: dyp [rows, d] (g * dY per packed row), da [rows, R1]
+ * (gradient at the expert's pre-activations), dxp [rows, d] (gradient at
+ * x_perm), dg [T, k] fp32 (gradient at the gates), dh [T, E] fp32 (gradient
+ * at the router logits). Any output pointer may be NULL. */
+moe_status moe_backward_intermediates(const moe_config *cfg, void *ws, void **dyp, void **da,
+                                      void **dxp, float **dg, float **dh);
+
+/* Synchronises `stream`, returns the first error code a kernel recorded in
+ * `ws` since the last call (MOE_DEVERR_*) in *code, and clears it. */
+moe_status moe_get_device_error(void *ws, moe_stream_t stream, int32_t *code);
+
+const char *moe_status_string(moe_status s);
+/* Text of the last CUDA error seen by a call that returned MOE_ERR_CUDA. */
+const char *moe_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

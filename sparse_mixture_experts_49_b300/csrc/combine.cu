@@ -1,0 +1,208 @@
+// Combine of the MoE layer and the two token-side kernels of its backward pass.
+//
+// "Mixture of Experts (MoE) を1から解説 — Switch Transformerのルーティングと負荷
+// 分散", eq. (2): y = sum over the selected experts of p_i E_i(x); section
+// エキスパートには「定員」がある: a token over capacity skips the expert and
+// passes through the residual connection. The layer output is
+// out = x + sum over kept (t, j) of g[t, j] * y_perm[row(t, j)], accumulated in
+// fp32 and rounded once; a token with nothing kept returns x bit for bit.
+//
+// All three kernels give one warp to a token and stream its rows with
+// 16-byte vector accesses, so they run at HBM speed.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+struct KeptRows {
+  int n;
+  int row[8];
+  float g[8];
+  int j[8];
+};
+
+// The kept rows of token t, in ascending j. Lanes < k read, everyone gets the list.
+__device__ __forceinline__ KeptRows kept_rows(int t, int k, const int32_t *idx, const int32_t *slot,
+                                              const int32_t *offsets, const float *gate) {
+  const int lane = threadIdx.x & 31;
+  int row = -1;
+  float g = 0.0f;
+  if (lane < k) {
+    const int s = slot[(int64_t)t * k + lane];
+    if (s >= 0) {
+      row = offsets[idx[(int64_t)t * k + lane]] + s;
+      if (gate) g = gate[(int64_t)t * k + lane];
+    }
+  }
+  KeptRows kr;
+  kr.n = 0;
+  for (int j = 0; j < k; ++j) {
+    const int r = __shfl_sync(0xffffffffu, row, j);
+    const float gj = __shfl_sync(0xffffffffu, g, j);
+    if (r >= 0) {
+      kr.row[kr.n] = r;
+      kr.g[kr.n] = gj;
+      kr.j[kr.n] = j;
+      ++kr.n;
+    }
+  }
+  return kr;
+}
+
+template <typename XT>
+__global__ void __launch_bounds__(256) combine_kernel(const XT *x, const XT *y_perm, const int32_t *idx,
+                                                      const float *gate, const int32_t *slot,
+                                                      const int32_t *offsets, int T, int d, int k, XT *out) {
+  constexpr int V = Vec16<XT>::N;
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / V;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, gate);
+    const XT *xr = x + (int64_t)t * d;
+    XT *orow = out + (int64_t)t * d;
+    if (kr.n == 0) {
+      for (int v = lane; v < nvec; v += 32)
+        *reinterpret_cast<uint4 *>(orow + v * V) = *reinterpret_cast<const uint4 *>(xr + v * V);
+      continue;
+    }
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[V], y[V];
+      Vec16<XT>::load(xr + v * V, acc);
+      for (int j = 0; j < kr.n; ++j) {
+        Vec16<XT>::load(y_perm + (int64_t)kr.row[j] * d + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = fmaf(kr.g[j], y[i], acc[i]);
+      }
+      Vec16<XT>::store(orow + v * V, acc);
+    }
+  }
+}
+
+// dg[t, j] = <dY_t, y_perm[row]> and dYp[row] = g[t, j] dY_t for kept pairs; dg = 0 otherwise.
+template <typename XT>
+__global__ void __launch_bounds__(256) combine_backward_kernel(const XT *dy, const XT *y_perm, const int32_t *idx,
+                                                               const float *gate, const int32_t *slot,
+                                                               const int32_t *offsets, int T, int d, int k,
+                                                               XT *dyp, float *dg) {
+  constexpr int V = Vec16<XT>::N;
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / V;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, gate);
+    float dot[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) dot[j] = 0.0f;
+    const XT *dr = dy + (int64_t)t * d;
+    for (int v = lane; v < nvec; v += 32) {
+      float g[V], y[V], o[V];
+      Vec16<XT>::load(dr + v * V, g);
+      for (int j = 0; j < kr.n; ++j) {
+        Vec16<XT>::load(y_perm + (int64_t)kr.row[j] * d + v * V, y);
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          s = fmaf(g[i], y[i], s);
+          o[i] = kr.g[j] * g[i];
+        }
+        dot[j] += s;
+        Vec16<XT>::store(dyp + (int64_t)kr.row[j] * d + v * V, o);
+      }
+    }
+    for (int j = 0; j < kr.n; ++j) {
+      float s = dot[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      dot[j] = s;
+    }
+    if (lane < k) {
+      float v = 0.0f;
+      for (int j = 0; j < kr.n; ++j)
+        if (kr.j[j] == lane) v = dot[j];
+      dg[(int64_t)t * k + lane] = v;
+    }
+  }
+}
+
+// dX_t = dY_t + sum over kept rows of dXp[row] + dXr_t (router path, fp32), rounded once.
+template <typename XT>
+__global__ void __launch_bounds__(256) unpermute_kernel(const XT *dy, const XT *dxp, const float *dxr,
+                                                        const int32_t *idx, const int32_t *slot,
+                                                        const int32_t *offsets, int T, int d, int k, XT *dx) {
+  constexpr int V = Vec16<XT>::N;
+  const int lane = threadIdx.x & 31;
+  const int nvec = d / V;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, nullptr);
+    for (int v = lane; v < nvec; v += 32) {
+      float acc[V], y[V];
+      Vec16<XT>::load(dy + (int64_t)t * d + v * V, acc);
+      for (int j = 0; j < kr.n; ++j) {
+        Vec16<XT>::load(dxp + (int64_t)kr.row[j] * d + v * V, y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] += y[i];
+      }
+      Vec16<float>::load(dxr + (int64_t)t * d + v * V, y);
+      if (V == 8) Vec16<float>::load(dxr + (int64_t)t * d + v * V + 4, y + 4);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += y[i];
+      Vec16<XT>::store(dx + (int64_t)t * d + v * V, acc);
+    }
+  }
+}
+
+int token_grid(int T) {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  int grid = (T + 7) / 8;
+  return grid > sms * 8 ? sms * 8 : grid;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
+                           const float *gate, const int32_t *slot, const int32_t *offsets, void *out,
+                           cudaStream_t stream) {
+  const int grid = token_grid(sh.T);
+  if (sh.dtype == MOE_BF16)
+    combine_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)x, (const bf16 *)y_perm, idx, gate, slot, offsets,
+                                                   sh.T, sh.d, sh.k, (bf16 *)out);
+  else
+    combine_kernel<float><<<grid, 256, 0, stream>>>((const float *)x, (const float *)y_perm, idx, gate, slot,
+                                                    offsets, sh.T, sh.d, sh.k, (float *)out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
+                                    const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp,
+                                    float *dg, cudaStream_t stream) {
+  const int grid = token_grid(sh.T);
+  if (sh.dtype == MOE_BF16)
+    combine_backward_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)dy, (const bf16 *)y_perm, idx, gate,
+                                                            slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dyp, dg);
+  else
+    combine_backward_kernel<float><<<grid, 256, 0, stream>>>((const float *)dy, (const float *)y_perm, idx, gate,
+                                                             slot, offsets, sh.T, sh.d, sh.k, (float *)dyp, dg);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr,
+                             const int32_t *idx, const int32_t *slot, const int32_t *offsets, void *dx,
+                             cudaStream_t stream) {
+  const int grid = token_grid(sh.T);
+  if (sh.dtype == MOE_BF16)
+    unpermute_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)dy, (const bf16 *)dxp, dxr, idx, slot, offsets,
+                                                     sh.T, sh.d, sh.k, (bf16 *)dx);
+  else
+    unpermute_kernel<float><<<grid, 256, 0, stream>>>((const float *)dy, (const float *)dxp, dxr, idx, slot,
+                                                      offsets, sh.T, sh.d, sh.k, (float *)dx);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

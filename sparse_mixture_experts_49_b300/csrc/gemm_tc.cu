@@ -1,0 +1,561 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM, operands
+// staged by TMA), for the expert FFNs of the MoE layer.
+//
+// The experts' token groups are the variable-size groups that compaction of
+// the kept token-expert pairs produces ("LRMoE: Demand-Side Load
+// Re-Calibration for Efficient MoE Training on Memory-Constrained Nodes",
+// section この記事のポイント: physical compaction -> variable-size grouped
+// GEMM). Group sizes stay on the device: a persistent kernel reads the expert
+// offsets and walks its tiles itself, so no host synchronisation is needed.
+//
+// Two grouping modes:
+//   grouped-M: C[rows of e, N] = A[rows of e, K] * B_e[N, K]^T
+//              (forward GEMMs, and the dgrad GEMMs of the backward pass with
+//              B_e read MN-major from the weight tensor);
+//   grouped-K: C_e[M, N] = sum over rows r of e of A[r, M]^T B[r, N]
+//              (weight gradients; K is the group size, which varies).
+// Tile 128 x 256 x 64 (bf16, fp32 accumulator in TMEM), 4-stage TMA ring,
+// warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
+// warps 2-5 epilogue. Two TMEM accumulators let the epilogue of one tile run
+// under the MMAs of the next.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
+constexpr int THREADS = 192;
+constexpr int MAX_E = 256;
+
+struct __align__(8) Smem {
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int tile_start[MAX_E + 1];
+  int off[MAX_E + 1];
+};
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Smem);
+
+struct Args {
+  const int32_t *offsets;  // [E + 1] row offsets of the groups
+  int E;
+  int M, N, K;             // grouped-M: N (output columns), K; grouped-K: M, N
+  int F;                   // SwiGLU: offset of the up half (rows of W1, columns of pre_act / dA)
+  bf16 *C;
+  int64_t ldc;
+  int64_t sce;             // grouped-K: C_e = C + e * sce
+  bf16 *C2;                // SwiGLU forward: pre-activations [rows, 2F]
+  int64_t ldc2;
+  const bf16 *aux;         // ReLU bwd: h; SwiGLU bwd: pre-activations
+  int64_t ldaux;
+  DeviceStatus *st;
+};
+
+__device__ __forceinline__ int find_group(const int *tile_start, int E, int tile) {
+  int lo = 0, hi = E - 1;  // largest e with tile_start[e] <= tile
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Bounded wait used only after an abort, to let copies already in flight land.
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (global_timer_ns() - t0 > 200000000ull) break;  // 0.2 s
+}
+
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const Args p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  Smem &s = *reinterpret_cast<Smem *>(tiles + (size_t)STAGES * STAGE_BYTES);
+  volatile int *abort_flag = &s.abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int E = p.E;
+  constexpr bool SWIGLU_FWD = (EPI == EPI_SWIGLU);
+  // Output columns one tile covers (SwiGLU forward: 128 gate + 128 up accumulators -> 128 outputs).
+  constexpr int TN_OUT = SWIGLU_FWD ? 128 : BN;
+  const int n_tiles = (p.N + TN_OUT - 1) / TN_OUT;
+  const int m_tiles_k = GROUP_K ? (p.M + BM - 1) / BM : 0;
+
+  // ---------------------------------------------------------------- set-up
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+      for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], 4); }
+      mbar_init(&s.drain, 1);
+      s.abort_flag = 0;
+      fence_barrier_init();
+    }
+    // tile_start[e] = number of tiles of groups before e
+    int carry = 0;
+    if (lane == 0) s.tile_start[0] = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int e = base + lane;
+      int t = 0;
+      if (e < E) {
+        const int lo = p.offsets[e], hi = p.offsets[e + 1];
+        s.off[e] = lo;
+        if (e == E - 1) s.off[E] = hi;
+        t = GROUP_K ? m_tiles_k * n_tiles : ((hi - lo + BM - 1) / BM) * n_tiles;
+      }
+      int incl = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (e < E) s.tile_start[e + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  } else if (warp == 1) {
+    tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s.tmem_base;
+  const int total_tiles = s.tile_start[E];
+
+  auto decode = [&](int tile, int &e, int &mt, int &nt) {
+    e = find_group(s.tile_start, E, tile);
+    const int local = tile - s.tile_start[e];
+    mt = local / n_tiles;
+    nt = local - mt * n_tiles;
+  };
+  auto k_steps = [&](int e) -> int {
+    return GROUP_K ? (s.off[e + 1] - s.off[e] + BK - 1) / BK : (p.K + BK - 1) / BK;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_a = policy_evict_last();
+      const uint64_t pol_b = GROUP_K ? policy_evict_last() : policy_evict_first();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0, issued_parity = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        int e, mt, nt;
+        decode(tile, e, mt, nt);
+        const int nk = k_steps(e);
+        for (int ks = 0; ks < nk; ++ks) {
+          if (!mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st)) { ok = false; break; }
+          uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
+          uint8_t *b_s = a_s + A_BYTES;
+          mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+          const int k0 = ks * BK;
+          if (!GROUP_K) {
+            const int row0 = s.off[e] + mt * BM;
+            tma_load_2d(a_s, &tmA, &s.full[stage], k0, row0, pol_a);
+            if (!B_MN) {
+              int r0, r1;
+              if (SWIGLU_FWD) { r0 = nt * 128; r1 = p.F + nt * 128; }
+              else { r0 = nt * BN; r1 = nt * BN + 128; }
+              tma_load_3d(b_s, &tmB, &s.full[stage], k0, r0, e, pol_b);
+              tma_load_3d(b_s + 16384, &tmB, &s.full[stage], k0, r1, e, pol_b);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                tma_load_3d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, k0, e, pol_b);
+            }
+          } else {
+            const int r0 = s.off[e] + k0;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d(a_s + j * 8192, &tmA, &s.full[stage], mt * BM + 64 * j, r0, pol_a);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_2d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, r0, pol_b);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (*abort_flag) {
+        for (int i = 0; i < STAGES; ++i)
+          if (issued & (1u << i)) drain_wait(&s.full[i], (issued_parity >> i) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      const int nk = k_steps(e);
+      if (!mbar_wait_bounded(&s.acc_empty[acc], acc_phase ^ 1, abort_flag, p.st)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+      for (int ks = 0; ks < nk; ++ks) {
+        if (!mbar_wait_bounded(&s.full[stage], phase, abort_flag, p.st)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
+        uint8_t *b_s = a_s + A_BYTES;
+        if (GROUP_K) {
+          // The last K step of a group may run past its rows: zero those K rows
+          // of both operands (each is one 128-byte line per 64-wide block).
+          const int valid = s.off[e + 1] - (s.off[e] + ks * BK);
+          if (valid < BK) {
+            const int nrows = BK - valid;
+            const int chunks = nrows * 8;  // 16-byte chunks per block
+            for (int i = lane; i < 6 * chunks; i += 32) {
+              const int blk = i / chunks, rem = i - blk * chunks;
+              const int row = valid + (rem >> 3), c = rem & 7;
+              uint8_t *base = (blk < 2) ? (a_s + blk * 8192) : (b_s + (blk - 2) * 8192);
+              *reinterpret_cast<uint4 *>(base + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const uint32_t a0 = smem_u32(a_s), b0 = smem_u32(b_s);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
+                                     : smem_desc_sw128(b0 + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&s.empty[stage]);
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(&s.acc_full[acc]);
+      __syncwarp();
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&s.drain);
+      __syncwarp();
+      drain_wait(&s.drain, 0);
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int r = q * 32 + lane;       // row inside the 128-row tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      if (!mbar_wait_bounded(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      float v[32], w[32];
+      if (!GROUP_K) {
+        const int rows_e = s.off[e + 1] - s.off[e];
+        const bool valid = mt * BM + r < rows_e;
+        const int64_t row = (int64_t)s.off[e] + mt * BM + r;
+        if (EPI == EPI_SWIGLU) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            const int col = nt * 128 + c * 32;
+            tmem_ld32(t_row + c * 32, v);
+            tmem_ld32(t_row + 128 + c * 32, w);
+            if (valid && col < p.N) {
+              float hv[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) hv[i] = silu_f(v[i]) * w[i];
+              bf16 *hp = p.C + row * p.ldc + col;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
+              if (p.C2) {
+                bf16 *gp = p.C2 + row * p.ldc2 + col;
+                bf16 *up = gp + p.F;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  Vec16<bf16>::store(gp + 8 * i, v + 8 * i);
+                  Vec16<bf16>::store(up + 8 * i, w + 8 * i);
+                }
+              }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            const int col = nt * BN + c * 32;
+            tmem_ld32(t_row + c * 32, v);
+            if (!valid || col >= p.N) continue;
+            if (EPI == EPI_RELU) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+            } else if (EPI == EPI_RELU_BWD) {
+              const bf16 *hp = p.aux + row * p.ldaux + col;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) Vec16<bf16>::load(hp + 8 * i, w + 8 * i);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = (w[i] > 0.0f) ? v[i] : 0.0f;
+            } else if (EPI == EPI_SWIGLU_BWD) {
+              const bf16 *gp = p.aux + row * p.ldaux + col;
+              const bf16 *up = gp + p.F;
+              float gu[32];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                Vec16<bf16>::load(gp + 8 * i, w + 8 * i);
+                Vec16<bf16>::load(up + 8 * i, gu + 8 * i);
+              }
+              float dup[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const float g = w[i], u = gu[i];
+                const float sg = 1.0f / (1.0f + expf(-g));
+                dup[i] = v[i] * g * sg;                                  // dU = dH * silu(G)
+                v[i] = v[i] * u * (sg * (1.0f + g * (1.0f - sg)));      // dG = dH * U * silu'(G)
+              }
+              bf16 *dp2 = p.C + row * p.ldc + p.F + col;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(dp2 + 8 * i, dup + 8 * i);
+            }
+            bf16 *cp = p.C + row * p.ldc + col;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+          }
+        }
+      } else {
+        const bool empty_group = s.off[e + 1] == s.off[e];
+        const int m = mt * BM + r;
+        bf16 *cbase = p.C + (int64_t)e * p.sce + (int64_t)m * p.ldc;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col = nt * BN + c * 32;
+          if (!empty_group) tmem_ld32(t_row + c * 32, v);
+          else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          if (m < p.M && col < p.N) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cbase + col + 8 * i, v + 8 * i);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s.acc_empty[acc]);
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 map over [outer, inner] (inner contiguous), box [box_outer, box_inner], 128-byte swizzle.
+static bool make_map_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                        uint32_t box_outer) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [d2, d1, d0] (d0 contiguous), box [1, box1, box0].
+static bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                        uint32_t box1) {
+  EncodeTiledFn enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<GROUP_K, A_MN, B_MN, EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<sm_count(), THREADS, SMEM_BYTES, stream>>>(ma, mb, a);
+  return cudaGetLastError();
+}
+
+}  // namespace tc
+
+// ---------------------------------------------------------------- launchers used by the C ABI
+cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
+                              const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
+                              cudaStream_t stream) {
+  using namespace tc;
+  CUtensorMap ma, mb;
+  const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;  // a map needs at least one row
+  Args a{};
+  a.offsets = offsets;
+  a.E = sh.E;
+  a.F = sh.F;
+  a.st = st;
+  // GEMM 1 (+ activation): A = x_perm [rows, d], B = W1 [E, R1, d]
+  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
+    return cudaErrorInvalidValue;
+  a.N = sh.F;
+  a.K = sh.d;
+  a.C = (bf16 *)h;
+  a.ldc = sh.F;
+  cudaError_t err;
+  if (sh.act == MOE_ACT_SWIGLU) {
+    a.C2 = (bf16 *)pre_act;
+    a.ldc2 = 2 * (int64_t)sh.F;
+    err = launch<0, 0, 0, EPI_SWIGLU>(ma, mb, a, stream);
+  } else {
+    err = launch<0, 0, 0, EPI_RELU>(ma, mb, a, stream);
+  }
+  if (err != cudaSuccess) return err;
+  // GEMM 2: A = h [rows, F], B = W2 [E, d, F]
+  if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
+    return cudaErrorInvalidValue;
+  Args b{};
+  b.offsets = offsets;
+  b.E = sh.E;
+  b.F = sh.F;
+  b.st = st;
+  b.N = sh.d;
+  b.K = sh.F;
+  b.C = (bf16 *)y_perm;
+  b.ldc = sh.d;
+  return launch<0, 0, 0, EPI_STORE>(ma, mb, b, stream);
+}
+
+cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
+                               const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
+                               void *dxp, void *dw1, void *dw2, DeviceStatus *st, cudaStream_t stream) {
+  using namespace tc;
+  CUtensorMap ma, mb;
+  const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;
+  cudaError_t err;
+  const bool swiglu = sh.act == MOE_ACT_SWIGLU;
+  // dH = dYp W2_e (B MN-major from W2 [E, d, F]), fused activation backward -> dA [rows, R1]
+  {
+    Args a{};
+    a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
+    a.N = sh.F; a.K = sh.d;
+    a.C = (bf16 *)da; a.ldc = sh.R1;
+    if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 64))
+      return cudaErrorInvalidValue;
+    if (swiglu) {
+      a.aux = (const bf16 *)pre_act; a.ldaux = 2 * (int64_t)sh.F;
+      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(ma, mb, a, stream);
+    } else {
+      a.aux = (const bf16 *)h; a.ldaux = sh.F;
+      err = launch<0, 0, 1, EPI_RELU_BWD>(ma, mb, a, stream);
+    }
+    if (err != cudaSuccess) return err;
+  }
+  // dW2_e = dYp_e^T H_e   (grouped over K = rows of e): M = d, N = F
+  {
+    Args a{};
+    a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
+    a.M = sh.d; a.N = sh.F;
+    a.C = (bf16 *)dw2; a.ldc = sh.F; a.sce = (int64_t)sh.d * sh.F;
+    if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 64) || !make_map_2d(&mb, h, sh.F, rows, 64, 64))
+      return cudaErrorInvalidValue;
+    err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
+    if (err != cudaSuccess) return err;
+  }
+  // dXp = dA W1_e (B MN-major from W1 [E, R1, d]): N = d, K = R1
+  {
+    Args a{};
+    a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
+    a.N = sh.d; a.K = sh.R1;
+    a.C = (bf16 *)dxp; a.ldc = sh.d;
+    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 64))
+      return cudaErrorInvalidValue;
+    err = launch<0, 0, 1, EPI_STORE>(ma, mb, a, stream);
+    if (err != cudaSuccess) return err;
+  }
+  // dW1_e = dA_e^T X_e: M = R1, N = d
+  {
+    Args a{};
+    a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
+    a.M = sh.R1; a.N = sh.d;
+    a.C = (bf16 *)dw1; a.ldc = sh.d; a.sce = (int64_t)sh.R1 * sh.d;
+    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 64) || !make_map_2d(&mb, x_perm, sh.d, rows, 64, 64))
+      return cudaErrorInvalidValue;
+    err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
+  }
+  return err;
+}
+
+}  // namespace moe

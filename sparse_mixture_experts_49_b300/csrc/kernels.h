@@ -1,0 +1,78 @@
+// Internal launchers behind the C ABI (C++ linkage, not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct DeviceStatus;
+
+// moe_config after validation, with derived sizes.
+struct Shape {
+  int T, d, E, k, F, R1, act, dtype, renorm;
+  int64_t C;      // capacity, < 0 = none
+  float alpha;
+  int64_t rows;   // rows of the packed buffers
+  int elt;        // bytes per element of the x dtype
+};
+
+enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4 };
+
+// Workspace carve-up (byte offsets from the workspace base).
+struct WsLayout {
+  size_t status;                 // DeviceStatus
+  size_t router_imp, router_load;  // [router blocks, E] partial sums
+  size_t disp_counts, disp_base;   // [dispatch blocks, E]
+  size_t disp_load;                // [E]
+  size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
+  size_t dg, dh, dxr, dwr_acc;     // backward: [T, k], [T, E], [T, d] fp32
+  size_t total;
+};
+WsLayout ws_layout(const Shape &sh);
+
+constexpr int ROUTER_TOKENS = 64;     // tokens per router block
+constexpr int DISPATCH_TOKENS = 256;  // tokens per dispatch block
+
+int router_blocks(const Shape &sh);
+int dispatch_blocks(const Shape &sh);
+
+cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, float *probs,
+                          int32_t *idx, float *gate, float *importance, int32_t *load, float *aux, void *ws,
+                          cudaStream_t stream);
+
+cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,
+                            int32_t *offsets, int32_t *row_token, void *x_perm, void *ws, cudaStream_t stream);
+
+cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
+                           const float *gate, const int32_t *slot, const int32_t *offsets, void *out,
+                           cudaStream_t stream);
+
+// Expert FFN forward on tensor cores (bf16) / CUDA cores (fp32).
+cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
+                              const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
+                              cudaStream_t stream);
+cudaError_t simt_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
+                                const void *w2, void *pre_act, void *h, void *y_perm, cudaStream_t stream);
+
+cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
+                               const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
+                               void *dxp, void *dw1, void *dw2, DeviceStatus *st, cudaStream_t stream);
+cudaError_t simt_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
+                                 const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
+                                 void *dxp, void *dw1, void *dw2, cudaStream_t stream);
+
+// Backward pieces outside the grouped GEMMs.
+cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
+                                    const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp,
+                                    float *dg, cudaStream_t stream);
+cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *w_r, const float *probs,
+                                   const int32_t *idx, const float *gate, const int32_t *load, const float *dg,
+                                   float *dh, float *dw_r, float *dxr, cudaStream_t stream);
+cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr,
+                             const int32_t *idx, const int32_t *slot, const int32_t *offsets, void *dx,
+                             cudaStream_t stream);
+
+}  // namespace moe

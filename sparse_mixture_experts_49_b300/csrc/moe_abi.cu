@@ -1,0 +1,263 @@
+// The C ABI of the MoE layer (declared in include/moe.h): argument
+// validation on the host, workspace carve-up, and the launch sequence of each
+// call. No call allocates device memory or synchronises the host, except
+// moe_get_device_error, which is documented to synchronise.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+static thread_local char g_cuda_error[256] = "";
+
+static moe_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static moe_status make_shape(const moe_config *c, Shape *sh) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 1 || c->d_model < 1 || c->n_experts < 1 || c->top_k < 1 || c->d_ff < 1) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c->reserved != 0 || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
+  if (c->n_experts > 256 || c->top_k > 8) return MOE_ERR_UNSUPPORTED;
+  const int mult = c->dtype == MOE_BF16 ? 64 : 4;
+  if (c->d_model % mult != 0 || c->d_ff % mult != 0) return MOE_ERR_ALIGNMENT;
+  const int64_t Tk = (int64_t)c->T * c->top_k;
+  if (Tk > (int64_t)1 << 30 || (int64_t)c->d_model * c->d_ff * 2 > ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  sh->T = c->T;
+  sh->d = c->d_model;
+  sh->E = c->n_experts;
+  sh->k = c->top_k;
+  sh->F = c->d_ff;
+  sh->R1 = c->act == MOE_ACT_SWIGLU ? 2 * c->d_ff : c->d_ff;
+  sh->act = c->act;
+  sh->dtype = c->dtype;
+  sh->renorm = c->renormalize;
+  sh->C = c->capacity < 0 ? -1 : c->capacity;
+  sh->alpha = c->aux_alpha;
+  int64_t rows = Tk;
+  if (sh->C >= 0 && sh->C * sh->E < rows) rows = sh->C * sh->E;
+  sh->rows = rows;
+  sh->elt = c->dtype == MOE_BF16 ? 2 : 4;
+  return MOE_OK;
+}
+
+WsLayout ws_layout(const Shape &sh) {
+  WsLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = round_up(o + bytes, 256);
+    return at;
+  };
+  L.status = take(256);
+  const size_t rb = (size_t)router_blocks(sh), db = (size_t)dispatch_blocks(sh);
+  L.router_imp = take(rb * sh.E * 4);
+  L.router_load = take(rb * sh.E * 4);
+  L.disp_counts = take(db * sh.E * 4);
+  L.disp_base = take(db * sh.E * 4);
+  L.disp_load = take((size_t)sh.E * 4);
+  const size_t rows = (size_t)(sh.rows > 0 ? sh.rows : 1);
+  L.dyp = take(rows * sh.d * sh.elt);
+  L.da = take(rows * sh.R1 * sh.elt);
+  L.dxp = take(rows * sh.d * sh.elt);
+  L.dg = take((size_t)sh.T * sh.k * 4);
+  L.dh = take((size_t)sh.T * sh.E * 4);
+  L.dxr = take((size_t)sh.T * sh.d * 4);
+  L.dwr_acc = 0;
+  L.total = o;
+  return L;
+}
+
+static DeviceStatus *status_of(void *ws) { return reinterpret_cast<DeviceStatus *>(ws); }
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_CHECK(expr)                 \
+  do {                                  \
+    moe_status _s = (expr);             \
+    if (_s != MOE_OK) return _s;        \
+  } while (0)
+#define MOE_REQUIRE(cond, code) \
+  do {                          \
+    if (!(cond)) return (code); \
+  } while (0)
+#define MOE_PTR(p) \
+  do {                                               \
+    if ((p) == nullptr) return MOE_ERR_INVALID_ARG;  \
+    if (!aligned16(p)) return MOE_ERR_ALIGNMENT;     \
+  } while (0)
+#define MOE_OPT_PTR(p) \
+  do {                                                    \
+    if ((p) != nullptr && !aligned16(p)) return MOE_ERR_ALIGNMENT; \
+  } while (0)
+
+extern "C" {
+
+int64_t moe_capacity(int64_t T, int32_t E, int32_t k, int32_t cf_num, int32_t cf_den, int32_t count_assignments) {
+  if (T < 0 || E <= 0 || k <= 0 || cf_num < 0 || cf_den <= 0) return -1;
+  const int64_t n = count_assignments ? T * (int64_t)k : T;
+  return (n * (int64_t)cf_num) / ((int64_t)E * (int64_t)cf_den);
+}
+
+int64_t moe_max_rows(const moe_config *cfg) {
+  Shape sh;
+  if (make_shape(cfg, &sh) != MOE_OK) return -1;
+  return sh.rows;
+}
+
+moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(bytes != nullptr, MOE_ERR_INVALID_ARG);
+  *bytes = ws_layout(sh).total;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(ws);
+  return cuda_status(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+}
+
+moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
+                      float *probs, int32_t *topk_idx, float *topk_gate, float *importance, int32_t *load,
+                      float *aux_loss, void *ws, moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance); MOE_PTR(load);
+  MOE_PTR(ws);
+  MOE_OPT_PTR(logit_bias); MOE_OPT_PTR(probs); MOE_OPT_PTR(aux_loss);
+  return cuda_status(launch_router(sh, x, w_r, logit_bias, probs, topk_idx, topk_gate, importance, load, aux_loss,
+                                   ws, (cudaStream_t)stream));
+}
+
+moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx, int32_t *slot,
+                        int32_t *kept, int32_t *expert_offsets, int32_t *row_token, void *x_perm, void *ws,
+                        moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(x); MOE_PTR(topk_idx); MOE_PTR(slot); MOE_PTR(kept); MOE_PTR(expert_offsets); MOE_PTR(row_token);
+  MOE_PTR(x_perm); MOE_PTR(ws);
+  return cuda_status(launch_dispatch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, ws,
+                                     (cudaStream_t)stream));
+}
+
+moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm, const int32_t *expert_offsets,
+                           const void *w1, const void *w2, void *pre_act, void *h, void *y_perm, void *ws,
+                           moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(x_perm); MOE_PTR(expert_offsets); MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(h); MOE_PTR(y_perm); MOE_PTR(ws);
+  MOE_OPT_PTR(pre_act);
+  MOE_REQUIRE(!(sh.act == MOE_ACT_RELU && pre_act != nullptr), MOE_ERR_INVALID_ARG);
+  DeviceStatus *st = status_of(ws);
+  cudaError_t e = sh.dtype == MOE_BF16
+                      ? tc_expert_forward(sh, x_perm, expert_offsets, w1, w2, pre_act, h, y_perm, st,
+                                          (cudaStream_t)stream)
+                      : simt_expert_forward(sh, x_perm, expert_offsets, w1, w2, pre_act, h, y_perm,
+                                            (cudaStream_t)stream);
+  return cuda_status(e);
+}
+
+moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm, const int32_t *topk_idx,
+                       const float *topk_gate, const int32_t *slot, const int32_t *expert_offsets, void *out,
+                       moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(x); MOE_PTR(y_perm); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(slot); MOE_PTR(expert_offsets);
+  MOE_PTR(out);
+  MOE_REQUIRE(out != x && out != y_perm, MOE_ERR_INVALID_ARG);
+  return cuda_status(
+      launch_combine(sh, x, y_perm, topk_idx, topk_gate, slot, expert_offsets, out, (cudaStream_t)stream));
+}
+
+moe_status moe_backward(const moe_config *cfg, const moe_saved *sv, const void *dy, void *dx, float *dw_r,
+                        void *dw1, void *dw2, void *ws, moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sv != nullptr, MOE_ERR_INVALID_ARG);
+  MOE_PTR(sv->x); MOE_PTR(sv->w_r); MOE_PTR(sv->w1); MOE_PTR(sv->w2); MOE_PTR(sv->probs); MOE_PTR(sv->topk_idx);
+  MOE_PTR(sv->topk_gate); MOE_PTR(sv->slot); MOE_PTR(sv->expert_offsets); MOE_PTR(sv->load);
+  MOE_PTR(sv->x_perm); MOE_PTR(sv->h); MOE_PTR(sv->y_perm);
+  if (sh.act == MOE_ACT_SWIGLU) MOE_PTR(sv->pre_act);
+  MOE_PTR(dy); MOE_PTR(dx); MOE_PTR(dw_r); MOE_PTR(dw1); MOE_PTR(dw2); MOE_PTR(ws);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  void *dyp = w + L.dyp, *da = w + L.da, *dxp = w + L.dxp;
+  float *dg = reinterpret_cast<float *>(w + L.dg);
+  float *dh = reinterpret_cast<float *>(w + L.dh);
+  float *dxr = reinterpret_cast<float *>(w + L.dxr);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_combine_backward(sh, dy, sv->y_perm, sv->topk_idx, sv->topk_gate, sv->slot,
+                                          sv->expert_offsets, dyp, dg, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = sh.dtype == MOE_BF16 ? tc_expert_backward(sh, sv->expert_offsets, sv->x_perm, sv->w1, sv->w2, sv->pre_act,
+                                                sv->h, dyp, da, dxp, dw1, dw2, status_of(ws), s)
+                           : simt_expert_backward(sh, sv->expert_offsets, sv->x_perm, sv->w1, sv->w2,
+                                                  sv->pre_act, sv->h, dyp, da, dxp, dw1, dw2, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_router_backward(sh, sv->x, sv->w_r, sv->probs, sv->topk_idx, sv->topk_gate, sv->load, dg, dh, dw_r,
+                             dxr, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_unpermute(sh, dy, dxp, dxr, sv->topk_idx, sv->slot, sv->expert_offsets, dx, s));
+}
+
+moe_status moe_backward_intermediates(const moe_config *cfg, void *ws, void **dyp, void **da, void **dxp,
+                                      float **dg, float **dh) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(ws != nullptr, MOE_ERR_INVALID_ARG);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  if (dyp) *dyp = w + L.dyp;
+  if (da) *da = w + L.da;
+  if (dxp) *dxp = w + L.dxp;
+  if (dg) *dg = reinterpret_cast<float *>(w + L.dg);
+  if (dh) *dh = reinterpret_cast<float *>(w + L.dh);
+  return MOE_OK;
+}
+
+moe_status moe_get_device_error(void *ws, moe_stream_t stream, int32_t *code) {
+  MOE_REQUIRE(ws != nullptr && code != nullptr, MOE_ERR_INVALID_ARG);
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  DeviceStatus st;
+  e = cudaMemcpy(&st, ws, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = cudaMemset(ws, 0, sizeof(st));
+  if (e != cudaSuccess) return cuda_status(e);
+  *code = st.code;
+  return MOE_OK;
+}
+
+const char *moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_ALIGNMENT: return "misaligned pointer or size";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE: return "device-side error recorded";
+  }
+  return "unknown status";
+}
+
+const char *moe_last_cuda_error(void) { return g_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
+
+Routing (top-k indices, load, slots, kept counts, group offsets, row owners)
+must match bit for bit; the fp32 router's values within 1e-5 x max|ref|; the
+layer's floating outputs and gradients within 2e-2 x max|ref| for bf16
+experts (fp32 accumulation) and 1e-5 x max|ref| for the fp32 layer.
+"""
+import numpy as np
+import pytest
+
+import moe_synth as syn
+from oracle import moe_oracle as O
+from moe_cases import (SMALL, TOL_BF16, TOL_F32, assert_close, check_router_values, check_routing,
+                             expert_reference, oracle_kw, run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_mixture_experts_49_b300 as moe
+    moe.lib()   # fails loudly if the library is not built
+
+
+def _ref_all(w, inp, backward):
+    kw = oracle_kw(w)
+    experts = (inp["w1"], inp["w2"])
+    f = O.forward(inp["x"], inp["w_r"], inp["bias"], experts, **kw)
+    b = O.backward(inp["x"], inp["w_r"], inp["bias"], experts, inp["dy"], **kw) if backward else None
+    return f, b
+
+
+def _check_full(w, res, inp, f, b):
+    tol = TOL_F32 if w.dtype == "f32" else TOL_BF16
+    check_routing(res, f, w)
+    check_router_values(res, f)
+    assert res["device_error"] == 0
+    assert np.array_equal(res["x_perm"], inp["x"].astype(np.float64)[f["row_token"]])
+    h_ref, y_ref = expert_reference(w, inp, f)
+    assert_close(res["h"], h_ref, tol, "h")
+    assert_close(res["y_perm"], y_ref, tol, "y_perm")
+    assert_close(res["out"], f["out"], tol, "out")
+    dropped = np.all(f["slot"] < 0, axis=1)
+    assert np.array_equal(res["out"][dropped], inp["x"].astype(np.float64)[dropped]), "dropped tokens must return x"
+    if b is not None:
+        assert_close(res["dg"], b["dg"], tol, "dg")
+        assert_close(res["dh"], b["dh"], tol, "dh")
+        assert_close(res["dx"], b["dx"], tol, "dx")
+        assert_close(res["dw_r"], b["dw_r"], tol, "dw_r")
+        assert_close(res["dw1"], np.stack([b["dw1"][e] for e in range(w.E)]), tol, "dw1")
+        assert_close(res["dw2"], np.stack([b["dw2"][e] for e in range(w.E)]), tol, "dw2")
+
+
+def test_tiny_f32_forward_backward():
+    w = syn.WORKLOADS["tiny-top1-f32"]
+    inp = syn.make_inputs(w)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_bf16_small_layers(name):
+    w = SMALL[name]
+    inp = syn.make_inputs(w, dy=w.backward)
+    res = run_gpu(w, inp, backward=w.backward)
+    f, b = _ref_all(w, inp, w.backward)
+    _check_full(w, res, inp, f, b)
+
+
+@pytest.mark.parametrize("name", ["tiny-top1-f32", "switch-small", "dropless-small"])
+def test_deterministic(name):
+    w = syn.WORKLOADS.get(name) or SMALL[name]
+    inp = syn.make_inputs(w, dy=True)
+    r1 = run_gpu(w, inp, backward=True)
+    r2 = run_gpu(w, inp, backward=True)
+    for key in ("out", "probs", "importance", "aux", "dx", "dw_r", "dw1", "dw2"):
+        assert np.array_equal(np.asarray(r1[key]), np.asarray(r2[key])), key
+
+
+# ------------------------------------------------------------------ edge cases
+def test_capacity_zero_drops_everything():
+    w = SMALL["switch-small"].with_(cf=(0, 1), backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    assert np.all(res["slot"] == -1) and np.all(res["kept"] == 0)
+    assert np.array_equal(res["out"], inp["x"].astype(np.float64))
+    f, b = _ref_all(w, inp, True)
+    assert_close(res["dx"], b["dx"], TOL_BF16, "dx")
+    assert np.all(res["dw1"] == 0) and np.all(res["dw2"] == 0)
+
+
+def test_single_token():
+    w = SMALL["large-small"].with_(T=1, cf=None)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+
+
+def test_k_equals_E():
+    w = syn.Workload("k-eq-e", T=300, d=128, E=4, k=4, F=128, act="swiglu", dtype="bf16", cf=None,
+                     renormalize=True, backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+
+
+def test_replayed_routing_all_on_one_expert():
+    """Caller-supplied top-k (replay of a recorded routing): every token on expert 3."""
+    w = SMALL["switch-small"].with_(cf=None)
+    inp = syn.make_inputs(w)
+    idx = np.full((w.T, 1), 3, np.int64)
+    res = run_gpu(w, inp, topk_idx=idx)
+    assert np.array_equal(res["kept"], np.eye(w.E, dtype=np.int64)[3] * w.T)
+    assert np.array_equal(res["slot"][:, 0], np.arange(w.T))
+    x = inp["x"].astype(np.float64)
+    y = O.expert_ffn(x, inp["w1"][3].astype(np.float64), inp["w2"][3].astype(np.float64), "relu")["y"]
+    assert_close(res["out"], x + res["gate"][:, :1] * y, TOL_BF16, "out")
+
+
+def test_bad_and_repeated_expert_indices_are_reported_and_dropped():
+    import sparse_mixture_experts_49_b300 as moe
+    w = SMALL["gshard-small"].with_(T=256, cf=None)
+    inp = syn.make_inputs(w)
+    idx = np.stack([np.arange(w.T) % w.E, (np.arange(w.T) + 1) % w.E], axis=1)
+    idx[5, 1] = w.E + 3          # out of range
+    res = run_gpu(w, inp, topk_idx=idx)
+    assert res["device_error"] == moe.MOE_DEVERR_BAD_EXPERT
+    assert res["slot"][5, 1] == -1 and res["slot"][5, 0] >= 0
+    idx[5, 1] = idx[5, 0]        # repeated expert
+    res = run_gpu(w, inp, topk_idx=idx)
+    assert res["device_error"] == moe.MOE_DEVERR_DUP_EXPERT
+    assert res["slot"][5, 1] == -1 and res["slot"][5, 0] >= 0
+
+
+def test_empty_experts_and_heavy_skew():
+    """Zipf-biased routing with a small capacity: many drops, some experts empty."""
+    w = SMALL["gshard-small"].with_(cf=(1, 2), zipf_s=2.5)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    assert (f["load"] == 0).any() and (f["slot"] < 0).mean() > 0.3
+    _check_full(w, res, inp, f, b)
+
+
+# ------------------------------------------------------------------ full sizes, sampled outputs
+@pytest.mark.parametrize("name", ["switch-base-top1", "gshard-top2-zipf", "dropless-top8-swiglu"])
+def test_full_size_forward_sampled(name):
+    w = syn.WORKLOADS[name]
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp)
+    sample = np.random.default_rng(7).choice(w.T, 256, replace=False)
+    f = O.forward(inp["x"], inp["w_r"], inp["bias"], (inp["w1"], inp["w2"]), tokens=sample, **oracle_kw(w))
+    check_routing(res, f, w)
+    check_router_values(res, f)
+    assert res["device_error"] == 0
+    assert_close(res["out"][sample], f["out"], TOL_BF16, "out (sampled tokens)")
