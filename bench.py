@@ -105,6 +105,25 @@ class ClockSampler:
                 "samples": len(sm), "reasons": reasons}
 
 
+# ---------------------------------------------------------------- measured DRAM traffic (from an ncu capture)
+def gemm_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "sparse_mixture_experts_49_b300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def gemm_traffic():
+    """dram read+write bytes per moe_expert_gemm call, from profiles/traffic.json, or None when the
+    counters were taken on a different version of the GEMM kernel source."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[WORKLOAD]
+        return t["gemm_bytes_per_call"] if t.get("source_hash") == gemm_source_hash() else None
+    except Exception:
+        return None
+
+
 # ---------------------------------------------------------------- algorithmic traffic and flops
 def algorithmic(w, K_a: int):
     """Bytes / FLOPs each step must move or do (kept assignments only, weights read once)."""
@@ -211,13 +230,7 @@ def run_ours(args):
     gemm_tf = alg["gemm_flops"] / (mean_call["gemm"] * 1e-3) / 1e12
     kernels["gemm"].update({"TFLOP/s": round(gemm_tf, 1), "frac_bf16_peak": round(gemm_tf / tflops, 4)})
     gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        try:
-            traffic = json.load(open(tpath)).get(WORKLOAD, {}).get("gemm_bytes_per_call")
-        except Exception:
-            traffic = None
+    traffic = gemm_traffic()
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",

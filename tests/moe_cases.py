@@ -61,7 +61,6 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None):
     idx_t = None if topk_idx is None else torch.from_numpy(np.asarray(topk_idx, np.int32)).cuda()
     layer.forward(x, w_r, w1, w2, bias, idx_t)
     res = {}
-    rows = None
     if backward:
         dy = to_dev(torch, inp["dy"], dt)
         dx, dw_r, dw1, dw2 = layer.backward(dy)
@@ -76,10 +75,10 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None):
                importance=np64(layer.importance), load=np64(layer.load), aux=float(layer.aux.item()),
                slot=np64(layer.slot), kept=np64(layer.kept), offsets=np64(layer.offsets))
     n = int(res["offsets"][-1])
-    res["row_token"] = np64(layer.row_token)[:n]
-    res["x_perm"] = np64(layer.x_perm)[:n]
-    res["h"] = np64(layer.h)[:n]
-    res["y_perm"] = np64(layer.y_perm)[:n]
+    res["row_token"] = np64(layer.row_token[:n])
+    res["x_perm"] = np64(layer.x_perm[:n])
+    res["h"] = np64(layer.h[:n])
+    res["y_perm"] = np64(layer.y_perm[:n])
     res["device_error"] = layer.device_error()
     return res
 
