@@ -152,6 +152,33 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
                         int32_t *row_token, void *x_perm, void *ws, moe_stream_t stream);
 
 /*
+ * Workspace-free dispatch. The pages have no counterpart: this is an
+ * interface convenience, not a step of the method.
+ *
+ * Same computation and outputs as moe_dispatch, for callers that cannot give
+ * the library any scratch memory because they cannot allocate device memory
+ * at all (a plugin inside a host framework that owns every device
+ * allocation, or a latency-critical path that cannot pay for cudaMalloc's
+ * device-wide synchronisation). The dispatch's scratch lives in one fixed
+ * array inside the library instead, about 257 KB, held by every GPU that
+ * loads the library until the process exits. The call allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *   - T <= MOE_NOALLOC_MAX_TOKENS, else MOE_ERR_UNSUPPORTED before any launch.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the array, which keeps the last call's contents:
+ *     calls whose work can overlap on the GPU (unordered streams) race and
+ *     give wrong results. Order them on one stream, or use moe_dispatch with
+ *     one workspace per stream.
+ *   - Bad or repeated expert indices are treated as dropped, as in
+ *     moe_dispatch, but are not reported (the error word is private).
+ */
+#define MOE_NOALLOC_MAX_TOKENS 32768
+moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                                int32_t *slot, int32_t *kept, int32_t *expert_offsets,
+                                int32_t *row_token, void *x_perm, moe_stream_t stream);
+
+/*
  * Expert FFNs over the packed groups ([Switch] section 直感: each expert is a
  * copy of the FFN; [LRMoE] variable-size grouped GEMM). For the rows of
  * expert e (expert_offsets[e] .. expert_offsets[e+1]):

@@ -22,10 +22,11 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_ALIGNMENT, MOE_ERR_CUD
 MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1
 MOE_F32, MOE_BF16 = 0, 1
 MOE_DEVERR_NONE, MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_DUP_EXPERT, MOE_DEVERR_TIMEOUT = range(4)
+MOE_NOALLOC_MAX_TOKENS = 32768
 
 EXPORTED = [
     "moe_capacity", "moe_max_rows", "moe_workspace_size", "moe_workspace_init", "moe_router",
-    "moe_dispatch", "moe_expert_gemm", "moe_combine", "moe_backward", "moe_backward_intermediates",
+    "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_backward", "moe_backward_intermediates",
     "moe_get_device_error", "moe_status_string", "moe_last_cuda_error",
 ]
 
@@ -71,6 +72,7 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_init": (ctypes.c_int, [C, P, P]),
             "moe_router": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P]),
             "moe_dispatch": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
+            "moe_dispatch_noalloc": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
             "moe_expert_gemm": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
             "moe_combine": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
             "moe_backward": (ctypes.c_int, [C, ctypes.POINTER(moe_saved), P, P, P, P, P, P, P]),
@@ -158,6 +160,15 @@ def moe_dispatch(cfg, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm
     _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(slot), _ptr(kept),
                               _ptr(expert_offsets), _ptr(row_token), _ptr(x_perm), _ptr(ws), _stream(stream)),
            "moe_dispatch")
+
+
+def moe_dispatch_noalloc(cfg, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, stream=None):
+    """moe_dispatch without a workspace, for callers that cannot allocate device memory at all: the
+    scratch is a fixed array inside the library (T <= MOE_NOALLOC_MAX_TOKENS; calls that overlap on
+    the GPU race; bad expert indices are dropped but not reported)."""
+    _check(lib().moe_dispatch_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(slot), _ptr(kept),
+                                      _ptr(expert_offsets), _ptr(row_token), _ptr(x_perm), _stream(stream)),
+           "moe_dispatch_noalloc")
 
 
 def moe_expert_gemm(cfg, x_perm, expert_offsets, w1, w2, pre_act, h, y_perm, ws, stream=None):

@@ -233,4 +233,33 @@ cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, 
   return cudaGetLastError();
 }
 
+// The same launch sequence as launch_dispatch, with the scratch arrays given
+// explicitly (used by the workspace-free entry point).
+cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
+                                         int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
+                                         int32_t *counts, int32_t *base, int32_t *load, DeviceStatus *st,
+                                         cudaStream_t stream) {
+  const int nblk = dispatch_blocks(sh);
+  const size_t bm = sizeof(uint32_t) * (size_t)sh.E * WORDS;
+  dispatch_count_kernel<<<nblk, DT, bm, stream>>>(idx, sh.T, sh.E, sh.k, counts, st);
+  dispatch_scan_kernel<<<sh.E, 256, 0, stream>>>(counts, nblk, sh.E, base, load);
+  dispatch_assign_kernel<<<nblk, DT, bm, stream>>>(idx, sh.T, sh.E, sh.k, sh.C, base, load, slot, kept, offsets,
+                                                   row_token);
+  int sms = 148;
+  {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  }
+  int grid = (sh.T + 7) / 8;
+  if (grid > sms * 8) grid = sms * 8;
+  if (sh.dtype == MOE_BF16)
+    dispatch_gather_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)x, idx, slot, offsets, sh.T, sh.d, sh.k,
+                                                           (bf16 *)x_perm);
+  else
+    dispatch_gather_kernel<float><<<grid, 256, 0, stream>>>((const float *)x, idx, slot, offsets, sh.T, sh.d,
+                                                            sh.k, (float *)x_perm);
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -46,6 +46,13 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,
                             int32_t *offsets, int32_t *row_token, void *x_perm, void *ws, cudaStream_t stream);
 
+cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
+                                         int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
+                                         int32_t *counts, int32_t *base, int32_t *load, DeviceStatus *st,
+                                         cudaStream_t stream);
+moe_status dispatch_shape(const moe_config *cfg, Shape *sh);
+moe_status report_cuda(cudaError_t e);
+
 cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
                            const float *gate, const int32_t *slot, const int32_t *offsets, void *out,
                            cudaStream_t stream);

@@ -83,6 +83,10 @@ WsLayout ws_layout(const Shape &sh) {
 
 static DeviceStatus *status_of(void *ws) { return reinterpret_cast<DeviceStatus *>(ws); }
 
+// Validation and error text shared with the workspace-free entry point.
+moe_status dispatch_shape(const moe_config *cfg, Shape *sh) { return make_shape(cfg, sh); }
+moe_status report_cuda(cudaError_t e) { return cuda_status(e); }
+
 }  // namespace moe
 
 using namespace moe;
