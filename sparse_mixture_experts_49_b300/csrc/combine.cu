@@ -51,29 +51,57 @@ __device__ __forceinline__ KeptRows kept_rows(int t, int k, const int32_t *idx, 
   return kr;
 }
 
-template <typename XT>
-__global__ void __launch_bounds__(256) combine_kernel(const XT *x, const XT *y_perm, const int32_t *idx,
-                                                      const float *gate, const int32_t *slot,
-                                                      const int32_t *offsets, int T, int d, int k, XT *out) {
+// Rows and gates of token t's k assignments, in registers (row = -1 when dropped).
+template <int KMAX>
+__device__ __forceinline__ void token_rows(int t, int k, const int32_t *__restrict__ idx,
+                                           const int32_t *__restrict__ slot, const int32_t *__restrict__ offsets,
+                                           const float *__restrict__ gate, int (&row)[KMAX], float (&g)[KMAX]) {
+  const int lane = threadIdx.x & 31;
+  int r = -1;
+  float gv = 0.0f;
+  if (lane < k) {
+    const int s = slot[(int64_t)t * k + lane];
+    const int e = idx[(int64_t)t * k + lane];
+    if (gate) gv = gate[(int64_t)t * k + lane];
+    if (s >= 0) r = offsets[e] + s;
+  }
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    row[j] = __shfl_sync(0xffffffffu, r, j);
+    g[j] = __shfl_sync(0xffffffffu, gv, j);
+  }
+}
+
+template <typename XT, int KMAX>
+__global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, const XT *__restrict__ y_perm,
+                                                      const int32_t *__restrict__ idx, const float *__restrict__ gate,
+                                                      const int32_t *__restrict__ slot,
+                                                      const int32_t *__restrict__ offsets, int T, int d, int k,
+                                                      XT *__restrict__ out) {
   constexpr int V = Vec16<XT>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
-    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, gate);
+    int row[KMAX];
+    float g[KMAX];
+    token_rows<KMAX>(t, k, idx, slot, offsets, gate, row, g);
     const XT *xr = x + (int64_t)t * d;
     XT *orow = out + (int64_t)t * d;
-    if (kr.n == 0) {
-      for (int v = lane; v < nvec; v += 32)
-        *reinterpret_cast<uint4 *>(orow + v * V) = *reinterpret_cast<const uint4 *>(xr + v * V);
-      continue;
-    }
+#pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
-      float acc[V], y[V];
-      Vec16<XT>::load(xr + v * V, acc);
-      for (int j = 0; j < kr.n; ++j) {
-        Vec16<XT>::load(y_perm + (int64_t)kr.row[j] * d + v * V, y);
+      uint4 raw[KMAX + 1];
+      raw[0] = *reinterpret_cast<const uint4 *>(xr + v * V);
 #pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = fmaf(kr.g[j], y[i], acc[i]);
+      for (int j = 0; j < KMAX; ++j)
+        if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(y_perm + (int64_t)row[j] * d + v * V);
+      float acc[V], y[V];
+      Vec16<XT>::unpack(raw[0], acc);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (row[j] < 0) continue;
+        Vec16<XT>::unpack(raw[j + 1], y);
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], y[i], acc[i]);
       }
       Vec16<XT>::store(orow + v * V, acc);
     }
@@ -166,16 +194,27 @@ int token_grid(int T) {
 
 }  // namespace
 
+template <typename XT, int KMAX>
+void run_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
+                 const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
+  combine_kernel<XT, KMAX><<<token_grid(sh.T), 256, 0, stream>>>((const XT *)x, (const XT *)y_perm, idx, gate, slot,
+                                                                 offsets, sh.T, sh.d, sh.k, (XT *)out);
+}
+
+template <typename XT>
+void run_combine_k(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
+                   const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
+  if (sh.k == 1) run_combine<XT, 1>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  else if (sh.k == 2) run_combine<XT, 2>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  else if (sh.k <= 4) run_combine<XT, 4>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  else run_combine<XT, 8>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+}
+
 cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
                            const float *gate, const int32_t *slot, const int32_t *offsets, void *out,
                            cudaStream_t stream) {
-  const int grid = token_grid(sh.T);
-  if (sh.dtype == MOE_BF16)
-    combine_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)x, (const bf16 *)y_perm, idx, gate, slot, offsets,
-                                                   sh.T, sh.d, sh.k, (bf16 *)out);
-  else
-    combine_kernel<float><<<grid, 256, 0, stream>>>((const float *)x, (const float *)y_perm, idx, gate, slot,
-                                                    offsets, sh.T, sh.d, sh.k, (float *)out);
+  if (sh.dtype == MOE_BF16) run_combine_k<bf16>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  else run_combine_k<float>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
   return cudaGetLastError();
 }
 

@@ -36,8 +36,8 @@ template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __f
 template <typename T> struct Vec16;
 template <> struct Vec16<bf16> {
   static constexpr int N = 8;
-  __device__ __forceinline__ static void load(const void *p, float *o) {
-    uint4 u = *reinterpret_cast<const uint4 *>(p);
+  __device__ __forceinline__ static void load(const void *p, float *o) { unpack(*reinterpret_cast<const uint4 *>(p), o); }
+  __device__ __forceinline__ static void unpack(const uint4 &u, float *o) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -60,6 +60,9 @@ template <> struct Vec16<float> {
   __device__ __forceinline__ static void load(const void *p, float *o) {
     float4 f = *reinterpret_cast<const float4 *>(p);
     o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
+  }
+  __device__ __forceinline__ static void unpack(const uint4 &u, float *o) {
+    o[0] = __uint_as_float(u.x); o[1] = __uint_as_float(u.y); o[2] = __uint_as_float(u.z); o[3] = __uint_as_float(u.w);
   }
   __device__ __forceinline__ static void store(void *p, const float *v) {
     *reinterpret_cast<float4 *>(p) = make_float4(v[0], v[1], v[2], v[3]);

@@ -25,6 +25,8 @@ enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU
 struct WsLayout {
   size_t status;                 // DeviceStatus
   size_t router_imp, router_load;  // [router blocks, E] partial sums
+  size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
+  size_t router_partial;           // [splits, T, E] fp32 partial logits (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
   size_t disp_load;                // [E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
@@ -37,6 +39,16 @@ constexpr int ROUTER_TOKENS = 64;     // tokens per router block
 constexpr int DISPATCH_TOKENS = 256;  // tokens per dispatch block
 
 int router_blocks(const Shape &sh);
+
+// How the router runs for a shape: tensor cores for bf16 x (logits of 128
+// tokens x EP padded experts per CTA, K split into `splits` ranges so that
+// about kRouterTargetCtas CTAs run), CUDA cores for fp32 x.
+constexpr int kRouterTargetCtas = 148;
+struct RouterPlan {
+  bool tensor_cores;
+  int ep, m_tiles, splits, kb_per_split;
+};
+RouterPlan router_plan(const Shape &sh);
 int dispatch_blocks(const Shape &sh);
 
 cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, float *probs,

@@ -66,6 +66,9 @@ WsLayout ws_layout(const Shape &sh) {
   const size_t rb = (size_t)router_blocks(sh), db = (size_t)dispatch_blocks(sh);
   L.router_imp = take(rb * sh.E * 4);
   L.router_load = take(rb * sh.E * 4);
+  const RouterPlan rp = router_plan(sh);
+  L.router_parts = take(rp.tensor_cores ? (size_t)3 * rp.ep * sh.d * 2 : 0);
+  L.router_partial = take(rp.tensor_cores ? (size_t)rp.splits * sh.T * sh.E * 4 : 0);
   L.disp_counts = take(db * sh.E * 4);
   L.disp_base = take(db * sh.E * 4);
   L.disp_load = take((size_t)sh.E * 4);

@@ -7,22 +7,33 @@
 // aux = alpha N sum f P), section 学習を安定させる3つの工夫 (the router runs in
 // float32 even when the rest is bf16).
 //
-// One block handles 64 tokens against all E <= 256 experts: a register-tiled
-// fp32 GEMM over d (8 tokens x E/32 experts per thread), then one warp per
-// token for the softmax and the top-k (descending logit, ties to the lower
-// index). Importance and load are reduced per block in a fixed order and
-// finished by a second kernel, so the statistics are bitwise reproducible.
+// bf16 layers compute the logits on the tensor cores without giving up fp32:
+// W_r (fp32) is split exactly into three bf16 parts, hi + mid + lo, which
+// carry its 24-bit significand; x is already bf16, so every product
+// x_i * part_e,i is exact in the fp32 accumulator, and h = x W_hi^T +
+// x W_mid^T + x W_lo^T is the fp32 dot product up to the order of the fp32
+// additions. A tcgen05 kernel (128 tokens x all experts per CTA, K split
+// across CTAs when there are few token tiles) writes fp32 partial logits;
+// a selection kernel sums the partials in a fixed order and does softmax and
+// top-k. fp32 layers use a register-tiled CUDA-core kernel instead.
+//
+// Selection: one warp per token, softmax in fp32 with the row maximum
+// subtracted, then k rounds of a warp arg-max (descending logit, ties to the
+// lower index). Importance and load are reduced per block in a fixed order
+// and finished by a second kernel, so the statistics are bitwise
+// reproducible.
 #include <cfloat>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tma_host.h"
 
 namespace moe {
 
 namespace {
 
-constexpr int RT = ROUTER_TOKENS;  // 64 tokens per block
-constexpr int RBK = 16;            // d-slice per smem stage
+constexpr int RT = ROUTER_TOKENS;  // 64 tokens per selection block
+constexpr int RBK = 16;            // d-slice per smem stage of the CUDA-core GEMM
 
 struct RouterArgs {
   const void *x;
@@ -47,79 +58,23 @@ template <> __device__ __forceinline__ void load4<bf16>(const bf16 *p, float *o)
   o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
-template <int EPT> constexpr size_t router_smem_bytes() {
+template <int EPT> constexpr size_t select_smem_bytes() {
   constexpr int EP = 32 * EPT;
-  return sizeof(float) * ((size_t)RBK * RT + (size_t)RBK * EP + (size_t)RT * (EP + 1) + 8 * EP) +
-         sizeof(int) * EP;
+  return sizeof(float) * ((size_t)RT * (EP + 1) + 8 * EP) + sizeof(int) * EP;
+}
+template <int EPT> constexpr size_t simt_router_smem_bytes() {
+  constexpr int EP = 32 * EPT;
+  return sizeof(float) * ((size_t)RBK * RT + (size_t)RBK * EP) + select_smem_bytes<EPT>();
 }
 
-template <typename XT, int EPT>
-__global__ void __launch_bounds__(256) router_kernel(const RouterArgs a) {
+// Softmax, top-k and per-block statistics for the block's 64 tokens, whose
+// logits (bias included) are in lg[64][EP + 1]. Needs cnt[] zeroed and a
+// __syncthreads() before the call.
+template <int EPT>
+__device__ __forceinline__ void select_block(const float *lg, float *impw, int *cnt, const RouterArgs &a, int t0) {
   constexpr int EP = 32 * EPT;
-  extern __shared__ float sm[];
-  float *xs = sm;                      // [RBK][RT]
-  float *wsm = xs + RBK * RT;          // [RBK][EP]
-  float *lg = wsm + RBK * EP;          // [RT][EP + 1]
-  float *impw = lg + RT * (EP + 1);    // [8][EP]
-  int *cnt = reinterpret_cast<int *>(impw + 8 * EP);  // [EP]
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * RT;
-  const XT *x = reinterpret_cast<const XT *>(a.x);
-  const int d = a.d, E = a.E;
-
-  float acc[8][EPT];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
-
-  for (int k0 = 0; k0 < d; k0 += RBK) {
-    {  // x slice: 64 tokens x 16, four consecutive elements per thread
-      const int tk = tid >> 2, kq = (tid & 3) * 4;
-      const int t = t0 + tk;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (t < a.T && k0 + kq < d) load4<XT>(x + (int64_t)t * d + k0 + kq, v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) xs[(kq + q) * RT + tk] = v[q];
-    }
-    for (int i = tid; i < EP * 4; i += 256) {  // W_r slice, transposed to [kk][e]
-      const int e = i >> 2, kq = (i & 3) * 4;
-      float v[4] = {0.f, 0.f, 0.f, 0.f};
-      if (e < E && k0 + kq < d) load4<float>(a.w_r + (int64_t)e * d + k0 + kq, v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) wsm[(kq + q) * EP + e] = v[q];
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int kk = 0; kk < RBK; ++kk) {
-      float xv[8], wv[EPT];
-      const float4 x0 = *reinterpret_cast<const float4 *>(xs + kk * RT + warp * 8);
-      const float4 x1 = *reinterpret_cast<const float4 *>(xs + kk * RT + warp * 8 + 4);
-      xv[0] = x0.x; xv[1] = x0.y; xv[2] = x0.z; xv[3] = x0.w;
-      xv[4] = x1.x; xv[5] = x1.y; xv[6] = x1.z; xv[7] = x1.w;
-#pragma unroll
-      for (int j = 0; j < EPT; ++j) wv[j] = wsm[kk * EP + lane * EPT + j];
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-
-  // logits (+ fixed bias) to shared memory
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = lane * EPT + j;
-      const float b = (a.bias != nullptr && e < E) ? a.bias[e] : 0.0f;
-      lg[(warp * 8 + i) * (EP + 1) + e] = acc[i][j] + b;
-    }
-  for (int e = tid; e < EP; e += 256) cnt[e] = 0;
-  __syncthreads();
-
+  const int E = a.E;
   float imp[EPT];
 #pragma unroll
   for (int j = 0; j < EPT; ++j) imp[j] = 0.0f;
@@ -200,12 +155,274 @@ __global__ void __launch_bounds__(256) router_kernel(const RouterArgs a) {
   }
 }
 
+// ---------------------------------------------------------------- CUDA-core path (fp32 layers)
+template <typename XT, int EPT>
+__global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a) {
+  constexpr int EP = 32 * EPT;
+  extern __shared__ float sm[];
+  float *xs = sm;                      // [RBK][RT]
+  float *wsm = xs + RBK * RT;          // [RBK][EP]
+  float *lg = wsm + RBK * EP;          // [RT][EP + 1]
+  float *impw = lg + RT * (EP + 1);    // [8][EP]
+  int *cnt = reinterpret_cast<int *>(impw + 8 * EP);  // [EP]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * RT;
+  const XT *x = reinterpret_cast<const XT *>(a.x);
+  const int d = a.d, E = a.E;
+
+  float acc[8][EPT];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) acc[i][j] = 0.0f;
+
+  for (int k0 = 0; k0 < d; k0 += RBK) {
+    {  // x slice: 64 tokens x 16, four consecutive elements per thread
+      const int tk = tid >> 2, kq = (tid & 3) * 4;
+      const int t = t0 + tk;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (t < a.T && k0 + kq < d) load4<XT>(x + (int64_t)t * d + k0 + kq, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xs[(kq + q) * RT + tk] = v[q];
+    }
+    for (int i = tid; i < EP * 4; i += 256) {  // W_r slice, transposed to [kk][e]
+      const int e = i >> 2, kq = (i & 3) * 4;
+      float v[4] = {0.f, 0.f, 0.f, 0.f};
+      if (e < E && k0 + kq < d) load4<float>(a.w_r + (int64_t)e * d + k0 + kq, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) wsm[(kq + q) * EP + e] = v[q];
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = 0; kk < RBK; ++kk) {
+      float xv[8], wv[EPT];
+      const float4 x0 = *reinterpret_cast<const float4 *>(xs + kk * RT + warp * 8);
+      const float4 x1 = *reinterpret_cast<const float4 *>(xs + kk * RT + warp * 8 + 4);
+      xv[0] = x0.x; xv[1] = x0.y; xv[2] = x0.z; xv[3] = x0.w;
+      xv[4] = x1.x; xv[5] = x1.y; xv[6] = x1.z; xv[7] = x1.w;
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) wv[j] = wsm[kk * EP + lane * EPT + j];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = lane * EPT + j;
+      const float b = (a.bias != nullptr && e < E) ? a.bias[e] : 0.0f;
+      lg[(warp * 8 + i) * (EP + 1) + e] = acc[i][j] + b;
+    }
+  for (int e = tid; e < EP; e += 256) cnt[e] = 0;
+  __syncthreads();
+  select_block<EPT>(lg, impw, cnt, a, t0);
+}
+
+// ---------------------------------------------------------------- tensor-core path (bf16 layers)
+// W_r [E, d] fp32 -> parts [3][EP][d] bf16 with W = hi + mid + lo (rows >= E are zero).
+__global__ void __launch_bounds__(256) router_split_kernel(const float *w_r, int E, int EP, int d, bf16 *parts) {
+  const int64_t n = (int64_t)EP * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / d);
+    const float w = (e < E) ? w_r[i] : 0.0f;
+    const bf16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);          // exact
+    const bf16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);        // exact
+    parts[i] = hi;
+    parts[n + i] = mid;
+    parts[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+namespace rt {
+constexpr int BM = 128;
+constexpr int BK = 64;
+template <int EP> struct Geo {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = EP * BK * 2;  // one part
+  static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
+  static constexpr int STAGES = EP >= 256 ? 2 : (EP >= 128 ? 3 : 4);
+  static constexpr int TMEM_COLS = EP < 32 ? 32 : EP;
+  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+};
+struct __align__(8) Bars {
+  uint64_t full[4];
+  uint64_t empty[4];
+  uint64_t acc_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+struct Args {
+  int T, E, kb_per_split, KB;
+  float *partial;   // [splits, T, E]
+  DeviceStatus *st;
+};
+
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(a, parity))
+    if (global_timer_ns() - t0 > 200000000ull) break;
+}
+
+// Partial logits of 128 tokens x all experts over the CTA's K range. Warp 0
+// loads (x tile once, then the hi/mid/lo parts of W_r), warp 1 issues
+// 3 x 4 MMAs per 64-deep K step into one TMEM accumulator, warps 2-5 store it.
+template <int EP>
+__global__ void __launch_bounds__(192, 1)
+    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args a) {
+  using G = Geo<EP>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  Bars &b = *reinterpret_cast<Bars *>(tiles + (size_t)G::STAGES * G::STAGE_BYTES);
+  volatile int *abort_flag = &b.abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+    for (int i = 0; i < G::STAGES; ++i) { mbar_init(&b.full[i], 1); mbar_init(&b.empty[i], 1); }
+    mbar_init(&b.acc_full, 1);
+    mbar_init(&b.drain, 1);
+    b.abort_flag = 0;
+    fence_barrier_init();
+  } else if (warp == 1) {
+    tmem_alloc(&b.tmem_base, G::TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = b.tmem_base;
+  const int m0 = blockIdx.x * BM;
+  const int kb0 = blockIdx.y * a.kb_per_split;
+  const int kb1 = min(a.KB, kb0 + a.kb_per_split);
+  const int nk = max(0, kb1 - kb0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint64_t pol_x = policy_evict_first();
+      const uint64_t pol_w = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_parity = 0;
+      for (int ks = 0; ks < nk; ++ks) {
+        if (!mbar_wait_bounded(&b.empty[stage], phase ^ 1, abort_flag, a.st)) break;
+        uint8_t *a_s = tiles + (size_t)stage * G::STAGE_BYTES;
+        mbar_arrive_expect_tx(&b.full[stage], G::STAGE_BYTES);
+        const int k0 = (kb0 + ks) * BK;
+        tma_load_2d(a_s, &tmX, &b.full[stage], k0, m0, pol_x);
+#pragma unroll
+        for (int part = 0; part < 3; ++part)
+          tma_load_2d(a_s + G::A_BYTES + part * G::B_BYTES, &tmW, &b.full[stage], k0, part * EP, pol_w);
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == G::STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (*abort_flag)
+        for (int i = 0; i < G::STAGES; ++i)
+          if (issued & (1u << i)) drain_wait(&b.full[i], (issued_parity >> i) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, EP, 0, 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int ks = 0; ks < nk; ++ks) {
+      if (!mbar_wait_bounded(&b.full[stage], phase, abort_flag, a.st)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t a0 = smem_u32(tiles + (size_t)stage * G::STAGE_BYTES);
+#pragma unroll
+        for (int part = 0; part < 3; ++part) {
+          const uint32_t b0 = a0 + G::A_BYTES + part * G::B_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
+                        IDESC, (ks > 0 || part > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&b.empty[stage]);
+      }
+      __syncwarp();
+      if (++stage == G::STAGES) { stage = 0; phase ^= 1; }
+    }
+    if (ok && lane == 0) tc_commit(&b.acc_full);
+    __syncwarp();
+    if (*abort_flag) {
+      if (lane == 0) tc_commit(&b.drain);
+      __syncwarp();
+      drain_wait(&b.drain, 0);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = m0 + q * 32 + lane;
+    if (nk > 0 && mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st)) {
+      tc_fence_after();
+      float v[32];
+      float *dst = a.partial + ((int64_t)blockIdx.y * a.T + row) * a.E;
+#pragma unroll 1
+      for (int c = 0; c < EP / 32; ++c) {
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
+        if (row < a.T) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < a.E) dst[c * 32 + i] = v[i];
+        }
+      }
+      tc_fence_before();
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, G::TMEM_COLS);
+  }
+}
+}  // namespace rt
+
+// Logits = sum of the split partials in split order (+ bias), then selection.
+template <int EPT>
+__global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a) {
+  constexpr int EP = 32 * EPT;
+  extern __shared__ float sm[];
+  float *lg = sm;                      // [RT][EP + 1]
+  float *impw = lg + RT * (EP + 1);    // [8][EP]
+  int *cnt = reinterpret_cast<int *>(impw + 8 * EP);
+  const int t0 = blockIdx.x * RT;
+  const int E = a.E;
+  for (int i = threadIdx.x; i < RT * EP; i += 256) {
+    const int tl = i / EP, e = i - tl * EP, t = t0 + tl;
+    float v = 0.0f;
+    if (t < a.T && e < E) {
+      for (int s = 0; s < splits; ++s) v += partial[((int64_t)s * a.T + t) * E + e];
+      if (a.bias) v += a.bias[e];
+    }
+    lg[tl * (EP + 1) + e] = v;
+  }
+  for (int e = threadIdx.x; e < EP; e += 256) cnt[e] = 0;
+  __syncthreads();
+  select_block<EPT>(lg, impw, cnt, a, t0);
+}
+
+// importance[e], load[e] from the per-block partials (fixed order); the last
+// block to finish computes aux from them and re-arms the counter.
 __global__ void __launch_bounds__(256) router_finish_kernel(const float *part_imp, const int32_t *part_load,
                                                             int nblk, int T, int E, int k, float alpha,
-                                                            float *importance, int32_t *load, float *aux) {
-  __shared__ float term[256];
+                                                            float *importance, int32_t *load, float *aux,
+                                                            unsigned int *counter) {
+  __shared__ bool last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int e = warp; e < E; e += 8) {
+  const int e = blockIdx.x * 8 + warp;
+  if (e < E) {
     float s = 0.0f;
     int c = 0;
     for (int b = lane; b < nblk; b += 32) {
@@ -220,42 +437,77 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float *part_im
     if (lane == 0) {
       importance[e] = s;
       load[e] = c;
-      term[e] = ((float)c / ((float)T * (float)k)) * (s / (float)T);
     }
   }
+  __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0 && aux != nullptr) {
+  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
     float acc = 0.0f;
-    for (int e = 0; e < E; ++e) acc += term[e];
-    *aux = alpha * (float)E * acc;
+    for (int j = 0; j < E; ++j) {
+      const float imp = __ldcg(importance + j);
+      const int l = __ldcg(load + j);
+      acc += ((float)l / ((float)T * (float)k)) * (imp / (float)T);
+    }
+    if (aux) *aux = alpha * (float)E * acc;
+    *counter = 0u;
   }
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
 template <typename XT, int EPT>
-cudaError_t run(const RouterArgs &a, int nblk, cudaStream_t stream) {
-  constexpr size_t smem = router_smem_bytes<EPT>();
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(router_kernel<XT, EPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  router_kernel<XT, EPT><<<nblk, 256, smem, stream>>>(a);
+cudaError_t run_simt(const RouterArgs &a, int nblk, cudaStream_t stream) {
+  constexpr size_t smem = simt_router_smem_bytes<EPT>();
+  static cudaError_t attr = set_smem(router_simt_kernel<XT, EPT>, smem);
+  if (attr != cudaSuccess) return attr;
+  router_simt_kernel<XT, EPT><<<nblk, 256, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
-template <typename XT>
-cudaError_t run_dtype(const RouterArgs &a, int nblk, cudaStream_t stream) {
-  if (a.E <= 32) return run<XT, 1>(a, nblk, stream);
-  if (a.E <= 64) return run<XT, 2>(a, nblk, stream);
-  if (a.E <= 128) return run<XT, 4>(a, nblk, stream);
-  return run<XT, 8>(a, nblk, stream);
+template <int EPT>
+cudaError_t run_select(const float *partial, int splits, const RouterArgs &a, int nblk, cudaStream_t stream) {
+  constexpr size_t smem = select_smem_bytes<EPT>();
+  static cudaError_t attr = set_smem(router_select_kernel<EPT>, smem);
+  if (attr != cudaSuccess) return attr;
+  router_select_kernel<EPT><<<nblk, 256, smem, stream>>>(partial, splits, a);
+  return cudaGetLastError();
 }
+
+template <int EP>
+cudaError_t run_tc(const CUtensorMap &mx, const CUtensorMap &mw, const rt::Args &ta, int m_tiles, int splits,
+                   cudaStream_t stream) {
+  static cudaError_t attr = set_smem(rt::router_tc_kernel<EP>, rt::Geo<EP>::SMEM);
+  if (attr != cudaSuccess) return attr;
+  rt::router_tc_kernel<EP><<<dim3(m_tiles, splits), 192, rt::Geo<EP>::SMEM, stream>>>(mx, mw, ta);
+  return cudaGetLastError();
+}
+
+int epad_of(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
 
 }  // namespace
 
 int router_blocks(const Shape &sh) { return (sh.T + RT - 1) / RT; }
+
+RouterPlan router_plan(const Shape &sh) {
+  RouterPlan p;
+  p.tensor_cores = sh.dtype == MOE_BF16;
+  p.ep = epad_of(sh.E);
+  p.m_tiles = (sh.T + rt::BM - 1) / rt::BM;
+  const int KB = (sh.d + rt::BK - 1) / rt::BK;
+  int splits = kRouterTargetCtas / p.m_tiles;
+  if (splits < 1) splits = 1;
+  if (splits > KB) splits = KB;
+  p.kb_per_split = (KB + splits - 1) / splits;
+  p.splits = (KB + p.kb_per_split - 1) / p.kb_per_split;
+  return p;
+}
 
 cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, float *probs,
                           int32_t *idx, float *gate, float *importance, int32_t *load, float *aux, void *ws,
@@ -268,10 +520,43 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   a.part_load = reinterpret_cast<int32_t *>(w + L.router_load);
   a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
   const int nblk = router_blocks(sh);
-  cudaError_t e = sh.dtype == MOE_BF16 ? run_dtype<bf16>(a, nblk, stream) : run_dtype<float>(a, nblk, stream);
+  const RouterPlan plan = router_plan(sh);
+  cudaError_t e;
+  if (!plan.tensor_cores) {
+    if (sh.E <= 32) e = run_simt<float, 1>(a, nblk, stream);
+    else if (sh.E <= 64) e = run_simt<float, 2>(a, nblk, stream);
+    else if (sh.E <= 128) e = run_simt<float, 4>(a, nblk, stream);
+    else e = run_simt<float, 8>(a, nblk, stream);
+  } else {
+    bf16 *parts = reinterpret_cast<bf16 *>(w + L.router_parts);
+    float *partial = reinterpret_cast<float *>(w + L.router_partial);
+    const int64_t n = (int64_t)plan.ep * sh.d;
+    int sgrid = (int)((n + 255) / 256);
+    if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
+    router_split_kernel<<<sgrid, 256, 0, stream>>>(w_r, sh.E, plan.ep, sh.d, parts);
+    CUtensorMap mx, mw;
+    if (!make_map_2d(&mx, x, sh.d, sh.T, 64, 128) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
+      return cudaErrorInvalidValue;
+    rt::Args ta;
+    ta.T = sh.T; ta.E = sh.E; ta.kb_per_split = plan.kb_per_split; ta.KB = (sh.d + rt::BK - 1) / rt::BK;
+    ta.partial = partial;
+    ta.st = reinterpret_cast<DeviceStatus *>(w + L.status);
+    switch (plan.ep) {
+      case 32: e = run_tc<32>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+      case 64: e = run_tc<64>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+      case 128: e = run_tc<128>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+      default: e = run_tc<256>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+    }
+    if (e != cudaSuccess) return e;
+    if (sh.E <= 32) e = run_select<1>(partial, plan.splits, a, nblk, stream);
+    else if (sh.E <= 64) e = run_select<2>(partial, plan.splits, a, nblk, stream);
+    else if (sh.E <= 128) e = run_select<4>(partial, plan.splits, a, nblk, stream);
+    else e = run_select<8>(partial, plan.splits, a, nblk, stream);
+  }
   if (e != cudaSuccess) return e;
-  router_finish_kernel<<<1, 256, 0, stream>>>(a.part_imp, a.part_load, nblk, sh.T, sh.E, sh.k, sh.alpha,
-                                              importance, load, aux);
+  unsigned int *counter = reinterpret_cast<unsigned int *>(w + L.status + 64);
+  router_finish_kernel<<<(sh.E + 7) / 8, 256, 0, stream>>>(a.part_imp, a.part_load, nblk, sh.T, sh.E, sh.k,
+                                                           sh.alpha, importance, load, aux, counter);
   return cudaGetLastError();
 }
 

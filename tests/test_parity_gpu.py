@@ -1,7 +1,8 @@
 """CUDA path vs the CPU oracle, through the C ABI, on seeded inputs.
 
 Routing (top-k indices, load, slots, kept counts, group offsets, row owners)
-must match bit for bit; the fp32 router's values within 1e-5 x max|ref|; the
+must match bit for bit; the fp32 router's values within 1e-5 x max|ref| (fp32
+layer) or 1e-4 x max|ref| (bf16 layers, tensor-core fp32 accumulation); the
 layer's floating outputs and gradients within 2e-2 x max|ref| for bf16
 experts (fp32 accumulation) and 1e-5 x max|ref| for the fp32 layer.
 """
@@ -37,7 +38,7 @@ def _ref_all(w, inp, backward):
 def _check_full(w, res, inp, f, b):
     tol = TOL_F32 if w.dtype == "f32" else TOL_BF16
     check_routing(res, f, w)
-    check_router_values(res, f)
+    check_router_values(res, f, w.dtype)
     assert res["device_error"] == 0
     assert np.array_equal(res["x_perm"], inp["x"].astype(np.float64)[f["row_token"]])
     h_ref, y_ref = expert_reference(w, inp, f)
@@ -158,6 +159,6 @@ def test_full_size_forward_sampled(name):
     sample = np.random.default_rng(7).choice(w.T, 256, replace=False)
     f = O.forward(inp["x"], inp["w_r"], inp["bias"], (inp["w1"], inp["w2"]), tokens=sample, **oracle_kw(w))
     check_routing(res, f, w)
-    check_router_values(res, f)
+    check_router_values(res, f, w.dtype)
     assert res["device_error"] == 0
     assert_close(res["out"][sample], f["out"], TOL_BF16, "out (sampled tokens)")
