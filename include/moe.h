@@ -160,7 +160,7 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
  * at all (a plugin inside a host framework that owns every device
  * allocation, or a latency-critical path that cannot pay for cudaMalloc's
  * device-wide synchronisation). The dispatch's scratch lives in one fixed
- * array inside the library instead, about 257 KB, held by every GPU that
+ * array inside the library instead, about 256 KB, held by every GPU that
  * loads the library until the process exits. The call allocates nothing
  * (no cudaMalloc, no cudaFree, no allocating library routine).
  *   - T <= MOE_NOALLOC_MAX_TOKENS, else MOE_ERR_UNSUPPORTED before any launch.

@@ -12,7 +12,7 @@
 //
 // Costs and limits of that choice:
 //   - the array has a fixed size: T <= MOE_NOALLOC_MAX_TOKENS (32768) tokens
-//     and E <= 256 experts, about 257 KB, and every GPU that loads the library
+//     and E <= 256 experts, about 256 KB, and every GPU that loads the library
 //     holds it until the process exits;
 //   - the first call on a device looks the array's address up with
 //     cudaGetSymbolAddress; that first call should come before any stream
@@ -34,10 +34,10 @@ constexpr int kMaxBlocks = MOE_NOALLOC_MAX_TOKENS / DISPATCH_TOKENS;
 constexpr int kMaxExperts = 256;
 constexpr size_t kStatusInts = 64;  // keeps the count arrays 256-byte aligned
 constexpr size_t kCountInts = (size_t)kMaxBlocks * kMaxExperts;
-constexpr size_t kScratchInts = kStatusInts + 2 * kCountInts + kMaxExperts;
+constexpr size_t kScratchInts = kStatusInts + 2 * kCountInts;
 constexpr int kMaxDevices = 64;
 
-// Layout (int32 units): [error word | per-block counts | per-block bases | loads].
+// Layout (int32 units): [error word, completion counter | per-block counts | per-block bases].
 static __device__ __align__(256) int32_t g_dispatch_scratch[kScratchInts];
 
 std::mutex g_mutex;
@@ -85,10 +85,11 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x,
   DeviceStatus *status = reinterpret_cast<DeviceStatus *>(base);
   int32_t *counts = base + kStatusInts;
   int32_t *bases = counts + kCountInts;
-  int32_t *load = bases + kCountInts;
-  // Only the error word must start at zero; the kernels overwrite everything else they read.
-  e = cudaMemsetAsync(status, 0, sizeof(DeviceStatus), (cudaStream_t)stream);
+  unsigned int *counter = reinterpret_cast<unsigned int *>(base + 32);
+  // Only the error word and the completion counter must start at zero; the
+  // kernels overwrite everything else they read.
+  e = cudaMemsetAsync(base, 0, kStatusInts * sizeof(int32_t), (cudaStream_t)stream);
   if (e != cudaSuccess) return report_cuda(e);
   return report_cuda(launch_dispatch_with_scratch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm,
-                                                  counts, bases, load, status, (cudaStream_t)stream));
+                                                  counts, bases, counter, status, (cudaStream_t)stream));
 }

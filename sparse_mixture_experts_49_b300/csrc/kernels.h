@@ -21,14 +21,15 @@ struct Shape {
 
 enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4 };
 
-// Workspace carve-up (byte offsets from the workspace base).
+// Workspace carve-up (byte offsets from the workspace base). The first 256
+// bytes hold the error word (offset 0), the router's completion counter (64)
+// and the dispatch's completion counter (128); all start at zero.
 struct WsLayout {
   size_t status;                 // DeviceStatus
   size_t router_imp, router_load;  // [router blocks, E] partial sums
   size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
-  size_t router_partial;           // [splits, T, E] fp32 partial logits (tensor-core router)
+  size_t router_partial;           // [splits, T, EP] fp32 partial logits (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
-  size_t disp_load;                // [E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
   size_t dg, dh, dxr, dwr_acc;     // backward: [T, k], [T, E], [T, d] fp32
   size_t total;
@@ -60,7 +61,7 @@ cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, 
 
 cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
                                          int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
-                                         int32_t *counts, int32_t *base, int32_t *load, DeviceStatus *st,
+                                         int32_t *counts, int32_t *base, unsigned int *counter, DeviceStatus *st,
                                          cudaStream_t stream);
 moe_status dispatch_shape(const moe_config *cfg, Shape *sh);
 moe_status report_cuda(cudaError_t e);

@@ -68,10 +68,9 @@ WsLayout ws_layout(const Shape &sh) {
   L.router_load = take(rb * sh.E * 4);
   const RouterPlan rp = router_plan(sh);
   L.router_parts = take(rp.tensor_cores ? (size_t)3 * rp.ep * sh.d * 2 : 0);
-  L.router_partial = take(rp.tensor_cores ? (size_t)rp.splits * sh.T * sh.E * 4 : 0);
+  L.router_partial = take(rp.tensor_cores ? (size_t)rp.splits * sh.T * rp.ep * 4 : 0);
   L.disp_counts = take(db * sh.E * 4);
   L.disp_base = take(db * sh.E * 4);
-  L.disp_load = take((size_t)sh.E * 4);
   const size_t rows = (size_t)(sh.rows > 0 ? sh.rows : 1);
   L.dyp = take(rows * sh.d * sh.elt);
   L.da = take(rows * sh.R1 * sh.elt);

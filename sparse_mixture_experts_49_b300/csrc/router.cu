@@ -262,7 +262,7 @@ struct __align__(8) Bars {
 };
 struct Args {
   int T, E, kb_per_split, KB;
-  float *partial;   // [splits, T, E]
+  float *partial;   // [splits, T, EP]
   DeviceStatus *st;
 };
 
@@ -363,20 +363,26 @@ __global__ void __launch_bounds__(192, 1)
       drain_wait(&b.drain, 0);
     }
   } else {
+    // Each warp owns 32 rows. TMEM gives a thread one row; a 32 x 33 shared
+    // transpose (in the now idle stage buffers) turns that into 128-byte
+    // coalesced row stores. Partial rows have stride EP (padding columns are 0).
     const int q = warp & 3;
-    const int row = m0 + q * 32 + lane;
     if (nk > 0 && mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st)) {
       tc_fence_after();
+      float *tr = reinterpret_cast<float *>(tiles) + q * (32 * 33);
       float v[32];
-      float *dst = a.partial + ((int64_t)blockIdx.y * a.T + row) * a.E;
+      const int row0 = m0 + q * 32;
+      float *dst = a.partial + ((int64_t)blockIdx.y * a.T + row0) * EP;
 #pragma unroll 1
       for (int c = 0; c < EP / 32; ++c) {
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
-        if (row < a.T) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < a.E) dst[c * 32 + i] = v[i];
-        }
+        for (int i = 0; i < 32; ++i) tr[lane * 33 + i] = v[i];
+        __syncwarp();
+#pragma unroll 8
+        for (int r = 0; r < 32; ++r)
+          if (row0 + r < a.T) dst[(int64_t)r * EP + c * 32 + lane] = tr[r * 33 + lane];
+        __syncwarp();
       }
       tc_fence_before();
     }
@@ -390,23 +396,42 @@ __global__ void __launch_bounds__(192, 1)
 }  // namespace rt
 
 // Logits = sum of the split partials in split order (+ bias), then selection.
+// Partial rows have stride EP; every thread loads its float4 chunks of all
+// splits before adding, so the loads overlap.
 template <int EPT>
 __global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a) {
   constexpr int EP = 32 * EPT;
+  constexpr int Q = EP / 4;              // float4 per row
+  constexpr int CH = RT * Q / 256;       // float4 chunks per thread
   extern __shared__ float sm[];
   float *lg = sm;                      // [RT][EP + 1]
   float *impw = lg + RT * (EP + 1);    // [8][EP]
   int *cnt = reinterpret_cast<int *>(impw + 8 * EP);
   const int t0 = blockIdx.x * RT;
   const int E = a.E;
-  for (int i = threadIdx.x; i < RT * EP; i += 256) {
-    const int tl = i / EP, e = i - tl * EP, t = t0 + tl;
-    float v = 0.0f;
-    if (t < a.T && e < E) {
-      for (int s = 0; s < splits; ++s) v += partial[((int64_t)s * a.T + t) * E + e];
-      if (a.bias) v += a.bias[e];
+  float4 acc[CH];
+#pragma unroll
+  for (int c = 0; c < CH; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < splits; ++s) {
+    float4 v[CH];
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int i = threadIdx.x + 256 * c, tl = i / Q, e4 = i - tl * Q, t = t0 + tl;
+      v[c] = (t < a.T) ? __ldcs(reinterpret_cast<const float4 *>(partial + ((int64_t)s * a.T + t) * EP) + e4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    lg[tl * (EP + 1) + e] = v;
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      acc[c].x += v[c].x; acc[c].y += v[c].y; acc[c].z += v[c].z; acc[c].w += v[c].w;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < CH; ++c) {
+    const int i = threadIdx.x + 256 * c, tl = i / Q, e = (i - tl * Q) * 4;
+    const float vv[4] = {acc[c].x, acc[c].y, acc[c].z, acc[c].w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      lg[tl * (EP + 1) + e + u] = vv[u] + ((a.bias != nullptr && e + u < E) ? a.bias[e + u] : 0.0f);
   }
   for (int e = threadIdx.x; e < EP; e += 256) cnt[e] = 0;
   __syncthreads();
@@ -425,6 +450,7 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float *part_im
   if (e < E) {
     float s = 0.0f;
     int c = 0;
+#pragma unroll 4
     for (int b = lane; b < nblk; b += 32) {
       s += part_imp[(int64_t)b * E + e];
       c += part_load[(int64_t)b * E + e];
@@ -444,15 +470,22 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float *part_im
   if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!last) return;
+  // aux = alpha E sum_e f_e P_e, summed as a fixed-shape tree over 256 slots
+  __shared__ float term[256];
+  __threadfence();
+  {
+    const int j = threadIdx.x;
+    float v = 0.0f;
+    if (j < E) v = ((float)__ldcg(load + j) / ((float)T * (float)k)) * (__ldcg(importance + j) / (float)T);
+    term[j] = v;
+  }
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) term[threadIdx.x] += term[threadIdx.x + w];
+    __syncthreads();
+  }
   if (threadIdx.x == 0) {
-    __threadfence();
-    float acc = 0.0f;
-    for (int j = 0; j < E; ++j) {
-      const float imp = __ldcg(importance + j);
-      const int l = __ldcg(load + j);
-      acc += ((float)l / ((float)T * (float)k)) * (imp / (float)T);
-    }
-    if (aux) *aux = alpha * (float)E * acc;
+    if (aux) *aux = alpha * (float)E * term[0];
     *counter = 0u;
   }
 }
