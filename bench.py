@@ -35,8 +35,8 @@ WORKLOAD = "switch-base-top1"
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; dispatch % HBM BW"
 L2_FLUSH_BYTES = 256 << 20
 # kernels of the library per forward step of the bf16 layer: router (W_r split, tensor-core logits,
-# selection, statistics) 4, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1
-LAUNCHES_PER_STEP = 9
+# selection + statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1
+LAUNCHES_PER_STEP = 8
 
 
 def load_peaks():

@@ -16,10 +16,11 @@
 //      and its per-expert popcounts; the last block to finish scans those
 //      counts over blocks for every expert (block bases), and derives
 //      kept = min(load, C) and the group offsets (exclusive scan over experts);
-//   2. per block of 64 tokens, rank = block base + popcount of the bitmap
+//   2. per block of 32 tokens, rank = block base + popcount of the bitmap
 //      below the token, slot = rank if rank < C else -1, and the copy of the
 //      token's row to each of its kept rows with 16-byte loads and stores
-//      (64-token blocks spread the copy over four times more SMs).
+//      (small blocks spread the copy over eight times more SMs; each thread
+//      keeps eight 16-byte loads in flight).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -29,7 +30,7 @@ namespace {
 
 constexpr int DT = DISPATCH_TOKENS;   // 256 tokens per counting block
 constexpr int WORDS = DT / 32;        // bitmap words per expert
-constexpr int SUB = 64;               // tokens per placing block
+constexpr int SUB = 32;               // tokens per placing block
 
 // Marks (token, expert) pairs of the 256 tokens from t0 (one per thread).
 // A pair with an expert outside [0, E) or a repeat within one token is left
@@ -79,10 +80,17 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
   const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
   int run = 0;
   if (e < E) {
-#pragma unroll 8
-    for (int b = 0; b < (int)gridDim.x; ++b) {
-      block_base[(int64_t)b * E + e] = run;
-      run += __ldcg(block_counts + (int64_t)b * E + e);
+    // eight counts in flight per step, then the running sums
+    for (int b0 = 0; b0 < (int)gridDim.x; b0 += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        c[u] = (b0 + u < (int)gridDim.x) ? __ldcg(block_counts + (int64_t)(b0 + u) * E + e) : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b0 + u < (int)gridDim.x) block_base[(int64_t)(b0 + u) * E + e] = run;
+        run += c[u];
+      }
     }
   }
   const int kept = (e < E) ? ((C >= 0 && (int64_t)run > C) ? (int)C : run) : 0;
@@ -104,7 +112,7 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
   if (threadIdx.x == 0) *counter = 0u;
 }
 
-// Slots, row owners and the row copies for 64 tokens. The bitmap covers the
+// Slots, row owners and the row copies for 32 tokens. The bitmap covers the
 // whole 256-token counting block the 64 tokens sit in, because ranks count
 // every earlier token of that block.
 template <typename XT>
@@ -117,6 +125,7 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
   extern __shared__ uint32_t present[];           // [E][WORDS]
   __shared__ int pre[256 * WORDS];                 // popcount prefix per (expert, word)
   __shared__ int rows[SUB][8];
+  __shared__ int has_rows[SUB];
   const int B = blockIdx.x / (DT / SUB), sub = blockIdx.x % (DT / SUB);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   build_bitmap(present, idx, T, E, k, B * DT, nullptr);
@@ -134,6 +143,7 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
     const int t = B * DT + threadIdx.x;
     const int word = threadIdx.x >> 5;
     const uint32_t below = (1u << lane) - 1u;
+    int any = 0;
     for (int j = 0; j < 8; ++j) {
       int r = -1;
       if (j < k && t < T) {
@@ -153,31 +163,35 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
         slot[(int64_t)t * k + j] = s;
       }
       rows[tl][j] = r;
+      any |= (r >= 0);
     }
+    has_rows[tl] = any;
   }
   __syncthreads();
-  // copy: warp w moves tokens w*8 .. w*8+7 of the 64
+  // copy: (token, 16-byte chunk) items spread over the block, 8 loads in flight per thread
   constexpr int V = Vec16<XT>::N;
   const int nvec = d / V;
-  for (int i = 0; i < SUB / 8; ++i) {
-    const int q = warp * (SUB / 8) + i;
-    const int t = B * DT + sub * SUB + q;
-    if (t >= T) break;
-    int rr[8];
-    int any = 0;
+  const int items = SUB * nvec;
+  const int64_t tbase = (int64_t)B * DT + sub * SUB;
+  for (int i0 = 0; i0 < items; i0 += 8 * DT) {
+    uint4 u[8];
+    int q[8], v[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      rr[j] = rows[q][j];
-      any |= (rr[j] >= 0);
+    for (int b = 0; b < 8; ++b) {
+      const int it = i0 + b * DT + threadIdx.x;
+      q[b] = it / nvec;
+      v[b] = it - q[b] * nvec;
+      if (it < items && tbase + q[b] < T && has_rows[q[b]])
+        u[b] = *reinterpret_cast<const uint4 *>(x + (tbase + q[b]) * d + (int64_t)v[b] * V);
     }
-    if (!any) continue;
-    const XT *src = x + (int64_t)t * d;
-#pragma unroll 4
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = *reinterpret_cast<const uint4 *>(src + v * V);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (rr[j] >= 0) *reinterpret_cast<uint4 *>(x_perm + (int64_t)rr[j] * d + v * V) = u;
+    for (int b = 0; b < 8; ++b) {
+      const int it = i0 + b * DT + threadIdx.x;
+      if (it >= items || tbase + q[b] >= T || !has_rows[q[b]]) continue;
+      for (int j = 0; j < k; ++j) {
+        const int r = rows[q[b]][j];
+        if (r >= 0) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)v[b] * V) = u[b];
+      }
     }
   }
 }

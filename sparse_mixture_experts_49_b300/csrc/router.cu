@@ -19,9 +19,9 @@
 //
 // Selection: one warp per token, softmax in fp32 with the row maximum
 // subtracted, then k rounds of a warp arg-max (descending logit, ties to the
-// lower index). Importance and load are reduced per block in a fixed order
-// and finished by a second kernel, so the statistics are bitwise
-// reproducible.
+// lower index). Importance and load are reduced per block in a fixed order;
+// the last block to finish reduces the blocks' partials in block order, so
+// the statistics are bitwise reproducible.
 #include <cfloat>
 
 #include "common.cuh"
@@ -58,19 +58,19 @@ template <> __device__ __forceinline__ void load4<bf16>(const bf16 *p, float *o)
   o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
-template <int EPT> constexpr size_t select_smem_bytes() {
+template <int EPT, int TOKENS> constexpr size_t select_smem_bytes() {
   constexpr int EP = 32 * EPT;
-  return sizeof(float) * ((size_t)RT * (EP + 1) + 8 * EP) + sizeof(int) * EP;
+  return sizeof(float) * ((size_t)TOKENS * (EP + 1) + 8 * EP) + sizeof(int) * EP;
 }
 template <int EPT> constexpr size_t simt_router_smem_bytes() {
   constexpr int EP = 32 * EPT;
-  return sizeof(float) * ((size_t)RBK * RT + (size_t)RBK * EP) + select_smem_bytes<EPT>();
+  return sizeof(float) * ((size_t)RBK * RT + (size_t)RBK * EP) + select_smem_bytes<EPT, RT>();
 }
 
-// Softmax, top-k and per-block statistics for the block's 64 tokens, whose
-// logits (bias included) are in lg[64][EP + 1]. Needs cnt[] zeroed and a
-// __syncthreads() before the call.
-template <int EPT>
+// Softmax, top-k and per-block statistics for the block's 8 * TPW tokens,
+// whose logits (bias included) are in lg[8 * TPW][EP + 1]. Needs cnt[] zeroed
+// and a __syncthreads() before the call.
+template <int EPT, int TPW>
 __device__ __forceinline__ void select_block(const float *lg, float *impw, int *cnt, const RouterArgs &a, int t0) {
   constexpr int EP = 32 * EPT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -79,8 +79,8 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
 #pragma unroll
   for (int j = 0; j < EPT; ++j) imp[j] = 0.0f;
 
-  for (int i = 0; i < 8; ++i) {
-    const int tl = warp * 8 + i, t = t0 + tl;
+  for (int i = 0; i < TPW; ++i) {
+    const int tl = warp * TPW + i, t = t0 + tl;
     if (t >= a.T) break;
     float h[EPT], p[EPT];
     float m = -FLT_MAX;
@@ -155,9 +155,66 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
   }
 }
 
+// Run by every block after it wrote its partial statistics: the last block to
+// arrive reduces them (per expert, blocks in order) into importance and load,
+// sums the aux terms as a fixed-shape tree, and re-arms the counter.
+__device__ __forceinline__ void finish_if_last(const RouterArgs &a, int nblk, float alpha, float *importance,
+                                               int32_t *load, float *aux, unsigned int *counter) {
+  __shared__ bool last;
+  __shared__ float term[256];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const int e = threadIdx.x;
+  float v = 0.0f;
+  if (e < a.E) {
+    float s = 0.0f;
+    int c = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 8) {
+      float ps[8];
+      int pc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const bool in = b0 + u < nblk;
+        ps[u] = in ? __ldcg(a.part_imp + (int64_t)(b0 + u) * a.E + e) : 0.0f;
+        pc[u] = in ? __ldcg(a.part_load + (int64_t)(b0 + u) * a.E + e) : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        s += ps[u];
+        c += pc[u];
+      }
+    }
+    importance[e] = s;
+    load[e] = c;
+    v = ((float)c / ((float)a.T * (float)a.k)) * (s / (float)a.T);
+  }
+  term[e] = v;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (e < w) term[e] += term[e + w];
+    __syncthreads();
+  }
+  if (e == 0) {
+    if (aux) *aux = alpha * (float)a.E * term[0];
+    *counter = 0u;
+  }
+}
+
+struct StatsOut {
+  float alpha;
+  float *importance;
+  int32_t *load;
+  float *aux;
+  unsigned int *counter;
+};
+
 // ---------------------------------------------------------------- CUDA-core path (fp32 layers)
 template <typename XT, int EPT>
-__global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a) {
+__global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a, const StatsOut so) {
   constexpr int EP = 32 * EPT;
   extern __shared__ float sm[];
   float *xs = sm;                      // [RBK][RT]
@@ -221,7 +278,8 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a) {
     }
   for (int e = tid; e < EP; e += 256) cnt[e] = 0;
   __syncthreads();
-  select_block<EPT>(lg, impw, cnt, a, t0);
+  select_block<EPT, 8>(lg, impw, cnt, a, t0);
+  finish_if_last(a, gridDim.x, so.alpha, so.importance, so.load, so.aux, so.counter);
 }
 
 // ---------------------------------------------------------------- tensor-core path (bf16 layers)
@@ -395,19 +453,21 @@ __global__ void __launch_bounds__(192, 1)
 }
 }  // namespace rt
 
-// Logits = sum of the split partials in split order (+ bias), then selection.
-// Partial rows have stride EP; every thread loads its float4 chunks of all
-// splits before adding, so the loads overlap.
+// Logits = sum of the split partials in split order (+ bias), then selection
+// of 32 tokens per block. Partial rows have stride EP; every thread loads its
+// float4 chunks of all splits before adding, so the loads overlap.
+constexpr int RT_TC = 32;
 template <int EPT>
-__global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a) {
+__global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a,
+                                                            const StatsOut so) {
   constexpr int EP = 32 * EPT;
   constexpr int Q = EP / 4;              // float4 per row
-  constexpr int CH = RT * Q / 256;       // float4 chunks per thread
+  constexpr int CH = RT_TC * Q / 256;    // float4 chunks per thread
   extern __shared__ float sm[];
-  float *lg = sm;                      // [RT][EP + 1]
-  float *impw = lg + RT * (EP + 1);    // [8][EP]
+  float *lg = sm;                      // [RT_TC][EP + 1]
+  float *impw = lg + RT_TC * (EP + 1); // [8][EP]
   int *cnt = reinterpret_cast<int *>(impw + 8 * EP);
-  const int t0 = blockIdx.x * RT;
+  const int t0 = blockIdx.x * RT_TC;
   const int E = a.E;
   float4 acc[CH];
 #pragma unroll
@@ -435,59 +495,8 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *partial
   }
   for (int e = threadIdx.x; e < EP; e += 256) cnt[e] = 0;
   __syncthreads();
-  select_block<EPT>(lg, impw, cnt, a, t0);
-}
-
-// importance[e], load[e] from the per-block partials (fixed order); the last
-// block to finish computes aux from them and re-arms the counter.
-__global__ void __launch_bounds__(256) router_finish_kernel(const float *part_imp, const int32_t *part_load,
-                                                            int nblk, int T, int E, int k, float alpha,
-                                                            float *importance, int32_t *load, float *aux,
-                                                            unsigned int *counter) {
-  __shared__ bool last;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + warp;
-  if (e < E) {
-    float s = 0.0f;
-    int c = 0;
-#pragma unroll 4
-    for (int b = lane; b < nblk; b += 32) {
-      s += part_imp[(int64_t)b * E + e];
-      c += part_load[(int64_t)b * E + e];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      s += __shfl_xor_sync(0xffffffffu, s, o);
-      c += __shfl_xor_sync(0xffffffffu, c, o);
-    }
-    if (lane == 0) {
-      importance[e] = s;
-      load[e] = c;
-    }
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!last) return;
-  // aux = alpha E sum_e f_e P_e, summed as a fixed-shape tree over 256 slots
-  __shared__ float term[256];
-  __threadfence();
-  {
-    const int j = threadIdx.x;
-    float v = 0.0f;
-    if (j < E) v = ((float)__ldcg(load + j) / ((float)T * (float)k)) * (__ldcg(importance + j) / (float)T);
-    term[j] = v;
-  }
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) term[threadIdx.x] += term[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    if (aux) *aux = alpha * (float)E * term[0];
-    *counter = 0u;
-  }
+  select_block<EPT, RT_TC / 8>(lg, impw, cnt, a, t0);
+  finish_if_last(a, gridDim.x, so.alpha, so.importance, so.load, so.aux, so.counter);
 }
 
 template <typename K>
@@ -496,20 +505,21 @@ cudaError_t set_smem(K kern, size_t bytes) {
 }
 
 template <typename XT, int EPT>
-cudaError_t run_simt(const RouterArgs &a, int nblk, cudaStream_t stream) {
+cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStream_t stream) {
   constexpr size_t smem = simt_router_smem_bytes<EPT>();
   static cudaError_t attr = set_smem(router_simt_kernel<XT, EPT>, smem);
   if (attr != cudaSuccess) return attr;
-  router_simt_kernel<XT, EPT><<<nblk, 256, smem, stream>>>(a);
+  router_simt_kernel<XT, EPT><<<nblk, 256, smem, stream>>>(a, so);
   return cudaGetLastError();
 }
 
 template <int EPT>
-cudaError_t run_select(const float *partial, int splits, const RouterArgs &a, int nblk, cudaStream_t stream) {
-  constexpr size_t smem = select_smem_bytes<EPT>();
+cudaError_t run_select(const float *partial, int splits, const RouterArgs &a, const StatsOut &so, int nblk,
+                       cudaStream_t stream) {
+  constexpr size_t smem = select_smem_bytes<EPT, RT_TC>();
   static cudaError_t attr = set_smem(router_select_kernel<EPT>, smem);
   if (attr != cudaSuccess) return attr;
-  router_select_kernel<EPT><<<nblk, 256, smem, stream>>>(partial, splits, a);
+  router_select_kernel<EPT><<<nblk, 256, smem, stream>>>(partial, splits, a, so);
   return cudaGetLastError();
 }
 
@@ -526,7 +536,10 @@ int epad_of(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; 
 
 }  // namespace
 
-int router_blocks(const Shape &sh) { return (sh.T + RT - 1) / RT; }
+int router_blocks(const Shape &sh) {
+  const int per = sh.dtype == MOE_BF16 ? RT_TC : RT;
+  return (sh.T + per - 1) / per;
+}
 
 RouterPlan router_plan(const Shape &sh) {
   RouterPlan p;
@@ -554,43 +567,41 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
   const int nblk = router_blocks(sh);
   const RouterPlan plan = router_plan(sh);
+  StatsOut so;
+  so.alpha = sh.alpha; so.importance = importance; so.load = load; so.aux = aux;
+  so.counter = reinterpret_cast<unsigned int *>(w + L.status + 64);
   cudaError_t e;
   if (!plan.tensor_cores) {
-    if (sh.E <= 32) e = run_simt<float, 1>(a, nblk, stream);
-    else if (sh.E <= 64) e = run_simt<float, 2>(a, nblk, stream);
-    else if (sh.E <= 128) e = run_simt<float, 4>(a, nblk, stream);
-    else e = run_simt<float, 8>(a, nblk, stream);
-  } else {
-    bf16 *parts = reinterpret_cast<bf16 *>(w + L.router_parts);
-    float *partial = reinterpret_cast<float *>(w + L.router_partial);
-    const int64_t n = (int64_t)plan.ep * sh.d;
-    int sgrid = (int)((n + 255) / 256);
-    if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
-    router_split_kernel<<<sgrid, 256, 0, stream>>>(w_r, sh.E, plan.ep, sh.d, parts);
-    CUtensorMap mx, mw;
-    if (!make_map_2d(&mx, x, sh.d, sh.T, 64, 128) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
-      return cudaErrorInvalidValue;
-    rt::Args ta;
-    ta.T = sh.T; ta.E = sh.E; ta.kb_per_split = plan.kb_per_split; ta.KB = (sh.d + rt::BK - 1) / rt::BK;
-    ta.partial = partial;
-    ta.st = reinterpret_cast<DeviceStatus *>(w + L.status);
-    switch (plan.ep) {
-      case 32: e = run_tc<32>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-      case 64: e = run_tc<64>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-      case 128: e = run_tc<128>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-      default: e = run_tc<256>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-    }
-    if (e != cudaSuccess) return e;
-    if (sh.E <= 32) e = run_select<1>(partial, plan.splits, a, nblk, stream);
-    else if (sh.E <= 64) e = run_select<2>(partial, plan.splits, a, nblk, stream);
-    else if (sh.E <= 128) e = run_select<4>(partial, plan.splits, a, nblk, stream);
-    else e = run_select<8>(partial, plan.splits, a, nblk, stream);
+    if (sh.E <= 32) e = run_simt<float, 1>(a, so, nblk, stream);
+    else if (sh.E <= 64) e = run_simt<float, 2>(a, so, nblk, stream);
+    else if (sh.E <= 128) e = run_simt<float, 4>(a, so, nblk, stream);
+    else e = run_simt<float, 8>(a, so, nblk, stream);
+    return e;
+  }
+  bf16 *parts = reinterpret_cast<bf16 *>(w + L.router_parts);
+  float *partial = reinterpret_cast<float *>(w + L.router_partial);
+  const int64_t n = (int64_t)plan.ep * sh.d;
+  int sgrid = (int)((n + 255) / 256);
+  if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
+  router_split_kernel<<<sgrid, 256, 0, stream>>>(w_r, sh.E, plan.ep, sh.d, parts);
+  CUtensorMap mx, mw;
+  if (!make_map_2d(&mx, x, sh.d, sh.T, 64, 128) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
+    return cudaErrorInvalidValue;
+  rt::Args ta;
+  ta.T = sh.T; ta.E = sh.E; ta.kb_per_split = plan.kb_per_split; ta.KB = (sh.d + rt::BK - 1) / rt::BK;
+  ta.partial = partial;
+  ta.st = reinterpret_cast<DeviceStatus *>(w + L.status);
+  switch (plan.ep) {
+    case 32: e = run_tc<32>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+    case 64: e = run_tc<64>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+    case 128: e = run_tc<128>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+    default: e = run_tc<256>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
   }
   if (e != cudaSuccess) return e;
-  unsigned int *counter = reinterpret_cast<unsigned int *>(w + L.status + 64);
-  router_finish_kernel<<<(sh.E + 7) / 8, 256, 0, stream>>>(a.part_imp, a.part_load, nblk, sh.T, sh.E, sh.k,
-                                                           sh.alpha, importance, load, aux, counter);
-  return cudaGetLastError();
+  if (sh.E <= 32) return run_select<1>(partial, plan.splits, a, so, nblk, stream);
+  if (sh.E <= 64) return run_select<2>(partial, plan.splits, a, so, nblk, stream);
+  if (sh.E <= 128) return run_select<4>(partial, plan.splits, a, so, nblk, stream);
+  return run_select<8>(partial, plan.splits, a, so, nblk, stream);
 }
 
 }  // namespace moe
