@@ -1,12 +1,14 @@
 """Benchmark of the MoE FFN layer on B300.
 
-One step = one forward pass of the whole layer (router -> dispatch -> expert
-grouped GEMM -> combine) over one batch of the Switch-Base-like top-1
-workload: T = 8192 tokens (16 x 512), d_model 768, 128 experts, ReLU FFN
-768 -> 3072 -> 768, capacity factor 1.25, bf16 activations and experts with
-an fp32 router. Inputs are seeded synthetic data of that shape, resident in
-HBM before timing. The L2 cache is flushed (a 256 MiB write) before every
-timed step, outside the step's CUDA events.
+One step = one pass of the whole layer over one batch. By default that is
+the forward pass (router -> dispatch -> expert grouped GEMM -> combine) of
+the Switch-Base-like top-1 workload: T = 8192 tokens (16 x 512), d_model 768,
+128 experts, ReLU FFN 768 -> 3072 -> 768, capacity factor 1.25, bf16
+activations and experts with an fp32 router. `--workload` picks another of
+the bf16 workloads and `--pass fwdbwd` adds the backward pass (moe_backward)
+to every step. Inputs are seeded synthetic data of the workload's shape,
+resident in HBM before timing. The L2 cache is flushed (a 256 MiB write)
+before every timed step, outside the step's CUDA events.
 
 Prints one JSON line. `--impl reference` times the CPU oracle instead (the
 reference arm of this build: a plain fp64 restatement of the layer).
@@ -37,6 +39,9 @@ L2_FLUSH_BYTES = 256 << 20
 # kernels of the library per forward step of the bf16 layer: router (W_r split, tensor-core logits,
 # selection + statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1
 LAUNCHES_PER_STEP = 8
+# moe_backward of the bf16 layer: combine backward 1, grouped GEMMs 4, router logit gradient 1, router weight
+# gradients 2, unpermute-reduce 1
+LAUNCHES_BACKWARD = 9
 
 
 def load_peaks():
@@ -117,11 +122,11 @@ def gemm_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def gemm_traffic():
+def gemm_traffic(workload):
     """dram read+write bytes per moe_expert_gemm call, from profiles/traffic.json, or None when the
     counters were taken on a different version of the GEMM kernel source."""
     try:
-        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[WORKLOAD]
+        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[workload]
         return t["gemm_bytes_per_call"] if t.get("source_hash") == gemm_source_hash() else None
     except Exception:
         return None
@@ -129,15 +134,57 @@ def gemm_traffic():
 
 # ---------------------------------------------------------------- algorithmic traffic and flops
 def algorithmic(w, K_a: int):
-    """Bytes / FLOPs each step must move or do (kept assignments only, weights read once)."""
+    """Bytes / FLOPs each call must move or do (kept assignments only, weights read once)."""
     s = 2  # bf16
-    d, F, E, T, k = w.d, w.F, w.E, w.T, w.k
+    d, F, E, T, k, R1 = w.d, w.F, w.E, w.T, w.k, w.R1
     router_b = T * d * s + E * d * 4 + T * k * 8 + T * E * 4   # x, W_r, idx+gate, probs
     dispatch_b = T * d * s + K_a * d * s + T * k * 4 * 3 + K_a * 4
-    gemm_b = w.nm * E * F * d * s + K_a * d * s * 2 + K_a * F * s * 2   # weights, x_perm in, y out, h out+in
+    act_b = K_a * F * s * 2 + (K_a * 2 * F * s if w.act == "swiglu" else 0)   # h out+in, pre-activations out
+    gemm_b = w.nm * E * F * d * s + K_a * d * s * 2 + act_b   # weights, x_perm in, y_perm out, activations
     combine_b = T * d * s * 2 + K_a * d * s + T * k * 12
     gemm_flops = 2 * K_a * d * F * w.nm
-    return dict(router=router_b, dispatch=dispatch_b, gemm=gemm_b, combine=combine_b, gemm_flops=gemm_flops)
+    # backward: combine bwd (dY, y_perm in; dYp out), four grouped GEMMs (weights in, weight gradients out,
+    # dYp / h / pre-activations / dA / x_perm in, dA and dXp out), router gradient, unpermute-reduce
+    bwd_gemm_b = (2 * w.nm * E * F * d * s + 2 * K_a * d * s + K_a * F * s + (K_a * 2 * F * s if w.act == "swiglu" else 0)
+                  + 3 * K_a * R1 * s + K_a * d * s + K_a * d * s)
+    backward_b = (T * d * s + 2 * K_a * d * s + bwd_gemm_b + T * E * 4 * 2 + T * d * s + E * d * 4 * 2
+                  + T * d * 4 * 2 + T * d * s * 2 + K_a * d * s)
+    backward_flops = 2 * gemm_flops + 4 * T * E * d
+    return dict(router=router_b, dispatch=dispatch_b, gemm=gemm_b, combine=combine_b, gemm_flops=gemm_flops,
+                backward=backward_b, backward_flops=backward_flops, bwd_gemm_flops=2 * gemm_flops)
+
+
+# ---------------------------------------------------------------- inputs on the device
+DEVICE_DRAW_BYTES = 8 << 30   # expert weights above this size are drawn on the GPU (host draws take minutes)
+
+
+def device_inputs(w, want_dy: bool):
+    """x, W_r, bias (and dY) from moe_synth (margin-conditioned); expert weights per expert from moe_synth,
+    or, for the largest workloads, from torch's seeded Philox generator on the GPU with the same
+    distribution N(0, 0.1 / sqrt(fan_in)), rounded to bf16."""
+    import torch
+    bf = torch.bfloat16
+    inp = syn.make_inputs(w, experts=False, dy=want_dy)
+    dev = {"x": torch.from_numpy(inp["x"]).cuda().to(bf), "w_r": torch.from_numpy(inp["w_r"]).cuda(),
+           "bias": None if inp["bias"] is None else torch.from_numpy(inp["bias"]).cuda(),
+           "dy": torch.from_numpy(inp["dy"]).cuda().to(bf) if want_dy else None}
+    w1 = torch.empty(w.E, w.R1, w.d, dtype=bf, device="cuda")
+    w2 = torch.empty(w.E, w.d, w.F, dtype=bf, device="cuda")
+    host_draw = w.E * (w.R1 * w.d + w.d * w.F) * 2 <= DEVICE_DRAW_BYTES
+    if host_draw:
+        for e in range(w.E):
+            a, b = syn.expert_weights(w, e)
+            w1[e].copy_(torch.from_numpy(a).to(bf))
+            w2[e].copy_(torch.from_numpy(b).to(bf))
+    else:
+        g = torch.Generator(device="cuda")
+        for e in range(w.E):
+            g.manual_seed(w.seed * 1000003 + e)
+            w1[e].copy_(torch.randn(w.R1, w.d, generator=g, device="cuda") * (w.expert_scale / math.sqrt(w.d)))
+            w2[e].copy_(torch.randn(w.d, w.F, generator=g, device="cuda") * (w.expert_scale / math.sqrt(w.F)))
+    dev["w1"], dev["w2"] = w1, w2
+    dev["weights"] = "moe_synth (host, per expert)" if host_draw else "torch Philox on the GPU, seeded per expert"
+    return inp, dev
 
 
 # ---------------------------------------------------------------- our arm
@@ -150,33 +197,42 @@ def run_ours(args):
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
-    w = syn.WORKLOADS[WORKLOAD]
-    inp = syn.make_inputs(w, dy=False)
-    cap = moe.moe_capacity(w.T, w.E, w.k, w.cf[0], w.cf[1], w.count_assignments)
+    w = syn.WORKLOADS[args.workload]
+    bwd = args.pass_ == "fwdbwd"
+    inp, dv = device_inputs(w, bwd)
+    cap = -1 if w.cf is None else moe.moe_capacity(w.T, w.E, w.k, w.cf[0], w.cf[1], w.count_assignments)
     cfg = moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=w.k, d_ff=w.F, act=w.act, dtype=w.dtype,
                           renormalize=w.renormalize, capacity=cap, aux_alpha=w.alpha)
     stream = torch.cuda.current_stream()
     L = moe.MoELayer(cfg)
-    bf = torch.bfloat16
-    x = torch.from_numpy(inp["x"]).cuda().to(bf)
-    w_r = torch.from_numpy(inp["w_r"]).cuda()
-    w1 = torch.from_numpy(inp["w1"]).cuda().to(bf)
-    w2 = torch.from_numpy(inp["w2"]).cuda().to(bf)
+    x, w_r, bias, w1, w2, dy = dv["x"], dv["w_r"], dv["bias"], dv["w1"], dv["w2"], dv["dy"]
+    if bwd:
+        dx = torch.empty_like(x)
+        dw_r = torch.empty(w.E, w.d, dtype=torch.float32, device="cuda")
+        dw1 = torch.empty_like(w1)
+        dw2 = torch.empty_like(w2)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    calls = ["router", "dispatch", "gemm", "combine"]
+    calls = ["router", "dispatch", "gemm", "combine"] + (["backward"] if bwd else [])
+    saved = dict(x=x, w_r=w_r, w1=w1, w2=w2, probs=L.probs, topk_idx=L.topk_idx, topk_gate=L.topk_gate,
+                 slot=L.slot, expert_offsets=L.offsets, load=L.load, x_perm=L.x_perm, pre_act=L.pre_act, h=L.h,
+                 y_perm=L.y_perm)
+    pre_act = L.pre_act if bwd else None
 
     def step(marks=None):
         if marks: marks[0].record(stream)
-        moe.moe_router(cfg, x, w_r, None, L.probs, L.topk_idx, L.topk_gate, L.importance, L.load, L.aux, L.ws)
+        moe.moe_router(cfg, x, w_r, bias, L.probs, L.topk_idx, L.topk_gate, L.importance, L.load, L.aux, L.ws)
         if marks: marks[1].record(stream)
         moe.moe_dispatch(cfg, x, L.topk_idx, L.slot, L.kept, L.offsets, L.row_token, L.x_perm, L.ws)
         if marks: marks[2].record(stream)
-        moe.moe_expert_gemm(cfg, L.x_perm, L.offsets, w1, w2, None, L.h, L.y_perm, L.ws)
+        moe.moe_expert_gemm(cfg, L.x_perm, L.offsets, w1, w2, pre_act, L.h, L.y_perm, L.ws)
         if marks: marks[3].record(stream)
         moe.moe_combine(cfg, x, L.y_perm, L.topk_idx, L.topk_gate, L.slot, L.offsets, L.out)
         if marks: marks[4].record(stream)
+        if bwd:
+            moe.moe_backward(cfg, saved, dy, dx, dw_r, dw1, dw2, L.ws)
+            if marks: marks[5].record(stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -186,17 +242,18 @@ def run_ours(args):
         raise RuntimeError("device error during warm-up")
     K_a = int(L.offsets[-1].item())
 
-    # per-call breakdown (eager launches, CUDA events between the four ABI calls)
+    # per-call breakdown (eager launches, CUDA events between the ABI calls)
     n_eager = min(args.steps, 200)
-    marks = [[ev() for _ in range(5)] for _ in range(n_eager)]
+    nc = len(calls)
+    marks = [[ev() for _ in range(nc + 1)] for _ in range(n_eager)]
     for i in range(n_eager):
         flush.zero_()
         step(marks[i])
     torch.cuda.synchronize()
     per_call = {c: [m[j].elapsed_time(m[j + 1]) for m in marks] for j, c in enumerate(calls)}
-    eager_ms = statistics.mean(m[0].elapsed_time(m[4]) for m in marks)
+    eager_ms = statistics.mean(m[0].elapsed_time(m[nc]) for m in marks)
 
-    # the timed steps: the whole layer captured once in a CUDA graph, replayed
+    # the timed steps: the whole step captured once in a CUDA graph, replayed
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()
     side.wait_stream(stream)
@@ -234,9 +291,13 @@ def run_ours(args):
     total_ms = max_over_ranks(sum(per_step), world)
     value = world * w.T * args.steps / (total_ms / 1e3)
 
-    # end to end: pinned host x in, host out back, through the same C-ABI calls
+    # end to end: pinned host x (and dY) in, host out (and dX) back, through the same C-ABI calls
+    bf = torch.bfloat16
     x_host = torch.from_numpy(inp["x"]).to(bf).pin_memory()
     out_host = torch.empty(w.T, w.d, dtype=bf).pin_memory()
+    if bwd:
+        dy_host = torch.from_numpy(inp["dy"]).to(bf).pin_memory()
+        dx_host = torch.empty(w.T, w.d, dtype=bf).pin_memory()
     e2e_steps = max(10, args.steps // 4)
     barrier(world)
     torch.cuda.synchronize()
@@ -244,49 +305,68 @@ def run_ours(args):
     e0.record(stream)
     for _ in range(e2e_steps):
         x.copy_(x_host, non_blocking=True)
+        if bwd:
+            dy.copy_(dy_host, non_blocking=True)
         step()
         out_host.copy_(L.out, non_blocking=True)
+        if bwd:
+            dx_host.copy_(dx, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * w.T * e2e_steps / (e2e_ms / 1e3)
+    io_bytes = w.T * w.d * 2 * (2 if bwd else 1)
 
     hbm, tflops, tflops_sus, peak_src = load_peaks()
     alg = algorithmic(w, K_a)
     mean_call = {c: statistics.mean(v) for c, v in per_call.items()}
     kernels = {}
-    for c in ["router", "dispatch", "combine", "gemm"]:
+    for c in calls:
         gbs = alg[c] / (mean_call[c] * 1e-3) / 1e9
         kernels[c] = {"ms": round(mean_call[c], 5), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
     gemm_tf = alg["gemm_flops"] / (mean_call["gemm"] * 1e-3) / 1e12
     kernels["gemm"].update({"TFLOP/s": round(gemm_tf, 1), "frac_bf16_peak": round(gemm_tf / tflops, 4)})
+    if bwd:
+        btf = alg["bwd_gemm_flops"] / (mean_call["backward"] * 1e-3) / 1e12
+        kernels["backward"].update({"gemm_TFLOP/s": round(btf, 1), "frac_bf16_peak": round(btf / tflops, 4)})
     gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
-    traffic = gemm_traffic()
+    # the binding roof of the forward grouped GEMM: max(FLOPs / tensor peak, bytes / HBM peak)
+    tensor_bound = alg["gemm_flops"] / (tflops * 1e12) > alg["gemm"] / (hbm * 1e9)
+    traffic = gemm_traffic(args.workload)
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": tflops, "unit": "TFLOP/s",
+                "frac": round(gemm_tf / tflops, 4)}
+    else:
+        roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gemm_gbs / hbm, 4)}
+    roof.update({"kernel": "moe_expert_gemm (forward grouped GEMM, 2 launches)", "traffic": traffic,
+                 "peak_source": peak_src, "algorithmic_bytes_per_call": alg["gemm"],
+                 "algorithmic_flops_per_call": alg["gemm_flops"]})
+    launches = LAUNCHES_PER_STEP + (LAUNCHES_BACKWARD if bwd else 0)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "pass": "fwd", "T": w.T, "d_model": w.d, "experts": w.E, "top_k": w.k,
-                   "d_ff": w.F, "act": w.act, "capacity_factor": "1.25", "capacity": cap,
-                   "capacity_reading": "floor(k*T*cf/E)", "kept_assignments": K_a,
+        "config": {"workload": args.workload, "pass": args.pass_, "T": w.T, "d_model": w.d, "experts": w.E,
+                   "top_k": w.k, "d_ff": w.F, "act": w.act, "renormalize": w.renormalize,
+                   "capacity_factor": None if w.cf is None else f"{w.cf[0]}/{w.cf[1]}", "capacity": cap,
+                   "capacity_reading": "floor(k*T*cf/E)" if w.cf is not None else "none (dropless)",
+                   "kept_assignments": K_a, "expert_weights": dv["weights"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside the step's events)"},
-        "roofline": {"kernel": "moe_expert_gemm (grouped GEMM, 2 launches: W1+ReLU, W2)", "bound": "hbm",
-                     "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(gemm_gbs / hbm, 4), "traffic": traffic, "peak_source": peak_src,
-                     "algorithmic_bytes_per_call": alg["gemm"]},
+        "roofline": roof,
         "kernels": kernels,
-        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": w.T * w.d * 2,
-                "d2h_bytes_per_step": w.T * w.d * 2},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                "d2h_bytes_per_step": io_bytes},
+        "gpu_launches": launches * args.steps,
         "eager_ms_per_step": round(eager_ms, 5),
-        "timing": "layer replayed as one CUDA graph per step; per-kernel figures from an eager pass with events "
+        "timing": "step replayed as one CUDA graph; per-call figures from an eager pass with events "
                   "between the ABI calls",
         "clocks": clk,
         "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, inp)
+        res["cpu_baseline"] = cpu_baseline(w, inp, bwd)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -304,59 +384,92 @@ def _oracle_threads():
         return os.cpu_count()
 
 
-def _oracle_step(w, x, w_r, bias, w1_64, w2_64):
+HOST_F64_WEIGHTS_MAX = 16 << 30   # the oracle's fp64 copy of the expert weights must fit in host RAM
+
+
+def _oracle_weights(w):
+    if w.E * (w.R1 * w.d + w.d * w.F) * 8 > HOST_F64_WEIGHTS_MAX:
+        return None
+    w1, w2 = syn.all_expert_weights(w)
+    return w1.astype(np.float64), w2.astype(np.float64)
+
+
+def _oracle_step(w, inp, Ts, weights, bwd):
     from oracle import moe_oracle as O
-    O.forward(x, w_r, bias, (w1_64, w2_64), k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments,
-              renormalize=w.renormalize, alpha=w.alpha)
+    kw = dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments, renormalize=w.renormalize,
+              alpha=w.alpha)
+    x = inp["x"][:Ts]
+    O.forward(x, inp["w_r"], inp["bias"], weights, **kw)
+    if bwd:
+        O.backward(x, inp["w_r"], inp["bias"], weights, inp["dy"][:Ts], **kw)
 
 
-def cpu_baseline(w, inp):
-    w1_64 = inp["w1"].astype(np.float64)
-    w2_64 = inp["w2"].astype(np.float64)
+def _oracle_batch(w, inp, weights, bwd, budget_s):
+    """Largest batch of the first Ts tokens (T halved until one step fits the budget)."""
+    Ts = w.T
+    while Ts > 64:
+        t0 = time.perf_counter()
+        _oracle_step(w.with_(T=Ts), inp, Ts, weights, bwd)
+        if time.perf_counter() - t0 <= budget_s:
+            break
+        Ts //= 2
+    return Ts
+
+
+def _sample_text(w, Ts, bwd):
+    what = "forward + backward" if bwd else "forward"
+    part = f"the full batch (T={w.T})" if Ts == w.T else f"the first {Ts} of the {w.T} tokens as one batch " \
+                                                          "(same capacity factor)"
+    return f"one {what} of {part} of {w.name}, fp64 numpy oracle, expert weights widened to fp64 before timing"
+
+
+def cpu_baseline(w, inp, bwd):
+    weights = _oracle_weights(w)
+    if weights is None:
+        return {"value": None, "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
+                "sample": f"not run: the oracle's fp64 expert weights of {w.name} exceed {HOST_F64_WEIGHTS_MAX >> 30} GiB "
+                          "of host memory"}
+    Ts = _oracle_batch(w, inp, weights, bwd, 20.0)
     t0 = time.perf_counter()
-    _oracle_step(w, inp["x"], inp["w_r"], inp["bias"], w1_64, w2_64)
+    _oracle_step(w.with_(T=Ts), inp, Ts, weights, bwd)
     dt = time.perf_counter() - t0
-    return {"value": round(w.T / dt, 1), "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
-            "sample": f"one full forward of the {WORKLOAD} batch (T={w.T}), fp64 numpy, weights widened to fp64 "
-                      f"before timing; {dt:.2f} s"}
+    return {"value": round(Ts / dt, 1), "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
+            "sample": _sample_text(w, Ts, bwd) + f"; {dt:.2f} s"}
 
 
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    w = syn.WORKLOADS[WORKLOAD]
-    inp = syn.make_inputs(w, dy=False)
-    w1_64 = inp["w1"].astype(np.float64)
-    w2_64 = inp["w2"].astype(np.float64)
+    w = syn.WORKLOADS[args.workload]
+    bwd = args.pass_ == "fwdbwd"
+    inp = syn.make_inputs(w, experts=False, dy=bwd)
+    weights = _oracle_weights(w)
+    if weights is None:
+        print(json.dumps({"impl": "reference", "unavailable": f"the oracle's fp64 expert weights of {w.name} do not "
+                                                              "fit in host memory"}), flush=True)
+        return
     budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    # calibrate a sub-batch size whose step fits the per-step budget
-    Ts = w.T
-    while Ts > 64:
-        ws = w.with_(T=Ts)
-        t0 = time.perf_counter()
-        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
-        if time.perf_counter() - t0 <= budget:
-            break
-        Ts //= 2
+    Ts = _oracle_batch(w, inp, weights, bwd, budget)
     ws = w.with_(T=Ts)
     for _ in range(args.warmup):
-        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
+        _oracle_step(ws, inp, Ts, weights, bwd)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(ws, inp["x"][:Ts], inp["w_r"], inp["bias"], w1_64, w2_64)
+        _oracle_step(ws, inp, Ts, weights, bwd)
     dt = time.perf_counter() - t0
     value = Ts * args.steps / dt
-    sample = (f"each step: the first {Ts} of the {w.T} tokens as one batch (same capacity factor), "
-              f"fp64 numpy oracle, weights widened to fp64 before timing")
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": WORKLOAD, "pass": "fwd", "T_sample": Ts},
+           "config": {"workload": w.name, "pass": args.pass_, "T_sample": Ts},
            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": _oracle_threads(),
-                            "kind": "oracle", "sample": sample},
+                            "kind": "oracle", "sample": "each step: " + _sample_text(w, Ts, bwd)},
            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
+
+
+BENCH_WORKLOADS = [n for n, w in syn.WORKLOADS.items() if w.dtype == "bf16"]
 
 
 def main(argv=None):
@@ -365,10 +478,15 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=BENCH_WORKLOADS, default=WORKLOAD)
+    ap.add_argument("--pass", dest="pass_", choices=["fwd", "fwdbwd"], default=None,
+                    help="default: fwdbwd for the workloads that include the backward pass, else fwd")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.pass_ is None:
+        args.pass_ = "fwdbwd" if syn.WORKLOADS[args.workload].backward else "fwd"
     if args.impl == "reference":
         run_reference(args)
     else:

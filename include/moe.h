@@ -101,7 +101,9 @@ int64_t moe_max_rows(const moe_config *cfg);
  * scratch, and the device error word). */
 moe_status moe_workspace_size(const moe_config *cfg, size_t *bytes);
 
-/* Clears the workspace's error word. Call once after allocating it. */
+/* Clears the workspace's error word, completion counters and statistics
+ * accumulators (its first few KB). Call once after allocating it; every
+ * call below leaves that region cleared again. */
 moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stream);
 
 /*
@@ -120,7 +122,9 @@ moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stre
  *   load       [E]     int32 out: number of tokens with e in their top-k
  *   aux_loss   [1]     fp32 out or NULL: alpha * E * sum_e f_e P_e with
  *                      f_e = load_e / (T k), P_e = importance_e / T
- * Reductions are in a fixed order: results are bitwise reproducible.
+ * Statistics are summed per block in a fixed order, then across blocks in
+ * integers (load) and 64-bit fixed point (importance, units of 2^-32): the
+ * results are bitwise reproducible whatever the order the blocks run in.
  */
 moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r,
                       const float *logit_bias, float *probs, int32_t *topk_idx,

@@ -1,5 +1,9 @@
 // Router part of the backward pass: gradient at the router logits, then the
-// two fp32 GEMMs for dW_r and the router's contribution to dX.
+// two GEMMs for dW_r and the router's contribution to dX. For bf16 layers the
+// GEMMs run on the tensor cores from exact bf16 parts of dh and W_r (a value
+// v in fp32 is h1 + h2 + h3 with h1 = bf16(v), h2 = bf16(v - h1),
+// h3 = bf16(v - h1 - h2), every subtraction exact), so the products keep
+// fp32 accuracy; fp32 layers use the CUDA-core fp32 GEMM.
 //
 // "Mixture of Experts (MoE) を1から解説 — Switch Transformerのルーティングと負荷
 // 分散": eq. (2) multiplies each selected expert's output by p_i, which is how
@@ -9,6 +13,7 @@
 // maps dp to dh = p * (dp - <p, dp>).
 #include "common.cuh"
 #include "kernels.h"
+#include "tma_host.h"
 
 namespace moe {
 
@@ -17,11 +22,34 @@ cudaError_t router_weight_grads(const Shape &sh, const float *dh, const void *x,
 
 namespace {
 
-// Warp per token; lane holds experts lane, lane + 32, ...
+// Exact split of an fp32 value into three bf16 parts.
+struct Parts3 {
+  bf16 h[3];
+};
+__device__ __forceinline__ Parts3 split3(float v) {
+  Parts3 q;
+  q.h[0] = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(q.h[0]);
+  q.h[1] = __float2bfloat16_rn(r1);
+  q.h[2] = __float2bfloat16_rn(r1 - __bfloat162float(q.h[1]));
+  return q;
+}
+
+// Which part of dh (A) and of W_r (B) each of the six EP-wide K blocks of the
+// dX_r GEMM pairs: (1,1) (1,2) (2,1) (1,3) (2,2) (3,1). Blocks 3..5 are
+// h1, h2, h3 in order, which the dW_r GEMM reads as its A operand.
+__constant__ int kPartA[6] = {0, 0, 1, 0, 1, 2};
+__constant__ int kPartB[6] = {0, 1, 0, 2, 1, 0};
+
+// Warp per token; lane holds experts lane, lane + 32, ... When a6 is given
+// (bf16 layers) the row of dh is also written as the six part blocks
+// a6[t, b * EP + e] (zero for e >= E), and offs2 = {0, T}.
 template <int EPT>
 __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, const int32_t *idx, const float *gate,
                                                         const int32_t *load, const float *dg, int T, int E, int k,
-                                                        int renorm, float alpha, float *dh) {
+                                                        int renorm, float alpha, float *dh, bf16 *a6, int EP,
+                                                        int32_t *offs2) {
+  if (a6 && blockIdx.x == 0 && threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
   const int lane = threadIdx.x & 31;
   const float aux_scale = alpha * (float)E / ((float)T * (float)T * (float)k);  // alpha E f_e / T = this * load_e
   float base[EPT];
@@ -74,27 +102,66 @@ __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, cons
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
       const int e = lane + 32 * j;
-      if (e < E) dh[(int64_t)t * E + e] = p[j] * (dp[j] - s);
+      const float v = p[j] * (dp[j] - s);
+      if (e < E) dh[(int64_t)t * E + e] = v;
+      if (a6 && e < EP) {
+        const Parts3 q = split3(e < E ? v : 0.0f);
+        bf16 *row = a6 + (int64_t)t * 6 * EP + e;
+#pragma unroll
+        for (int b = 0; b < 6; ++b) row[b * EP] = q.h[kPartA[b]];
+      }
     }
   }
+}
+
+// W_r [E, d] fp32 -> b6 [6 EP, d] bf16: block b holds part kPartB[b] (rows >= E zero).
+__global__ void __launch_bounds__(256) router_wsplit6_kernel(const float *w_r, int E, int EP, int d, bf16 *b6) {
+  const int64_t n = (int64_t)EP * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / d);
+    const Parts3 q = split3(e < E ? w_r[i] : 0.0f);
+#pragma unroll
+    for (int b = 0; b < 6; ++b) b6[b * n + i] = q.h[kPartB[b]];
+  }
+}
+
+// dW_r[e] = (h1^T x)[e] + (h2^T x)[e] + (h3^T x)[e], rows of c3 [3 EP, d].
+__global__ void __launch_bounds__(256) router_dwr_sum_kernel(const float *c3, int E, int EP, int d, float *dw_r) {
+  const int64_t n = (int64_t)E * d;
+  const int64_t part = (int64_t)EP * d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 4; i += (int64_t)gridDim.x * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4 *>(c3)[i];
+    const float4 b = reinterpret_cast<const float4 *>(c3 + part)[i];
+    const float4 c = reinterpret_cast<const float4 *>(c3 + 2 * part)[i];
+    reinterpret_cast<float4 *>(dw_r)[i] = make_float4(a.x + b.x + c.x, a.y + b.y + c.y, a.z + b.z + c.z,
+                                                      a.w + b.w + c.w);
+  }
+}
+
+int grid_for(int64_t n) {
+  const int64_t g = (n + 255) / 256;
+  const int cap = 4 * sm_count();
+  return (int)(g < cap ? (g > 0 ? g : 1) : cap);
 }
 
 }  // namespace
 
 cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *w_r, const float *probs,
                                    const int32_t *idx, const float *gate, const int32_t *load, const float *dg,
-                                   float *dh, float *dw_r, float *dxr, cudaStream_t stream) {
-  int sms = 148;
-  {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  }
+                                   float *dh, float *dw_r, float *dxr, void *ws, cudaStream_t stream) {
+  const bool tc = sh.dtype == MOE_BF16;
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  const int EP = router_plan(sh).ep;
+  bf16 *a6 = tc ? reinterpret_cast<bf16 *>(w + L.rg_a6) : nullptr;
+  bf16 *b6 = reinterpret_cast<bf16 *>(w + L.rg_b6);
+  float *c3 = reinterpret_cast<float *>(w + L.rg_c3);
+  int32_t *offs2 = reinterpret_cast<int32_t *>(w + L.rg_offs);
   int grid = (sh.T + 7) / 8;
-  if (grid > sms * 8) grid = sms * 8;
+  if (grid > sm_count() * 8) grid = sm_count() * 8;
 #define MOE_DH(EPT)                                                                                         \
   router_dh_kernel<EPT><<<grid, 256, 0, stream>>>(probs, idx, gate, load, dg, sh.T, sh.E, sh.k, sh.renorm, \
-                                                  sh.alpha, dh)
+                                                  sh.alpha, dh, a6, EP, offs2)
   if (sh.E <= 32) MOE_DH(1);
   else if (sh.E <= 64) MOE_DH(2);
   else if (sh.E <= 128) MOE_DH(4);
@@ -102,7 +169,14 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
 #undef MOE_DH
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  return router_weight_grads(sh, dh, x, w_r, dw_r, dxr, stream);
+  if (!tc) return router_weight_grads(sh, dh, x, w_r, dw_r, dxr, stream);
+  router_wsplit6_kernel<<<grid_for((int64_t)EP * sh.d), 256, 0, stream>>>(w_r, sh.E, EP, sh.d, b6);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  err = tc_router_grads(sh, EP, a6, b6, x, offs2, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status), stream);
+  if (err != cudaSuccess) return err;
+  router_dwr_sum_kernel<<<grid_for((int64_t)sh.E * sh.d / 4), 256, 0, stream>>>(c3, sh.E, EP, sh.d, dw_r);
+  return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -14,8 +14,9 @@
 // order, so the result is exact and reproducible. Two launches:
 //   1. per block of 256 tokens, a bitmap present[e][token] in shared memory
 //      and its per-expert popcounts; the last block to finish scans those
-//      counts over blocks for every expert (block bases), and derives
-//      kept = min(load, C) and the group offsets (exclusive scan over experts);
+//      counts over blocks for every expert (block bases, one warp per expert
+//      and 32 blocks per shuffle scan), and derives kept = min(load, C) and
+//      the group offsets (exclusive scan over experts);
 //   2. per block of 32 tokens, rank = block base + popcount of the bitmap
 //      below the token, slot = rank if rank < C else -1, and the copy of the
 //      token's row to each of its kept rows with 16-byte loads and stores
@@ -77,22 +78,47 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
   __syncthreads();
   if (!last) return;
   __threadfence();
-  const int e = threadIdx.x, lane = e & 31, warp = e >> 5;
-  int run = 0;
-  if (e < E) {
-    // eight counts in flight per step, then the running sums
-    for (int b0 = 0; b0 < (int)gridDim.x; b0 += 8) {
-      int c[8];
+  // Block bases: per expert, an exclusive scan of the blocks' counts in block
+  // order. A warp scans one expert at a time, 32 blocks per step; the loads of
+  // all the warp's experts are issued before any is scanned.
+  __shared__ int total[256];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nb = (int)gridDim.x;
+  constexpr int EPW = 256 / (DT / 32);  // experts per warp at most (E <= 256, 8 warps)
+  int carry[EPW];
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        c[u] = (b0 + u < (int)gridDim.x) ? __ldcg(block_counts + (int64_t)(b0 + u) * E + e) : 0;
+  for (int i = 0; i < EPW; ++i) carry[i] = 0;
+  for (int b0 = 0; b0 < nb; b0 += 32) {
+    const int b = b0 + lane;
+    int c[EPW];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (b0 + u < (int)gridDim.x) block_base[(int64_t)(b0 + u) * E + e] = run;
-        run += c[u];
+    for (int i = 0; i < EPW; ++i) {
+      const int e = warp + 8 * i;
+      c[i] = (e < E && b < nb) ? __ldcg(block_counts + (int64_t)b * E + e) : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < EPW; ++i) {
+      const int e = warp + 8 * i;
+      if (e >= E) break;
+      int incl = c[i];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
       }
+      if (b < nb) block_base[(int64_t)b * E + e] = carry[i] + incl - c[i];
+      carry[i] += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
+#pragma unroll
+  for (int i = 0; i < EPW; ++i) {
+    const int e = warp + 8 * i;
+    if (e < E && lane == 0) total[e] = carry[i];
+  }
+  __syncthreads();
+  // kept = min(load, C) and the group offsets (exclusive scan over experts)
+  const int e = threadIdx.x;
+  const int run = (e < E) ? total[e] : 0;
   const int kept = (e < E) ? ((C >= 0 && (int64_t)run > C) ? (int)C : run) : 0;
   int incl = kept;
 #pragma unroll

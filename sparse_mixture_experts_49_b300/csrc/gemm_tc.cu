@@ -16,8 +16,9 @@
 //              (weight gradients; K is the group size, which varies).
 // Tile 128 x 256 x 64 (bf16, fp32 accumulator in TMEM), 4-stage TMA ring,
 // warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
-// warps 2-5 epilogue. Two TMEM accumulators let the epilogue of one tile run
-// under the MMAs of the next.
+// warps 2-9 epilogue (two per TMEM lane quarter, one per column half). Two
+// TMEM accumulators let the epilogue of one tile run under the MMAs of the
+// next.
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -34,7 +35,7 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAX_E = 256;
 
 struct __align__(8) Smem {
@@ -55,7 +56,7 @@ struct Args {
   int E;
   int M, N, K;             // grouped-M: N (output columns), K; grouped-K: M, N
   int F;                   // SwiGLU: offset of the up half (rows of W1, columns of pre_act / dA)
-  bf16 *C;
+  void *C;                 // bf16, or fp32 for EPI_STORE_F32
   int64_t ldc;
   int64_t sce;             // grouped-K: C_e = C + e * sce
   bf16 *C2;                // SwiGLU forward: pre-activations [rows, 2F]
@@ -107,7 +108,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-      for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], 4); }
+      for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], 8); }
       mbar_init(&s.drain, 1);
       s.abort_flag = 0;
       fence_barrier_init();
@@ -267,9 +268,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       drain_wait(&s.drain, 0);
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    // ---------------------------------------------------------------- epilogue (warps 2..9)
+    // Two warps per TMEM lane quarter: warp w reads lanes 32 (w % 4) .. + 31
+    // (its rows) and the column half (w - 2) / 4 of the tile.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // row inside the 128-row tile
+    const int half = (warp - 2) >> 2;  // column half of the tile
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -285,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int64_t row = (int64_t)s.off[e] + mt * BM + r;
         if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 2 * half; c < 2 * half + 2; ++c) {
             const int col = nt * 128 + c * 32;
             tmem_ld32(t_row + c * 32, v);
             tmem_ld32(t_row + 128 + c * 32, w);
@@ -293,7 +297,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               float hv[32];
 #pragma unroll
               for (int i = 0; i < 32; ++i) hv[i] = silu_f(v[i]) * w[i];
-              bf16 *hp = p.C + row * p.ldc + col;
+              bf16 *hp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
 #pragma unroll
               for (int i = 0; i < 4; ++i) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
               if (p.C2) {
@@ -308,52 +312,77 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         } else {
+          // The backward epilogues read saved activations; the loads of G
+          // chunks are issued together before any of them is used.
+          constexpr int NAUX = (EPI == EPI_SWIGLU_BWD) ? 8 : (EPI == EPI_RELU_BWD ? 4 : 0);  // uint4 per chunk
+          constexpr int G = (EPI == EPI_SWIGLU_BWD) ? 2 : 4;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
-            const int col = nt * BN + c * 32;
-            tmem_ld32(t_row + c * 32, v);
-            if (!valid || col >= p.N) continue;
-            if (EPI == EPI_RELU) {
+          for (int c0 = 4 * half; c0 < 4 * half + 4; c0 += G) {
+            uint4 aux[NAUX > 0 ? G * NAUX : 1];
+            if (NAUX > 0) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
-            } else if (EPI == EPI_RELU_BWD) {
-              const bf16 *hp = p.aux + row * p.ldaux + col;
+              for (int g = 0; g < G; ++g) {
+                const int col = nt * BN + (c0 + g) * 32;
+                if (valid && col < p.N) {
+                  const bf16 *ap = p.aux + row * p.ldaux + col;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) Vec16<bf16>::load(hp + 8 * i, w + 8 * i);
+                  for (int i = 0; i < 4; ++i) aux[g * NAUX + i] = *reinterpret_cast<const uint4 *>(ap + 8 * i);
+                  if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = (w[i] > 0.0f) ? v[i] : 0.0f;
-            } else if (EPI == EPI_SWIGLU_BWD) {
-              const bf16 *gp = p.aux + row * p.ldaux + col;
-              const bf16 *up = gp + p.F;
-              float gu[32];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                Vec16<bf16>::load(gp + 8 * i, w + 8 * i);
-                Vec16<bf16>::load(up + 8 * i, gu + 8 * i);
+                    for (int i = 0; i < 4; ++i)
+                      aux[g * NAUX + 4 + i] = *reinterpret_cast<const uint4 *>(ap + p.F + 8 * i);
+                  }
+                }
               }
-              float dup[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const float g = w[i], u = gu[i];
-                const float sg = 1.0f / (1.0f + expf(-g));
-                dup[i] = v[i] * g * sg;                                  // dU = dH * silu(G)
-                v[i] = v[i] * u * (sg * (1.0f + g * (1.0f - sg)));      // dG = dH * U * silu'(G)
-              }
-              bf16 *dp2 = p.C + row * p.ldc + p.F + col;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(dp2 + 8 * i, dup + 8 * i);
             }
-            bf16 *cp = p.C + row * p.ldc + col;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+            for (int g = 0; g < G; ++g) {
+              const int col = nt * BN + (c0 + g) * 32;
+              tmem_ld32(t_row + (c0 + g) * 32, v);
+              if (!valid || col >= p.N) continue;
+              if (EPI == EPI_RELU) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+              } else if (EPI == EPI_RELU_BWD) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Vec16<bf16>::unpack(aux[g * NAUX + i], w + 8 * i);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = (w[i] > 0.0f) ? v[i] : 0.0f;
+              } else if (EPI == EPI_SWIGLU_BWD) {
+                bf16 *dp2 = static_cast<bf16 *>(p.C) + row * p.ldc + p.F + col;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  float gg[8], uu[8], du[8];
+                  Vec16<bf16>::unpack(aux[g * NAUX + i], gg);
+                  Vec16<bf16>::unpack(aux[g * NAUX + 4 + i], uu);
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) {
+                    const float sg = 1.0f / (1.0f + expf(-gg[j]));
+                    const float dh = v[8 * i + j];
+                    du[j] = dh * gg[j] * sg;                                      // dU = dH * silu(G)
+                    v[8 * i + j] = dh * uu[j] * (sg * (1.0f + gg[j] * (1.0f - sg)));  // dG = dH * U * silu'(G)
+                  }
+                  Vec16<bf16>::store(dp2 + 8 * i, du);
+                }
+              }
+              if (EPI == EPI_STORE_F32) {
+                float *cp = static_cast<float *>(p.C) + row * p.ldc + col;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, v + 4 * i);
+              } else {
+                bf16 *cp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+              }
+            }
           }
         }
       } else {
         const bool empty_group = s.off[e + 1] == s.off[e];
         const int m = mt * BM + r;
-        bf16 *cbase = p.C + (int64_t)e * p.sce + (int64_t)m * p.ldc;
+        const int64_t cofs = (int64_t)e * p.sce + (int64_t)m * p.ldc;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
           const int col = nt * BN + c * 32;
           if (!empty_group) tmem_ld32(t_row + c * 32, v);
           else {
@@ -361,8 +390,15 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
           if (m < p.M && col < p.N) {
+            if (EPI == EPI_STORE_F32) {
+              float *cp = static_cast<float *>(p.C) + cofs + col;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cbase + col + 8 * i, v + 8 * i);
+              for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, v + 4 * i);
+            } else {
+              bf16 *cp = static_cast<bf16 *>(p.C) + cofs + col;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+            }
           }
         }
       }
@@ -413,7 +449,7 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
     return cudaErrorInvalidValue;
   a.N = sh.F;
   a.K = sh.d;
-  a.C = (bf16 *)h;
+  a.C = h;
   a.ldc = sh.F;
   cudaError_t err;
   if (sh.act == MOE_ACT_SWIGLU) {
@@ -434,7 +470,7 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   b.st = st;
   b.N = sh.d;
   b.K = sh.F;
-  b.C = (bf16 *)y_perm;
+  b.C = y_perm;
   b.ldc = sh.d;
   return launch<0, 0, 0, EPI_STORE>(ma, mb, b, stream);
 }
@@ -452,7 +488,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.N = sh.F; a.K = sh.d;
-    a.C = (bf16 *)da; a.ldc = sh.R1;
+    a.C = da; a.ldc = sh.R1;
     if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 64))
       return cudaErrorInvalidValue;
     if (swiglu) {
@@ -469,7 +505,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.d; a.N = sh.F;
-    a.C = (bf16 *)dw2; a.ldc = sh.F; a.sce = (int64_t)sh.d * sh.F;
+    a.C = dw2; a.ldc = sh.F; a.sce = (int64_t)sh.d * sh.F;
     if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 64) || !make_map_2d(&mb, h, sh.F, rows, 64, 64))
       return cudaErrorInvalidValue;
     err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
@@ -480,7 +516,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.N = sh.d; a.K = sh.R1;
-    a.C = (bf16 *)dxp; a.ldc = sh.d;
+    a.C = dxp; a.ldc = sh.d;
     if (!make_map_2d(&ma, da, sh.R1, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 64))
       return cudaErrorInvalidValue;
     err = launch<0, 0, 1, EPI_STORE>(ma, mb, a, stream);
@@ -491,10 +527,48 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.R1; a.N = sh.d;
-    a.C = (bf16 *)dw1; a.ldc = sh.d; a.sce = (int64_t)sh.R1 * sh.d;
+    a.C = dw1; a.ldc = sh.d; a.sce = (int64_t)sh.R1 * sh.d;
     if (!make_map_2d(&ma, da, sh.R1, rows, 64, 64) || !make_map_2d(&mb, x_perm, sh.d, rows, 64, 64))
       return cudaErrorInvalidValue;
     err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
+  }
+  return err;
+}
+
+// Router gradient GEMMs of a bf16 layer on the tensor cores, from exact bf16
+// parts (dh = h1 + h2 + h3, W_r = w1 + w2 + w3):
+//   dXr [T, d] fp32 = A6 [T, 6EP] * B6 [6EP, d], where the six EP-wide blocks
+//     pair (h1,w1) (h1,w2) (h2,w1) (h1,w3) (h2,w2) (h3,w1); the pairs left out
+//     are below 2^-24 of the result;
+//   C3 [3EP, d] fp32 = A6[:, 3EP:6EP]^T x, i.e. h1^T x, h2^T x and h3^T x
+//     (x is bf16, so every product is exact), summed into dW_r afterwards.
+// offs2 = {0, T}: both GEMMs run as one group of T rows.
+cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void *b6, const void *x,
+                            const int32_t *offs2, float *dxr, float *c3, DeviceStatus *st, cudaStream_t stream) {
+  using namespace tc;
+  CUtensorMap ma, mb;
+  cudaError_t err;
+  {
+    Args a{};
+    a.offsets = offs2; a.E = 1; a.F = 0; a.st = st;
+    a.N = sh.d; a.K = 6 * ep;
+    a.C = dxr; a.ldc = sh.d;
+    if (!make_map_2d(&ma, a6, 6 * (uint64_t)ep, sh.T, 64, 128) ||
+        !make_map_3d(&mb, b6, sh.d, 6 * (uint64_t)ep, 1, 64, 64))
+      return cudaErrorInvalidValue;
+    err = launch<0, 0, 1, EPI_STORE_F32>(ma, mb, a, stream);
+    if (err != cudaSuccess) return err;
+  }
+  {
+    Args a{};
+    a.offsets = offs2; a.E = 1; a.F = 0; a.st = st;
+    a.M = 3 * ep; a.N = sh.d;
+    a.C = c3; a.ldc = sh.d; a.sce = 0;
+    if (!make_map_2d_strided(&ma, static_cast<const bf16 *>(a6) + 3 * ep, 3 * (uint64_t)ep, sh.T,
+                             6 * (uint64_t)ep * 2, 64, 64) ||
+        !make_map_2d(&mb, x, sh.d, sh.T, 64, 64))
+      return cudaErrorInvalidValue;
+    err = launch<1, 1, 1, EPI_STORE_F32>(ma, mb, a, stream);
   }
   return err;
 }

@@ -19,19 +19,23 @@ struct Shape {
   int elt;        // bytes per element of the x dtype
 };
 
-enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4 };
+enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4, EPI_STORE_F32 = 5 };
 
 // Workspace carve-up (byte offsets from the workspace base). The first 256
 // bytes hold the error word (offset 0), the router's completion counter (64)
-// and the dispatch's completion counter (128); all start at zero.
+// and the dispatch's completion counter (128); the router's statistics
+// accumulators follow. All of [0, zeroed) starts at zero (moe_workspace_init)
+// and every call leaves it at zero again.
 struct WsLayout {
   size_t status;                 // DeviceStatus
-  size_t router_imp, router_load;  // [router blocks, E] partial sums
+  size_t router_acc;               // [E] u64 importance (units of 2^-32), then [E] int32 load
+  size_t zeroed;                   // end of the region that must start at zero
   size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
   size_t router_partial;           // [splits, T, EP] fp32 partial logits (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
-  size_t dg, dh, dxr, dwr_acc;     // backward: [T, k], [T, E], [T, d] fp32
+  size_t dg, dh, dxr;              // backward: [T, k], [T, E], [T, d] fp32
+  size_t rg_a6, rg_b6, rg_c3, rg_offs;  // bf16 router gradient: [T, 6EP], [6EP, d] bf16; [3EP, d] fp32; {0, T}
   size_t total;
 };
 WsLayout ws_layout(const Shape &sh);
@@ -84,13 +88,18 @@ cudaError_t simt_expert_backward(const Shape &sh, const int32_t *offsets, const 
                                  const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
                                  void *dxp, void *dw1, void *dw2, cudaStream_t stream);
 
+// Router gradient GEMMs of a bf16 layer on the tensor cores (exact bf16 parts
+// of dh and W_r; see gemm_tc.cu).
+cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void *b6, const void *x,
+                            const int32_t *offs2, float *dxr, float *c3, DeviceStatus *st, cudaStream_t stream);
+
 // Backward pieces outside the grouped GEMMs.
 cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
                                     const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp,
                                     float *dg, cudaStream_t stream);
 cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *w_r, const float *probs,
                                    const int32_t *idx, const float *gate, const int32_t *load, const float *dg,
-                                   float *dh, float *dw_r, float *dxr, cudaStream_t stream);
+                                   float *dh, float *dw_r, float *dxr, void *ws, cudaStream_t stream);
 cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr,
                              const int32_t *idx, const int32_t *slot, const int32_t *offsets, void *dx,
                              cudaStream_t stream);

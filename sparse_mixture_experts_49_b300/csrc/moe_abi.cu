@@ -63,9 +63,9 @@ WsLayout ws_layout(const Shape &sh) {
     return at;
   };
   L.status = take(256);
-  const size_t rb = (size_t)router_blocks(sh), db = (size_t)dispatch_blocks(sh);
-  L.router_imp = take(rb * sh.E * 4);
-  L.router_load = take(rb * sh.E * 4);
+  const size_t db = (size_t)dispatch_blocks(sh);
+  L.router_acc = take((size_t)sh.E * 12);
+  L.zeroed = o;
   const RouterPlan rp = router_plan(sh);
   L.router_parts = take(rp.tensor_cores ? (size_t)3 * rp.ep * sh.d * 2 : 0);
   L.router_partial = take(rp.tensor_cores ? (size_t)rp.splits * sh.T * rp.ep * 4 : 0);
@@ -78,7 +78,11 @@ WsLayout ws_layout(const Shape &sh) {
   L.dg = take((size_t)sh.T * sh.k * 4);
   L.dh = take((size_t)sh.T * sh.E * 4);
   L.dxr = take((size_t)sh.T * sh.d * 4);
-  L.dwr_acc = 0;
+  const bool tc = sh.dtype == MOE_BF16;
+  L.rg_a6 = take(tc ? (size_t)sh.T * 6 * rp.ep * 2 : 0);
+  L.rg_b6 = take(tc ? (size_t)6 * rp.ep * sh.d * 2 : 0);
+  L.rg_c3 = take(tc ? (size_t)3 * rp.ep * sh.d * 4 : 0);
+  L.rg_offs = take(tc ? 8 : 0);
   L.total = o;
   return L;
 }
@@ -138,7 +142,7 @@ moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stre
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(ws);
-  return cuda_status(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_layout(sh).zeroed, (cudaStream_t)stream));
 }
 
 moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
@@ -219,7 +223,7 @@ moe_status moe_backward(const moe_config *cfg, const moe_saved *sv, const void *
                                                   sv->pre_act, sv->h, dyp, da, dxp, dw1, dw2, s);
   if (e != cudaSuccess) return cuda_status(e);
   e = launch_router_backward(sh, sv->x, sv->w_r, sv->probs, sv->topk_idx, sv->topk_gate, sv->load, dg, dh, dw_r,
-                             dxr, s);
+                             dxr, ws, s);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_unpermute(sh, dy, dxp, dxr, sv->topk_idx, sv->slot, sv->expert_offsets, dx, s));
 }

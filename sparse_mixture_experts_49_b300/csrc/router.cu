@@ -19,9 +19,13 @@
 //
 // Selection: one warp per token, softmax in fp32 with the row maximum
 // subtracted, then k rounds of a warp arg-max (descending logit, ties to the
-// lower index). Importance and load are reduced per block in a fixed order;
-// the last block to finish reduces the blocks' partials in block order, so
-// the statistics are bitwise reproducible.
+// lower index). Importance and load are summed per block in a fixed order;
+// each block then adds its sums into per-expert accumulators in the
+// workspace: the loads as 32-bit integers, the importance as 64-bit fixed
+// point (units of 2^-32). Integer addition is associative, so the totals do
+// not depend on the order in which blocks arrive and the statistics are
+// bitwise reproducible. The last block to finish converts the totals, forms
+// the aux loss with a fixed-shape tree and clears the accumulators.
 #include <cfloat>
 
 #include "common.cuh"
@@ -42,8 +46,8 @@ struct RouterArgs {
   float *probs;
   int32_t *idx;
   float *gate;
-  float *part_imp;    // [blocks, E]
-  int32_t *part_load; // [blocks, E]
+  unsigned long long *acc_imp;  // [E] importance in units of 2^-32
+  int32_t *acc_load;             // [E]
   int T, d, E, k, renorm;
 };
 
@@ -150,16 +154,19 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
     float s = 0.0f;
 #pragma unroll
     for (int w = 0; w < 8; ++w) s += impw[w * EP + e];
-    a.part_imp[(int64_t)blockIdx.x * E + e] = s;
-    a.part_load[(int64_t)blockIdx.x * E + e] = cnt[e];
+    // s <= 8 * TPW tokens, so s * 2^32 < 2^41: exact to 2^-33 in a 64-bit integer
+    const unsigned long long q = (unsigned long long)llrint((double)s * 4294967296.0);
+    if (q) atomicAdd(a.acc_imp + e, q);
+    if (cnt[e]) atomicAdd(a.acc_load + e, cnt[e]);
   }
 }
 
-// Run by every block after it wrote its partial statistics: the last block to
-// arrive reduces them (per expert, blocks in order) into importance and load,
-// sums the aux terms as a fixed-shape tree, and re-arms the counter.
-__device__ __forceinline__ void finish_if_last(const RouterArgs &a, int nblk, float alpha, float *importance,
-                                               int32_t *load, float *aux, unsigned int *counter) {
+// Run by every block after it added its statistics: the last block to arrive
+// converts the accumulated importance and load, sums the aux terms as a
+// fixed-shape tree, and clears the accumulators and the counter for the next
+// call.
+__device__ __forceinline__ void finish_if_last(const RouterArgs &a, float alpha, float *importance, int32_t *load,
+                                               float *aux, unsigned int *counter) {
   __shared__ bool last;
   __shared__ float term[256];
   __threadfence();
@@ -171,23 +178,11 @@ __device__ __forceinline__ void finish_if_last(const RouterArgs &a, int nblk, fl
   const int e = threadIdx.x;
   float v = 0.0f;
   if (e < a.E) {
-    float s = 0.0f;
-    int c = 0;
-    for (int b0 = 0; b0 < nblk; b0 += 8) {
-      float ps[8];
-      int pc[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const bool in = b0 + u < nblk;
-        ps[u] = in ? __ldcg(a.part_imp + (int64_t)(b0 + u) * a.E + e) : 0.0f;
-        pc[u] = in ? __ldcg(a.part_load + (int64_t)(b0 + u) * a.E + e) : 0;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        s += ps[u];
-        c += pc[u];
-      }
-    }
+    const unsigned long long q = __ldcg(a.acc_imp + e);
+    const int c = __ldcg(a.acc_load + e);
+    const float s = (float)((double)q * (1.0 / 4294967296.0));
+    a.acc_imp[e] = 0ull;
+    a.acc_load[e] = 0;
     importance[e] = s;
     load[e] = c;
     v = ((float)c / ((float)a.T * (float)a.k)) * (s / (float)a.T);
@@ -279,7 +274,7 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a, co
   for (int e = tid; e < EP; e += 256) cnt[e] = 0;
   __syncthreads();
   select_block<EPT, 8>(lg, impw, cnt, a, t0);
-  finish_if_last(a, gridDim.x, so.alpha, so.importance, so.load, so.aux, so.counter);
+  finish_if_last(a, so.alpha, so.importance, so.load, so.aux, so.counter);
 }
 
 // ---------------------------------------------------------------- tensor-core path (bf16 layers)
@@ -496,7 +491,7 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float *partial
   for (int e = threadIdx.x; e < EP; e += 256) cnt[e] = 0;
   __syncthreads();
   select_block<EPT, RT_TC / 8>(lg, impw, cnt, a, t0);
-  finish_if_last(a, gridDim.x, so.alpha, so.importance, so.load, so.aux, so.counter);
+  finish_if_last(a, so.alpha, so.importance, so.load, so.aux, so.counter);
 }
 
 template <typename K>
@@ -562,8 +557,8 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   uint8_t *w = static_cast<uint8_t *>(ws);
   RouterArgs a;
   a.x = x; a.w_r = w_r; a.bias = bias; a.probs = probs; a.idx = idx; a.gate = gate;
-  a.part_imp = reinterpret_cast<float *>(w + L.router_imp);
-  a.part_load = reinterpret_cast<int32_t *>(w + L.router_load);
+  a.acc_imp = reinterpret_cast<unsigned long long *>(w + L.router_acc);
+  a.acc_load = reinterpret_cast<int32_t *>(w + L.router_acc + 8 * (size_t)sh.E);
   a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
   const int nblk = router_blocks(sh);
   const RouterPlan plan = router_plan(sh);

@@ -32,10 +32,15 @@ EncodeTiledFn get_encoder() {
 
 bool make_map_2d(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
                  uint32_t box_outer) {
+  return make_map_2d_strided(m, ptr, inner, outer, inner * 2, box_inner, box_outer);
+}
+
+bool make_map_2d_strided(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint64_t row_stride_bytes,
+                         uint32_t box_inner, uint32_t box_outer) {
   EncodeTiledFn enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * 2};
+  cuuint64_t strides[1] = {row_stride_bytes};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t es[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
