@@ -39,9 +39,9 @@ L2_FLUSH_BYTES = 256 << 20
 # kernels of the library per forward step of the bf16 layer: router (W_r split, tensor-core logits,
 # selection + statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1
 LAUNCHES_PER_STEP = 8
-# moe_backward of the bf16 layer: combine backward 1, grouped GEMMs 4, router logit gradient 1, router weight
-# gradients 2, unpermute-reduce 1
-LAUNCHES_BACKWARD = 9
+# moe_backward of the bf16 layer: combine backward 1, grouped GEMMs 4, router logit gradient 1, W_r split 1,
+# router gradient GEMMs 2, dW_r part sum 1, unpermute-reduce 1
+LAUNCHES_BACKWARD = 11
 
 
 def load_peaks():

@@ -159,24 +159,24 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   int32_t *offs2 = reinterpret_cast<int32_t *>(w + L.rg_offs);
   int grid = (sh.T + 7) / 8;
   if (grid > sm_count() * 8) grid = sm_count() * 8;
-#define MOE_DH(EPT)                                                                                         \
-  router_dh_kernel<EPT><<<grid, 256, 0, stream>>>(probs, idx, gate, load, dg, sh.T, sh.E, sh.k, sh.renorm, \
-                                                  sh.alpha, dh, a6, EP, offs2)
+  cudaError_t err;
+#define MOE_DH(EPT)                                                                                            \
+  err = launch_kernel(router_dh_kernel<EPT>, dim3(grid), dim3(256), 0, stream, probs, idx, gate, load, dg, sh.T, sh.E, \
+                   sh.k, sh.renorm, sh.alpha, dh, a6, EP, offs2)
   if (sh.E <= 32) MOE_DH(1);
   else if (sh.E <= 64) MOE_DH(2);
   else if (sh.E <= 128) MOE_DH(4);
   else MOE_DH(8);
 #undef MOE_DH
-  cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   if (!tc) return router_weight_grads(sh, dh, x, w_r, dw_r, dxr, stream);
-  router_wsplit6_kernel<<<grid_for((int64_t)EP * sh.d), 256, 0, stream>>>(w_r, sh.E, EP, sh.d, b6);
-  err = cudaGetLastError();
+  err = launch_kernel(router_wsplit6_kernel, dim3(grid_for((int64_t)EP * sh.d)), dim3(256), 0, stream, w_r, sh.E, EP,
+                   sh.d, b6);
   if (err != cudaSuccess) return err;
   err = tc_router_grads(sh, EP, a6, b6, x, offs2, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status), stream);
   if (err != cudaSuccess) return err;
-  router_dwr_sum_kernel<<<grid_for((int64_t)sh.E * sh.d / 4), 256, 0, stream>>>(c3, sh.E, EP, sh.d, dw_r);
-  return cudaGetLastError();
+  return launch_kernel(router_dwr_sum_kernel, dim3(grid_for((int64_t)sh.E * sh.d / 4)), dim3(256), 0, stream, c3, sh.E,
+                    EP, sh.d, dw_r);
 }
 
 }  // namespace moe

@@ -195,27 +195,26 @@ int token_grid(int T) {
 }  // namespace
 
 template <typename XT, int KMAX>
-void run_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
-                 const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
-  combine_kernel<XT, KMAX><<<token_grid(sh.T), 256, 0, stream>>>((const XT *)x, (const XT *)y_perm, idx, gate, slot,
-                                                                 offsets, sh.T, sh.d, sh.k, (XT *)out);
+cudaError_t run_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
+                        const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
+  return launch_kernel(combine_kernel<XT, KMAX>, dim3(token_grid(sh.T)), dim3(256), 0, stream, (const XT *)x,
+                    (const XT *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (XT *)out);
 }
 
 template <typename XT>
-void run_combine_k(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
-                   const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
-  if (sh.k == 1) run_combine<XT, 1>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
-  else if (sh.k == 2) run_combine<XT, 2>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
-  else if (sh.k <= 4) run_combine<XT, 4>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
-  else run_combine<XT, 8>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+cudaError_t run_combine_k(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
+                          const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
+  if (sh.k == 1) return run_combine<XT, 1>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  if (sh.k == 2) return run_combine<XT, 2>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  if (sh.k <= 4) return run_combine<XT, 4>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  return run_combine<XT, 8>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
 }
 
 cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
                            const float *gate, const int32_t *slot, const int32_t *offsets, void *out,
                            cudaStream_t stream) {
-  if (sh.dtype == MOE_BF16) run_combine_k<bf16>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
-  else run_combine_k<float>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
-  return cudaGetLastError();
+  if (sh.dtype == MOE_BF16) return run_combine_k<bf16>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
+  return run_combine_k<float>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
 }
 
 cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
@@ -223,12 +222,10 @@ cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void 
                                     float *dg, cudaStream_t stream) {
   const int grid = token_grid(sh.T);
   if (sh.dtype == MOE_BF16)
-    combine_backward_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)dy, (const bf16 *)y_perm, idx, gate,
-                                                            slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dyp, dg);
-  else
-    combine_backward_kernel<float><<<grid, 256, 0, stream>>>((const float *)dy, (const float *)y_perm, idx, gate,
-                                                             slot, offsets, sh.T, sh.d, sh.k, (float *)dyp, dg);
-  return cudaGetLastError();
+    return launch_kernel(combine_backward_kernel<bf16>, dim3(grid), dim3(256), 0, stream, (const bf16 *)dy,
+                      (const bf16 *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dyp, dg);
+  return launch_kernel(combine_backward_kernel<float>, dim3(grid), dim3(256), 0, stream, (const float *)dy,
+                    (const float *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (float *)dyp, dg);
 }
 
 cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr,
@@ -236,12 +233,10 @@ cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, c
                              cudaStream_t stream) {
   const int grid = token_grid(sh.T);
   if (sh.dtype == MOE_BF16)
-    unpermute_kernel<bf16><<<grid, 256, 0, stream>>>((const bf16 *)dy, (const bf16 *)dxp, dxr, idx, slot, offsets,
-                                                     sh.T, sh.d, sh.k, (bf16 *)dx);
-  else
-    unpermute_kernel<float><<<grid, 256, 0, stream>>>((const float *)dy, (const float *)dxp, dxr, idx, slot,
-                                                      offsets, sh.T, sh.d, sh.k, (float *)dx);
-  return cudaGetLastError();
+    return launch_kernel(unpermute_kernel<bf16>, dim3(grid), dim3(256), 0, stream, (const bf16 *)dy, (const bf16 *)dxp,
+                      dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dx);
+  return launch_kernel(unpermute_kernel<float>, dim3(grid), dim3(256), 0, stream, (const float *)dy,
+                    (const float *)dxp, dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (float *)dx);
 }
 
 }  // namespace moe

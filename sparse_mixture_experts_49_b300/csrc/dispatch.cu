@@ -17,11 +17,12 @@
 //      counts over blocks for every expert (block bases, one warp per expert
 //      and 32 blocks per shuffle scan), and derives kept = min(load, C) and
 //      the group offsets (exclusive scan over experts);
-//   2. per block of 32 tokens, rank = block base + popcount of the bitmap
-//      below the token, slot = rank if rank < C else -1, and the copy of the
-//      token's row to each of its kept rows with 16-byte loads and stores
-//      (small blocks spread the copy over eight times more SMs; each thread
-//      keeps eight 16-byte loads in flight).
+//      The same kernel writes each pair's rank inside its block (popcount of
+//      the bitmap below the token) into slot;
+//   2. per block of 32 tokens, rank = block base + that rank, slot = rank if
+//      rank < C else -1, and the copy of the token's row to each of its kept
+//      rows with 16-byte loads and stores (small blocks spread the copy over
+//      eight times more SMs; each thread keeps eight 16-byte loads in flight).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -56,12 +57,14 @@ __device__ __forceinline__ void build_bitmap(uint32_t *present, const int32_t *_
   __syncthreads();
 }
 
-// Per-block expert counts; the last block scans them into block bases and
-// writes kept[] and the group offsets.
+// Per-block expert counts and each pair's rank inside its block (written to
+// local_rank, which is the caller's slot array); the last block scans the
+// counts into block bases and writes kept[] and the group offsets.
 __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__restrict__ idx, int T, int E, int k,
                                                             int64_t C, int32_t *block_counts, int32_t *block_base,
                                                             int32_t *kept_out, int32_t *offsets_out,
-                                                            unsigned int *counter, DeviceStatus *st) {
+                                                            int32_t *__restrict__ local_rank, unsigned int *counter,
+                                                            DeviceStatus *st) {
   extern __shared__ uint32_t present[];
   __shared__ bool last;
   __shared__ int warp_sums[8];
@@ -71,6 +74,27 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
 #pragma unroll
     for (int w = 0; w < WORDS; ++w) c += __popc(present[e * WORDS + w]);
     block_counts[(int64_t)blockIdx.x * E + e] = c;
+  }
+  {
+    // rank of each of this thread's pairs among the block's tokens that chose
+    // the same expert (popcount of the bitmap below the token), or -1 for a
+    // pair the bitmap left out (bad index, or a repeat within the token)
+    const int t = blockIdx.x * DT + threadIdx.x;
+    const int word = threadIdx.x >> 5;
+    const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
+    if (t < T) {
+      for (int j = 0; j < k; ++j) {
+        const int e = idx[(int64_t)t * k + j];
+        bool ok = (e >= 0 && e < E);
+        for (int jj = 0; ok && jj < j; ++jj) ok = idx[(int64_t)t * k + jj] != e;
+        int r = -1;
+        if (ok) {
+          r = __popc(present[e * WORDS + word] & below);
+          for (int w = 0; w < word; ++w) r += __popc(present[e * WORDS + w]);
+        }
+        local_rank[(int64_t)t * k + j] = r;
+      }
+    }
   }
   __threadfence();
   __syncthreads();
@@ -138,9 +162,9 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
   if (threadIdx.x == 0) *counter = 0u;
 }
 
-// Slots, row owners and the row copies for 32 tokens. The bitmap covers the
-// whole 256-token counting block the 64 tokens sit in, because ranks count
-// every earlier token of that block.
+// Slots, row owners and the row copies for 32 tokens: rank = block base +
+// the rank inside the 256-token block that the counting kernel left in slot;
+// slot = rank if rank < C else -1.
 template <typename XT>
 __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict__ x, const int32_t *__restrict__ idx,
                                                             int T, int d, int E, int k, int64_t C,
@@ -148,57 +172,38 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
                                                             const int32_t *__restrict__ offsets,
                                                             int32_t *__restrict__ slot, int32_t *__restrict__ row_token,
                                                             XT *__restrict__ x_perm) {
-  extern __shared__ uint32_t present[];           // [E][WORDS]
-  __shared__ int pre[256 * WORDS];                 // popcount prefix per (expert, word)
   __shared__ int rows[SUB][8];
   __shared__ int has_rows[SUB];
-  const int B = blockIdx.x / (DT / SUB), sub = blockIdx.x % (DT / SUB);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  build_bitmap(present, idx, T, E, k, B * DT, nullptr);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-#pragma unroll
-    for (int w = 0; w < WORDS; ++w) {
-      pre[e * WORDS + w] = run;
-      run += __popc(present[e * WORDS + w]);
-    }
-  }
-  __syncthreads();
-  const int tl = threadIdx.x - sub * SUB;
-  if (tl >= 0 && tl < SUB) {
-    const int t = B * DT + threadIdx.x;
-    const int word = threadIdx.x >> 5;
-    const uint32_t below = (1u << lane) - 1u;
-    int any = 0;
-    for (int j = 0; j < 8; ++j) {
-      int r = -1;
-      if (j < k && t < T) {
-        const int e = idx[(int64_t)t * k + j];
-        int s = -1;
-        bool ok = (e >= 0 && e < E);
-        for (int jj = 0; ok && jj < j; ++jj) ok = idx[(int64_t)t * k + jj] != e;  // repeats count as dropped
-        if (ok) {
-          const int local = pre[e * WORDS + word] + __popc(present[e * WORDS + word] & below);
-          const int64_t rank = (int64_t)block_base[(int64_t)B * E + e] + local;
-          if (C < 0 || rank < C) {
-            s = (int)rank;
-            r = offsets[e] + s;
-            row_token[r] = t;
-          }
+  const int64_t tbase = (int64_t)blockIdx.x * SUB;
+  {
+    // one thread per (token, j) pair of the block's 32 tokens
+    const int tl = threadIdx.x >> 3, j = threadIdx.x & 7;
+    const int64_t t = tbase + tl;
+    int r = -1;
+    if (j < k && t < T) {
+      const int64_t at = t * k + j;
+      const int local = slot[at];
+      int s = -1;
+      if (local >= 0) {
+        const int e = idx[at];
+        const int64_t rank = (int64_t)block_base[(t / DT) * E + e] + local;
+        if (C < 0 || rank < C) {
+          s = (int)rank;
+          r = offsets[e] + s;
+          row_token[r] = (int)t;
         }
-        slot[(int64_t)t * k + j] = s;
       }
-      rows[tl][j] = r;
-      any |= (r >= 0);
+      slot[at] = s;
     }
-    has_rows[tl] = any;
+    rows[tl][j] = r;
+    const unsigned any = __ballot_sync(0xffffffffu, r >= 0);
+    if (j == 0) has_rows[tl] = (any >> (threadIdx.x & 24)) & 0xffu ? 1 : 0;
   }
   __syncthreads();
   // copy: (token, 16-byte chunk) items spread over the block, 8 loads in flight per thread
   constexpr int V = Vec16<XT>::N;
   const int nvec = d / V;
   const int items = SUB * nvec;
-  const int64_t tbase = (int64_t)B * DT + sub * SUB;
   for (int i0 = 0; i0 < items; i0 += 8 * DT) {
     uint4 u[8];
     int q[8], v[8];
@@ -235,16 +240,15 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
                                          cudaStream_t stream) {
   const int nblk = dispatch_blocks(sh);
   const size_t bm = sizeof(uint32_t) * (size_t)sh.E * WORDS;
-  dispatch_count_kernel<<<nblk, DT, bm, stream>>>(idx, sh.T, sh.E, sh.k, sh.C, counts, base, kept, offsets, counter,
-                                                  st);
-  const int nsub = nblk * (DT / SUB);
+  cudaError_t e = launch_kernel(dispatch_count_kernel, dim3(nblk), dim3(DT), bm, stream, idx, sh.T, sh.E, sh.k, sh.C,
+                             counts, base, kept, offsets, slot, counter, st);
+  if (e != cudaSuccess) return e;
+  const int nsub = (sh.T + SUB - 1) / SUB;
   if (sh.dtype == MOE_BF16)
-    dispatch_place_kernel<bf16><<<nsub, DT, bm, stream>>>((const bf16 *)x, idx, sh.T, sh.d, sh.E, sh.k, sh.C, base,
-                                                          offsets, slot, row_token, (bf16 *)x_perm);
-  else
-    dispatch_place_kernel<float><<<nsub, DT, bm, stream>>>((const float *)x, idx, sh.T, sh.d, sh.E, sh.k, sh.C,
-                                                           base, offsets, slot, row_token, (float *)x_perm);
-  return cudaGetLastError();
+    return launch_kernel(dispatch_place_kernel<bf16>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T, sh.d,
+                      sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm);
+  return launch_kernel(dispatch_place_kernel<float>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T, sh.d,
+                    sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm);
 }
 
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,

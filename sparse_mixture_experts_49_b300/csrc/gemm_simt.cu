@@ -137,8 +137,7 @@ template <typename TA, typename TB, typename TC, int GROUP_K, int EPI>
 cudaError_t run(const SimtArgs &a, int64_t max_rows, cudaStream_t stream) {
   dim3 grid((a.N + TN - 1) / TN, (unsigned)((GROUP_K ? a.M : max_rows) + TM - 1) / TM, a.groups);
   if (grid.y == 0) return cudaSuccess;
-  simt_gemm_kernel<TA, TB, TC, GROUP_K, EPI><<<grid, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(simt_gemm_kernel<TA, TB, TC, GROUP_K, EPI>, grid, dim3(256), 0, stream, a);
 }
 
 }  // namespace

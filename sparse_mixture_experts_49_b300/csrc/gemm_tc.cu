@@ -30,7 +30,7 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;             // TMA ring depth (weight-gradient GEMMs: 3, see stages_of)
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -47,15 +47,30 @@ struct __align__(8) Smem {
   uint32_t tmem_base;
   int abort_flag;
   int tile_start[MAX_E + 1];
-  int off[MAX_E + 1];
 };
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(Smem);
+// Plain-store epilogues (EPI_STORE, EPI_STORE_F32) stage each warp's 32-row
+// slice in shared memory (128-byte swizzled rows, 4 KB per warp) and write it
+// with a TMA tile store.
+// The weight-gradient GEMMs (grouped-K) have a few K steps per tile and a
+// full tile to store, so they trade one ring stage for a second staging
+// buffer per warp: a warp fills one buffer while the TMA engine reads the other.
+constexpr int STAGE_OUT_BYTES = 4096;
+constexpr int EPI_WARPS = 8;
+template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
+template <int GROUP_K> constexpr int stages_of() { return GROUP_K ? 3 : STAGES; }
+template <int GROUP_K, int EPI> constexpr int out_bufs() { return tma_store_epi<EPI>() ? (GROUP_K ? 2 : 1) : 0; }
+template <int GROUP_K, int EPI> constexpr size_t smem_bytes() {
+  return 1024 /*align slack*/ + (size_t)stages_of<GROUP_K>() * STAGE_BYTES +
+         (size_t)out_bufs<GROUP_K, EPI>() * EPI_WARPS * STAGE_OUT_BYTES + sizeof(Smem);
+}
+static_assert(smem_bytes<0, EPI_STORE>() <= 232448 && smem_bytes<1, EPI_STORE>() <= 232448, "shared memory budget");
 
 struct Args {
   const int32_t *offsets;  // [E + 1] row offsets of the groups
   int E;
   int M, N, K;             // grouped-M: N (output columns), K; grouped-K: M, N
   int F;                   // SwiGLU: offset of the up half (rows of W1, columns of pre_act / dA)
+  int b_once;              // grouped-M: each weight tile is read by one m-tile only (L2 evict-first)
   void *C;                 // bf16, or fp32 for EPI_STORE_F32
   int64_t ldc;
   int64_t sce;             // grouped-K: C_e = C + e * sce
@@ -86,11 +101,15 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const Args p) {
+                        const __grid_constant__ CUtensorMap tmC, const Args p) {
+  constexpr bool TMA_STORE = tma_store_epi<EPI>();
+  constexpr int NST = stages_of<GROUP_K>();
+  constexpr int NBUF = out_bufs<GROUP_K, EPI>();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  Smem &s = *reinterpret_cast<Smem *>(tiles + (size_t)STAGES * STAGE_BYTES);
+  uint8_t *stage_out = tiles + (size_t)NST * STAGE_BYTES;  // TMA_STORE only: [EPI_WARPS][NBUF][4 KB]
+  Smem &s = *reinterpret_cast<Smem *>(stage_out + NBUF * EPI_WARPS * STAGE_OUT_BYTES);
   volatile int *abort_flag = &s.abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -107,12 +126,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      for (int i = 0; i < STAGES; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
+      if (TMA_STORE) prefetch_tmap(&tmC);
+      for (int i = 0; i < NST; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
       for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], 8); }
       mbar_init(&s.drain, 1);
       s.abort_flag = 0;
       fence_barrier_init();
     }
+  } else if (warp == 1) {
+    tmem_alloc(&s.tmem_base, TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  if (warp == 0) {
     // tile_start[e] = number of tiles of groups before e
     int carry = 0;
     if (lane == 0) s.tile_start[0] = 0;
@@ -121,8 +147,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       int t = 0;
       if (e < E) {
         const int lo = p.offsets[e], hi = p.offsets[e + 1];
-        s.off[e] = lo;
-        if (e == E - 1) s.off[E] = hi;
         t = GROUP_K ? m_tiles_k * n_tiles : ((hi - lo + BM - 1) / BM) * n_tiles;
       }
       int incl = t;
@@ -134,31 +158,40 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (e < E) s.tile_start[e + 1] = carry + incl;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-  } else if (warp == 1) {
-    tmem_alloc(&s.tmem_base, TMEM_COLS);
-    tmem_relinquish();
-    tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int total_tiles = s.tile_start[E];
 
+  // Group row offsets, written by the dispatch before this launch (read-only here).
+  auto off = [&](int i) -> int { return __ldg(p.offsets + i); };
+  // Tile order inside a group. Grouped-M: m-tiles fastest, so the m-tiles
+  // that read the same weight tile run side by side and share it through L2.
+  // Grouped-K: n-tiles fastest (the activation tiles are small and shared).
   auto decode = [&](int tile, int &e, int &mt, int &nt) {
     e = find_group(s.tile_start, E, tile);
     const int local = tile - s.tile_start[e];
-    mt = local / n_tiles;
-    nt = local - mt * n_tiles;
+    if (GROUP_K) {
+      mt = local / n_tiles;
+      nt = local - mt * n_tiles;
+    } else {
+      const int m_tiles = (s.tile_start[e + 1] - s.tile_start[e]) / n_tiles;
+      nt = local / m_tiles;
+      mt = local - nt * m_tiles;
+    }
   };
   auto k_steps = [&](int e) -> int {
-    return GROUP_K ? (s.off[e + 1] - s.off[e] + BK - 1) / BK : (p.K + BK - 1) / BK;
+    return GROUP_K ? (off(e + 1) - off(e) + BK - 1) / BK : (p.K + BK - 1) / BK;
   };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       const uint64_t pol_a = policy_evict_last();
-      const uint64_t pol_b = GROUP_K ? policy_evict_last() : policy_evict_first();
+      // Weight tiles that no other m-tile will read are streamed (evict-first);
+      // when groups span several m-tiles they are kept for the other m-tiles.
+      const uint64_t pol_b = (!GROUP_K && p.b_once) ? policy_evict_first() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0, issued_parity = 0;
@@ -174,7 +207,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
           const int k0 = ks * BK;
           if (!GROUP_K) {
-            const int row0 = s.off[e] + mt * BM;
+            const int row0 = off(e) + mt * BM;
             tma_load_2d(a_s, &tmA, &s.full[stage], k0, row0, pol_a);
             if (!B_MN) {
               int r0, r1;
@@ -188,7 +221,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_3d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, k0, e, pol_b);
             }
           } else {
-            const int r0 = s.off[e] + k0;
+            const int r0 = off(e) + k0;
 #pragma unroll
             for (int j = 0; j < 2; ++j) tma_load_2d(a_s + j * 8192, &tmA, &s.full[stage], mt * BM + 64 * j, r0, pol_a);
 #pragma unroll
@@ -196,11 +229,11 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
       }
       if (*abort_flag) {
-        for (int i = 0; i < STAGES; ++i)
+        for (int i = 0; i < NST; ++i)
           if (issued & (1u << i)) drain_wait(&s.full[i], (issued_parity >> i) & 1);
       }
     }
@@ -225,20 +258,26 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
         uint8_t *b_s = a_s + A_BYTES;
+        int nkk = BK / 16;  // K16 slices of this step that hold rows of the group
         if (GROUP_K) {
-          // The last K step of a group may run past its rows: zero those K rows
-          // of both operands (each is one 128-byte line per 64-wide block).
-          const int valid = s.off[e + 1] - (s.off[e] + ks * BK);
+          // The last K step of a group may run past its rows: only the slices
+          // holding group rows are issued, and the rows past the group inside
+          // the last of them are zeroed in both operands (each row is one
+          // 128-byte line per 64-wide block).
+          const int valid = off(e + 1) - (off(e) + ks * BK);
           if (valid < BK) {
-            const int nrows = BK - valid;
-            const int chunks = nrows * 8;  // 16-byte chunks per block
-            for (int i = lane; i < 6 * chunks; i += 32) {
-              const int blk = i / chunks, rem = i - blk * chunks;
-              const int row = valid + (rem >> 3), c = rem & 7;
-              uint8_t *base = (blk < 2) ? (a_s + blk * 8192) : (b_s + (blk - 2) * 8192);
-              *reinterpret_cast<uint4 *>(base + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+            nkk = (valid + 15) >> 4;
+            const int nrows = nkk * 16 - valid;
+            if (nrows > 0) {
+              const int chunks = nrows * 8;  // 16-byte chunks per block
+              for (int i = lane; i < 6 * chunks; i += 32) {
+                const int blk = i / chunks, rem = i - blk * chunks;
+                const int row = valid + (rem >> 3), c = rem & 7;
+                uint8_t *base = (blk < 2) ? (a_s + blk * 8192) : (b_s + (blk - 2) * 8192);
+                *reinterpret_cast<uint4 *>(base + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             __syncwarp();
           }
         }
@@ -246,6 +285,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t a0 = smem_u32(a_s), b0 = smem_u32(b_s);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
+            if (kk >= nkk) break;
             const uint64_t ad = A_MN ? smem_desc_sw128(a0 + kk * 2048, 8192, 1024)
                                      : smem_desc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
@@ -255,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_commit(&s.empty[stage]);
         }
         __syncwarp();
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
       if (lane == 0) tc_commit(&s.acc_full[acc]);
@@ -274,6 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // row inside the 128-row tile
     const int half = (warp - 2) >> 2;  // column half of the tile
+    int obuf = 0;                      // staging buffer the next TMA store uses
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -283,10 +324,76 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       float v[32], w[32];
-      if (!GROUP_K) {
-        const int rows_e = s.off[e + 1] - s.off[e];
+      if (TMA_STORE) {
+        // This warp's 32-row slice: whole slices go through the staging buffer
+        // and a TMA store; a slice cut by the end of its group (grouped-M) is
+        // stored row by row, so the next group's rows are never touched.
+        constexpr bool F32 = (EPI == EPI_STORE_F32);
+        constexpr int CPB = F32 ? 1 : 2;  // 32-column chunks per 128-byte staging row
+        uint8_t *stg_base = stage_out + (warp - 2) * NBUF * STAGE_OUT_BYTES;
+        int nvalid = 32;
+        int r0;
+        const bool zero = GROUP_K && off(e + 1) == off(e);
+        if (!GROUP_K) {
+          const int lo = mt * BM + q * 32;
+          nvalid = min(32, max(0, off(e + 1) - off(e) - lo));
+          r0 = off(e) + lo;
+        } else {
+          r0 = mt * BM + q * 32;
+        }
+#pragma unroll 1
+        for (int c = 4 * half; c < 4 * half + 4; c += CPB) {
+          const int col = nt * BN + c * 32;
+          if (nvalid == 0 || col >= p.N) continue;
+          float x[32 * CPB];
+#pragma unroll
+          for (int u = 0; u < CPB; ++u) {
+            if (!zero) tmem_ld32(t_row + (c + u) * 32, x + 32 * u);
+            else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) x[32 * u + i] = 0.0f;
+            }
+          }
+          if (nvalid == 32) {
+            // the store issued from this buffer NBUF stores ago has left it
+            uint8_t *stg = stg_base + obuf * STAGE_OUT_BYTES;
+            if (lane == 0) {
+              if (NBUF == 2) bulk_wait_read_1();
+              else bulk_wait_read_all();
+            }
+            __syncwarp();
+            uint8_t *rowp = stg + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              uint8_t *dst = rowp + ((j ^ (lane & 7)) << 4);
+              if (F32) Vec16<float>::store(dst, x + 4 * j);
+              else Vec16<bf16>::store(dst, x + 8 * j);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (GROUP_K) tma_store_3d(&tmC, stg, col, r0, e);
+              else tma_store_2d(&tmC, stg, col, r0);
+              bulk_commit();
+            }
+            if (NBUF == 2) obuf ^= 1;
+          } else if (lane < nvalid) {
+            const int64_t row = (int64_t)r0 + lane;
+            if (F32) {
+              float *cp = static_cast<float *>(p.C) + row * p.ldc + col;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, x + 4 * i);
+            } else {
+              bf16 *cp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
+#pragma unroll
+              for (int i = 0; i < 8; ++i) Vec16<bf16>::store(cp + 8 * i, x + 8 * i);
+            }
+          }
+        }
+      } else if (!GROUP_K) {
+        const int rows_e = off(e + 1) - off(e);
         const bool valid = mt * BM + r < rows_e;
-        const int64_t row = (int64_t)s.off[e] + mt * BM + r;
+        const int64_t row = (int64_t)off(e) + mt * BM + r;
         if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
           for (int c = 2 * half; c < 2 * half + 2; ++c) {
@@ -378,7 +485,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
-        const bool empty_group = s.off[e + 1] == s.off[e];
+        const bool empty_group = off(e + 1) == off(e);
         const int m = mt * BM + r;
         const int64_t cofs = (int64_t)e * p.sce + (int64_t)m * p.ldc;
 #pragma unroll 1
@@ -407,6 +514,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&s.acc_empty[acc]);
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
+    if (TMA_STORE && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   __syncthreads();
@@ -417,33 +525,46 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
+// mc is the output's tile map for the plain-store epilogues (ignored otherwise).
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
-static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, cudaStream_t stream) {
+static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Args &a,
+                          cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<GROUP_K, A_MN, B_MN, EPI>;
+  constexpr size_t smem = smem_bytes<GROUP_K, EPI>();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  kern<<<sm_count(), THREADS, SMEM_BYTES, stream>>>(ma, mb, a);
-  return cudaGetLastError();
+  return launch_kernel(kern, dim3(sm_count()), dim3(THREADS), smem, stream, ma, mb, mc, a);
+}
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, cudaStream_t stream) {
+  static_assert(!tma_store_epi<EPI>(), "plain-store epilogues need the output map");
+  return launch<GROUP_K, A_MN, B_MN, EPI>(ma, mb, ma, a, stream);
 }
 
 }  // namespace tc
 
 // ---------------------------------------------------------------- launchers used by the C ABI
+// True when the groups average at most one 128-row tile, so that each weight
+// tile is read by a single m-tile.
+static int weights_read_once(const Shape &sh) { return sh.rows <= (int64_t)tc::BM * sh.E ? 1 : 0; }
+
 cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
                               cudaStream_t stream) {
   using namespace tc;
   CUtensorMap ma, mb;
   const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;  // a map needs at least one row
+  const int b_once = weights_read_once(sh);
   Args a{};
   a.offsets = offsets;
   a.E = sh.E;
   a.F = sh.F;
   a.st = st;
+  a.b_once = b_once;
   // GEMM 1 (+ activation): A = x_perm [rows, d], B = W1 [E, R1, d]
   if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
     return cudaErrorInvalidValue;
@@ -468,11 +589,14 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   b.E = sh.E;
   b.F = sh.F;
   b.st = st;
+  b.b_once = b_once;
   b.N = sh.d;
   b.K = sh.F;
   b.C = y_perm;
   b.ldc = sh.d;
-  return launch<0, 0, 0, EPI_STORE>(ma, mb, b, stream);
+  CUtensorMap mc;
+  if (!make_map_2d(&mc, y_perm, sh.d, rows, 64, 32)) return cudaErrorInvalidValue;
+  return launch<0, 0, 0, EPI_STORE>(ma, mb, mc, b, stream);
 }
 
 cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
@@ -483,12 +607,14 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
   const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;
   cudaError_t err;
   const bool swiglu = sh.act == MOE_ACT_SWIGLU;
+  const int b_once = weights_read_once(sh);
   // dH = dYp W2_e (B MN-major from W2 [E, d, F]), fused activation backward -> dA [rows, R1]
   {
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.N = sh.F; a.K = sh.d;
     a.C = da; a.ldc = sh.R1;
+    a.b_once = b_once;
     if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 64))
       return cudaErrorInvalidValue;
     if (swiglu) {
@@ -506,9 +632,11 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.d; a.N = sh.F;
     a.C = dw2; a.ldc = sh.F; a.sce = (int64_t)sh.d * sh.F;
-    if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 64) || !make_map_2d(&mb, h, sh.F, rows, 64, 64))
+    CUtensorMap mc;
+    if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 64) || !make_map_2d(&mb, h, sh.F, rows, 64, 64) ||
+        !make_map_3d(&mc, dw2, sh.F, sh.d, sh.E, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
+    err = launch<1, 1, 1, EPI_STORE>(ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   // dXp = dA W1_e (B MN-major from W1 [E, R1, d]): N = d, K = R1
@@ -517,9 +645,12 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.N = sh.d; a.K = sh.R1;
     a.C = dxp; a.ldc = sh.d;
-    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 64))
+    a.b_once = b_once;
+    CUtensorMap mc;
+    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 64) ||
+        !make_map_2d(&mc, dxp, sh.d, rows, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<0, 0, 1, EPI_STORE>(ma, mb, a, stream);
+    err = launch<0, 0, 1, EPI_STORE>(ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   // dW1_e = dA_e^T X_e: M = R1, N = d
@@ -528,9 +659,11 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.R1; a.N = sh.d;
     a.C = dw1; a.ldc = sh.d; a.sce = (int64_t)sh.R1 * sh.d;
-    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 64) || !make_map_2d(&mb, x_perm, sh.d, rows, 64, 64))
+    CUtensorMap mc;
+    if (!make_map_2d(&ma, da, sh.R1, rows, 64, 64) || !make_map_2d(&mb, x_perm, sh.d, rows, 64, 64) ||
+        !make_map_3d(&mc, dw1, sh.d, sh.R1, sh.E, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE>(ma, mb, a, stream);
+    err = launch<1, 1, 1, EPI_STORE>(ma, mb, mc, a, stream);
   }
   return err;
 }
@@ -553,10 +686,11 @@ cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void 
     a.offsets = offs2; a.E = 1; a.F = 0; a.st = st;
     a.N = sh.d; a.K = 6 * ep;
     a.C = dxr; a.ldc = sh.d;
+    CUtensorMap mc;
     if (!make_map_2d(&ma, a6, 6 * (uint64_t)ep, sh.T, 64, 128) ||
-        !make_map_3d(&mb, b6, sh.d, 6 * (uint64_t)ep, 1, 64, 64))
+        !make_map_3d(&mb, b6, sh.d, 6 * (uint64_t)ep, 1, 64, 64) || !make_map_2d_f32(&mc, dxr, sh.d, sh.T, 32, 32))
       return cudaErrorInvalidValue;
-    err = launch<0, 0, 1, EPI_STORE_F32>(ma, mb, a, stream);
+    err = launch<0, 0, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   {
@@ -564,11 +698,12 @@ cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void 
     a.offsets = offs2; a.E = 1; a.F = 0; a.st = st;
     a.M = 3 * ep; a.N = sh.d;
     a.C = c3; a.ldc = sh.d; a.sce = 0;
+    CUtensorMap mc;
     if (!make_map_2d_strided(&ma, static_cast<const bf16 *>(a6) + 3 * ep, 3 * (uint64_t)ep, sh.T,
                              6 * (uint64_t)ep * 2, 64, 64) ||
-        !make_map_2d(&mb, x, sh.d, sh.T, 64, 64))
+        !make_map_2d(&mb, x, sh.d, sh.T, 64, 64) || !make_map_3d_f32(&mc, c3, sh.d, 3 * (uint64_t)ep, 1, 32, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE_F32>(ma, mb, a, stream);
+    err = launch<1, 1, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
   }
   return err;
 }

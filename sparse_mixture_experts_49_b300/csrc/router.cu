@@ -504,8 +504,7 @@ cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStre
   constexpr size_t smem = simt_router_smem_bytes<EPT>();
   static cudaError_t attr = set_smem(router_simt_kernel<XT, EPT>, smem);
   if (attr != cudaSuccess) return attr;
-  router_simt_kernel<XT, EPT><<<nblk, 256, smem, stream>>>(a, so);
-  return cudaGetLastError();
+  return launch_kernel(router_simt_kernel<XT, EPT>, dim3(nblk), dim3(256), smem, stream, a, so);
 }
 
 template <int EPT>
@@ -514,8 +513,7 @@ cudaError_t run_select(const float *partial, int splits, const RouterArgs &a, co
   constexpr size_t smem = select_smem_bytes<EPT, RT_TC>();
   static cudaError_t attr = set_smem(router_select_kernel<EPT>, smem);
   if (attr != cudaSuccess) return attr;
-  router_select_kernel<EPT><<<nblk, 256, smem, stream>>>(partial, splits, a, so);
-  return cudaGetLastError();
+  return launch_kernel(router_select_kernel<EPT>, dim3(nblk), dim3(256), smem, stream, partial, splits, a, so);
 }
 
 template <int EP>
@@ -523,8 +521,8 @@ cudaError_t run_tc(const CUtensorMap &mx, const CUtensorMap &mw, const rt::Args 
                    cudaStream_t stream) {
   static cudaError_t attr = set_smem(rt::router_tc_kernel<EP>, rt::Geo<EP>::SMEM);
   if (attr != cudaSuccess) return attr;
-  rt::router_tc_kernel<EP><<<dim3(m_tiles, splits), 192, rt::Geo<EP>::SMEM, stream>>>(mx, mw, ta);
-  return cudaGetLastError();
+  return launch_kernel(rt::router_tc_kernel<EP>, dim3(m_tiles, splits), dim3(192), rt::Geo<EP>::SMEM, stream, mx, mw,
+                    ta);
 }
 
 int epad_of(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
@@ -578,7 +576,8 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   const int64_t n = (int64_t)plan.ep * sh.d;
   int sgrid = (int)((n + 255) / 256);
   if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
-  router_split_kernel<<<sgrid, 256, 0, stream>>>(w_r, sh.E, plan.ep, sh.d, parts);
+  e = launch_kernel(router_split_kernel, dim3(sgrid), dim3(256), 0, stream, w_r, sh.E, plan.ep, sh.d, parts);
+  if (e != cudaSuccess) return e;
   CUtensorMap mx, mw;
   if (!make_map_2d(&mx, x, sh.d, sh.T, 64, 128) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
     return cudaErrorInvalidValue;

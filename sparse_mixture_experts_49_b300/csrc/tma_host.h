@@ -15,6 +15,11 @@ bool make_map_2d_strided(CUtensorMap *m, const void *ptr, uint64_t inner, uint64
 // 3-D bf16 map over [d2, d1, d0] (d0 contiguous), box [1, box1, box0], 128-byte swizzle.
 bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
                  uint32_t box1);
+// fp32 versions (outputs written by TMA stores).
+bool make_map_2d_f32(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                     uint32_t box_outer);
+bool make_map_3d_f32(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                     uint32_t box1);
 // Streaming multiprocessors of the current device.
 int sm_count();
 
