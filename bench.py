@@ -1,8 +1,8 @@
 """Benchmark of the MoE FFN layer on B300.
 
 One step = one pass of the whole layer over one batch. By default that is
-the forward pass (router -> dispatch -> expert grouped GEMM -> combine) of
-the Switch-Base-like top-1 workload: T = 8192 tokens (16 x 512), d_model 768,
+the forward pass (router -> dispatch -> expert grouped GEMM -> combine, as
+the single moe_forward call) of the Switch-Base-like top-1 workload: T = 8192 tokens (16 x 512), d_model 768,
 128 experts, ReLU FFN 768 -> 3072 -> 768, capacity factor 1.25, bf16
 activations and experts with an fp32 router. `--workload` picks another of
 the bf16 workloads and `--pass fwdbwd` adds the backward pass (moe_backward)
@@ -36,9 +36,12 @@ import moe_synth as syn  # noqa: E402
 WORKLOAD = "switch-base-top1"
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; dispatch % HBM BW"
 L2_FLUSH_BYTES = 256 << 20
-# kernels of the library per forward step of the bf16 layer: router (W_r split, tensor-core logits,
-# selection + statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1
-LAUNCHES_PER_STEP = 8
+# kernels of the library per call of the bf16 layer: router (W_r split, tensor-core logits, selection +
+# statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1. moe_forward runs
+# the same, but top-1 layers combine inside the second grouped-GEMM launch.
+def forward_launches(w, fused_call: bool) -> int:
+    combine = 0 if (fused_call and w.k == 1) else 1
+    return 3 + 2 + 2 + combine
 # moe_backward of the bf16 layer: combine backward 1, grouped GEMMs 4, router logit gradient 1, W_r split 1,
 # router gradient GEMMs 2, dW_r part sum 1, unpermute-reduce 1
 LAUNCHES_BACKWARD = 11
@@ -234,6 +237,15 @@ def run_ours(args):
             moe.moe_backward(cfg, saved, dy, dx, dw_r, dw1, dw2, L.ws)
             if marks: marks[5].record(stream)
 
+    def step_fused():
+        # the whole forward layer in one call (inference): no y_perm and no combine launch for top-1
+        # (inference: the [T, E] probabilities are only needed by the backward pass and are not written)
+        moe.moe_forward(cfg, x, w_r, bias, w1, w2, None, L.topk_idx, L.topk_gate, L.importance, L.load, L.aux,
+                        L.slot, L.kept, L.offsets, L.row_token, L.x_perm, L.h, L.y_perm if w.k > 1 else None, L.out,
+                        L.ws)
+
+    timed_step = step if bwd else step_fused
+
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -253,19 +265,37 @@ def run_ours(args):
     per_call = {c: [m[j].elapsed_time(m[j + 1]) for m in marks] for j, c in enumerate(calls)}
     eager_ms = statistics.mean(m[0].elapsed_time(m[nc]) for m in marks)
 
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(g, stream=side):
+                fn()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        return g
+
+    # the separate ABI calls as one graph (reported beside the timed step for forward-only workloads)
+    unfused_ms = None
+    if not bwd:
+        g_sep = capture(step)
+        ue = [(ev(), ev()) for _ in range(n_eager)]
+        for a_, b_ in ue:
+            flush.zero_()
+            a_.record(stream)
+            g_sep.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        unfused_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ue)
+        del g_sep
+
     # the timed steps: the whole step captured once in a CUDA graph, replayed
-    graph = torch.cuda.CUDAGraph()
-    side = torch.cuda.Stream()
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        with torch.cuda.graph(graph, stream=side):
-            step()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize()
+    graph = capture(timed_step)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -307,7 +337,7 @@ def run_ours(args):
         x.copy_(x_host, non_blocking=True)
         if bwd:
             dy.copy_(dy_host, non_blocking=True)
-        step()
+        timed_step()
         out_host.copy_(L.out, non_blocking=True)
         if bwd:
             dx_host.copy_(dx, non_blocking=True)
@@ -342,7 +372,7 @@ def run_ours(args):
     roof.update({"kernel": "moe_expert_gemm (forward grouped GEMM, 2 launches)", "traffic": traffic,
                  "peak_source": peak_src, "algorithmic_bytes_per_call": alg["gemm"],
                  "algorithmic_flops_per_call": alg["gemm_flops"]})
-    launches = LAUNCHES_PER_STEP + (LAUNCHES_BACKWARD if bwd else 0)
+    launches = forward_launches(w, not bwd) + (LAUNCHES_BACKWARD if bwd else 0)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -360,8 +390,12 @@ def run_ours(args):
                 "d2h_bytes_per_step": io_bytes},
         "gpu_launches": launches * args.steps,
         "eager_ms_per_step": round(eager_ms, 5),
-        "timing": "step replayed as one CUDA graph; per-call figures from an eager pass with events "
-                  "between the ABI calls",
+        "step_call": "moe_forward (one call: router, dispatch, expert GEMMs, combine fused into the second GEMM "
+                     "for top-1)" if not bwd else
+                     "moe_router, moe_dispatch, moe_expert_gemm, moe_combine, moe_backward",
+        "separate_calls_graph_ms_per_step": None if unfused_ms is None else round(unfused_ms, 5),
+        "timing": "step replayed as one CUDA graph; per-call figures from an eager pass of the separate ABI calls "
+                  "with events between them",
         "clocks": clk,
         "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
     }

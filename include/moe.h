@@ -218,6 +218,34 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
                        const int32_t *topk_idx, const float *topk_gate, const int32_t *slot,
                        const int32_t *expert_offsets, void *out, moe_stream_t stream);
 
+/*
+ * The whole forward layer in one call, for inference: router, dispatch,
+ * expert FFNs and combine ([Switch] eqs. (1)-(4) and the dropped-token rule;
+ * [LRMoE] compaction into variable-size groups). For top-1 layers the
+ * second expert GEMM writes out[t] = x[t] + g[t] * E_e(x[t]) in its
+ * epilogue (no y_perm and no combine launch; the dispatch copies x to out
+ * for dropped tokens); k > 1 layers combine as moe_combine does. Results match
+ * the separate calls except that, for top-1 layers, y is not rounded to the
+ * x dtype before the gated residual sum (one rounding instead of two).
+ * Nothing only the backward pass needs is stored (no pre-activations; no
+ * y_perm for top-1): train with the separate calls.
+ *
+ * Arguments as in moe_router, moe_dispatch and moe_combine, plus
+ *   w1, w2   expert weights as in moe_expert_gemm
+ *   x_perm   [rows, d]  x dtype out (packed token rows)
+ *   h        [rows, F]  x dtype out (hidden activations, packed rows)
+ *   y_perm   [rows, d]  x dtype scratch, required when top_k > 1, ignored
+ *                       (may be NULL) when top_k == 1
+ *   out      [T, d]     x dtype out (may not alias x)
+ * MOE_BF16 only (MOE_ERR_UNSUPPORTED for MOE_F32).
+ */
+moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
+                       const float *logit_bias, const void *w1, const void *w2, float *probs,
+                       int32_t *topk_idx, float *topk_gate, float *importance, int32_t *load,
+                       float *aux_loss, int32_t *slot, int32_t *kept, int32_t *expert_offsets,
+                       int32_t *row_token, void *x_perm, void *h, void *y_perm, void *out, void *ws,
+                       moe_stream_t stream);
+
 /* Everything the forward pass produced that the backward pass reads. */
 typedef struct moe_saved {
   const void *x;                  /* [T, d] */

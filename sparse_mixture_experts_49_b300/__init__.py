@@ -26,7 +26,8 @@ MOE_NOALLOC_MAX_TOKENS = 32768
 
 EXPORTED = [
     "moe_capacity", "moe_max_rows", "moe_workspace_size", "moe_workspace_init", "moe_router",
-    "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_backward", "moe_backward_intermediates",
+    "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_forward", "moe_backward",
+    "moe_backward_intermediates",
     "moe_get_device_error", "moe_status_string", "moe_last_cuda_error",
 ]
 
@@ -75,6 +76,7 @@ def lib() -> ctypes.CDLL:
             "moe_dispatch_noalloc": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
             "moe_expert_gemm": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
             "moe_combine": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
+            "moe_forward": (ctypes.c_int, [C] + [P] * 21),
             "moe_backward": (ctypes.c_int, [C, ctypes.POINTER(moe_saved), P, P, P, P, P, P, P]),
             "moe_backward_intermediates": (ctypes.c_int, [C, P, ctypes.POINTER(P), ctypes.POINTER(P),
                                                           ctypes.POINTER(P), ctypes.POINTER(P),
@@ -182,6 +184,15 @@ def moe_combine(cfg, x, y_perm, topk_idx, topk_gate, slot, expert_offsets, out, 
                              _ptr(slot), _ptr(expert_offsets), _ptr(out), _stream(stream)), "moe_combine")
 
 
+def moe_forward(cfg, x, w_r, logit_bias, w1, w2, probs, topk_idx, topk_gate, importance, load, aux_loss, slot, kept,
+                expert_offsets, row_token, x_perm, h, y_perm, out, ws, stream=None):
+    """The whole forward layer in one call (inference; top-1 layers combine inside the second expert GEMM)."""
+    _check(lib().moe_forward(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_bias), _ptr(w1), _ptr(w2), _ptr(probs),
+                             _ptr(topk_idx), _ptr(topk_gate), _ptr(importance), _ptr(load), _ptr(aux_loss), _ptr(slot),
+                             _ptr(kept), _ptr(expert_offsets), _ptr(row_token), _ptr(x_perm), _ptr(h), _ptr(y_perm),
+                             _ptr(out), _ptr(ws), _stream(stream)), "moe_forward")
+
+
 def moe_backward(cfg, saved: dict, dy, dx, dw_r, dw1, dw2, ws, stream=None):
     sv = moe_saved(**{k: _ptr(saved.get(k)) for k, _ in moe_saved._fields_})
     _check(lib().moe_backward(ctypes.byref(cfg), ctypes.byref(sv), _ptr(dy), _ptr(dx), _ptr(dw_r), _ptr(dw1),
@@ -246,6 +257,14 @@ class MoELayer:
         self._saved = dict(x=x, w_r=w_r, w1=w1, w2=w2, probs=self.probs, topk_idx=idx, topk_gate=self.topk_gate,
                            slot=self.slot, expert_offsets=self.offsets, load=self.load, x_perm=self.x_perm,
                            pre_act=self.pre_act, h=self.h, y_perm=self.y_perm)
+        return self.out
+
+    def infer(self, x, w_r, w1, w2, logit_bias=None):
+        """out = x + MoE(x) through moe_forward (one call; nothing kept for the backward pass)."""
+        c = self.cfg
+        moe_forward(c, x, w_r, logit_bias, w1, w2, self.probs, self.topk_idx, self.topk_gate, self.importance,
+                    self.load, self.aux, self.slot, self.kept, self.offsets, self.row_token, self.x_perm, self.h,
+                    self.y_perm if c.top_k > 1 else None, self.out, self.ws, self.stream)
         return self.out
 
     def backward(self, dy, dx=None, dw_r=None, dw1=None, dw2=None):

@@ -16,41 +16,6 @@ namespace moe {
 
 namespace {
 
-struct KeptRows {
-  int n;
-  int row[8];
-  float g[8];
-  int j[8];
-};
-
-// The kept rows of token t, in ascending j. Lanes < k read, everyone gets the list.
-__device__ __forceinline__ KeptRows kept_rows(int t, int k, const int32_t *idx, const int32_t *slot,
-                                              const int32_t *offsets, const float *gate) {
-  const int lane = threadIdx.x & 31;
-  int row = -1;
-  float g = 0.0f;
-  if (lane < k) {
-    const int s = slot[(int64_t)t * k + lane];
-    if (s >= 0) {
-      row = offsets[idx[(int64_t)t * k + lane]] + s;
-      if (gate) g = gate[(int64_t)t * k + lane];
-    }
-  }
-  KeptRows kr;
-  kr.n = 0;
-  for (int j = 0; j < k; ++j) {
-    const int r = __shfl_sync(0xffffffffu, row, j);
-    const float gj = __shfl_sync(0xffffffffu, g, j);
-    if (r >= 0) {
-      kr.row[kr.n] = r;
-      kr.g[kr.n] = gj;
-      kr.j[kr.n] = j;
-      ++kr.n;
-    }
-  }
-  return kr;
-}
-
 // Rows and gates of token t's k assignments, in registers (row = -1 when dropped).
 template <int KMAX>
 __device__ __forceinline__ void token_rows(int t, int k, const int32_t *__restrict__ idx,
@@ -109,72 +74,94 @@ __global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, 
 }
 
 // dg[t, j] = <dY_t, y_perm[row]> and dYp[row] = g[t, j] dY_t for kept pairs; dg = 0 otherwise.
-template <typename XT>
-__global__ void __launch_bounds__(256) combine_backward_kernel(const XT *dy, const XT *y_perm, const int32_t *idx,
-                                                               const float *gate, const int32_t *slot,
-                                                               const int32_t *offsets, int T, int d, int k,
-                                                               XT *dyp, float *dg) {
+// All k rows of a 16-byte chunk are loaded before any is used.
+template <typename XT, int KMAX>
+__global__ void __launch_bounds__(256) combine_backward_kernel(const XT *__restrict__ dy, const XT *__restrict__ y_perm,
+                                                               const int32_t *__restrict__ idx,
+                                                               const float *__restrict__ gate,
+                                                               const int32_t *__restrict__ slot,
+                                                               const int32_t *__restrict__ offsets, int T, int d, int k,
+                                                               XT *__restrict__ dyp, float *__restrict__ dg) {
   constexpr int V = Vec16<XT>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
-    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, gate);
-    float dot[8];
+    int row[KMAX];
+    float g[KMAX];
+    token_rows<KMAX>(t, k, idx, slot, offsets, gate, row, g);
+    float dot[KMAX];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) dot[j] = 0.0f;
+    for (int j = 0; j < KMAX; ++j) dot[j] = 0.0f;
     const XT *dr = dy + (int64_t)t * d;
     for (int v = lane; v < nvec; v += 32) {
-      float g[V], y[V], o[V];
-      Vec16<XT>::load(dr + v * V, g);
-      for (int j = 0; j < kr.n; ++j) {
-        Vec16<XT>::load(y_perm + (int64_t)kr.row[j] * d + v * V, y);
-        float s = 0.0f;
+      uint4 raw[KMAX + 1];
+      raw[0] = *reinterpret_cast<const uint4 *>(dr + v * V);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(y_perm + (int64_t)row[j] * d + v * V);
+      float gv[V], y[V], o[V];
+      Vec16<XT>::unpack(raw[0], gv);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (row[j] < 0) continue;
+        Vec16<XT>::unpack(raw[j + 1], y);
+        float sacc = 0.0f;
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-          s = fmaf(g[i], y[i], s);
-          o[i] = kr.g[j] * g[i];
+          sacc = fmaf(gv[i], y[i], sacc);
+          o[i] = g[j] * gv[i];
         }
-        dot[j] += s;
-        Vec16<XT>::store(dyp + (int64_t)kr.row[j] * d + v * V, o);
+        dot[j] += sacc;
+        Vec16<XT>::store(dyp + (int64_t)row[j] * d + v * V, o);
       }
     }
-    for (int j = 0; j < kr.n; ++j) {
-      float s = dot[j];
+    float mine = 0.0f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      dot[j] = s;
+    for (int j = 0; j < KMAX; ++j) {
+      float sacc = dot[j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sacc += __shfl_xor_sync(0xffffffffu, sacc, o);
+      if (lane == j && row[j] >= 0) mine = sacc;
     }
-    if (lane < k) {
-      float v = 0.0f;
-      for (int j = 0; j < kr.n; ++j)
-        if (kr.j[j] == lane) v = dot[j];
-      dg[(int64_t)t * k + lane] = v;
-    }
+    if (lane < k) dg[(int64_t)t * k + lane] = mine;
   }
 }
 
-// dX_t = dY_t + sum over kept rows of dXp[row] + dXr_t (router path, fp32), rounded once.
-template <typename XT>
-__global__ void __launch_bounds__(256) unpermute_kernel(const XT *dy, const XT *dxp, const float *dxr,
-                                                        const int32_t *idx, const int32_t *slot,
-                                                        const int32_t *offsets, int T, int d, int k, XT *dx) {
+// dX_t = dY_t + sum over kept rows of dXp[row] + dXr_t (router path, fp32), rounded once; all k
+// rows of a chunk are loaded before the sum.
+template <typename XT, int KMAX>
+__global__ void __launch_bounds__(256) unpermute_kernel(const XT *__restrict__ dy, const XT *__restrict__ dxp,
+                                                        const float *__restrict__ dxr, const int32_t *__restrict__ idx,
+                                                        const int32_t *__restrict__ slot,
+                                                        const int32_t *__restrict__ offsets, int T, int d, int k,
+                                                        XT *__restrict__ dx) {
   constexpr int V = Vec16<XT>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
   for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
-    const KeptRows kr = kept_rows(t, k, idx, slot, offsets, nullptr);
+    int row[KMAX];
+    float g[KMAX];
+    token_rows<KMAX>(t, k, idx, slot, offsets, nullptr, row, g);
     for (int v = lane; v < nvec; v += 32) {
+      uint4 raw[KMAX + 1];
+      raw[0] = *reinterpret_cast<const uint4 *>(dy + (int64_t)t * d + v * V);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j)
+        if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(dxp + (int64_t)row[j] * d + v * V);
+      float r[V];
+      Vec16<float>::load(dxr + (int64_t)t * d + v * V, r);
+      if (V == 8) Vec16<float>::load(dxr + (int64_t)t * d + v * V + 4, r + 4);
       float acc[V], y[V];
-      Vec16<XT>::load(dy + (int64_t)t * d + v * V, acc);
-      for (int j = 0; j < kr.n; ++j) {
-        Vec16<XT>::load(dxp + (int64_t)kr.row[j] * d + v * V, y);
+      Vec16<XT>::unpack(raw[0], acc);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (row[j] < 0) continue;
+        Vec16<XT>::unpack(raw[j + 1], y);
 #pragma unroll
         for (int i = 0; i < V; ++i) acc[i] += y[i];
       }
-      Vec16<float>::load(dxr + (int64_t)t * d + v * V, y);
-      if (V == 8) Vec16<float>::load(dxr + (int64_t)t * d + v * V + 4, y + 4);
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] += y[i];
+      for (int i = 0; i < V; ++i) acc[i] += r[i];
       Vec16<XT>::store(dx + (int64_t)t * d + v * V, acc);
     }
   }
@@ -217,26 +204,53 @@ cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, c
   return run_combine_k<float>(sh, x, y_perm, idx, gate, slot, offsets, out, stream);
 }
 
+template <typename XT, int KMAX>
+cudaError_t run_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
+                                 const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp, float *dg,
+                                 cudaStream_t stream) {
+  return launch_kernel(combine_backward_kernel<XT, KMAX>, dim3(token_grid(sh.T)), dim3(256), 0, stream, (const XT *)dy,
+                       (const XT *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (XT *)dyp, dg);
+}
+
+template <typename XT>
+cudaError_t run_combine_backward_k(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
+                                   const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp,
+                                   float *dg, cudaStream_t stream) {
+  if (sh.k == 1) return run_combine_backward<XT, 1>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+  if (sh.k == 2) return run_combine_backward<XT, 2>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+  if (sh.k <= 4) return run_combine_backward<XT, 4>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+  return run_combine_backward<XT, 8>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+}
+
 cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,
                                     const float *gate, const int32_t *slot, const int32_t *offsets, void *dyp,
                                     float *dg, cudaStream_t stream) {
-  const int grid = token_grid(sh.T);
   if (sh.dtype == MOE_BF16)
-    return launch_kernel(combine_backward_kernel<bf16>, dim3(grid), dim3(256), 0, stream, (const bf16 *)dy,
-                      (const bf16 *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dyp, dg);
-  return launch_kernel(combine_backward_kernel<float>, dim3(grid), dim3(256), 0, stream, (const float *)dy,
-                    (const float *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (float *)dyp, dg);
+    return run_combine_backward_k<bf16>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+  return run_combine_backward_k<float>(sh, dy, y_perm, idx, gate, slot, offsets, dyp, dg, stream);
+}
+
+template <typename XT, int KMAX>
+cudaError_t run_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr, const int32_t *idx,
+                          const int32_t *slot, const int32_t *offsets, void *dx, cudaStream_t stream) {
+  return launch_kernel(unpermute_kernel<XT, KMAX>, dim3(token_grid(sh.T)), dim3(256), 0, stream, (const XT *)dy,
+                       (const XT *)dxp, dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (XT *)dx);
+}
+
+template <typename XT>
+cudaError_t run_unpermute_k(const Shape &sh, const void *dy, const void *dxp, const float *dxr, const int32_t *idx,
+                            const int32_t *slot, const int32_t *offsets, void *dx, cudaStream_t stream) {
+  if (sh.k == 1) return run_unpermute<XT, 1>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
+  if (sh.k == 2) return run_unpermute<XT, 2>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
+  if (sh.k <= 4) return run_unpermute<XT, 4>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
+  return run_unpermute<XT, 8>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
 }
 
 cudaError_t launch_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr,
                              const int32_t *idx, const int32_t *slot, const int32_t *offsets, void *dx,
                              cudaStream_t stream) {
-  const int grid = token_grid(sh.T);
-  if (sh.dtype == MOE_BF16)
-    return launch_kernel(unpermute_kernel<bf16>, dim3(grid), dim3(256), 0, stream, (const bf16 *)dy, (const bf16 *)dxp,
-                      dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (bf16 *)dx);
-  return launch_kernel(unpermute_kernel<float>, dim3(grid), dim3(256), 0, stream, (const float *)dy,
-                    (const float *)dxp, dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (float *)dx);
+  if (sh.dtype == MOE_BF16) return run_unpermute_k<bf16>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
+  return run_unpermute_k<float>(sh, dy, dxp, dxr, idx, slot, offsets, dx, stream);
 }
 
 }  // namespace moe

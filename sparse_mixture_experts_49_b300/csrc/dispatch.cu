@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
                                                             const int32_t *__restrict__ block_base,
                                                             const int32_t *__restrict__ offsets,
                                                             int32_t *__restrict__ slot, int32_t *__restrict__ row_token,
-                                                            XT *__restrict__ x_perm) {
+                                                            XT *__restrict__ x_perm, XT *__restrict__ out_dropped) {
   __shared__ int rows[SUB][8];
   __shared__ int has_rows[SUB];
   const int64_t tbase = (int64_t)blockIdx.x * SUB;
@@ -200,25 +200,33 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
     if (j == 0) has_rows[tl] = (any >> (threadIdx.x & 24)) & 0xffu ? 1 : 0;
   }
   __syncthreads();
-  // copy: (token, 16-byte chunk) items spread over the block, 8 loads in flight per thread
+  // copy: (token, 16-byte chunk) items spread over the block, 8 loads in flight per thread;
+  // a kept token's row goes to its rows of x_perm (if given), a token with no
+  // kept assignment goes to out_dropped (if given)
+  if (x_perm == nullptr && out_dropped == nullptr) return;
   constexpr int V = Vec16<XT>::N;
   const int nvec = d / V;
   const int items = SUB * nvec;
   for (int i0 = 0; i0 < items; i0 += 8 * DT) {
     uint4 u[8];
     int q[8], v[8];
+    bool want[8];
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
       const int it = i0 + b * DT + threadIdx.x;
       q[b] = it / nvec;
       v[b] = it - q[b] * nvec;
-      if (it < items && tbase + q[b] < T && has_rows[q[b]])
-        u[b] = *reinterpret_cast<const uint4 *>(x + (tbase + q[b]) * d + (int64_t)v[b] * V);
+      want[b] = it < items && tbase + q[b] < T &&
+                (has_rows[q[b]] ? x_perm != nullptr : out_dropped != nullptr);
+      if (want[b]) u[b] = *reinterpret_cast<const uint4 *>(x + (tbase + q[b]) * d + (int64_t)v[b] * V);
     }
 #pragma unroll
     for (int b = 0; b < 8; ++b) {
-      const int it = i0 + b * DT + threadIdx.x;
-      if (it >= items || tbase + q[b] >= T || !has_rows[q[b]]) continue;
+      if (!want[b]) continue;
+      if (!has_rows[q[b]]) {
+        *reinterpret_cast<uint4 *>(out_dropped + (tbase + q[b]) * d + (int64_t)v[b] * V) = u[b];
+        continue;
+      }
       for (int j = 0; j < k; ++j) {
         const int r = rows[q[b]][j];
         if (r >= 0) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)v[b] * V) = u[b];
@@ -236,8 +244,8 @@ int dispatch_blocks(const Shape &sh) { return (sh.T + DT - 1) / DT; }
 // error word.
 cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
                                          int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
-                                         int32_t *counts, int32_t *base, unsigned int *counter, DeviceStatus *st,
-                                         cudaStream_t stream) {
+                                         void *out_dropped, int32_t *counts, int32_t *base, unsigned int *counter,
+                                         DeviceStatus *st, cudaStream_t stream) {
   const int nblk = dispatch_blocks(sh);
   const size_t bm = sizeof(uint32_t) * (size_t)sh.E * WORDS;
   cudaError_t e = launch_kernel(dispatch_count_kernel, dim3(nblk), dim3(DT), bm, stream, idx, sh.T, sh.E, sh.k, sh.C,
@@ -245,17 +253,18 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
   if (e != cudaSuccess) return e;
   const int nsub = (sh.T + SUB - 1) / SUB;
   if (sh.dtype == MOE_BF16)
-    return launch_kernel(dispatch_place_kernel<bf16>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T, sh.d,
-                      sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm);
-  return launch_kernel(dispatch_place_kernel<float>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T, sh.d,
-                    sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm);
+    return launch_kernel(dispatch_place_kernel<bf16>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T,
+                         sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped);
+  return launch_kernel(dispatch_place_kernel<float>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T,
+                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm, (float *)out_dropped);
 }
 
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,
-                            int32_t *offsets, int32_t *row_token, void *x_perm, void *ws, cudaStream_t stream) {
+                            int32_t *offsets, int32_t *row_token, void *x_perm, void *out_dropped, void *ws,
+                            cudaStream_t stream) {
   const WsLayout L = ws_layout(sh);
   uint8_t *w = static_cast<uint8_t *>(ws);
-  return launch_dispatch_with_scratch(sh, x, idx, slot, kept, offsets, row_token, x_perm,
+  return launch_dispatch_with_scratch(sh, x, idx, slot, kept, offsets, row_token, x_perm, out_dropped,
                                       reinterpret_cast<int32_t *>(w + L.disp_counts),
                                       reinterpret_cast<int32_t *>(w + L.disp_base),
                                       reinterpret_cast<unsigned int *>(w + L.status + 128),

@@ -91,5 +91,5 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x,
   e = cudaMemsetAsync(base, 0, kStatusInts * sizeof(int32_t), (cudaStream_t)stream);
   if (e != cudaSuccess) return report_cuda(e);
   return report_cuda(launch_dispatch_with_scratch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm,
-                                                  counts, bases, counter, status, (cudaStream_t)stream));
+                                                  nullptr, counts, bases, counter, status, (cudaStream_t)stream));
 }

@@ -76,8 +76,10 @@ struct Args {
   int64_t sce;             // grouped-K: C_e = C + e * sce
   bf16 *C2;                // SwiGLU forward: pre-activations [rows, 2F]
   int64_t ldc2;
-  const bf16 *aux;         // ReLU bwd: h; SwiGLU bwd: pre-activations
+  const bf16 *aux;         // ReLU bwd: h; SwiGLU bwd: pre-activations; combine: x (residual)
   int64_t ldaux;
+  const int32_t *a_rows;   // EPI_COMBINE: token of each packed row (row_token)
+  const float *gate;       // EPI_COMBINE: gate of each token (top-1)
   DeviceStatus *st;
 };
 
@@ -187,25 +189,30 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    if (lane == 0) {
-      const uint64_t pol_a = policy_evict_last();
-      // Weight tiles that no other m-tile will read are streamed (evict-first);
-      // when groups span several m-tiles they are kept for the other m-tiles.
-      const uint64_t pol_b = (!GROUP_K && p.b_once) ? policy_evict_first() : policy_evict_last();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued = 0, issued_parity = 0;
-      bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-        int e, mt, nt;
-        decode(tile, e, mt, nt);
-        const int nk = k_steps(e);
-        for (int ks = 0; ks < nk; ++ks) {
-          if (!mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st)) { ok = false; break; }
-          uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
-          uint8_t *b_s = a_s + A_BYTES;
-          mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
-          const int k0 = ks * BK;
+    // Lane 0 waits for free stages and issues the tile loads.
+    const uint64_t pol_a = policy_evict_last();
+    // Weight tiles that no other m-tile will read are streamed (evict-first);
+    // when groups span several m-tiles they are kept for the other m-tiles.
+    const uint64_t pol_b = (!GROUP_K && p.b_once) ? policy_evict_first() : policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      const int nk = k_steps(e);
+      for (int ks = 0; ks < nk; ++ks) {
+        int got = 1;
+        if (lane == 0) got = mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st) ? 1 : 0;
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) { ok = false; break; }
+        uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
+        uint8_t *b_s = a_s + A_BYTES;
+        if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+        __syncwarp();
+        const int k0 = ks * BK;
+        if (lane == 0) {
           if (!GROUP_K) {
             const int row0 = off(e) + mt * BM;
             tma_load_2d(a_s, &tmA, &s.full[stage], k0, row0, pol_a);
@@ -229,13 +236,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == NST) { stage = 0; phase ^= 1; }
         }
+        if (++stage == NST) { stage = 0; phase ^= 1; }
       }
-      if (*abort_flag) {
-        for (int i = 0; i < NST; ++i)
-          if (issued & (1u << i)) drain_wait(&s.full[i], (issued_parity >> i) & 1);
-      }
+    }
+    if (lane == 0 && *abort_flag) {
+      for (int i = 0; i < NST; ++i)
+        if (issued & (1u << i)) drain_wait(&s.full[i], (issued_parity >> i) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -421,8 +428,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           // The backward epilogues read saved activations; the loads of G
           // chunks are issued together before any of them is used.
-          constexpr int NAUX = (EPI == EPI_SWIGLU_BWD) ? 8 : (EPI == EPI_RELU_BWD ? 4 : 0);  // uint4 per chunk
+          constexpr int NAUX = (EPI == EPI_SWIGLU_BWD) ? 8 : ((EPI == EPI_RELU_BWD || EPI == EPI_COMBINE) ? 4 : 0);
           constexpr int G = (EPI == EPI_SWIGLU_BWD) ? 2 : 4;
+          // combine (top-1): the output and residual rows are the token's own
+          int64_t orow = row;
+          float gt = 0.0f;
+          if (EPI == EPI_COMBINE && valid) {
+            orow = __ldg(p.a_rows + row);
+            gt = __ldg(p.gate + orow);
+          }
 #pragma unroll 1
           for (int c0 = 4 * half; c0 < 4 * half + 4; c0 += G) {
             uint4 aux[NAUX > 0 ? G * NAUX : 1];
@@ -431,7 +445,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int g = 0; g < G; ++g) {
                 const int col = nt * BN + (c0 + g) * 32;
                 if (valid && col < p.N) {
-                  const bf16 *ap = p.aux + row * p.ldaux + col;
+                  const bf16 *ap = p.aux + orow * p.ldaux + col;
 #pragma unroll
                   for (int i = 0; i < 4; ++i) aux[g * NAUX + i] = *reinterpret_cast<const uint4 *>(ap + 8 * i);
                   if (EPI == EPI_SWIGLU_BWD) {
@@ -450,6 +464,11 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (EPI == EPI_RELU) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+              } else if (EPI == EPI_COMBINE) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Vec16<bf16>::unpack(aux[g * NAUX + i], w + 8 * i);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = fmaf(gt, v[i], w[i]);   // out = x + g * y, rounded once
               } else if (EPI == EPI_RELU_BWD) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Vec16<bf16>::unpack(aux[g * NAUX + i], w + 8 * i);
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, v + 4 * i);
               } else {
-                bf16 *cp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
+                bf16 *cp = static_cast<bf16 *>(p.C) + orow * p.ldc + col;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
               }
@@ -548,9 +567,9 @@ static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Ar
 }  // namespace tc
 
 // ---------------------------------------------------------------- launchers used by the C ABI
-// True when the groups average at most one 128-row tile, so that each weight
-// tile is read by a single m-tile.
-static int weights_read_once(const Shape &sh) { return sh.rows <= (int64_t)tc::BM * sh.E ? 1 : 0; }
+// True when the capacity keeps every group within one 128-row tile, so that
+// each weight tile is read by a single m-tile.
+static int weights_read_once(const Shape &sh) { return (sh.C >= 0 && sh.C <= tc::BM) ? 1 : 0; }
 
 cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
@@ -597,6 +616,54 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   CUtensorMap mc;
   if (!make_map_2d(&mc, y_perm, sh.d, rows, 64, 32)) return cudaErrorInvalidValue;
   return launch<0, 0, 0, EPI_STORE>(ma, mb, mc, b, stream);
+}
+
+// Forward expert FFNs whose second GEMM, for top-1 layers, combines in its
+// epilogue: out[t] = x[t] + g[t] * y for the row's token t (no y_perm). For
+// k > 1 the second GEMM writes y_perm and the caller combines.
+cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void *x_perm, const int32_t *row_token,
+                                      const int32_t *offsets, const void *w1, const void *w2, void *h,
+                                      const float *gate, void *out, void *y_perm, DeviceStatus *st,
+                                      cudaStream_t stream) {
+  using namespace tc;
+  if (sh.k != 1) return tc_expert_forward(sh, x_perm, offsets, w1, w2, nullptr, h, y_perm, st, stream);
+  CUtensorMap ma, mb;
+  const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;
+  const int b_once = weights_read_once(sh);
+  Args a{};
+  a.offsets = offsets;
+  a.E = sh.E;
+  a.F = sh.F;
+  a.st = st;
+  a.b_once = b_once;
+  // GEMM 1 (+ activation): A = x_perm [rows, d], B = W1 [E, R1, d]
+  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
+    return cudaErrorInvalidValue;
+  a.N = sh.F;
+  a.K = sh.d;
+  a.C = h;
+  a.ldc = sh.F;
+  cudaError_t err = sh.act == MOE_ACT_SWIGLU ? launch<0, 0, 0, EPI_SWIGLU>(ma, mb, a, stream)
+                                             : launch<0, 0, 0, EPI_RELU>(ma, mb, a, stream);
+  if (err != cudaSuccess) return err;
+  // GEMM 2 + combine: A = h [rows, F], B = W2 [E, d, F]
+  if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
+    return cudaErrorInvalidValue;
+  Args b{};
+  b.offsets = offsets;
+  b.E = sh.E;
+  b.F = sh.F;
+  b.st = st;
+  b.b_once = b_once;
+  b.N = sh.d;
+  b.K = sh.F;
+  b.ldc = sh.d;
+  b.C = out;
+  b.aux = (const bf16 *)x;
+  b.ldaux = sh.d;
+  b.a_rows = row_token;
+  b.gate = gate;
+  return launch<0, 0, 0, EPI_COMBINE>(ma, mb, b, stream);
 }
 
 cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,

@@ -19,7 +19,8 @@ struct Shape {
   int elt;        // bytes per element of the x dtype
 };
 
-enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4, EPI_STORE_F32 = 5 };
+enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU_BWD = 4, EPI_STORE_F32 = 5,
+       EPI_COMBINE = 6 };
 
 // Workspace carve-up (byte offsets from the workspace base). The first 256
 // bytes hold the error word (offset 0), the router's completion counter (64)
@@ -60,13 +61,16 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
                           int32_t *idx, float *gate, float *importance, int32_t *load, float *aux, void *ws,
                           cudaStream_t stream);
 
+// x_perm may be null (rows are not copied); out_dropped, when given, gets
+// x[t] for every token with no kept assignment.
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,
-                            int32_t *offsets, int32_t *row_token, void *x_perm, void *ws, cudaStream_t stream);
+                            int32_t *offsets, int32_t *row_token, void *x_perm, void *out_dropped, void *ws,
+                            cudaStream_t stream);
 
 cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
                                          int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
-                                         int32_t *counts, int32_t *base, unsigned int *counter, DeviceStatus *st,
-                                         cudaStream_t stream);
+                                         void *out_dropped, int32_t *counts, int32_t *base, unsigned int *counter,
+                                         DeviceStatus *st, cudaStream_t stream);
 moe_status dispatch_shape(const moe_config *cfg, Shape *sh);
 moe_status report_cuda(cudaError_t e);
 
@@ -81,6 +85,12 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
 cudaError_t simt_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
                                 const void *w2, void *pre_act, void *h, void *y_perm, cudaStream_t stream);
 
+// Forward whose second GEMM combines in its epilogue for top-1 layers (out);
+// k > 1 layers write y_perm.
+cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void *x_perm, const int32_t *row_token,
+                                      const int32_t *offsets, const void *w1, const void *w2, void *h,
+                                      const float *gate, void *out, void *y_perm, DeviceStatus *st,
+                                      cudaStream_t stream);
 cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
                                const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
                                void *dxp, void *dw1, void *dw2, DeviceStatus *st, cudaStream_t stream);

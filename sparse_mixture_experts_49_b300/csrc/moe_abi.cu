@@ -164,7 +164,7 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(x); MOE_PTR(topk_idx); MOE_PTR(slot); MOE_PTR(kept); MOE_PTR(expert_offsets); MOE_PTR(row_token);
   MOE_PTR(x_perm); MOE_PTR(ws);
-  return cuda_status(launch_dispatch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, ws,
+  return cuda_status(launch_dispatch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, nullptr, ws,
                                      (cudaStream_t)stream));
 }
 
@@ -195,6 +195,33 @@ moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm,
   MOE_REQUIRE(out != x && out != y_perm, MOE_ERR_INVALID_ARG);
   return cuda_status(
       launch_combine(sh, x, y_perm, topk_idx, topk_gate, slot, expert_offsets, out, (cudaStream_t)stream));
+}
+
+moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
+                       const void *w1, const void *w2, float *probs, int32_t *topk_idx, float *topk_gate,
+                       float *importance, int32_t *load, float *aux_loss, int32_t *slot, int32_t *kept,
+                       int32_t *expert_offsets, int32_t *row_token, void *x_perm, void *h, void *y_perm, void *out,
+                       void *ws, moe_stream_t stream) {
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.dtype == MOE_BF16, MOE_ERR_UNSUPPORTED);
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance);
+  MOE_PTR(load); MOE_PTR(slot); MOE_PTR(kept); MOE_PTR(expert_offsets); MOE_PTR(row_token); MOE_PTR(x_perm);
+  MOE_PTR(h); MOE_PTR(out); MOE_PTR(ws);
+  MOE_OPT_PTR(logit_bias); MOE_OPT_PTR(probs); MOE_OPT_PTR(aux_loss); MOE_OPT_PTR(y_perm);
+  if (sh.k > 1) MOE_PTR(y_perm);
+  MOE_REQUIRE(out != x, MOE_ERR_INVALID_ARG);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_router(sh, x, w_r, logit_bias, probs, topk_idx, topk_gate, importance, load, aux_loss, ws, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_dispatch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, sh.k == 1 ? out : nullptr, ws,
+                      s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = tc_expert_forward_combine(sh, x, x_perm, row_token, expert_offsets, w1, w2, h, topk_gate, out, y_perm,
+                                status_of(ws), s);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (sh.k == 1) return MOE_OK;
+  return cuda_status(launch_combine(sh, x, y_perm, topk_idx, topk_gate, slot, expert_offsets, out, s));
 }
 
 moe_status moe_backward(const moe_config *cfg, const moe_saved *sv, const void *dy, void *dx, float *dw_r,

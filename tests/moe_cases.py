@@ -54,7 +54,7 @@ def np64(t):
         else t.cpu().numpy().astype(np.int64)
 
 
-def run_gpu(w, inp, backward=False, topk_idx=None, layer=None):
+def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False):
     import torch
     import sparse_mixture_experts_49_b300 as moe
     cfg = config_for(moe, w)
@@ -66,7 +66,10 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None):
     w1 = to_dev(torch, inp["w1"], dt)
     w2 = to_dev(torch, inp["w2"], dt)
     idx_t = None if topk_idx is None else torch.from_numpy(np.asarray(topk_idx, np.int32)).cuda()
-    layer.forward(x, w_r, w1, w2, bias, idx_t)
+    if fused:
+        layer.infer(x, w_r, w1, w2, bias)
+    else:
+        layer.forward(x, w_r, w1, w2, bias, idx_t)
     res = {}
     if backward:
         dy = to_dev(torch, inp["dy"], dt)
@@ -85,7 +88,7 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None):
     res["row_token"] = np64(layer.row_token[:n])
     res["x_perm"] = np64(layer.x_perm[:n])
     res["h"] = np64(layer.h[:n])
-    res["y_perm"] = np64(layer.y_perm[:n])
+    res["y_perm"] = None if (fused and w.k == 1) else np64(layer.y_perm[:n])   # top-1 moe_forward writes no y_perm
     res["device_error"] = layer.device_error()
     return res
 

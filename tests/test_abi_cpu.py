@@ -115,6 +115,25 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     assert st == moe.MOE_ERR_INVALID_ARG
 
 
+def test_forward_call_validation():
+    L = moe.lib()
+    P = 1 << 20
+    null = None
+
+    def fwd(c, **over):
+        a = dict(x=P, w_r=P, bias=null, w1=P, w2=P, probs=null, idx=P, gate=P, imp=P, load=P, aux=null, slot=P,
+                 kept=P, offsets=P, row_token=P, x_perm=P, h=P, y_perm=P, out=P + 4096, ws=P)
+        a.update(over)
+        return L.moe_forward(ctypes.byref(c), *a.values(), null)
+
+    assert fwd(cfg(dtype="f32", d_model=64, d_ff=128)) == moe.MOE_ERR_UNSUPPORTED   # bf16 only
+    assert fwd(cfg(), y_perm=null) == moe.MOE_ERR_INVALID_ARG      # top-2 combines through y_perm
+    assert fwd(cfg(), out=P) == moe.MOE_ERR_INVALID_ARG            # out may not alias x
+    assert fwd(cfg(), h=P + 8) == moe.MOE_ERR_ALIGNMENT
+    assert fwd(cfg(), row_token=null) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(cfg(), x_perm=null) == moe.MOE_ERR_INVALID_ARG
+
+
 def test_status_strings():
     L = moe.lib()
     for s in range(6):

@@ -83,6 +83,43 @@ def test_deterministic(name):
         assert np.array_equal(np.asarray(r1[key]), np.asarray(r2[key])), key
 
 
+@pytest.mark.parametrize("E,k", [(256, 2), (20, 1), (64, 8)])
+def test_router_expert_counts_and_many_tiles(E, k):
+    """49 token tiles (a ragged last one) with the K range split over CTAs:
+    256 experts, a padded narrow layer (20 experts in 32 columns), top-8."""
+    w = syn.Workload(f"many-tiles-{E}-{k}", T=6200, d=320, E=E, k=k, F=128, act="relu", dtype="bf16",
+                     cf=(5, 4), router_std=1 / np.sqrt(320))
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp)
+    f, _ = _ref_all(w, inp, False)
+    _check_full(w, res, inp, f, None)
+
+
+@pytest.mark.parametrize("name", ["switch-small", "gshard-small", "dropless-small", "top1-many-tiles"])
+def test_fused_forward_call(name):
+    """moe_forward (router, dispatch, expert GEMMs with the top-1 combine in the
+    second one's epilogue) against the oracle and the separate calls."""
+    if name == "top1-many-tiles":
+        w = syn.Workload(name, T=6200, d=320, E=40, k=1, F=192, act="relu", dtype="bf16", cf=(1, 1),
+                         router_std=1 / np.sqrt(320))
+    else:
+        w = SMALL[name]
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp, fused=True)
+    sep = run_gpu(w, inp)
+    f, _ = _ref_all(w, inp, False)
+    check_routing(res, f, w)
+    check_router_values(res, f, w.dtype)
+    assert res["device_error"] == 0
+    h_ref, _ = expert_reference(w, inp, f)
+    assert_close(res["h"], h_ref, TOL_BF16, "h")
+    assert_close(res["out"], f["out"], TOL_BF16, "out")
+    assert_close(res["out"], sep["out"], TOL_BF16, "out vs separate calls")
+    dropped = np.all(f["slot"] < 0, axis=1)
+    assert dropped.any() == (w.cf is not None and (f["slot"] < 0).any())
+    assert np.array_equal(res["out"][dropped], inp["x"].astype(np.float64)[dropped]), "dropped tokens must return x"
+
+
 # ------------------------------------------------------------------ edge cases
 def test_capacity_zero_drops_everything():
     w = SMALL["switch-small"].with_(cf=(0, 1), backward=True)
