@@ -43,13 +43,20 @@ __constant__ int kPartB[6] = {0, 1, 0, 2, 1, 0};
 
 // Warp per token; lane holds experts lane, lane + 32, ... When a6 is given
 // (bf16 layers) the row of dh is also written as the six part blocks
-// a6[t, b * EP + e] (zero for e >= E), and offs2 = {0, T}.
+// a6[t, b * EP + e] (zero for e >= E), offs2 = {0, T} and the bounds of the
+// G token ranges of the dW_r split (multiples of 64 rows).
 template <int EPT>
 __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, const int32_t *idx, const float *gate,
                                                         const int32_t *load, const float *dg, int T, int E, int k,
                                                         int renorm, float alpha, float *dh, bf16 *a6, int EP,
-                                                        int32_t *offs2) {
-  if (a6 && blockIdx.x == 0 && threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
+                                                        int32_t *offs2, int G) {
+  if (a6 && blockIdx.x == 0) {
+    if (threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
+    if (threadIdx.x <= G) {
+      const int64_t b = ((int64_t)threadIdx.x * T / G + 63) / 64 * 64;
+      offs2[2 + threadIdx.x] = (int32_t)(b < T ? b : T);
+    }
+  }
   const int lane = threadIdx.x & 31;
   const float aux_scale = alpha * (float)E / ((float)T * (float)T * (float)k);  // alpha E f_e / T = this * load_e
   float base[EPT];
@@ -125,16 +132,22 @@ __global__ void __launch_bounds__(256) router_wsplit6_kernel(const float *w_r, i
   }
 }
 
-// dW_r[e] = (h1^T x)[e] + (h2^T x)[e] + (h3^T x)[e], rows of c3 [3 EP, d].
-__global__ void __launch_bounds__(256) router_dwr_sum_kernel(const float *c3, int E, int EP, int d, float *dw_r) {
+// dW_r[e] = sum over the G token ranges g (in order) of (h1^T x)[e] + (h2^T x)[e] + (h3^T x)[e], rows of
+// c3 [G][3 EP][d].
+__global__ void __launch_bounds__(256) router_dwr_sum_kernel(const float *c3, int E, int EP, int d, int G,
+                                                             float *dw_r) {
   const int64_t n = (int64_t)E * d;
   const int64_t part = (int64_t)EP * d;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n / 4; i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4 *>(c3)[i];
-    const float4 b = reinterpret_cast<const float4 *>(c3 + part)[i];
-    const float4 c = reinterpret_cast<const float4 *>(c3 + 2 * part)[i];
-    reinterpret_cast<float4 *>(dw_r)[i] = make_float4(a.x + b.x + c.x, a.y + b.y + c.y, a.z + b.z + c.z,
-                                                      a.w + b.w + c.w);
+    float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int g = 0; g < G; ++g) {
+      const float *cg = c3 + (int64_t)g * 3 * part;
+      const float4 a = reinterpret_cast<const float4 *>(cg)[i];
+      const float4 b = reinterpret_cast<const float4 *>(cg + part)[i];
+      const float4 c = reinterpret_cast<const float4 *>(cg + 2 * part)[i];
+      r.x += a.x + b.x + c.x; r.y += a.y + b.y + c.y; r.z += a.z + b.z + c.z; r.w += a.w + b.w + c.w;
+    }
+    reinterpret_cast<float4 *>(dw_r)[i] = r;
   }
 }
 
@@ -157,12 +170,13 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   bf16 *b6 = reinterpret_cast<bf16 *>(w + L.rg_b6);
   float *c3 = reinterpret_cast<float *>(w + L.rg_c3);
   int32_t *offs2 = reinterpret_cast<int32_t *>(w + L.rg_offs);
+  const int G = tc ? router_grad_splits(sh) : 0;
   int grid = (sh.T + 7) / 8;
   if (grid > sm_count() * 8) grid = sm_count() * 8;
   cudaError_t err;
 #define MOE_DH(EPT)                                                                                            \
   err = launch_kernel(router_dh_kernel<EPT>, dim3(grid), dim3(256), 0, stream, probs, idx, gate, load, dg, sh.T, sh.E, \
-                   sh.k, sh.renorm, sh.alpha, dh, a6, EP, offs2)
+                   sh.k, sh.renorm, sh.alpha, dh, a6, EP, offs2, G)
   if (sh.E <= 32) MOE_DH(1);
   else if (sh.E <= 64) MOE_DH(2);
   else if (sh.E <= 128) MOE_DH(4);
@@ -173,10 +187,11 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   err = launch_kernel(router_wsplit6_kernel, dim3(grid_for((int64_t)EP * sh.d)), dim3(256), 0, stream, w_r, sh.E, EP,
                    sh.d, b6);
   if (err != cudaSuccess) return err;
-  err = tc_router_grads(sh, EP, a6, b6, x, offs2, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status), stream);
+  err = tc_router_grads(sh, EP, a6, b6, x, offs2, offs2 + 2, G, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status),
+                        stream);
   if (err != cudaSuccess) return err;
   return launch_kernel(router_dwr_sum_kernel, dim3(grid_for((int64_t)sh.E * sh.d / 4)), dim3(256), 0, stream, c3, sh.E,
-                    EP, sh.d, dw_r);
+                       EP, sh.d, G, dw_r);
 }
 
 }  // namespace moe

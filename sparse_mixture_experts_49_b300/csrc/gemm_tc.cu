@@ -38,7 +38,8 @@ constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
 constexpr int THREADS = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAX_E = 256;
 
-struct __align__(8) Smem {
+// Grouped-K: every group has the same tiles, so no prefix array is kept.
+template <bool GK> struct __align__(8) SmemT {
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
   uint64_t acc_full[2];
@@ -46,7 +47,7 @@ struct __align__(8) Smem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
-  int tile_start[MAX_E + 1];
+  int tile_start[GK ? 1 : MAX_E + 1];  // grouped-M: tiles of the groups before e
 };
 // Plain-store epilogues (EPI_STORE, EPI_STORE_F32) stage each warp's 32-row
 // slice in shared memory (128-byte swizzled rows, 4 KB per warp) and write it
@@ -57,11 +58,16 @@ struct __align__(8) Smem {
 constexpr int STAGE_OUT_BYTES = 4096;
 constexpr int EPI_WARPS = 8;
 template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
-template <int GROUP_K> constexpr int stages_of() { return GROUP_K ? 3 : STAGES; }
-template <int GROUP_K, int EPI> constexpr int out_bufs() { return tma_store_epi<EPI>() ? (GROUP_K ? 2 : 1) : 0; }
+#ifndef MOE_GK_RING
+#define MOE_GK_RING 3
+#endif
+template <int GROUP_K> constexpr int stages_of() { return GROUP_K ? MOE_GK_RING : STAGES; }
+template <int GROUP_K, int EPI> constexpr int out_bufs() {
+  return tma_store_epi<EPI>() ? ((GROUP_K && MOE_GK_RING == 3) ? 2 : 1) : 0;
+}
 template <int GROUP_K, int EPI> constexpr size_t smem_bytes() {
   return 1024 /*align slack*/ + (size_t)stages_of<GROUP_K>() * STAGE_BYTES +
-         (size_t)out_bufs<GROUP_K, EPI>() * EPI_WARPS * STAGE_OUT_BYTES + sizeof(Smem);
+         (size_t)out_bufs<GROUP_K, EPI>() * EPI_WARPS * STAGE_OUT_BYTES + sizeof(SmemT<GROUP_K != 0>);
 }
 static_assert(smem_bytes<0, EPI_STORE>() <= 232448 && smem_bytes<1, EPI_STORE>() <= 232448, "shared memory budget");
 
@@ -107,6 +113,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
   constexpr int NST = stages_of<GROUP_K>();
   constexpr int NBUF = out_bufs<GROUP_K, EPI>();
+  using Smem = SmemT<GROUP_K != 0>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -140,7 +147,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
     tc_fence_before();
   }
-  if (warp == 0) {
+  if (!GROUP_K && warp == 0) {
     // tile_start[e] = number of tiles of groups before e
     int carry = 0;
     if (lane == 0) s.tile_start[0] = 0;
@@ -164,7 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
-  const int total_tiles = s.tile_start[E];
+  const int tiles_per_group_k = m_tiles_k * n_tiles;  // grouped-K
+  const int total_tiles = GROUP_K ? E * tiles_per_group_k : s.tile_start[E];
 
   // Group row offsets, written by the dispatch before this launch (read-only here).
   auto off = [&](int i) -> int { return __ldg(p.offsets + i); };
@@ -172,12 +180,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   // that read the same weight tile run side by side and share it through L2.
   // Grouped-K: n-tiles fastest (the activation tiles are small and shared).
   auto decode = [&](int tile, int &e, int &mt, int &nt) {
-    e = find_group(s.tile_start, E, tile);
-    const int local = tile - s.tile_start[e];
     if (GROUP_K) {
+      e = tile / tiles_per_group_k;
+      const int local = tile - e * tiles_per_group_k;
       mt = local / n_tiles;
       nt = local - mt * n_tiles;
     } else {
+      e = find_group(s.tile_start, E, tile);
+      const int local = tile - s.tile_start[e];
       const int m_tiles = (s.tile_start[e + 1] - s.tile_start[e]) / n_tiles;
       nt = local / m_tiles;
       mt = local - nt * m_tiles;
@@ -618,6 +628,16 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   return launch<0, 0, 0, EPI_STORE>(ma, mb, mc, b, stream);
 }
 
+int router_grad_splits(const Shape &sh) {
+  const int ep = sh.E <= 32 ? 32 : sh.E <= 64 ? 64 : sh.E <= 128 ? 128 : 256;
+  const int tiles = ((3 * ep + tc::BM - 1) / tc::BM) * ((sh.d + tc::BN - 1) / tc::BN);
+  int g = (sm_count() + tiles - 1) / tiles;
+  const int most = sh.T / 512 > 1 ? sh.T / 512 : 1;  // at least 512 tokens per range
+  if (g > most) g = most;
+  if (g > 64) g = 64;
+  return g < 1 ? 1 : g;
+}
+
 // Forward expert FFNs whose second GEMM, for top-1 layers, combines in its
 // epilogue: out[t] = x[t] + g[t] * y for the row's token t (no y_perm). For
 // k > 1 the second GEMM writes y_perm and the caller combines.
@@ -742,9 +762,12 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
 //     are below 2^-24 of the result;
 //   C3 [3EP, d] fp32 = A6[:, 3EP:6EP]^T x, i.e. h1^T x, h2^T x and h3^T x
 //     (x is bf16, so every product is exact), summed into dW_r afterwards.
-// offs2 = {0, T}: both GEMMs run as one group of T rows.
+// offs2 = {0, T}: dX_r runs as one group of T rows. dW_r is split over
+// `splits` token ranges (offs_split, multiples of 64 rows) so that enough
+// tiles run; range g writes its three part products to c3 + g [3EP, d].
 cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void *b6, const void *x,
-                            const int32_t *offs2, float *dxr, float *c3, DeviceStatus *st, cudaStream_t stream) {
+                            const int32_t *offs2, const int32_t *offs_split, int splits, float *dxr, float *c3,
+                            DeviceStatus *st, cudaStream_t stream) {
   using namespace tc;
   CUtensorMap ma, mb;
   cudaError_t err;
@@ -762,13 +785,14 @@ cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void 
   }
   {
     Args a{};
-    a.offsets = offs2; a.E = 1; a.F = 0; a.st = st;
+    a.offsets = offs_split; a.E = splits; a.F = 0; a.st = st;
     a.M = 3 * ep; a.N = sh.d;
-    a.C = c3; a.ldc = sh.d; a.sce = 0;
+    a.C = c3; a.ldc = sh.d; a.sce = (int64_t)3 * ep * sh.d;
     CUtensorMap mc;
     if (!make_map_2d_strided(&ma, static_cast<const bf16 *>(a6) + 3 * ep, 3 * (uint64_t)ep, sh.T,
                              6 * (uint64_t)ep * 2, 64, 64) ||
-        !make_map_2d(&mb, x, sh.d, sh.T, 64, 64) || !make_map_3d_f32(&mc, c3, sh.d, 3 * (uint64_t)ep, 1, 32, 32))
+        !make_map_2d(&mb, x, sh.d, sh.T, 64, 64) ||
+        !make_map_3d_f32(&mc, c3, sh.d, 3 * (uint64_t)ep, (uint64_t)splits, 32, 32))
       return cudaErrorInvalidValue;
     err = launch<1, 1, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
   }

@@ -36,7 +36,8 @@ struct WsLayout {
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
   size_t dg, dh, dxr;              // backward: [T, k], [T, E], [T, d] fp32
-  size_t rg_a6, rg_b6, rg_c3, rg_offs;  // bf16 router gradient: [T, 6EP], [6EP, d] bf16; [3EP, d] fp32; {0, T}
+  size_t rg_a6, rg_b6, rg_c3, rg_offs;  // bf16 router gradient: [T, 6EP], [6EP, d] bf16; [G, 3EP, d] fp32;
+                                       // {0, T} then the G + 1 token-range bounds of the dW_r split
   size_t total;
 };
 WsLayout ws_layout(const Shape &sh);
@@ -101,7 +102,10 @@ cudaError_t simt_expert_backward(const Shape &sh, const int32_t *offsets, const 
 // Router gradient GEMMs of a bf16 layer on the tensor cores (exact bf16 parts
 // of dh and W_r; see gemm_tc.cu).
 cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void *b6, const void *x,
-                            const int32_t *offs2, float *dxr, float *c3, DeviceStatus *st, cudaStream_t stream);
+                            const int32_t *offs2, const int32_t *offs_split, int splits, float *dxr, float *c3,
+                            DeviceStatus *st, cudaStream_t stream);
+// Token ranges the dW_r = dh^T x GEMM is split into, so that about one tile per SM runs.
+int router_grad_splits(const Shape &sh);
 
 // Backward pieces outside the grouped GEMMs.
 cudaError_t launch_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *idx,

@@ -81,8 +81,9 @@ WsLayout ws_layout(const Shape &sh) {
   const bool tc = sh.dtype == MOE_BF16;
   L.rg_a6 = take(tc ? (size_t)sh.T * 6 * rp.ep * 2 : 0);
   L.rg_b6 = take(tc ? (size_t)6 * rp.ep * sh.d * 2 : 0);
-  L.rg_c3 = take(tc ? (size_t)3 * rp.ep * sh.d * 4 : 0);
-  L.rg_offs = take(tc ? 8 : 0);
+  const int G = tc ? router_grad_splits(sh) : 0;
+  L.rg_c3 = take(tc ? (size_t)G * 3 * rp.ep * sh.d * 4 : 0);
+  L.rg_offs = take(tc ? (size_t)(2 + G + 1) * 4 : 0);
   L.total = o;
   return L;
 }

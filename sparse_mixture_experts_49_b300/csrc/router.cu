@@ -83,68 +83,107 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
 #pragma unroll
   for (int j = 0; j < EPT; ++j) imp[j] = 0.0f;
 
-  for (int i = 0; i < TPW; ++i) {
-    const int tl = warp * TPW + i, t = t0 + tl;
-    if (t >= a.T) break;
-    float h[EPT], p[EPT];
-    float m = -FLT_MAX;
+  // G tokens of the warp at a time: their reductions are independent, so the
+  // shuffles of one hide the latency of the others. Token order (and so the
+  // order of the importance sums) is unchanged.
+  constexpr int G = TPW < 4 ? TPW : 4;
+  static_assert(TPW % G == 0, "tokens per warp");
+  for (int i0 = 0; i0 < TPW; i0 += G) {
+    float h[G][EPT], p[G][EPT], m[G], z[G];
+    int tt[G];
+    bool live[G];
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = lane + 32 * j;
-      h[j] = (e < E) ? lg[tl * (EP + 1) + e] : -FLT_MAX;
-      m = fmaxf(m, h[j]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float z = 0.0f;
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = lane + 32 * j;
-      p[j] = (e < E) ? expf(h[j] - m) : 0.0f;
-      z += p[j];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    const float inv = 1.0f / z;
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = lane + 32 * j;
-      p[j] = p[j] * inv;
-      if (e < E) {
-        if (a.probs) a.probs[(int64_t)t * E + e] = p[j];
-        imp[j] += p[j];
-      }
-    }
-    // top-k: k rounds of a warp arg-max over the not yet selected experts
-    uint32_t taken = 0;
-    int my_e = 0;
-    float my_p = 0.0f, psum = 0.0f;
-    for (int r = 0; r < a.k; ++r) {
-      float bh = -FLT_MAX;
-      int be = 0x7fffffff;
+    for (int g = 0; g < G; ++g) {
+      const int tl = warp * TPW + i0 + g;
+      tt[g] = t0 + tl;
+      live[g] = tt[g] < a.T;
+      m[g] = -FLT_MAX;
 #pragma unroll
       for (int j = 0; j < EPT; ++j) {
         const int e = lane + 32 * j;
-        if (e < E && !((taken >> j) & 1u) && (h[j] > bh || (h[j] == bh && e < be))) { bh = h[j]; be = e; }
+        h[g][j] = (live[g] && e < E) ? lg[tl * (EP + 1) + e] : -FLT_MAX;
+        m[g] = fmaxf(m[g], h[g][j]);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float oh = __shfl_xor_sync(0xffffffffu, bh, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oh > bh || (oh == bh && oe < be)) { bh = oh; be = oe; }
-      }
-      float pv = 0.0f;
-#pragma unroll
-      for (int j = 0; j < EPT; ++j)
-        if (lane + 32 * j == be) { pv = p[j]; taken |= 1u << j; }
-      const float pe = __shfl_sync(0xffffffffu, pv, be & 31);
-      psum += pe;
-      if (lane == r) { my_e = be; my_p = pe; }
     }
-    if (lane < a.k) {
-      a.idx[(int64_t)t * a.k + lane] = my_e;
-      a.gate[(int64_t)t * a.k + lane] = a.renorm ? my_p / psum : my_p;
-      atomicAdd(&cnt[my_e], 1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) m[g] = fmaxf(m[g], __shfl_xor_sync(0xffffffffu, m[g], o));
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      z[g] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        const int e = lane + 32 * j;
+        p[g][j] = (e < E) ? expf(h[g][j] - m[g]) : 0.0f;
+        z[g] += p[g][j];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) z[g] += __shfl_xor_sync(0xffffffffu, z[g], o);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float inv = 1.0f / z[g];
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        const int e = lane + 32 * j;
+        p[g][j] = p[g][j] * inv;
+        if (live[g] && e < E) {
+          if (a.probs) a.probs[(int64_t)tt[g] * E + e] = p[g][j];
+          imp[j] += p[g][j];
+        }
+      }
+    }
+    // top-k: k rounds of a warp arg-max over the not yet selected experts
+    uint32_t taken[G];
+    int my_e[G];
+    float my_p[G], psum[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) { taken[g] = 0; my_e[g] = 0; my_p[g] = 0.0f; psum[g] = 0.0f; }
+    for (int r = 0; r < a.k; ++r) {
+      float bh[G];
+      int be[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        bh[g] = -FLT_MAX;
+        be[g] = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          const int e = lane + 32 * j;
+          if (e < E && !((taken[g] >> j) & 1u) && (h[g][j] > bh[g] || (h[g][j] == bh[g] && e < be[g]))) {
+            bh[g] = h[g][j];
+            be[g] = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float oh = __shfl_xor_sync(0xffffffffu, bh[g], o);
+          const int oe = __shfl_xor_sync(0xffffffffu, be[g], o);
+          if (oh > bh[g] || (oh == bh[g] && oe < be[g])) { bh[g] = oh; be[g] = oe; }
+        }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float pv = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j)
+          if (lane + 32 * j == be[g]) { pv = p[g][j]; taken[g] |= 1u << j; }
+        const float pe = __shfl_sync(0xffffffffu, pv, be[g] & 31);
+        psum[g] += pe;
+        if (lane == r) { my_e[g] = be[g]; my_p[g] = pe; }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (live[g] && lane < a.k) {
+        a.idx[(int64_t)tt[g] * a.k + lane] = my_e[g];
+        a.gate[(int64_t)tt[g] * a.k + lane] = a.renorm ? my_p[g] / psum[g] : my_p[g];
+        atomicAdd(&cnt[my_e[g]], 1);
+      }
     }
   }
 #pragma unroll
