@@ -136,19 +136,21 @@ def gemm_traffic(workload):
 
 
 # ---------------------------------------------------------------- algorithmic traffic and flops
-def algorithmic(w, K_a: int):
-    """Bytes / FLOPs each call must move or do (kept assignments only, weights read once)."""
+def algorithmic(w, K_a: int, E_used: int):
+    """Bytes / FLOPs each call must move or do (kept assignments only; the weights of the E_used experts
+    that keep at least one token, read once; the expert-gradient outputs cover all E experts)."""
     s = 2  # bf16
     d, F, E, T, k, R1 = w.d, w.F, w.E, w.T, w.k, w.R1
     router_b = T * d * s + E * d * 4 + T * k * 8 + T * E * 4   # x, W_r, idx+gate, probs
     dispatch_b = T * d * s + K_a * d * s + T * k * 4 * 3 + K_a * 4
     act_b = K_a * F * s * 2 + (K_a * 2 * F * s if w.act == "swiglu" else 0)   # h out+in, pre-activations out
-    gemm_b = w.nm * E * F * d * s + K_a * d * s * 2 + act_b   # weights, x_perm in, y_perm out, activations
+    gemm_b = w.nm * E_used * F * d * s + K_a * d * s * 2 + act_b   # weights, x_perm in, y_perm out, activations
     combine_b = T * d * s * 2 + K_a * d * s + T * k * 12
     gemm_flops = 2 * K_a * d * F * w.nm
     # backward: combine bwd (dY, y_perm in; dYp out), four grouped GEMMs (weights in, weight gradients out,
     # dYp / h / pre-activations / dA / x_perm in, dA and dXp out), router gradient, unpermute-reduce
-    bwd_gemm_b = (2 * w.nm * E * F * d * s + 2 * K_a * d * s + K_a * F * s + (K_a * 2 * F * s if w.act == "swiglu" else 0)
+    bwd_gemm_b = (w.nm * (E_used + E) * F * d * s + 2 * K_a * d * s + K_a * F * s
+                  + (K_a * 2 * F * s if w.act == "swiglu" else 0)
                   + 3 * K_a * R1 * s + K_a * d * s + K_a * d * s)
     backward_b = (T * d * s + 2 * K_a * d * s + bwd_gemm_b + T * E * 4 * 2 + T * d * s + E * d * 4 * 2
                   + T * d * 4 * 2 + T * d * s * 2 + K_a * d * s)
@@ -263,6 +265,7 @@ def run_ours(args):
     if L.device_error() != 0:
         raise RuntimeError("device error during warm-up")
     K_a = int(L.offsets[-1].item())
+    E_used = int((L.kept > 0).sum().item())   # experts whose weights the GEMMs read
 
     # per-call breakdown (eager launches, CUDA events between the ABI calls)
     n_eager = min(args.steps, 200)
@@ -397,7 +400,7 @@ def run_ours(args):
     io_bytes = w.T * w.d * 2 * (2 if bwd else 1)
 
     hbm, tflops, tflops_sus, peak_src = load_peaks()
-    alg = algorithmic(w, K_a)
+    alg = algorithmic(w, K_a, E_used)
     mean_call = {c: statistics.mean(v) for c, v in per_call.items()}
     kernels = {}
     for c in calls:
@@ -435,7 +438,7 @@ def run_ours(args):
                    "top_k": w.k, "d_ff": w.F, "act": w.act, "renormalize": w.renormalize,
                    "capacity_factor": None if w.cf is None else f"{w.cf[0]}/{w.cf[1]}", "capacity": cap,
                    "capacity_reading": "floor(k*T*cf/E)" if w.cf is not None else "none (dropless)",
-                   "kept_assignments": K_a, "expert_weights": dv["weights"],
+                   "kept_assignments": K_a, "experts_with_tokens": E_used, "expert_weights": dv["weights"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside the step's events)"},
         "roofline": roof,

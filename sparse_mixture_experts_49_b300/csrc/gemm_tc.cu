@@ -30,7 +30,7 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;             // TMA ring depth (weight-gradient GEMMs: 3, see stages_of)
+constexpr int STAGES = 4;             // TMA ring depth
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -52,22 +52,12 @@ template <bool GK> struct __align__(8) SmemT {
 // Plain-store epilogues (EPI_STORE, EPI_STORE_F32) stage each warp's 32-row
 // slice in shared memory (128-byte swizzled rows, 4 KB per warp) and write it
 // with a TMA tile store.
-// The weight-gradient GEMMs (grouped-K) have a few K steps per tile and a
-// full tile to store, so they trade one ring stage for a second staging
-// buffer per warp: a warp fills one buffer while the TMA engine reads the other.
 constexpr int STAGE_OUT_BYTES = 4096;
 constexpr int EPI_WARPS = 8;
 template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
-#ifndef MOE_GK_RING
-#define MOE_GK_RING 3
-#endif
-template <int GROUP_K> constexpr int stages_of() { return GROUP_K ? MOE_GK_RING : STAGES; }
-template <int GROUP_K, int EPI> constexpr int out_bufs() {
-  return tma_store_epi<EPI>() ? ((GROUP_K && MOE_GK_RING == 3) ? 2 : 1) : 0;
-}
 template <int GROUP_K, int EPI> constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + (size_t)stages_of<GROUP_K>() * STAGE_BYTES +
-         (size_t)out_bufs<GROUP_K, EPI>() * EPI_WARPS * STAGE_OUT_BYTES + sizeof(SmemT<GROUP_K != 0>);
+  return 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES +
+         (tma_store_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) + sizeof(SmemT<GROUP_K != 0>);
 }
 static_assert(smem_bytes<0, EPI_STORE>() <= 232448 && smem_bytes<1, EPI_STORE>() <= 232448, "shared memory budget");
 
@@ -111,14 +101,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const Args p) {
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
-  constexpr int NST = stages_of<GROUP_K>();
-  constexpr int NBUF = out_bufs<GROUP_K, EPI>();
+  constexpr int NST = STAGES;
   using Smem = SmemT<GROUP_K != 0>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t *stage_out = tiles + (size_t)NST * STAGE_BYTES;  // TMA_STORE only: [EPI_WARPS][NBUF][4 KB]
-  Smem &s = *reinterpret_cast<Smem *>(stage_out + NBUF * EPI_WARPS * STAGE_OUT_BYTES);
+  uint8_t *stage_out = tiles + (size_t)NST * STAGE_BYTES;  // TMA_STORE only: [EPI_WARPS][4 KB]
+  Smem &s = *reinterpret_cast<Smem *>(stage_out + (TMA_STORE ? EPI_WARPS * STAGE_OUT_BYTES : 0));
   volatile int *abort_flag = &s.abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -331,7 +320,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int r = q * 32 + lane;       // row inside the 128-row tile
     const int half = (warp - 2) >> 2;  // column half of the tile
-    int obuf = 0;                      // staging buffer the next TMA store uses
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
@@ -347,7 +335,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // stored row by row, so the next group's rows are never touched.
         constexpr bool F32 = (EPI == EPI_STORE_F32);
         constexpr int CPB = F32 ? 1 : 2;  // 32-column chunks per 128-byte staging row
-        uint8_t *stg_base = stage_out + (warp - 2) * NBUF * STAGE_OUT_BYTES;
+        uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
         int nvalid = 32;
         int r0;
         const bool zero = GROUP_K && off(e + 1) == off(e);
@@ -372,12 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
           if (nvalid == 32) {
-            // the store issued from this buffer NBUF stores ago has left it
-            uint8_t *stg = stg_base + obuf * STAGE_OUT_BYTES;
-            if (lane == 0) {
-              if (NBUF == 2) bulk_wait_read_1();
-              else bulk_wait_read_all();
-            }
+            if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
             __syncwarp();
             uint8_t *rowp = stg + lane * 128;
 #pragma unroll
@@ -393,7 +376,6 @@ __global__ void __launch_bounds__(THREADS, 1)
               else tma_store_2d(&tmC, stg, col, r0);
               bulk_commit();
             }
-            if (NBUF == 2) obuf ^= 1;
           } else if (lane < nvalid) {
             const int64_t row = (int64_t)r0 + lane;
             if (F32) {
