@@ -281,6 +281,70 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
     return dict(dx=dx, dw_r=dw_r, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r, slots=s)
 
 
+def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequence[int],
+                     experts_sampled: Sequence[int], k: int, act: str, cf: Optional[Tuple[int, int]],
+                     count_assignments: bool = True, renormalize: bool = False, alpha: float = 0.01) -> dict:
+    """The gradients of `backward` for a few tokens (dx rows) and a few experts
+    (dw1, dw2), without evaluating every expert on every token: the same chain
+    rule through eqs. (1), (2) and (4), taken token by token for dx (each
+    token's kept experts, its gate gradients, its softmax Jacobian, the aux
+    term that depends on the batch only through f) and expert by expert for
+    the weight gradients (the rows the expert kept). Routing and capacity
+    always cover the whole batch."""
+    x64, dy64 = _f64(x), _f64(dy)
+    T, d = x64.shape
+    wr64 = _f64(w_r)
+    E = wr64.shape[0]
+    r = route(x64, wr64, bias, k, renormalize, alpha)
+    C = capacity(T, E, k, cf, count_assignments)
+    s = assign_slots(r["idx"], E, C)
+    p, idx, gate = r["p"], r["idx"], r["gate"]
+
+    def expert_grads(z, dyv, g, e):
+        w1, w2 = _expert(experts, e)
+        fw = expert_ffn(z, w1, w2, act)
+        dyp = g[:, None] * dyv
+        dhid = dyp @ w2
+        if act == "relu":
+            da = dhid * (fw["a"] > 0)
+        else:
+            sg = 1.0 / (1.0 + np.exp(-fw["g"]))
+            da = np.concatenate([dhid * fw["u"] * (sg * (1.0 + fw["g"] * (1.0 - sg))), dhid * silu(fw["g"])], axis=1)
+        return fw, dyp, da, w1
+
+    dx = {}
+    for t in (int(t) for t in tokens):
+        acc = dy64[t].copy()
+        dg = np.zeros(k)
+        for j in range(k):
+            if s["slot"][t, j] < 0:
+                continue
+            e = int(idx[t, j])
+            fw, dyp, da, w1 = expert_grads(x64[t][None, :], dy64[t][None, :], np.array([gate[t, j]]), e)
+            dg[j] = float(np.dot(dy64[t], fw["y"][0]))
+            acc += (da @ w1)[0]
+        dp = np.zeros(E)
+        if renormalize:
+            psel = p[t, idx[t]]
+            dp[idx[t]] = (dg - np.dot(dg, gate[t])) / psel.sum()
+        else:
+            dp[idx[t]] = dg
+        dp += alpha * E * r["f"] / float(T)
+        dh = p[t] * (dp - np.dot(p[t], dp))
+        dx[t] = acc + dh @ wr64
+    dw1, dw2 = {}, {}
+    for e in (int(e) for e in experts_sampled):
+        tt, jj = np.nonzero((idx == e) & (s["slot"] >= 0))
+        w1, w2 = _expert(experts, e)
+        if len(tt) == 0:
+            dw1[e], dw2[e] = np.zeros_like(w1), np.zeros_like(w2)
+            continue
+        fw, dyp, da, _ = expert_grads(x64[tt], dy64[tt], gate[tt, jj], e)
+        dw2[e] = dyp.T @ fw["hid"]
+        dw1[e] = da.T @ x64[tt]
+    return dict(dx=dx, dw1=dw1, dw2=dw2, route=r, slots=s)
+
+
 def loss(x, w_r, bias, experts: ExpertSource, dy, **kw) -> float:
     """L = <dY, out> + aux, the scalar whose gradient `backward` returns."""
     f = forward(x, w_r, bias, experts, **kw)

@@ -52,7 +52,6 @@ __global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, 
     token_rows<KMAX>(t, k, idx, slot, offsets, gate, row, g);
     const XT *xr = x + (int64_t)t * d;
     XT *orow = out + (int64_t)t * d;
-#pragma unroll 2
     for (int v = lane; v < nvec; v += 32) {
       uint4 raw[KMAX + 1];
       raw[0] = *reinterpret_cast<const uint4 *>(xr + v * V);

@@ -333,3 +333,27 @@ def test_gradient_of_aux_term_alone():
     dh = r["p"] * (c[None, :] - (r["p"] * c[None, :]).sum(axis=1, keepdims=True))
     np.testing.assert_allclose(g["dh"], dh, rtol=1e-12, atol=1e-16)
     np.testing.assert_allclose(g["dw_r"], dh.T @ x, rtol=1e-12, atol=1e-16)
+
+
+@pytest.mark.parametrize("wl", [
+    syn.Workload("sampled-relu", T=96, d=16, E=6, k=2, F=12, act="relu", dtype="f32", cf=(3, 4), backward=True),
+    syn.Workload("sampled-swiglu", T=64, d=12, E=5, k=3, F=10, act="swiglu", dtype="f32", cf=None,
+                 renormalize=True, router_std=0.4, zipf_s=1.2, backward=True),
+])
+def test_sampled_backward_matches_full_backward(wl):
+    """The token-by-token / expert-by-expert gradients equal the full backward
+    (itself pinned by finite differences above) on the rows they cover."""
+    inp = syn.make_inputs(wl, dy=True)
+    kw = dict(k=wl.k, act=wl.act, cf=wl.cf, count_assignments=wl.count_assignments, renormalize=wl.renormalize,
+              alpha=wl.alpha)
+    experts = (inp["w1"], inp["w2"])
+    full = O.backward(inp["x"], inp["w_r"], inp["bias"], experts, inp["dy"], **kw)
+    toks = [0, 7, wl.T - 1, wl.T // 2]
+    exps = list(range(wl.E))
+    smp = O.backward_sampled(inp["x"], inp["w_r"], inp["bias"], experts, inp["dy"], tokens=toks,
+                             experts_sampled=exps, **kw)
+    for t in toks:
+        np.testing.assert_allclose(smp["dx"][t], full["dx"][t], rtol=1e-11, atol=1e-13)
+    for e in exps:
+        np.testing.assert_allclose(smp["dw1"][e], full["dw1"][e], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(smp["dw2"][e], full["dw2"][e], rtol=1e-11, atol=1e-13)

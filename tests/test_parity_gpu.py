@@ -199,3 +199,36 @@ def test_full_size_forward_sampled(name):
     check_router_values(res, f, w.dtype)
     assert res["device_error"] == 0
     assert_close(res["out"][sample], f["out"], TOL_BF16, "out (sampled tokens)")
+
+
+def test_full_size_dropless_backward_sampled():
+    """The dropless top-8 SwiGLU layer at its full size, forward + backward as
+    the benchmark runs it: routing bit-exact over the whole batch, dX on
+    sampled tokens and dW1 / dW2 on sampled experts against the oracle's
+    token-by-token / expert-by-expert backward."""
+    import sparse_mixture_experts_49_b300 as moe
+    w = syn.WORKLOADS["dropless-top8-swiglu"]
+    inp = syn.make_inputs(w, dy=True)
+    cfg = moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=w.k, d_ff=w.F, act=w.act, dtype=w.dtype,
+                          renormalize=w.renormalize, capacity=-1, aux_alpha=w.alpha)
+    bf = torch.bfloat16
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(dt)
+    L = moe.MoELayer(cfg)
+    x, w_r, w1, w2, dy = dev(inp["x"], bf), dev(inp["w_r"], torch.float32), dev(inp["w1"], bf), \
+        dev(inp["w2"], bf), dev(inp["dy"], bf)
+    L.forward(x, w_r, w1, w2)
+    dx, dw_r, dw1, dw2 = L.backward(dy)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    rng = np.random.default_rng(11)
+    toks = sorted(rng.choice(w.T, 48, replace=False).tolist())
+    exps = sorted(rng.choice(w.E, 3, replace=False).tolist())
+    ref = O.backward_sampled(inp["x"], inp["w_r"], inp["bias"], (inp["w1"], inp["w2"]), inp["dy"], tokens=toks,
+                             experts_sampled=exps, **oracle_kw(w))
+    assert np.array_equal(L.topk_idx.cpu().numpy(), ref["route"]["idx"])
+    assert np.array_equal(L.slot.cpu().numpy(), ref["slots"]["slot"])
+    got_dx = dx[toks].float().cpu().numpy().astype(np.float64)
+    assert_close(got_dx, np.stack([ref["dx"][t] for t in toks]), TOL_BF16, "dx (sampled tokens)")
+    for e in exps:
+        assert_close(dw1[e].float().cpu().numpy(), ref["dw1"][e], TOL_BF16, f"dw1[{e}]")
+        assert_close(dw2[e].float().cpu().numpy(), ref["dw2"][e], TOL_BF16, f"dw2[{e}]")
