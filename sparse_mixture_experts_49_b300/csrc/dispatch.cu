@@ -164,8 +164,8 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
 
 // Slots, row owners and the row copies for 32 tokens: rank = block base +
 // the rank inside the 256-token block that the counting kernel left in slot;
-// slot = rank if rank < C else -1.
-template <typename XT>
+// slot = rank if rank < C else -1. KMAX >= k bounds the unrolled row stores.
+template <typename XT, int KMAX>
 __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict__ x, const int32_t *__restrict__ idx,
                                                             int T, int d, int E, int k, int64_t C,
                                                             const int32_t *__restrict__ block_base,
@@ -227,8 +227,9 @@ __global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict
         *reinterpret_cast<uint4 *>(out_dropped + (tbase + q[b]) * d + (int64_t)v[b] * V) = u[b];
         continue;
       }
-      for (int j = 0; j < k; ++j) {
-        const int r = rows[q[b]][j];
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        const int r = rows[q[b]][j];   // -1 for j >= k
         if (r >= 0) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)v[b] * V) = u[b];
       }
     }
@@ -252,10 +253,17 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
                              counts, base, kept, offsets, slot, counter, st);
   if (e != cudaSuccess) return e;
   const int nsub = (sh.T + SUB - 1) / SUB;
-  if (sh.dtype == MOE_BF16)
-    return launch_kernel(dispatch_place_kernel<bf16>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T,
-                         sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped);
-  return launch_kernel(dispatch_place_kernel<float>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T,
+  if (sh.dtype == MOE_BF16) {
+#define MOE_PLACE(KM)                                                                                             \
+  return launch_kernel(dispatch_place_kernel<bf16, KM>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T, \
+                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped)
+    if (sh.k == 1) MOE_PLACE(1);
+    if (sh.k == 2) MOE_PLACE(2);
+    if (sh.k <= 4) MOE_PLACE(4);
+    MOE_PLACE(8);
+#undef MOE_PLACE
+  }
+  return launch_kernel(dispatch_place_kernel<float, 8>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T,
                        sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm, (float *)out_dropped);
 }
 
