@@ -236,18 +236,18 @@ def run_ours(args):
     pre_act = L.pre_act if bwd else None
 
     def step(marks=None):
-        if marks: marks[0].record(stream)
+        if marks: marks[0].record(torch.cuda.current_stream())
         moe.moe_router(cfg, x, w_r, bias, L.probs, L.topk_idx, L.topk_gate, L.importance, L.load, L.aux, L.ws)
-        if marks: marks[1].record(stream)
+        if marks: marks[1].record(torch.cuda.current_stream())
         moe.moe_dispatch(cfg, x, L.topk_idx, L.slot, L.kept, L.offsets, L.row_token, L.x_perm, L.ws)
-        if marks: marks[2].record(stream)
+        if marks: marks[2].record(torch.cuda.current_stream())
         moe.moe_expert_gemm(cfg, L.x_perm, L.offsets, w1, w2, pre_act, L.h, L.y_perm, L.ws)
-        if marks: marks[3].record(stream)
+        if marks: marks[3].record(torch.cuda.current_stream())
         moe.moe_combine(cfg, x, L.y_perm, L.topk_idx, L.topk_gate, L.slot, L.offsets, L.out)
-        if marks: marks[4].record(stream)
+        if marks: marks[4].record(torch.cuda.current_stream())
         if bwd:
             moe.moe_backward(cfg, saved, dy, dx, dw_r, dw1, dw2, L.ws)
-            if marks: marks[5].record(stream)
+            if marks: marks[5].record(torch.cuda.current_stream())
 
     def step_fused():
         # the whole forward layer in one call (inference): no y_perm and no combine launch for top-1
@@ -292,6 +292,24 @@ def run_ours(args):
             g.replay()
         torch.cuda.synchronize()
         return g
+
+    # per-call times inside a CUDA graph of the separate calls, with timing events between the calls (no host
+    # launch gaps); the eager figures above are the fallback
+    per_call_source = "eager"
+    try:
+        gm = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nc + 1)]
+        g_m = capture(lambda: step(gm))
+        reps = []
+        for _ in range(min(args.steps, 100)):
+            flush.zero_()
+            g_m.replay()
+            torch.cuda.synchronize()
+            reps.append([gm[j].elapsed_time(gm[j + 1]) for j in range(nc)])
+        per_call = {c: [r[j] for r in reps] for j, c in enumerate(calls)}
+        per_call_source = "graph"
+        del g_m
+    except Exception as exc:  # events inside captured graphs not available: keep the eager figures
+        per_call_source = f"eager ({type(exc).__name__})"
 
     # the separate ABI calls as one graph (reported beside the timed step for forward-only workloads)
     unfused_ms = None
@@ -452,8 +470,9 @@ def run_ours(args):
                      "for top-1)" if not bwd else
                      "moe_router, moe_dispatch, moe_expert_gemm, moe_combine, moe_backward",
         "separate_calls_graph_ms_per_step": None if unfused_ms is None else round(unfused_ms, 5),
-        "timing": "step replayed as one CUDA graph; per-call figures from an eager pass of the separate ABI calls "
-                  "with events between them",
+        "timing": "step replayed as one CUDA graph; per-call figures from the separate ABI calls with events "
+                  "between them, replayed as a CUDA graph (per_call_source)",
+        "per_call_source": per_call_source,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
     }
