@@ -19,6 +19,18 @@
 // warps 2-9 epilogue (two per TMEM lane quarter, one per column half). Two
 // TMEM accumulators let the epilogue of one tile run under the MMAs of the
 // next.
+//
+// Pair tiles (PAIR = 1): the two CTAs of a cluster share one tcgen05 MMA of
+// M = 256 (cta_group::2). Each CTA stages its own 128 rows of A and its half
+// of B's 256 columns (32 KB per K step instead of 48 KB, six stages), and
+// keeps its 128 rows of the accumulator in its own TMEM. The even CTA issues
+// the MMAs; both CTAs run the epilogue on their own rows. Grouped-M: the odd
+// CTA's loads complete on the even CTA's stage barrier, which expects the
+// bytes of both halves. Grouped-K (whose last K step of a group zeroes rows
+// in each CTA's own half): each CTA's loads complete locally and the odd
+// CTA's MMA warp forwards its stage to the even CTA.
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -27,21 +39,23 @@ namespace moe {
 
 namespace tc {
 
-constexpr int BM = 128;
+constexpr int BM = 128;                // accumulator rows per CTA
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;             // TMA ring depth
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
 constexpr int THREADS = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAX_E = 256;
+// TMA ring: four 48 KB stages (one CTA per tile), six 32 KB stages (pair tiles).
+template <int PAIR> constexpr int n_stages() { return PAIR ? 6 : 4; }
+template <int PAIR> constexpr int b_bytes() { return (PAIR ? BN / 2 : BN) * BK * 2; }
+template <int PAIR> constexpr int stage_bytes() { return A_BYTES + b_bytes<PAIR>(); }
 
 // Grouped-K: every group has the same tiles, so no prefix array is kept.
-template <bool GK> struct __align__(8) SmemT {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+template <bool GK, int NST> struct __align__(8) SmemT {
+  uint64_t full[NST];       // this CTA's TMA bytes of the stage have landed
+  uint64_t empty[NST];      // the MMAs reading the stage have completed
+  uint64_t peer_full[NST];  // pair tiles, even CTA: the odd CTA's half of the stage has landed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
@@ -55,11 +69,14 @@ template <bool GK> struct __align__(8) SmemT {
 constexpr int STAGE_OUT_BYTES = 4096;
 constexpr int EPI_WARPS = 8;
 template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
-template <int GROUP_K, int EPI> constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES +
-         (tma_store_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) + sizeof(SmemT<GROUP_K != 0>);
+template <int PAIR, int GROUP_K, int EPI> constexpr size_t smem_bytes() {
+  return 1024 /*align slack*/ + (size_t)n_stages<PAIR>() * stage_bytes<PAIR>() +
+         (tma_store_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) +
+         sizeof(SmemT<GROUP_K != 0, n_stages<PAIR>()>);
 }
-static_assert(smem_bytes<0, EPI_STORE>() <= 232448 && smem_bytes<1, EPI_STORE>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<0, 0, EPI_STORE>() <= 232448 && smem_bytes<0, 1, EPI_STORE>() <= 232448 &&
+                  smem_bytes<1, 0, EPI_STORE>() <= 232448 && smem_bytes<1, 1, EPI_STORE>() <= 232448,
+              "shared memory budget");
 
 struct Args {
   const int32_t *offsets;  // [E + 1] row offsets of the groups
@@ -96,28 +113,38 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 200000000ull) break;  // 0.2 s
 }
 
-template <int GROUP_K, int A_MN, int B_MN, int EPI>
+template <int PAIR, int GROUP_K, int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const Args p) {
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
-  constexpr int NST = STAGES;
-  using Smem = SmemT<GROUP_K != 0>;
+  constexpr int NST = n_stages<PAIR>();
+  constexpr int SB = stage_bytes<PAIR>();
+  constexpr int TM = PAIR ? 2 * BM : BM;  // rows of a tile (over both CTAs of a pair)
+  using Smem = SmemT<GROUP_K != 0, NST>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t *stage_out = tiles + (size_t)NST * STAGE_BYTES;  // TMA_STORE only: [EPI_WARPS][4 KB]
+  uint8_t *stage_out = tiles + (size_t)NST * SB;  // TMA_STORE only: [EPI_WARPS][4 KB]
   Smem &s = *reinterpret_cast<Smem *>(stage_out + (TMA_STORE ? EPI_WARPS * STAGE_OUT_BYTES : 0));
   volatile int *abort_flag = &s.abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int E = p.E;
+  // Pair tiles: rank of this CTA in its pair (0 issues the MMAs), the pair's
+  // index and count; one CTA per tile otherwise.
+  const int crank = PAIR ? (int)cluster_ctarank() : 0;
+  const int unit0 = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int half_row = crank * BM;  // first row of this CTA inside the tile
+  // grouped-M pair tiles: the odd CTA's loads complete on the even CTA's barriers
+  constexpr bool DIRECT = PAIR && !GROUP_K;
   constexpr bool SWIGLU_FWD = (EPI == EPI_SWIGLU);
   // Output columns one tile covers (SwiGLU forward: 128 gate + 128 up accumulators -> 128 outputs).
   constexpr int TN_OUT = SWIGLU_FWD ? 128 : BN;
   const int n_tiles = (p.N + TN_OUT - 1) / TN_OUT;
-  const int m_tiles_k = GROUP_K ? (p.M + BM - 1) / BM : 0;
+  const int m_tiles_k = GROUP_K ? (p.M + TM - 1) / TM : 0;
 
   // ---------------------------------------------------------------- set-up
   if (warp == 0) {
@@ -125,15 +152,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (TMA_STORE) prefetch_tmap(&tmC);
-      for (int i = 0; i < NST; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
-      for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], 8); }
+      for (int i = 0; i < NST; ++i) {
+        mbar_init(&s.full[i], 1);
+        mbar_init(&s.empty[i], 1);
+        mbar_init(&s.peer_full[i], 1);
+      }
+      // pair tiles: the even CTA's acc_empty collects the epilogue warps of both CTAs
+      for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], PAIR ? 16 : 8); }
       mbar_init(&s.drain, 1);
       s.abort_flag = 0;
       fence_barrier_init();
     }
   } else if (warp == 1) {
-    tmem_alloc(&s.tmem_base, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&s.tmem_base, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&s.tmem_base, TMEM_COLS);
+      tmem_relinquish();
+    }
     tc_fence_before();
   }
   if (!GROUP_K && warp == 0) {
@@ -145,7 +182,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       int t = 0;
       if (e < E) {
         const int lo = p.offsets[e], hi = p.offsets[e + 1];
-        t = GROUP_K ? m_tiles_k * n_tiles : ((hi - lo + BM - 1) / BM) * n_tiles;
+        t = ((hi - lo + TM - 1) / TM) * n_tiles;
       }
       int incl = t;
 #pragma unroll
@@ -158,6 +195,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   __syncthreads();
+  if (PAIR) cluster_sync_all();  // both CTAs' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = s.tmem_base;
   const int tiles_per_group_k = m_tiles_k * n_tiles;  // grouped-K
@@ -185,19 +223,49 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto k_steps = [&](int e) -> int {
     return GROUP_K ? (off(e + 1) - off(e) + BK - 1) / BK : (p.K + BK - 1) / BK;
   };
+  // Grouped-K: the last K step of a group may run past its rows. Only the
+  // K16 slices holding group rows are issued (returned), and the rows past
+  // the group inside the last of them are zeroed in this CTA's A and B blocks
+  // (each row is one 128-byte line per 64-wide block) by the calling warp.
+  auto trim_last_step = [&](uint8_t *a_s, int e, int ks, bool &zeroed) -> int {
+    int nkk = BK / 16;
+    zeroed = false;
+    if (GROUP_K) {
+      const int valid = off(e + 1) - (off(e) + ks * BK);
+      if (valid < BK) {
+        nkk = (valid + 15) >> 4;
+        const int nrows = nkk * 16 - valid;
+        zeroed = nrows > 0;
+        if (nrows > 0) {
+          constexpr int NBLK = SB / 8192;  // 64-wide blocks of A and B in the stage
+          const int chunks = nrows * 8;    // 16-byte chunks per block
+          for (int i = lane; i < NBLK * chunks; i += 32) {
+            const int blk = i / chunks, rem = i - blk * chunks;
+            const int row = valid + (rem >> 3), c = rem & 7;
+            *reinterpret_cast<uint4 *>(a_s + blk * 8192 + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        __syncwarp();
+      }
+    }
+    return nkk;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
-    // Lane 0 waits for free stages and issues the tile loads.
+    // Lane 0 waits for free stages and issues this CTA's tile loads.
     const uint64_t pol_a = policy_evict_last();
     // Weight tiles that no other m-tile will read are streamed (evict-first);
     // when groups span several m-tiles they are kept for the other m-tiles.
     const uint64_t pol_b = (!GROUP_K && p.b_once) ? policy_evict_first() : policy_evict_last();
+    // DIRECT, odd CTA: the even CTA's stage barriers (cluster addresses)
+    const uint32_t lead_full0 = DIRECT ? mapa_shared(smem_u32(&s.full[0]), 0) : 0u;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit0; ok && tile < total_tiles; tile += units) {
       int e, mt, nt;
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
@@ -206,32 +274,50 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) got = mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st) ? 1 : 0;
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) { ok = false; break; }
-        uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
+        uint8_t *a_s = tiles + (size_t)stage * SB;
         uint8_t *b_s = a_s + A_BYTES;
-        if (lane == 0) mbar_arrive_expect_tx(&s.full[stage], STAGE_BYTES);
+        // DIRECT: the even CTA expects both halves' bytes; the odd CTA only loads
+        if (lane == 0 && !(DIRECT && crank)) mbar_arrive_expect_tx(&s.full[stage], DIRECT ? 2 * SB : SB);
         __syncwarp();
         const int k0 = ks * BK;
         if (lane == 0) {
           if (!GROUP_K) {
-            const int row0 = off(e) + mt * BM;
-            tma_load_2d(a_s, &tmA, &s.full[stage], k0, row0, pol_a);
+            const uint32_t fb = lead_full0 + 8u * (uint32_t)stage;
+            auto ld2 = [&](void *dst, const CUtensorMap *m, int c0, int c1, uint64_t pol) {
+              if (DIRECT && crank) tma_load_2d_pair(dst, m, fb, c0, c1, pol);
+              else tma_load_2d(dst, m, &s.full[stage], c0, c1, pol);
+            };
+            auto ld3 = [&](void *dst, const CUtensorMap *m, int c0, int c1, int c2, uint64_t pol) {
+              if (DIRECT && crank) tma_load_3d_pair(dst, m, fb, c0, c1, c2, pol);
+              else tma_load_3d(dst, m, &s.full[stage], c0, c1, c2, pol);
+            };
+            const int row0 = off(e) + mt * TM + half_row;
+            ld2(a_s, &tmA, k0, row0, pol_a);
             if (!B_MN) {
+              // B rows of the tile: 128 per CTA of a pair, 256 (two boxes) otherwise
               int r0, r1;
               if (SWIGLU_FWD) { r0 = nt * 128; r1 = p.F + nt * 128; }
               else { r0 = nt * BN; r1 = nt * BN + 128; }
-              tma_load_3d(b_s, &tmB, &s.full[stage], k0, r0, e, pol_b);
-              tma_load_3d(b_s + 16384, &tmB, &s.full[stage], k0, r1, e, pol_b);
+              if (PAIR) {
+                ld3(b_s, &tmB, k0, crank ? r1 : r0, e, pol_b);
+              } else {
+                ld3(b_s, &tmB, k0, r0, e, pol_b);
+                ld3(b_s + 16384, &tmB, k0, r1, e, pol_b);
+              }
             } else {
+              const int c0 = nt * BN + (PAIR ? crank * 128 : 0);
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                tma_load_3d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, k0, e, pol_b);
+              for (int j = 0; j < (PAIR ? 2 : 4); ++j) ld3(b_s + j * 8192, &tmB, c0 + 64 * j, k0, e, pol_b);
             }
           } else {
             const int r0 = off(e) + k0;
+            const int m0 = mt * TM + half_row;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) tma_load_2d(a_s + j * 8192, &tmA, &s.full[stage], mt * BM + 64 * j, r0, pol_a);
+            for (int j = 0; j < 2; ++j) tma_load_2d(a_s + j * 8192, &tmA, &s.full[stage], m0 + 64 * j, r0, pol_a);
+            const int c0 = nt * BN + (PAIR ? crank * 128 : 0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, r0, pol_b);
+            for (int j = 0; j < (PAIR ? 2 : 4); ++j)
+              tma_load_2d(b_s + j * 8192, &tmB, &s.full[stage], c0 + 64 * j, r0, pol_b);
           }
           issued |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -239,54 +325,39 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (++stage == NST) { stage = 0; phase ^= 1; }
       }
     }
-    if (lane == 0 && *abort_flag) {
+    // (DIRECT, odd CTA: its bytes complete on the even CTA's barriers, which
+    // that CTA drains)
+    if (lane == 0 && *abort_flag && !(DIRECT && crank)) {
       for (int i = 0; i < NST; ++i)
         if (issued & (1u << i)) drain_wait(&s.full[i], (issued_parity >> i) & 1);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  } else if (warp == 1 && crank == 0) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC = idesc_bf16_f32(TM, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit0; ok && tile < total_tiles; tile += units) {
       int e, mt, nt;
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
-      if (!mbar_wait_bounded(&s.acc_empty[acc], acc_phase ^ 1, abort_flag, p.st)) { ok = false; break; }
+      if (!mbar_wait_bounded<PAIR != 0>(&s.acc_empty[acc], acc_phase ^ 1, abort_flag, p.st)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
       for (int ks = 0; ks < nk; ++ks) {
         if (!mbar_wait_bounded(&s.full[stage], phase, abort_flag, p.st)) { ok = false; break; }
-        tc_fence_after();
-        uint8_t *a_s = tiles + (size_t)stage * STAGE_BYTES;
+        uint8_t *a_s = tiles + (size_t)stage * SB;
         uint8_t *b_s = a_s + A_BYTES;
-        int nkk = BK / 16;  // K16 slices of this step that hold rows of the group
-        if (GROUP_K) {
-          // The last K step of a group may run past its rows: only the slices
-          // holding group rows are issued, and the rows past the group inside
-          // the last of them are zeroed in both operands (each row is one
-          // 128-byte line per 64-wide block).
-          const int valid = off(e + 1) - (off(e) + ks * BK);
-          if (valid < BK) {
-            nkk = (valid + 15) >> 4;
-            const int nrows = nkk * 16 - valid;
-            if (nrows > 0) {
-              const int chunks = nrows * 8;  // 16-byte chunks per block
-              for (int i = lane; i < 6 * chunks; i += 32) {
-                const int blk = i / chunks, rem = i - blk * chunks;
-                const int row = valid + (rem >> 3), c = rem & 7;
-                uint8_t *base = (blk < 2) ? (a_s + blk * 8192) : (b_s + (blk - 2) * 8192);
-                *reinterpret_cast<uint4 *>(base + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-            }
-            __syncwarp();
-          }
+        bool zeroed;
+        const int nkk = trim_last_step(a_s, e, ks, zeroed);
+        if (PAIR && !DIRECT && !mbar_wait_bounded<true>(&s.peer_full[stage], phase, abort_flag, p.st)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
         if (lane == 0) {
           const uint32_t a0 = smem_u32(a_s), b0 = smem_u32(b_s);
 #pragma unroll
@@ -296,38 +367,74 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      : smem_desc_sw128(a0 + kk * 32, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
                                      : smem_desc_sw128(b0 + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+            if (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+            else tc_mma_bf16(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&s.empty[stage]);
+          if (PAIR) tc_commit_pair_mc(&s.empty[stage], 0x3);
+          else tc_commit(&s.empty[stage]);
         }
         __syncwarp();
         if (++stage == NST) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(&s.acc_full[acc]);
+      if (lane == 0) {
+        if (PAIR) tc_commit_pair_mc(&s.acc_full[acc], 0x3);
+        else tc_commit(&s.acc_full[acc]);
+      }
       __syncwarp();
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (*abort_flag) {
-      if (lane == 0) tc_commit(&s.drain);
+      if (lane == 0) {
+        if (PAIR) tc_commit_pair(&s.drain);
+        else tc_commit(&s.drain);
+      }
       __syncwarp();
       drain_wait(&s.drain, 0);
     }
-  } else {
+  } else if (warp == 1 && !DIRECT) {
+    // ---------------------------------------------------------------- grouped-K pair tiles, odd CTA
+    // Forwards each stage to the even CTA once this CTA's half has landed
+    // (and, in the last K step of a group, its rows past the group are zeroed:
+    // then with release ordering, for those generic writes).
+    const uint32_t peer_full0 = mapa_shared(smem_u32(&s.peer_full[0]), 0);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = unit0; ok && tile < total_tiles; tile += units) {
+      int e, mt, nt;
+      decode(tile, e, mt, nt);
+      const int nk = k_steps(e);
+      for (int ks = 0; ks < nk; ++ks) {
+        if (!mbar_wait_bounded(&s.full[stage], phase, abort_flag, p.st)) { ok = false; break; }
+        bool zeroed;
+        trim_last_step(tiles + (size_t)stage * SB, e, ks, zeroed);
+        if (lane == 0) {
+          if (zeroed) mbar_arrive_cluster(peer_full0 + 8u * (uint32_t)stage);
+          else mbar_arrive_cluster_relaxed(peer_full0 + 8u * (uint32_t)stage);
+        }
+        __syncwarp();
+        if (++stage == NST) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp >= 2) {
     // ---------------------------------------------------------------- epilogue (warps 2..9)
     // Two warps per TMEM lane quarter: warp w reads lanes 32 (w % 4) .. + 31
     // (its rows) and the column half (w - 2) / 4 of the tile.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;       // row inside the 128-row tile
+    const int r = q * 32 + lane;       // row inside this CTA's 128 rows of the tile
     const int half = (warp - 2) >> 2;  // column half of the tile
+    // the accumulator's release goes to the MMA issuer's CTA (rank 0 of a pair)
+    const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(&s.acc_empty[0]), 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+    for (int tile = unit0; tile < total_tiles; tile += units) {
       int e, mt, nt;
       decode(tile, e, mt, nt);
-      if (!mbar_wait_bounded(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
+      if (!mbar_wait_bounded<PAIR != 0>(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
       tc_fence_after();
       const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const int mrow0 = mt * TM + half_row;  // this CTA's first row of the tile (group- or M-relative)
       float v[32], w[32];
       if (TMA_STORE) {
         // This warp's 32-row slice: whole slices go through the staging buffer
@@ -340,11 +447,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         int r0;
         const bool zero = GROUP_K && off(e + 1) == off(e);
         if (!GROUP_K) {
-          const int lo = mt * BM + q * 32;
+          const int lo = mrow0 + q * 32;
           nvalid = min(32, max(0, off(e + 1) - off(e) - lo));
           r0 = off(e) + lo;
         } else {
-          r0 = mt * BM + q * 32;
+          r0 = mrow0 + q * 32;
         }
 #pragma unroll 1
         for (int c = 4 * half; c < 4 * half + 4; c += CPB) {
@@ -391,8 +498,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else if (!GROUP_K) {
         const int rows_e = off(e + 1) - off(e);
-        const bool valid = mt * BM + r < rows_e;
-        const int64_t row = (int64_t)off(e) + mt * BM + r;
+        const bool valid = mrow0 + r < rows_e;
+        const int64_t row = (int64_t)off(e) + mrow0 + r;
         if (EPI == EPI_SWIGLU) {
 #pragma unroll 1
           for (int c = 2 * half; c < 2 * half + 2; ++c) {
@@ -497,7 +604,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         const bool empty_group = off(e + 1) == off(e);
-        const int m = mt * BM + r;
+        const int m = mrow0 + r;
         const int64_t cofs = (int64_t)e * p.sce + (int64_t)m * p.ldc;
 #pragma unroll 1
         for (int c = 4 * half; c < 4 * half + 4; ++c) {
@@ -522,46 +629,111 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s.acc_empty[acc]);
+      if (lane == 0) {
+        if (PAIR) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)acc);
+        else mbar_arrive(&s.acc_empty[acc]);
+      }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (TMA_STORE && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   __syncthreads();
+  // Pair tiles: neither CTA leaves while the other may still reach its shared
+  // memory or TMEM (remote arrivals, the even CTA's MMAs).
+  if (PAIR) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
+    if (PAIR) tmem_dealloc_pair(tmem, TMEM_COLS);
+    else tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 // ---------------------------------------------------------------- host side
-// mc is the output's tile map for the plain-store epilogues (ignored otherwise).
-template <int GROUP_K, int A_MN, int B_MN, int EPI>
-static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc, const Args &a,
-                          cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<GROUP_K, A_MN, B_MN, EPI>;
-  constexpr size_t smem = smem_bytes<GROUP_K, EPI>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
+// Persistent grid: one CTA per SM, or as many CTA pairs as can be resident
+// at once (0 when no cluster of two fits).
+template <int PAIR, int GROUP_K, int A_MN, int B_MN, int EPI>
+static int grid_size() {
+  static int grid = -1;
+  if (grid >= 0) return grid;
+  auto kern = grouped_gemm_kernel<PAIR, GROUP_K, A_MN, B_MN, EPI>;
+  constexpr size_t smem = smem_bytes<PAIR, GROUP_K, EPI>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  if (!PAIR) return grid = sm_count();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sm_count() & ~1);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, (const void *)kern, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    clusters = 0;
   }
-  return launch_kernel(kern, dim3(sm_count()), dim3(THREADS), smem, stream, ma, mb, mc, a);
+  if (clusters > sm_count() / 2) clusters = sm_count() / 2;
+  return grid = 2 * clusters;
+}
+
+// mc is the output's tile map for the plain-store epilogues (ignored otherwise).
+// pair: CTA-pair tiles when a cluster of two fits, one CTA per tile otherwise.
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                          const Args &a, cudaStream_t stream) {
+  if (pair) {
+    const int g = grid_size<1, GROUP_K, A_MN, B_MN, EPI>();
+    if (g > 0)
+      return launch_kernel_cluster(grouped_gemm_kernel<1, GROUP_K, A_MN, B_MN, EPI>, 2, dim3(g), dim3(THREADS),
+                                   smem_bytes<1, GROUP_K, EPI>(), stream, ma, mb, mc, a);
+  }
+  const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
+  if (g <= 0) return cudaErrorInvalidConfiguration;
+  return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, a);
 }
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
-static cudaError_t launch(const CUtensorMap &ma, const CUtensorMap &mb, const Args &a, cudaStream_t stream) {
+static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const Args &a,
+                          cudaStream_t stream) {
   static_assert(!tma_store_epi<EPI>(), "plain-store epilogues need the output map");
-  return launch<GROUP_K, A_MN, B_MN, EPI>(ma, mb, ma, a, stream);
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, ma, a, stream);
+}
+// One CTA per tile only (shapes whose M is not a multiple of a pair tile).
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch_single(const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                                 const Args &a, cudaStream_t stream) {
+  const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
+  if (g <= 0) return cudaErrorInvalidConfiguration;
+  return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, a);
 }
 
 }  // namespace tc
 
 // ---------------------------------------------------------------- launchers used by the C ABI
-// True when the capacity keeps every group within one 128-row tile, so that
-// each weight tile is read by a single m-tile.
-static int weights_read_once(const Shape &sh) { return (sh.C >= 0 && sh.C <= tc::BM) ? 1 : 0; }
+// CTA-pair tiles (256 rows) or one CTA per tile (128 rows). Pair tiles are
+// opt-in: MOE_GEMM_PAIR=1 in the environment selects them for every expert
+// GEMM (grouped-M and grouped-K), anything else or unset keeps one CTA per
+// tile. Measured on the B300: equal speed on the tensor-bound grouped-M
+// GEMMs (the per-SM operand bytes per MMA do not change, half of B arrives
+// from the peer's shared memory), slower on the HBM-bound layers and on
+// grouped-K, whose odd CTA forwards every stage.
+static bool pair_tiles() {
+  const char *v = getenv("MOE_GEMM_PAIR");
+  return v && v[0] == '1';
+}
+static bool pair_grouped_m(const Shape &) { return pair_tiles(); }
+static bool pair_grouped_k(int) { return pair_tiles(); }
+
+// True when the capacity keeps every group within one m-tile (128 rows, 256
+// for pair tiles), so that each weight tile is read by a single m-tile.
+static int weights_read_once(const Shape &sh, bool pair) {
+  return (sh.C >= 0 && sh.C <= (pair ? 2 : 1) * tc::BM) ? 1 : 0;
+}
 
 cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
@@ -569,7 +741,8 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   using namespace tc;
   CUtensorMap ma, mb;
   const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;  // a map needs at least one row
-  const int b_once = weights_read_once(sh);
+  const bool pair = pair_grouped_m(sh);
+  const int b_once = weights_read_once(sh, pair);
   Args a{};
   a.offsets = offsets;
   a.E = sh.E;
@@ -587,9 +760,9 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   if (sh.act == MOE_ACT_SWIGLU) {
     a.C2 = (bf16 *)pre_act;
     a.ldc2 = 2 * (int64_t)sh.F;
-    err = launch<0, 0, 0, EPI_SWIGLU>(ma, mb, a, stream);
+    err = launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, a, stream);
   } else {
-    err = launch<0, 0, 0, EPI_RELU>(ma, mb, a, stream);
+    err = launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
   }
   if (err != cudaSuccess) return err;
   // GEMM 2: A = h [rows, F], B = W2 [E, d, F]
@@ -607,7 +780,7 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   b.ldc = sh.d;
   CUtensorMap mc;
   if (!make_map_2d(&mc, y_perm, sh.d, rows, 64, 32)) return cudaErrorInvalidValue;
-  return launch<0, 0, 0, EPI_STORE>(ma, mb, mc, b, stream);
+  return launch<0, 0, 0, EPI_STORE>(pair, ma, mb, mc, b, stream);
 }
 
 int router_grad_splits(const Shape &sh) {
@@ -631,7 +804,8 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   if (sh.k != 1) return tc_expert_forward(sh, x_perm, offsets, w1, w2, nullptr, h, y_perm, st, stream);
   CUtensorMap ma, mb;
   const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;
-  const int b_once = weights_read_once(sh);
+  const bool pair = pair_grouped_m(sh);
+  const int b_once = weights_read_once(sh, pair);
   Args a{};
   a.offsets = offsets;
   a.E = sh.E;
@@ -645,8 +819,8 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   a.K = sh.d;
   a.C = h;
   a.ldc = sh.F;
-  cudaError_t err = sh.act == MOE_ACT_SWIGLU ? launch<0, 0, 0, EPI_SWIGLU>(ma, mb, a, stream)
-                                             : launch<0, 0, 0, EPI_RELU>(ma, mb, a, stream);
+  cudaError_t err = sh.act == MOE_ACT_SWIGLU ? launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, a, stream)
+                                             : launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
   if (err != cudaSuccess) return err;
   // GEMM 2 + combine: A = h [rows, F], B = W2 [E, d, F]
   if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
@@ -665,7 +839,7 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   b.ldaux = sh.d;
   b.a_rows = row_token;
   b.gate = gate;
-  return launch<0, 0, 0, EPI_COMBINE>(ma, mb, b, stream);
+  return launch<0, 0, 0, EPI_COMBINE>(pair, ma, mb, b, stream);
 }
 
 cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
@@ -676,7 +850,8 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
   const uint64_t rows = sh.rows > 0 ? (uint64_t)sh.rows : 1;
   cudaError_t err;
   const bool swiglu = sh.act == MOE_ACT_SWIGLU;
-  const int b_once = weights_read_once(sh);
+  const bool pair = pair_grouped_m(sh);
+  const int b_once = weights_read_once(sh, pair);
   // dH = dYp W2_e (B MN-major from W2 [E, d, F]), fused activation backward -> dA [rows, R1]
   {
     Args a{};
@@ -688,10 +863,10 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
       return cudaErrorInvalidValue;
     if (swiglu) {
       a.aux = (const bf16 *)pre_act; a.ldaux = 2 * (int64_t)sh.F;
-      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(ma, mb, a, stream);
+      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, a, stream);
     } else {
       a.aux = (const bf16 *)h; a.ldaux = sh.F;
-      err = launch<0, 0, 1, EPI_RELU_BWD>(ma, mb, a, stream);
+      err = launch<0, 0, 1, EPI_RELU_BWD>(pair, ma, mb, a, stream);
     }
     if (err != cudaSuccess) return err;
   }
@@ -705,7 +880,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     if (!make_map_2d(&ma, dyp, sh.d, rows, 64, 64) || !make_map_2d(&mb, h, sh.F, rows, 64, 64) ||
         !make_map_3d(&mc, dw2, sh.F, sh.d, sh.E, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE>(ma, mb, mc, a, stream);
+    err = launch<1, 1, 1, EPI_STORE>(pair_grouped_k(a.M), ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   // dXp = dA W1_e (B MN-major from W1 [E, R1, d]): N = d, K = R1
@@ -719,7 +894,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     if (!make_map_2d(&ma, da, sh.R1, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 64) ||
         !make_map_2d(&mc, dxp, sh.d, rows, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<0, 0, 1, EPI_STORE>(ma, mb, mc, a, stream);
+    err = launch<0, 0, 1, EPI_STORE>(pair, ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   // dW1_e = dA_e^T X_e: M = R1, N = d
@@ -732,7 +907,7 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     if (!make_map_2d(&ma, da, sh.R1, rows, 64, 64) || !make_map_2d(&mb, x_perm, sh.d, rows, 64, 64) ||
         !make_map_3d(&mc, dw1, sh.d, sh.R1, sh.E, 64, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE>(ma, mb, mc, a, stream);
+    err = launch<1, 1, 1, EPI_STORE>(pair_grouped_k(a.M), ma, mb, mc, a, stream);
   }
   return err;
 }
@@ -762,7 +937,7 @@ cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void 
     if (!make_map_2d(&ma, a6, 6 * (uint64_t)ep, sh.T, 64, 128) ||
         !make_map_3d(&mb, b6, sh.d, 6 * (uint64_t)ep, 1, 64, 64) || !make_map_2d_f32(&mc, dxr, sh.d, sh.T, 32, 32))
       return cudaErrorInvalidValue;
-    err = launch<0, 0, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
+    err = launch_single<0, 0, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
     if (err != cudaSuccess) return err;
   }
   {
@@ -776,7 +951,7 @@ cudaError_t tc_router_grads(const Shape &sh, int ep, const void *a6, const void 
         !make_map_2d(&mb, x, sh.d, sh.T, 64, 64) ||
         !make_map_3d_f32(&mc, c3, sh.d, 3 * (uint64_t)ep, (uint64_t)splits, 32, 32))
       return cudaErrorInvalidValue;
-    err = launch<1, 1, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
+    err = launch_single<1, 1, 1, EPI_STORE_F32>(ma, mb, mc, a, stream);
   }
   return err;
 }

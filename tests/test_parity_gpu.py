@@ -187,6 +187,46 @@ def test_empty_experts_and_heavy_skew():
     _check_full(w, res, inp, f, b)
 
 
+# ------------------------------------------------------------------ grouped-GEMM tile modes
+# Layers whose expert groups span several 256-row CTA-pair tiles with ragged
+# ends, and weight-gradient GEMMs whose M is a multiple of 256 (pair-*) or not
+# (dropless-small: d 320, 2F 384, read past M through the tensor map's zero fill).
+PAIR_CASES = {
+    "pair-relu": syn.Workload("pair-relu", T=2048, d=512, E=4, k=2, F=256, act="relu", dtype="bf16", cf=None,
+                              backward=True),
+    "pair-swiglu": syn.Workload("pair-swiglu", T=1536, d=512, E=6, k=4, F=256, act="swiglu", dtype="bf16",
+                                cf=(5, 4), renormalize=True, backward=True),
+    "dropless-small": SMALL["dropless-small"],
+    "gshard-small": SMALL["gshard-small"],
+}
+
+
+@pytest.mark.parametrize("mode", ["1", "0"])
+@pytest.mark.parametrize("name", list(PAIR_CASES))
+def test_gemm_tile_modes(name, mode, monkeypatch):
+    """Every expert GEMM forced onto CTA-pair tiles (MOE_GEMM_PAIR=1) or onto
+    one CTA per tile (0), forward and backward, against the oracle."""
+    monkeypatch.setenv("MOE_GEMM_PAIR", mode)
+    w = PAIR_CASES[name]
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+
+
+@pytest.mark.parametrize("mode", ["1", "0"])
+def test_fused_top1_tile_modes(mode, monkeypatch):
+    """moe_forward's combine epilogue (top-1) on both tile modes, groups of ~1000 rows."""
+    monkeypatch.setenv("MOE_GEMM_PAIR", mode)
+    w = syn.Workload("top1-pair", T=4096, d=256, E=4, k=1, F=512, act="relu", dtype="bf16", cf=(5, 4))
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp, fused=True)
+    f, _ = _ref_all(w, inp, False)
+    check_routing(res, f, w)
+    assert res["device_error"] == 0
+    assert_close(res["out"], f["out"], TOL_BF16, "out")
+
+
 # ------------------------------------------------------------------ full sizes, sampled outputs
 @pytest.mark.parametrize("name", ["switch-base-top1", "gshard-top2-zipf", "dropless-top8-swiglu"])
 def test_full_size_forward_sampled(name):
