@@ -14,134 +14,127 @@
 // order, so the result is exact and reproducible. Two launches:
 //   1. per block of 256 tokens, a bitmap present[e][token] in shared memory
 //      and its per-expert popcounts; the last block to finish scans those
-//      counts over blocks for every expert (block bases, one warp per expert
-//      and 32 blocks per shuffle scan), and derives kept = min(load, C) and
-//      the group offsets (exclusive scan over experts);
-//      The same kernel writes each pair's rank inside its block (popcount of
-//      the bitmap below the token) into slot;
-//   2. per block of 32 tokens, rank = block base + that rank, slot = rank if
-//      rank < C else -1, and the copy of the token's row to each of its kept
-//      rows with 16-byte loads and stores (small blocks spread the copy over
-//      eight times more SMs; each thread keeps eight 16-byte loads in flight).
+//      counts over blocks for every expert (block bases, one thread per
+//      expert with 32 loads in flight), and derives kept = min(load, C) and
+//      the group offsets (exclusive scan over experts). The same kernel
+//      writes each pair's rank inside its block (popcount of the bitmap below
+//      the token) into slot, as -2 - rank;
+//   2. a grid-stride loop over (token, 512-byte chunk) units, one warp per
+//      unit and four units in flight per warp: per (token, j) pair, rank =
+//      block base + that rank, slot = rank if rank < C else -1, the row owner
+//      of each kept pair, and the copy of the token's row to its kept rows.
+//      The loop keeps the 1-read-to-k-writes traffic spread evenly over every
+//      SM whatever the number of tokens.
 #include "common.cuh"
 #include "kernels.h"
+#include "tma_host.h"
 
 namespace moe {
 
 namespace {
 
+#ifndef MOE_DISPATCH_COPY_BLOCKS_PER_SM
+#define MOE_DISPATCH_COPY_BLOCKS_PER_SM 16  // copy grid cap (measured on the B300: 16 > 8 > 4)
+#endif
+
 constexpr int DT = DISPATCH_TOKENS;   // 256 tokens per counting block
 constexpr int WORDS = DT / 32;        // bitmap words per expert
-constexpr int SUB = 32;               // tokens per placing block
-
-// Marks (token, expert) pairs of the 256 tokens from t0 (one per thread).
-// A pair with an expert outside [0, E) or a repeat within one token is left
-// out and, when `st` is given, recorded.
-__device__ __forceinline__ void build_bitmap(uint32_t *present, const int32_t *__restrict__ idx, int T, int E,
-                                             int k, int t0, DeviceStatus *st) {
-  for (int i = threadIdx.x; i < E * WORDS; i += blockDim.x) present[i] = 0;
-  __syncthreads();
-  const int t = t0 + threadIdx.x;
-  if (t < T) {
-    const uint32_t bit = 1u << (threadIdx.x & 31);
-    for (int j = 0; j < k; ++j) {
-      const int e = idx[(int64_t)t * k + j];
-      if (e < 0 || e >= E) {
-        if (st) record_error(st, MOE_DEVERR_BAD_EXPERT, t);
-        continue;
-      }
-      const uint32_t old = atomicOr(&present[e * WORDS + (threadIdx.x >> 5)], bit);
-      if ((old & bit) && st) record_error(st, MOE_DEVERR_DUP_EXPERT, t);
-    }
-  }
-  __syncthreads();
-}
 
 // Per-block expert counts and each pair's rank inside its block (written to
-// local_rank, which is the caller's slot array); the last block scans the
-// counts into block bases and writes kept[] and the group offsets.
+// local_rank, which is the caller's slot array, as -2 - rank; -1 for a pair
+// left out); the last block scans the counts into block bases and writes
+// kept[] and the group offsets.
+//
+// One thread per token of the block: its k experts are read once; a pair
+// with an expert outside [0, E) or a repeat of an earlier pair of the same
+// token is left out (rank -1) and, when `st` is given, recorded. The kept
+// pairs set bit (token) of present[e]; a pair's rank is the number of set
+// bits of present[e] below its token (word prefix + popcount in the word).
+// KMAX >= k bounds the unrolled per-token loops.
+template <int KMAX>
 __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__restrict__ idx, int T, int E, int k,
                                                             int64_t C, int32_t *block_counts, int32_t *block_base,
                                                             int32_t *kept_out, int32_t *offsets_out,
                                                             int32_t *__restrict__ local_rank, unsigned int *counter,
                                                             DeviceStatus *st) {
-  extern __shared__ uint32_t present[];
+  extern __shared__ uint32_t present[];             // [E][WORDS] bitmap, then [E][WORDS] word prefixes
+  int *prefix = reinterpret_cast<int *>(present + E * WORDS);
   __shared__ bool last;
   __shared__ int warp_sums[8];
-  build_bitmap(present, idx, T, E, k, blockIdx.x * DT, st);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  __shared__ int total[256];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int t = blockIdx.x * DT + tid;
+  const bool live = t < T;
+  int ev[KMAX];
+  unsigned ok = 0;  // bit j: pair j is counted
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    ev[j] = (live && j < k) ? idx[(int64_t)t * k + j] : -1;
+    if (live && j < k) {
+      bool good = ev[j] >= 0 && ev[j] < E;
+      if (!good && st) record_error(st, MOE_DEVERR_BAD_EXPERT, t);
+#pragma unroll
+      for (int jj = 0; jj < j; ++jj)
+        if (good && ev[jj] == ev[j]) {
+          good = false;
+          if (st) record_error(st, MOE_DEVERR_DUP_EXPERT, t);
+        }
+      ok |= (good ? 1u : 0u) << j;
+    }
+  }
+  for (int i = tid; i < E * WORDS; i += DT) present[i] = 0;
+  __syncthreads();
+  const uint32_t bit = 1u << lane;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j)
+    if ((ok >> j) & 1u) atomicOr(&present[ev[j] * WORDS + warp], bit);
+  __syncthreads();
+  for (int e = tid; e < E; e += DT) {
     int c = 0;
 #pragma unroll
-    for (int w = 0; w < WORDS; ++w) c += __popc(present[e * WORDS + w]);
+    for (int w = 0; w < WORDS; ++w) {
+      prefix[e * WORDS + w] = c;
+      c += __popc(present[e * WORDS + w]);
+    }
     block_counts[(int64_t)blockIdx.x * E + e] = c;
   }
-  {
-    // rank of each of this thread's pairs among the block's tokens that chose
-    // the same expert (popcount of the bitmap below the token), or -1 for a
-    // pair the bitmap left out (bad index, or a repeat within the token)
-    const int t = blockIdx.x * DT + threadIdx.x;
-    const int word = threadIdx.x >> 5;
-    const uint32_t below = (1u << (threadIdx.x & 31)) - 1u;
-    if (t < T) {
-      for (int j = 0; j < k; ++j) {
-        const int e = idx[(int64_t)t * k + j];
-        bool ok = (e >= 0 && e < E);
-        for (int jj = 0; ok && jj < j; ++jj) ok = idx[(int64_t)t * k + jj] != e;
-        int r = -1;
-        if (ok) {
-          r = __popc(present[e * WORDS + word] & below);
-          for (int w = 0; w < word; ++w) r += __popc(present[e * WORDS + w]);
-        }
-        local_rank[(int64_t)t * k + j] = r;
-      }
+  __syncthreads();
+  if (live) {
+    const uint32_t below = bit - 1u;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      if (j >= k) break;
+      int r = -1;  // -2 - rank for a counted pair (see the placing kernel)
+      if ((ok >> j) & 1u) r = -2 - (prefix[ev[j] * WORDS + warp] + __popc(present[ev[j] * WORDS + warp] & below));
+      local_rank[(int64_t)t * k + j] = r;
     }
   }
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
+  if (tid == 0) last = atomicAdd(counter, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // Block bases: per expert, an exclusive scan of the blocks' counts in block
-  // order. A warp scans one expert at a time, 32 blocks per step; the loads of
-  // all the warp's experts are issued before any is scanned.
-  __shared__ int total[256];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Block bases: per expert (one thread each), an exclusive scan of the
+  // blocks' counts in block order; 32 loads in flight per step.
   const int nb = (int)gridDim.x;
-  constexpr int EPW = 256 / (DT / 32);  // experts per warp at most (E <= 256, 8 warps)
-  int carry[EPW];
+  if (tid < E) {
+    int run = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      int c[32];
 #pragma unroll
-  for (int i = 0; i < EPW; ++i) carry[i] = 0;
-  for (int b0 = 0; b0 < nb; b0 += 32) {
-    const int b = b0 + lane;
-    int c[EPW];
+      for (int i = 0; i < 32; ++i) c[i] = (b0 + i < nb) ? __ldcg(block_counts + (int64_t)(b0 + i) * E + tid) : 0;
 #pragma unroll
-    for (int i = 0; i < EPW; ++i) {
-      const int e = warp + 8 * i;
-      c[i] = (e < E && b < nb) ? __ldcg(block_counts + (int64_t)b * E + e) : 0;
-    }
-#pragma unroll
-    for (int i = 0; i < EPW; ++i) {
-      const int e = warp + 8 * i;
-      if (e >= E) break;
-      int incl = c[i];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
+      for (int i = 0; i < 32; ++i) {
+        if (b0 + i < nb) block_base[(int64_t)(b0 + i) * E + tid] = run;
+        run += c[i];
       }
-      if (b < nb) block_base[(int64_t)b * E + e] = carry[i] + incl - c[i];
-      carry[i] += __shfl_sync(0xffffffffu, incl, 31);
     }
-  }
-#pragma unroll
-  for (int i = 0; i < EPW; ++i) {
-    const int e = warp + 8 * i;
-    if (e < E && lane == 0) total[e] = carry[i];
+    total[tid] = run;
   }
   __syncthreads();
   // kept = min(load, C) and the group offsets (exclusive scan over experts)
-  const int e = threadIdx.x;
+  const int e = tid;
   const int run = (e < E) ? total[e] : 0;
   const int kept = (e < E) ? ((C >= 0 && (int64_t)run > C) ? (int)C : run) : 0;
   int incl = kept;
@@ -159,79 +152,82 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
     offsets_out[e] = before + incl - kept;
   }
   if (e == E - 1) offsets_out[E] = before + incl;
-  if (threadIdx.x == 0) *counter = 0u;
+  if (tid == 0) *counter = 0u;
 }
 
-// Slots, row owners and the row copies for 32 tokens: rank = block base +
-// the rank inside the 256-token block that the counting kernel left in slot;
-// slot = rank if rank < C else -1. KMAX >= k bounds the unrolled row stores.
+// Slots, row owners and row copies: a grid-stride loop over (token,
+// 512-byte chunk) units, one unit per warp and four units in flight per warp
+// (16-byte loads). Lanes j < k resolve the token's pairs: slot[t, j] holds
+// -2 - r (r = rank inside the token's 256-token block) until the unit of
+// chunk 0 replaces it with the final slot (rank = block base + r; slot =
+// rank if rank < C else -1) and writes the kept pair's row owner. Units of
+// other chunks may read either form and derive the same row, offsets[e] +
+// slot. The chunk goes to each kept row of x_perm (if given), or to
+// out_dropped (if given) when the token kept none. KMAX >= k bounds the
+// unrolled row stores.
 template <typename XT, int KMAX>
-__global__ void __launch_bounds__(DT) dispatch_place_kernel(const XT *__restrict__ x, const int32_t *__restrict__ idx,
-                                                            int T, int d, int E, int k, int64_t C,
-                                                            const int32_t *__restrict__ block_base,
-                                                            const int32_t *__restrict__ offsets,
-                                                            int32_t *__restrict__ slot, int32_t *__restrict__ row_token,
-                                                            XT *__restrict__ x_perm, XT *__restrict__ out_dropped) {
-  __shared__ int rows[SUB][8];
-  __shared__ int has_rows[SUB];
-  const int64_t tbase = (int64_t)blockIdx.x * SUB;
-  {
-    // one thread per (token, j) pair of the block's 32 tokens
-    const int tl = threadIdx.x >> 3, j = threadIdx.x & 7;
-    const int64_t t = tbase + tl;
-    int r = -1;
-    if (j < k && t < T) {
-      const int64_t at = t * k + j;
-      const int local = slot[at];
-      int s = -1;
-      if (local >= 0) {
-        const int e = idx[at];
-        const int64_t rank = (int64_t)block_base[(t / DT) * E + e] + local;
-        if (C < 0 || rank < C) {
-          s = (int)rank;
-          r = offsets[e] + s;
-          row_token[r] = (int)t;
-        }
-      }
-      slot[at] = s;
-    }
-    rows[tl][j] = r;
-    const unsigned any = __ballot_sync(0xffffffffu, r >= 0);
-    if (j == 0) has_rows[tl] = (any >> (threadIdx.x & 24)) & 0xffu ? 1 : 0;
-  }
-  __syncthreads();
-  // copy: (token, 16-byte chunk) items spread over the block, 8 loads in flight per thread;
-  // a kept token's row goes to its rows of x_perm (if given), a token with no
-  // kept assignment goes to out_dropped (if given)
-  if (x_perm == nullptr && out_dropped == nullptr) return;
+__global__ void __launch_bounds__(256) dispatch_place_kernel(
+    const XT *__restrict__ x, const int32_t *__restrict__ idx, int T, int d, int E, int k, int64_t C,
+    const int32_t *__restrict__ block_base, const int32_t *__restrict__ offsets, int32_t *slot,
+    int32_t *__restrict__ row_token, XT *__restrict__ x_perm, XT *__restrict__ out_dropped) {
   constexpr int V = Vec16<XT>::N;
+  constexpr int U = 4;  // units in flight per warp
+  const int lane = threadIdx.x & 31;
   const int nvec = d / V;
-  const int items = SUB * nvec;
-  for (int i0 = 0; i0 < items; i0 += 8 * DT) {
-    uint4 u[8];
-    int q[8], v[8];
-    bool want[8];
+  const int nchunk = (nvec + 31) / 32;
+  const int64_t units = (int64_t)T * nchunk;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const bool copy = x_perm != nullptr || out_dropped != nullptr;
+  for (int64_t u0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u0 < units; u0 += U * nwarps) {
+    uint4 val[U];
+    int row[U], tok[U], vv[U], chunk[U], sl[U], ex[U];
+    // x chunks first (they do not depend on the slots), then slot and expert
+    // of the lanes' pairs, then block bases and group offsets
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      const int it = i0 + b * DT + threadIdx.x;
-      q[b] = it / nvec;
-      v[b] = it - q[b] * nvec;
-      want[b] = it < items && tbase + q[b] < T &&
-                (has_rows[q[b]] ? x_perm != nullptr : out_dropped != nullptr);
-      if (want[b]) u[b] = *reinterpret_cast<const uint4 *>(x + (tbase + q[b]) * d + (int64_t)v[b] * V);
+    for (int b = 0; b < U; ++b) {
+      const int64_t u = u0 + b * nwarps;
+      const bool in = u < units;
+      tok[b] = in ? (int)(u / nchunk) : 0;
+      chunk[b] = in ? (int)(u - (int64_t)tok[b] * nchunk) : 0;
+      vv[b] = in ? chunk[b] * 32 + lane : nvec;
+      if (copy && vv[b] < nvec) val[b] = *reinterpret_cast<const uint4 *>(x + (int64_t)tok[b] * d + (int64_t)vv[b] * V);
+      sl[b] = -1;
+      ex[b] = 0;
+      if (in && lane < k) {
+        const int64_t at = (int64_t)tok[b] * k + lane;
+        sl[b] = slot[at];
+        ex[b] = idx[at];
+      }
     }
 #pragma unroll
-    for (int b = 0; b < 8; ++b) {
-      if (!want[b]) continue;
-      if (!has_rows[q[b]]) {
-        *reinterpret_cast<uint4 *>(out_dropped + (tbase + q[b]) * d + (int64_t)v[b] * V) = u[b];
-        continue;
+    for (int b = 0; b < U; ++b) {
+      row[b] = -1;
+      if (sl[b] != -1) {
+        const int e = ex[b];
+        int s2 = sl[b];
+        if (s2 <= -2) {
+          const int64_t rank = (int64_t)block_base[(tok[b] / DT) * E + e] + (-2 - s2);
+          s2 = (C < 0 || rank < C) ? (int)rank : -1;
+          if (chunk[b] == 0) {
+            slot[(int64_t)tok[b] * k + lane] = s2;
+            if (s2 >= 0) row_token[offsets[e] + s2] = tok[b];
+          }
+        }
+        if (s2 >= 0) row[b] = offsets[e] + s2;
       }
+    }
+    if (!copy) continue;
+#pragma unroll
+    for (int b = 0; b < U; ++b) {
+      const bool kept_any = __ballot_sync(0xffffffffu, row[b] >= 0) != 0u;
+      const bool lv = vv[b] < nvec;
 #pragma unroll
       for (int j = 0; j < KMAX; ++j) {
-        const int r = rows[q[b]][j];   // -1 for j >= k
-        if (r >= 0) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)v[b] * V) = u[b];
+        const int r = __shfl_sync(0xffffffffu, row[b], j);  // -1 for j >= k
+        if (lv && r >= 0 && x_perm) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)vv[b] * V) = val[b];
       }
+      if (lv && !kept_any && out_dropped)
+        *reinterpret_cast<uint4 *>(out_dropped + (int64_t)tok[b] * d + (int64_t)vv[b] * V) = val[b];
     }
   }
 }
@@ -248,14 +244,26 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
                                          void *out_dropped, int32_t *counts, int32_t *base, unsigned int *counter,
                                          DeviceStatus *st, cudaStream_t stream) {
   const int nblk = dispatch_blocks(sh);
-  const size_t bm = sizeof(uint32_t) * (size_t)sh.E * WORDS;
-  cudaError_t e = launch_kernel(dispatch_count_kernel, dim3(nblk), dim3(DT), bm, stream, idx, sh.T, sh.E, sh.k, sh.C,
-                             counts, base, kept, offsets, slot, counter, st);
+  const size_t bm = 2 * sizeof(uint32_t) * (size_t)sh.E * WORDS;  // bitmap + word prefixes
+  cudaError_t e;
+#define MOE_COUNT(KM)                                                                                        \
+  e = launch_kernel(dispatch_count_kernel<KM>, dim3(nblk), dim3(DT), bm, stream, idx, sh.T, sh.E, sh.k, sh.C, \
+                    counts, base, kept, offsets, slot, counter, st)
+  if (sh.k == 1) MOE_COUNT(1);
+  else if (sh.k == 2) MOE_COUNT(2);
+  else if (sh.k <= 4) MOE_COUNT(4);
+  else MOE_COUNT(8);
+#undef MOE_COUNT
   if (e != cudaSuccess) return e;
-  const int nsub = (sh.T + SUB - 1) / SUB;
+  // MOE_DISPATCH_COPY_BLOCKS_PER_SM blocks of 8 warps per SM at most (a grid-stride loop)
+  const int vec = sh.dtype == MOE_BF16 ? 8 : 4;
+  const int64_t units = (int64_t)sh.T * ((sh.d / vec + 31) / 32);
+  int64_t g = (units + 31) / 32;
+  if (g > (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count()) g = (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count();
+  const dim3 grid((unsigned)(g > 0 ? g : 1));
   if (sh.dtype == MOE_BF16) {
-#define MOE_PLACE(KM)                                                                                             \
-  return launch_kernel(dispatch_place_kernel<bf16, KM>, dim3(nsub), dim3(DT), 0, stream, (const bf16 *)x, idx, sh.T, \
+#define MOE_PLACE(KM)                                                                                            \
+  return launch_kernel(dispatch_place_kernel<bf16, KM>, grid, dim3(256), 0, stream, (const bf16 *)x, idx, sh.T,   \
                        sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped)
     if (sh.k == 1) MOE_PLACE(1);
     if (sh.k == 2) MOE_PLACE(2);
@@ -263,7 +271,7 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
     MOE_PLACE(8);
 #undef MOE_PLACE
   }
-  return launch_kernel(dispatch_place_kernel<float, 8>, dim3(nsub), dim3(DT), 0, stream, (const float *)x, idx, sh.T,
+  return launch_kernel(dispatch_place_kernel<float, 8>, grid, dim3(256), 0, stream, (const float *)x, idx, sh.T,
                        sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm, (float *)out_dropped);
 }
 

@@ -19,7 +19,8 @@
 //
 // Selection: one warp per token, softmax in fp32 with the row maximum
 // subtracted, then k rounds of a warp arg-max (descending logit, ties to the
-// lower index). Importance and load are summed per block in a fixed order;
+// lower index: a max reduction over order keys of the logits, then a min
+// reduction over the expert indices holding the maximum). Importance and load are summed per block in a fixed order;
 // each block then adds its sums into per-expert accumulators in the
 // workspace: the loads as 32-bit integers, the importance as 64-bit fixed
 // point (units of 2^-32). Integer addition is associative, so the totals do
@@ -62,6 +63,28 @@ template <> __device__ __forceinline__ void load4<bf16>(const bf16 *p, float *o)
   o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xFFFF0000u);
 }
 
+// Order key of a logit: a larger float gives a larger key (-0.0 counts as
+// +0.0, so equal logits have equal keys); every key is above 0.
+__device__ __forceinline__ uint32_t logit_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// The lane's best logit among its experts lane + 32 j (j < EPT) that are
+// below E and not taken: its key (0 if none) and position j. Strict
+// comparison: equal keys keep the lower j, i.e. the lower expert.
+template <int EPT>
+__device__ __forceinline__ void lane_head(const float (&hh)[EPT], uint32_t taken, bool live, int lane, int E,
+                                          uint32_t &hk, int &hj) {
+  hk = 0u;
+  hj = 0;
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const uint32_t key = (live && lane + 32 * j < E && !((taken >> j) & 1u)) ? logit_key(hh[j]) : 0u;
+    if (key > hk) { hk = key; hj = j; }
+  }
+}
+
 template <int EPT, int TOKENS> constexpr size_t select_smem_bytes() {
   constexpr int EP = 32 * EPT;
   return sizeof(float) * ((size_t)TOKENS * (EP + 1) + 8 * EP) + sizeof(int) * EP;
@@ -86,7 +109,7 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
   // G tokens of the warp at a time: their reductions are independent, so the
   // shuffles of one hide the latency of the others. Token order (and so the
   // order of the importance sums) is unchanged.
-  constexpr int G = TPW < 4 ? TPW : 4;
+  constexpr int G = EPT >= 4 ? (TPW < 2 ? TPW : 2) : (TPW < 4 ? TPW : 4);
   static_assert(TPW % G == 0, "tokens per warp");
   for (int i0 = 0; i0 < TPW; i0 += G) {
     float h[G][EPT], p[G][EPT], m[G], z[G];
@@ -136,42 +159,39 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
         }
       }
     }
-    // top-k: k rounds of a warp arg-max over the not yet selected experts
+    // top-k: k rounds of a warp arg-max over the not yet selected experts.
+    // Each lane keeps the order key of its best remaining logit (its head);
+    // a round takes the largest head (one max reduction) and, among the lanes
+    // holding it, the lowest expert index (one min reduction); the winning
+    // lane then drops that expert and recomputes its head.
+    uint32_t hk[G];   // head key (0: nothing left in this lane)
+    int hj[G];        // head position j (expert lane + 32 j)
     uint32_t taken[G];
     int my_e[G];
     float my_p[G], psum[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) { taken[g] = 0; my_e[g] = 0; my_p[g] = 0.0f; psum[g] = 0.0f; }
+    for (int g = 0; g < G; ++g) {
+      taken[g] = 0; my_e[g] = 0; my_p[g] = 0.0f; psum[g] = 0.0f;
+      lane_head<EPT>(h[g], taken[g], live[g], lane, E, hk[g], hj[g]);
+    }
     for (int r = 0; r < a.k; ++r) {
-      float bh[G];
+      uint32_t m[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) m[g] = __reduce_max_sync(0xffffffffu, hk[g]);
       int be[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        bh[g] = -FLT_MAX;
-        be[g] = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < EPT; ++j) {
-          const int e = lane + 32 * j;
-          if (e < E && !((taken[g] >> j) & 1u) && (h[g][j] > bh[g] || (h[g][j] == bh[g] && e < be[g]))) {
-            bh[g] = h[g][j];
-            be[g] = e;
-          }
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float oh = __shfl_xor_sync(0xffffffffu, bh[g], o);
-          const int oe = __shfl_xor_sync(0xffffffffu, be[g], o);
-          if (oh > bh[g] || (oh == bh[g] && oe < be[g])) { bh[g] = oh; be[g] = oe; }
-        }
+      for (int g = 0; g < G; ++g)
+        be[g] = (int)__reduce_min_sync(0xffffffffu, (m[g] != 0u && hk[g] == m[g]) ? (uint32_t)(lane + 32 * hj[g])
+                                                                                 : 0x7fffffffu);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float pv = 0.0f;
+        if (be[g] < E && lane == (be[g] & 31)) {
 #pragma unroll
-        for (int j = 0; j < EPT; ++j)
-          if (lane + 32 * j == be[g]) { pv = p[g][j]; taken[g] |= 1u << j; }
+          for (int j = 0; j < EPT; ++j)
+            if (lane + 32 * j == be[g]) { pv = p[g][j]; taken[g] |= 1u << j; }
+          lane_head<EPT>(h[g], taken[g], live[g], lane, E, hk[g], hj[g]);
+        }
         const float pe = __shfl_sync(0xffffffffu, pv, be[g] & 31);
         psum[g] += pe;
         if (lane == r) { my_e[g] = be[g]; my_p[g] = pe; }
