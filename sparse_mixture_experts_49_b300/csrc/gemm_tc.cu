@@ -69,13 +69,17 @@ template <bool GK, int NST> struct __align__(8) SmemT {
 constexpr int STAGE_OUT_BYTES = 4096;
 constexpr int EPI_WARPS = 8;
 template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
+// Epilogues that stage output tiles in shared memory for TMA tile stores: the
+// plain stores, and the SwiGLU forward (h and the saved pre-activations).
+template <int EPI> constexpr bool staged_epi() { return tma_store_epi<EPI>() || EPI == EPI_SWIGLU; }
 template <int PAIR, int GROUP_K, int EPI> constexpr size_t smem_bytes() {
   return 1024 /*align slack*/ + (size_t)n_stages<PAIR>() * stage_bytes<PAIR>() +
-         (tma_store_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) +
+         (staged_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) +
          sizeof(SmemT<GROUP_K != 0, n_stages<PAIR>()>);
 }
 static_assert(smem_bytes<0, 0, EPI_STORE>() <= 232448 && smem_bytes<0, 1, EPI_STORE>() <= 232448 &&
-                  smem_bytes<1, 0, EPI_STORE>() <= 232448 && smem_bytes<1, 1, EPI_STORE>() <= 232448,
+                  smem_bytes<1, 0, EPI_STORE>() <= 232448 && smem_bytes<1, 1, EPI_STORE>() <= 232448 &&
+                  smem_bytes<0, 0, EPI_SWIGLU>() <= 232448 && smem_bytes<1, 0, EPI_SWIGLU>() <= 232448,
               "shared memory budget");
 
 struct Args {
@@ -116,8 +120,10 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 template <int PAIR, int GROUP_K, int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const Args p) {
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                        const Args p) {
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
+  constexpr bool STAGED = staged_epi<EPI>();
   constexpr int NST = n_stages<PAIR>();
   constexpr int SB = stage_bytes<PAIR>();
   constexpr int TM = PAIR ? 2 * BM : BM;  // rows of a tile (over both CTAs of a pair)
@@ -125,8 +131,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t *stage_out = tiles + (size_t)NST * SB;  // TMA_STORE only: [EPI_WARPS][4 KB]
-  Smem &s = *reinterpret_cast<Smem *>(stage_out + (TMA_STORE ? EPI_WARPS * STAGE_OUT_BYTES : 0));
+  uint8_t *stage_out = tiles + (size_t)NST * SB;  // STAGED only: [EPI_WARPS][4 KB]
+  Smem &s = *reinterpret_cast<Smem *>(stage_out + (STAGED ? EPI_WARPS * STAGE_OUT_BYTES : 0));
   volatile int *abort_flag = &s.abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -151,7 +157,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      if (TMA_STORE) prefetch_tmap(&tmC);
+      if (STAGED) prefetch_tmap(&tmC);
+      if (SWIGLU_FWD) prefetch_tmap(&tmD);
       for (int i = 0; i < NST; ++i) {
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
@@ -501,25 +508,69 @@ __global__ void __launch_bounds__(THREADS, 1)
         const bool valid = mrow0 + r < rows_e;
         const int64_t row = (int64_t)off(e) + mrow0 + r;
         if (EPI == EPI_SWIGLU) {
+          // This warp's 32-row slice and 64 output columns [col0, col0 + 64):
+          // h = silu(G) U and, when saved, the pre-activations G and U. A whole
+          // slice goes through the staging buffer (128-byte swizzled rows,
+          // reused for h, G and U in turn) and one TMA tile store each; a
+          // slice cut by the end of its group is stored row by row, so the
+          // next group's rows are never touched. Accumulator columns: G at
+          // [c 32, + 32), U at 128 + [c 32, + 32) for the warp's chunks c.
+          const int col0 = nt * 128 + half * 64;
+          const int lo = mrow0 + q * 32;
+          const int nvalid = min(32, max(0, rows_e - lo));
+          if (nvalid == 32 && col0 < p.N) {
+            uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+            uint8_t *rowp = stg + lane * 128;
+            const int r0 = off(e) + lo;
+            const int nout = p.C2 ? 3 : 1;
 #pragma unroll 1
-          for (int c = 2 * half; c < 2 * half + 2; ++c) {
-            const int col = nt * 128 + c * 32;
-            tmem_ld32(t_row + c * 32, v);
-            tmem_ld32(t_row + 128 + c * 32, w);
-            if (valid && col < p.N) {
-              float hv[32];
+            for (int o = 0; o < nout; ++o) {  // 0: h, 1: G, 2: U
+              if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
+              __syncwarp();
+#pragma unroll 1
+              for (int c = 0; c < 2; ++c) {
+                const int cc = 2 * half + c;
+                if (o == 0) {
+                  tmem_ld32(t_row + cc * 32, v);
+                  tmem_ld32(t_row + 128 + cc * 32, w);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) hv[i] = silu_f(v[i]) * w[i];
-              bf16 *hp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
+                  for (int i = 0; i < 32; ++i) v[i] = silu_f(v[i]) * w[i];
+                } else {
+                  tmem_ld32(t_row + (o - 1) * 128 + cc * 32, v);
+                }
 #pragma unroll
-              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
-              if (p.C2) {
-                bf16 *gp = p.C2 + row * p.ldc2 + col;
-                bf16 *up = gp + p.F;
+                for (int j = 0; j < 4; ++j)
+                  Vec16<bf16>::store(rowp + (((c * 4 + j) ^ (lane & 7)) << 4), v + 8 * j);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                if (o == 0) tma_store_2d(&tmC, stg, col0, r0);
+                else tma_store_2d(&tmD, stg, (o - 1) * p.F + col0, r0);
+                bulk_commit();
+              }
+            }
+          } else if (nvalid > 0) {
+#pragma unroll 1
+            for (int c = 2 * half; c < 2 * half + 2; ++c) {
+              const int col = nt * 128 + c * 32;
+              tmem_ld32(t_row + c * 32, v);
+              tmem_ld32(t_row + 128 + c * 32, w);
+              if (valid && col < p.N) {
+                float hv[32];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  Vec16<bf16>::store(gp + 8 * i, v + 8 * i);
-                  Vec16<bf16>::store(up + 8 * i, w + 8 * i);
+                for (int i = 0; i < 32; ++i) hv[i] = silu_f(v[i]) * w[i];
+                bf16 *hp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
+                if (p.C2) {
+                  bf16 *gp = p.C2 + row * p.ldc2 + col;
+                  bf16 *up = gp + p.F;
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    Vec16<bf16>::store(gp + 8 * i, v + 8 * i);
+                    Vec16<bf16>::store(up + 8 * i, w + 8 * i);
+                  }
                 }
               }
             }
@@ -635,7 +686,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
-    if (TMA_STORE && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
+    if (STAGED && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   __syncthreads();
@@ -682,25 +733,32 @@ static int grid_size() {
 
 // mc is the output's tile map for the plain-store epilogues (ignored otherwise).
 // pair: CTA-pair tiles when a cluster of two fits, one CTA per tile otherwise.
+// md: the second output map (SwiGLU forward: the pre-activations).
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
-                          const Args &a, cudaStream_t stream) {
+                          const CUtensorMap &md, const Args &a, cudaStream_t stream) {
   if (pair) {
     const int g = grid_size<1, GROUP_K, A_MN, B_MN, EPI>();
     if (g > 0)
       return launch_kernel_cluster(grouped_gemm_kernel<1, GROUP_K, A_MN, B_MN, EPI>, 2, dim3(g), dim3(THREADS),
-                                   smem_bytes<1, GROUP_K, EPI>(), stream, ma, mb, mc, a);
+                                   smem_bytes<1, GROUP_K, EPI>(), stream, ma, mb, mc, md, a);
   }
   const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
   if (g <= 0) return cudaErrorInvalidConfiguration;
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
-                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, a);
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, md, a);
+}
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                          const Args &a, cudaStream_t stream) {
+  static_assert(EPI != EPI_SWIGLU, "the SwiGLU forward epilogue needs the pre-activation map");
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, mc, mc, a, stream);
 }
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const Args &a,
                           cudaStream_t stream) {
-  static_assert(!tma_store_epi<EPI>(), "plain-store epilogues need the output map");
-  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, ma, a, stream);
+  static_assert(!staged_epi<EPI>(), "staged epilogues need the output map");
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, ma, ma, a, stream);
 }
 // One CTA per tile only (shapes whose M is not a multiple of a pair tile).
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
@@ -709,7 +767,7 @@ static cudaError_t launch_single(const CUtensorMap &ma, const CUtensorMap &mb, c
   const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
   if (g <= 0) return cudaErrorInvalidConfiguration;
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
-                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, a);
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, mc, a);
 }
 
 }  // namespace tc
@@ -735,6 +793,23 @@ static int weights_read_once(const Shape &sh, bool pair) {
   return (sh.C >= 0 && sh.C <= (pair ? 2 : 1) * tc::BM) ? 1 : 0;
 }
 
+// GEMM 1 with its activation epilogue (a.C = h, a.C2 = pre-activations or
+// null). The SwiGLU epilogue writes h and the pre-activations through TMA
+// tile stores: output maps with 64-column x 32-row boxes.
+static cudaError_t gemm1_act(const Shape &sh, bool pair, const CUtensorMap &ma, const CUtensorMap &mb,
+                             const tc::Args &a, uint64_t rows, cudaStream_t stream) {
+  using namespace tc;
+  if (sh.act != MOE_ACT_SWIGLU) return launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
+  CUtensorMap mc, md;
+  if (!make_map_2d(&mc, a.C, sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
+  if (a.C2 != nullptr) {
+    if (!make_map_2d(&md, a.C2, 2 * (uint64_t)sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
+  } else {
+    md = mc;
+  }
+  return launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, mc, md, a, stream);
+}
+
 cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
                               const void *w2, void *pre_act, void *h, void *y_perm, DeviceStatus *st,
                               cudaStream_t stream) {
@@ -756,14 +831,9 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   a.K = sh.d;
   a.C = h;
   a.ldc = sh.F;
-  cudaError_t err;
-  if (sh.act == MOE_ACT_SWIGLU) {
-    a.C2 = (bf16 *)pre_act;
-    a.ldc2 = 2 * (int64_t)sh.F;
-    err = launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, a, stream);
-  } else {
-    err = launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
-  }
+  a.C2 = (bf16 *)pre_act;
+  a.ldc2 = 2 * (int64_t)sh.F;
+  cudaError_t err = gemm1_act(sh, pair, ma, mb, a, rows, stream);
   if (err != cudaSuccess) return err;
   // GEMM 2: A = h [rows, F], B = W2 [E, d, F]
   if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
@@ -819,8 +889,7 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   a.K = sh.d;
   a.C = h;
   a.ldc = sh.F;
-  cudaError_t err = sh.act == MOE_ACT_SWIGLU ? launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, a, stream)
-                                             : launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
+  cudaError_t err = gemm1_act(sh, pair, ma, mb, a, rows, stream);
   if (err != cudaSuccess) return err;
   // GEMM 2 + combine: A = h [rows, F], B = W2 [E, d, F]
   if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
