@@ -70,8 +70,11 @@ constexpr int STAGE_OUT_BYTES = 4096;
 constexpr int EPI_WARPS = 8;
 template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || EPI == EPI_STORE_F32; }
 // Epilogues that stage output tiles in shared memory for TMA tile stores: the
-// plain stores, and the SwiGLU forward (h and the saved pre-activations).
-template <int EPI> constexpr bool staged_epi() { return tma_store_epi<EPI>() || EPI == EPI_SWIGLU; }
+// plain stores, and the forward activations (h, and SwiGLU's saved
+// pre-activations).
+template <int EPI> constexpr bool staged_epi() {
+  return tma_store_epi<EPI>() || EPI == EPI_SWIGLU || EPI == EPI_RELU;
+}
 template <int PAIR, int GROUP_K, int EPI> constexpr size_t smem_bytes() {
   return 1024 /*align slack*/ + (size_t)n_stages<PAIR>() * stage_bytes<PAIR>() +
          (staged_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) +
@@ -575,6 +578,34 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
+        } else if (EPI == EPI_RELU && mrow0 + q * 32 + 32 <= rows_e) {
+          // ReLU forward, whole 32-row slice: per 64-column group, h =
+          // relu(acc) staged in 128-byte swizzled rows and written with one
+          // TMA tile store.
+          uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+          uint8_t *rowp = stg + lane * 128;
+          const int r0 = off(e) + mrow0 + q * 32;
+#pragma unroll 1
+          for (int gi = 0; gi < 2; ++gi) {
+            const int col0 = nt * BN + half * 128 + gi * 64;
+            if (col0 >= p.N) break;
+            if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
+            __syncwarp();
+#pragma unroll 1
+            for (int c = 0; c < 2; ++c) {
+              tmem_ld32(t_row + (half * 4 + gi * 2 + c) * 32, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) Vec16<bf16>::store(rowp + (((c * 4 + j) ^ (lane & 7)) << 4), v + 8 * j);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, stg, col0, r0);
+              bulk_commit();
+            }
+          }
         } else {
           // The backward epilogues read saved activations; the loads of G
           // chunks are issued together before any of them is used.
@@ -793,15 +824,15 @@ static int weights_read_once(const Shape &sh, bool pair) {
   return (sh.C >= 0 && sh.C <= (pair ? 2 : 1) * tc::BM) ? 1 : 0;
 }
 
-// GEMM 1 with its activation epilogue (a.C = h, a.C2 = pre-activations or
-// null). The SwiGLU epilogue writes h and the pre-activations through TMA
-// tile stores: output maps with 64-column x 32-row boxes.
+// GEMM 1 with its activation epilogue (a.C = h, a.C2 = SwiGLU pre-activations
+// or null). The epilogues write h (and the pre-activations) through TMA tile
+// stores: output maps with 64-column x 32-row boxes.
 static cudaError_t gemm1_act(const Shape &sh, bool pair, const CUtensorMap &ma, const CUtensorMap &mb,
                              const tc::Args &a, uint64_t rows, cudaStream_t stream) {
   using namespace tc;
-  if (sh.act != MOE_ACT_SWIGLU) return launch<0, 0, 0, EPI_RELU>(pair, ma, mb, a, stream);
   CUtensorMap mc, md;
   if (!make_map_2d(&mc, a.C, sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
+  if (sh.act != MOE_ACT_SWIGLU) return launch<0, 0, 0, EPI_RELU>(pair, ma, mb, mc, a, stream);
   if (a.C2 != nullptr) {
     if (!make_map_2d(&md, a.C2, 2 * (uint64_t)sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
   } else {
