@@ -236,6 +236,28 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
 
 int dispatch_blocks(const Shape &sh) { return (sh.T + DT - 1) / DT; }
 
+// Resident blocks per SM of the placing kernel for this layer's dtype and k
+// (queried once per instantiation).
+template <typename XT, int KMAX> static int place_occupancy() {
+  static int n = -1;
+  if (n < 0) {
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, dispatch_place_kernel<XT, KMAX>, 256, 0) != cudaSuccess) {
+      (void)cudaGetLastError();
+      v = 0;
+    }
+    n = v > 0 ? v : 1;
+  }
+  return n;
+}
+static int place_blocks_per_sm(const Shape &sh) {
+  if (sh.dtype != MOE_BF16) return place_occupancy<float, 8>();
+  if (sh.k == 1) return place_occupancy<bf16, 1>();
+  if (sh.k == 2) return place_occupancy<bf16, 2>();
+  if (sh.k <= 4) return place_occupancy<bf16, 4>();
+  return place_occupancy<bf16, 8>();
+}
+
 // The dispatch launch sequence with its scratch given explicitly: per-block
 // counts and bases [blocks, E], a zero-initialised completion counter, the
 // error word.
@@ -255,11 +277,19 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
   else MOE_COUNT(8);
 #undef MOE_COUNT
   if (e != cudaSuccess) return e;
-  // MOE_DISPATCH_COPY_BLOCKS_PER_SM blocks of 8 warps per SM at most (a grid-stride loop)
+  // Grid of the grid-stride loop (blocks of 8 warps, four units per warp per
+  // pass): one wave of resident blocks when the work fits in two such waves
+  // (latency-bound small layers), else MOE_DISPATCH_COPY_BLOCKS_PER_SM blocks
+  // per SM (measured faster for the large layers).
   const int vec = sh.dtype == MOE_BF16 ? 8 : 4;
   const int64_t units = (int64_t)sh.T * ((sh.d / vec + 31) / 32);
   int64_t g = (units + 31) / 32;
-  if (g > (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count()) g = (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count();
+  const int64_t wave = (int64_t)place_blocks_per_sm(sh) * sm_count();
+  if (g <= 2 * wave) {
+    if (g > wave) g = wave;
+  } else if (g > (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count()) {
+    g = (int64_t)MOE_DISPATCH_COPY_BLOCKS_PER_SM * sm_count();
+  }
   const dim3 grid((unsigned)(g > 0 ? g : 1));
   if (sh.dtype == MOE_BF16) {
 #define MOE_PLACE(KM)                                                                                            \
