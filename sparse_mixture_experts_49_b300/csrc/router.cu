@@ -510,7 +510,8 @@ __global__ void __launch_bounds__(192, 1)
 // Logits = sum of the split partials in split order (+ bias), then selection
 // of 32 tokens per block. Partial rows have stride EP; every thread loads its
 // float4 chunks of all splits before adding, so the loads overlap.
-constexpr int RT_TC = 32;  // tokens per selection block (measured best of 32, 64, 128)
+constexpr int RT_TC = 32;  // tokens per selection block (measured: 32 beats 64 and 128; 16 is faster
+                           // for 16384 tokens but slower for the 8192-token switch-base layer)
 template <int EPT>
 __global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a,
                                                             const StatsOut so) {
