@@ -199,6 +199,12 @@ moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int3
  *   h       [rows, F]      x dtype out
  *   y_perm  [rows, d]      x dtype out
  * Rows past expert_offsets[E] are not written.
+ *
+ * bf16 layers run on tcgen05 tiles of 128 rows, one CTA each. With the
+ * environment variable MOE_GEMM_PAIR=1 (read at every call) the expert GEMMs
+ * of this call and of moe_forward / moe_backward run on CTA-pair tiles
+ * instead (two CTAs of a cluster share an MMA of 256 rows); results agree to
+ * fp32 accumulation order.
  */
 moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm,
                            const int32_t *expert_offsets, const void *w1, const void *w2,
