@@ -18,7 +18,10 @@
 // warp roles: warp 0 TMA producer, warp 1 MMA issuer (and TMEM owner),
 // warps 2-9 epilogue (two per TMEM lane quarter, one per column half). Two
 // TMEM accumulators let the epilogue of one tile run under the MMAs of the
-// next.
+// next. The plain-store and forward-activation epilogues stage each warp's
+// 32 output rows in 128-byte-swizzled shared memory and write them with TMA
+// tile stores; the backward-activation and combine epilogues store rows
+// directly.
 //
 // Pair tiles (PAIR = 1): the two CTAs of a cluster share one tcgen05 MMA of
 // M = 256 (cta_group::2). Each CTA stages its own 128 rows of A and its half
