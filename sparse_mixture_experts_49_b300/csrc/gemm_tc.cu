@@ -49,8 +49,12 @@ constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
 constexpr int THREADS = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAX_E = 256;
-// TMA ring: four 48 KB stages (one CTA per tile), six 32 KB stages (pair tiles).
-template <int PAIR> constexpr int n_stages() { return PAIR ? 6 : 4; }
+// TMA ring: four 48 KB stages (one CTA per tile), six 32 KB stages (pair
+// tiles); one stage less for the SwiGLU backward, whose epilogue buffers the
+// saved activations (8 KB per warp).
+template <int PAIR, int EPI> constexpr int n_stages() {
+  return PAIR ? (EPI == EPI_SWIGLU_BWD ? 4 : 6) : (EPI == EPI_SWIGLU_BWD ? 3 : 4);
+}
 template <int PAIR> constexpr int b_bytes() { return (PAIR ? BN / 2 : BN) * BK * 2; }
 template <int PAIR> constexpr int stage_bytes() { return A_BYTES + b_bytes<PAIR>(); }
 
@@ -76,16 +80,21 @@ template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || E
 // plain stores, and the forward activations (h, and SwiGLU's saved
 // pre-activations).
 template <int EPI> constexpr bool staged_epi() {
-  return tma_store_epi<EPI>() || EPI == EPI_SWIGLU || EPI == EPI_RELU;
+  return tma_store_epi<EPI>() || EPI == EPI_SWIGLU || EPI == EPI_RELU || EPI == EPI_SWIGLU_BWD;
+}
+// Staging bytes per epilogue warp: one 4 KB buffer, two for the SwiGLU
+// backward (G and U in, dG and dU out).
+template <int EPI> constexpr int staging_per_warp() {
+  return staged_epi<EPI>() ? (EPI == EPI_SWIGLU_BWD ? 2 : 1) * STAGE_OUT_BYTES : 0;
 }
 template <int PAIR, int GROUP_K, int EPI> constexpr size_t smem_bytes() {
-  return 1024 /*align slack*/ + (size_t)n_stages<PAIR>() * stage_bytes<PAIR>() +
-         (staged_epi<EPI>() ? (size_t)EPI_WARPS * STAGE_OUT_BYTES : 0) +
-         sizeof(SmemT<GROUP_K != 0, n_stages<PAIR>()>);
+  return 1024 /*align slack*/ + (size_t)n_stages<PAIR, EPI>() * stage_bytes<PAIR>() +
+         (size_t)EPI_WARPS * staging_per_warp<EPI>() + sizeof(SmemT<GROUP_K != 0, n_stages<PAIR, EPI>()>);
 }
 static_assert(smem_bytes<0, 0, EPI_STORE>() <= 232448 && smem_bytes<0, 1, EPI_STORE>() <= 232448 &&
                   smem_bytes<1, 0, EPI_STORE>() <= 232448 && smem_bytes<1, 1, EPI_STORE>() <= 232448 &&
-                  smem_bytes<0, 0, EPI_SWIGLU>() <= 232448 && smem_bytes<1, 0, EPI_SWIGLU>() <= 232448,
+                  smem_bytes<0, 0, EPI_SWIGLU>() <= 232448 && smem_bytes<1, 0, EPI_SWIGLU>() <= 232448 &&
+                  smem_bytes<0, 0, EPI_SWIGLU_BWD>() <= 232448 && smem_bytes<1, 0, EPI_SWIGLU_BWD>() <= 232448,
               "shared memory budget");
 
 struct Args {
@@ -130,15 +139,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const Args p) {
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
   constexpr bool STAGED = staged_epi<EPI>();
-  constexpr int NST = n_stages<PAIR>();
+  constexpr int NST = n_stages<PAIR, EPI>();
+  constexpr int SPW = staging_per_warp<EPI>();
   constexpr int SB = stage_bytes<PAIR>();
   constexpr int TM = PAIR ? 2 * BM : BM;  // rows of a tile (over both CTAs of a pair)
   using Smem = SmemT<GROUP_K != 0, NST>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t *stage_out = tiles + (size_t)NST * SB;  // STAGED only: [EPI_WARPS][4 KB]
-  Smem &s = *reinterpret_cast<Smem *>(stage_out + (STAGED ? EPI_WARPS * STAGE_OUT_BYTES : 0));
+  uint8_t *stage_out = tiles + (size_t)NST * SB;  // STAGED only: [EPI_WARPS][SPW]
+  Smem &s = *reinterpret_cast<Smem *>(stage_out + EPI_WARPS * SPW);
   volatile int *abort_flag = &s.abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -455,7 +465,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // stored row by row, so the next group's rows are never touched.
         constexpr bool F32 = (EPI == EPI_STORE_F32);
         constexpr int CPB = F32 ? 1 : 2;  // 32-column chunks per 128-byte staging row
-        uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+        uint8_t *stg = stage_out + (warp - 2) * SPW;
         int nvalid = 32;
         int r0;
         const bool zero = GROUP_K && off(e + 1) == off(e);
@@ -525,7 +535,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const int lo = mrow0 + q * 32;
           const int nvalid = min(32, max(0, rows_e - lo));
           if (nvalid == 32 && col0 < p.N) {
-            uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+            uint8_t *stg = stage_out + (warp - 2) * SPW;
             uint8_t *rowp = stg + lane * 128;
             const int r0 = off(e) + lo;
             const int nout = p.C2 ? 3 : 1;
@@ -585,7 +595,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           // ReLU forward, whole 32-row slice: per 64-column group, h =
           // relu(acc) staged in 128-byte swizzled rows and written with one
           // TMA tile store.
-          uint8_t *stg = stage_out + (warp - 2) * STAGE_OUT_BYTES;
+          uint8_t *stg = stage_out + (warp - 2) * SPW;
           uint8_t *rowp = stg + lane * 128;
           const int r0 = off(e) + mrow0 + q * 32;
 #pragma unroll 1
@@ -609,11 +619,75 @@ __global__ void __launch_bounds__(THREADS, 1)
               bulk_commit();
             }
           }
+        } else if (EPI == EPI_SWIGLU_BWD && mrow0 + q * 32 + 32 <= rows_e) {
+          // SwiGLU backward, whole 32-row slice, per 64-column group: the
+          // slice's saved G and U are read with coalesced 16-byte loads (8
+          // lanes per 128-byte row piece, all 16 loads of a lane in flight
+          // together) into this warp's two 4 KB buffers (128-byte swizzled
+          // rows). Each lane then takes its row's G and U from them, forms
+          // dG = dH U silu'(G) and dU = dH silu(G) in place, and the two
+          // buffers go out as TMA tile stores into dA = [dG | dU].
+          uint8_t *bg = stage_out + (warp - 2) * SPW;  // G, then dG
+          uint8_t *bu = bg + STAGE_OUT_BYTES;          // U, then dU
+          const int64_t rbase = (int64_t)off(e) + mrow0 + q * 32;
+          const int piece = lane & 7;
+#pragma unroll 1
+          for (int gi = 0; gi < 2; ++gi) {
+            const int col0 = nt * BN + half * 128 + gi * 64;
+            if (col0 >= p.N) break;
+            if (lane == 0) bulk_wait_read_all();  // the previous group's stores have left the buffers
+            __syncwarp();
+            {
+              uint4 lg[8], lu[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int rr = 4 * i + (lane >> 3);
+                const bf16 *src = p.aux + (rbase + rr) * p.ldaux + col0 + piece * 8;
+                lg[i] = *reinterpret_cast<const uint4 *>(src);
+                lu[i] = *reinterpret_cast<const uint4 *>(src + p.F);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int rr = 4 * i + (lane >> 3);
+                const int o = rr * 128 + ((piece ^ (rr & 7)) << 4);
+                *reinterpret_cast<uint4 *>(bg + o) = lg[i];
+                *reinterpret_cast<uint4 *>(bu + o) = lu[i];
+              }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              tmem_ld32(t_row + (half * 4 + gi * 2 + c) * 32, v);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int o = lane * 128 + (((c * 4 + i) ^ (lane & 7)) << 4);
+                float gg[8], uu[8], dgv[8], duv[8];
+                Vec16<bf16>::load(bg + o, gg);
+                Vec16<bf16>::load(bu + o, uu);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float sg = 1.0f / (1.0f + expf(-gg[j]));
+                  const float dh = v[8 * i + j];
+                  duv[j] = dh * gg[j] * sg;                                      // dU = dH * silu(G)
+                  dgv[j] = dh * uu[j] * (sg * (1.0f + gg[j] * (1.0f - sg)));     // dG = dH * U * silu'(G)
+                }
+                Vec16<bf16>::store(bg + o, dgv);
+                Vec16<bf16>::store(bu + o, duv);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, bg, col0, (int)rbase);
+              tma_store_2d(&tmC, bu, p.F + col0, (int)rbase);
+              bulk_commit();
+            }
+          }
         } else {
           // The backward epilogues read saved activations; the loads of G
           // chunks are issued together before any of them is used.
           constexpr int NAUX = (EPI == EPI_SWIGLU_BWD) ? 8 : ((EPI == EPI_RELU_BWD || EPI == EPI_COMBINE) ? 4 : 0);
-          constexpr int G = (EPI == EPI_SWIGLU_BWD) ? 2 : 4;
+          constexpr int G = (EPI == EPI_SWIGLU_BWD) ? 1 : 4;  // (SwiGLU: only slices cut by a group end come here)
           // combine (top-1): the output and residual rows are the token's own
           int64_t orow = row;
           float gt = 0.0f;
@@ -966,7 +1040,9 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
       return cudaErrorInvalidValue;
     if (swiglu) {
       a.aux = (const bf16 *)pre_act; a.ldaux = 2 * (int64_t)sh.F;
-      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, a, stream);
+      CUtensorMap mc;  // dA [rows, 2F], 64-column x 32-row store boxes
+      if (!make_map_2d(&mc, da, sh.R1, rows, 64, 32)) return cudaErrorInvalidValue;
+      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, mc, a, stream);
     } else {
       a.aux = (const bf16 *)h; a.ldaux = sh.F;
       err = launch<0, 0, 1, EPI_RELU_BWD>(pair, ma, mb, a, stream);
