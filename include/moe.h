@@ -297,6 +297,14 @@ moe_status moe_backward_intermediates(const moe_config *cfg, void *ws, void **dy
  * `ws` since the last call (MOE_DEVERR_*) in *code, and clears it. */
 moe_status moe_get_device_error(void *ws, moe_stream_t stream, int32_t *code);
 
+/* Self-test of the bounded on-chip waits the kernels use (every mbarrier wait
+ * gives up after 4 s without progress, records MOE_DEVERR_TIMEOUT in the
+ * workspace's error word and lets its kernel return). Launches one block that
+ * runs that wait on a barrier nothing completes: after about 4 s the wait gives
+ * up and the block exits. Afterwards moe_get_device_error reports
+ * MOE_DEVERR_TIMEOUT. `ws` is any workspace (only its error word is used). */
+moe_status moe_selftest_bounded_wait(void *ws, moe_stream_t stream);
+
 const char *moe_status_string(moe_status s);
 /* Text of the last CUDA error seen by a call that returned MOE_ERR_CUDA. */
 const char *moe_last_cuda_error(void);

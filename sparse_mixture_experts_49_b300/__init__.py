@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_capacity", "moe_max_rows", "moe_workspace_size", "moe_workspace_init", "moe_router",
     "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_forward", "moe_backward",
     "moe_backward_intermediates",
-    "moe_get_device_error", "moe_status_string", "moe_last_cuda_error",
+    "moe_get_device_error", "moe_selftest_bounded_wait", "moe_status_string", "moe_last_cuda_error",
 ]
 
 
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
                                                           ctypes.POINTER(P), ctypes.POINTER(P),
                                                           ctypes.POINTER(P)]),
             "moe_get_device_error": (ctypes.c_int, [P, P, ctypes.POINTER(I32)]),
+            "moe_selftest_bounded_wait": (ctypes.c_int, [P, P]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "moe_last_cuda_error": (ctypes.c_char_p, []),
         }
@@ -210,6 +211,13 @@ def moe_get_device_error(ws, stream=None) -> int:
     code = ctypes.c_int32(0)
     _check(lib().moe_get_device_error(_ptr(ws), _stream(stream), ctypes.byref(code)), "moe_get_device_error")
     return code.value
+
+
+def moe_selftest_bounded_wait(ws, stream=None) -> None:
+    """Runs the kernels' bounded on-chip wait on a barrier nothing completes; the wait gives up after its
+    limit (about 4 s) and records MOE_DEVERR_TIMEOUT in the workspace's error word (read it with
+    moe_get_device_error)."""
+    _check(lib().moe_selftest_bounded_wait(_ptr(ws), _stream(stream)), "moe_selftest_bounded_wait")
 
 
 # ---------------------------------------------------------------- convenience wrapper

@@ -113,6 +113,9 @@ def test_null_and_misaligned_pointers_rejected_before_launch():
     s.pre_act = None
     st = L.moe_backward(ctypes.byref(cfg(act="swiglu")), ctypes.byref(s), P, P, P, P, P, P, null)
     assert st == moe.MOE_ERR_INVALID_ARG
+    # the bounded-wait self-test needs a workspace
+    assert L.moe_selftest_bounded_wait(null, null) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_bounded_wait(P + 4, null) == moe.MOE_ERR_ALIGNMENT
 
 
 def test_forward_call_validation():

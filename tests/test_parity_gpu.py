@@ -227,6 +227,29 @@ def test_fused_top1_tile_modes(mode, monkeypatch):
     assert_close(res["out"], f["out"], TOL_BF16, "out")
 
 
+# ------------------------------------------------------------------ bounded waits
+def test_bounded_wait_gives_up_and_reports_timeout():
+    """The kernels' on-chip wait, run on a barrier nothing completes, gives up
+    after its limit, records MOE_DEVERR_TIMEOUT and returns; the context stays
+    usable (a layer runs correctly afterwards)."""
+    import time
+    import sparse_mixture_experts_49_b300 as moe
+    ws = torch.zeros(4096, dtype=torch.uint8, device="cuda")
+    assert moe.moe_get_device_error(ws) == moe.MOE_DEVERR_NONE
+    t0 = time.perf_counter()
+    moe.moe_selftest_bounded_wait(ws)
+    code = moe.moe_get_device_error(ws)
+    dt = time.perf_counter() - t0
+    assert code == moe.MOE_DEVERR_TIMEOUT
+    assert 3.0 < dt < 30.0, dt
+    assert moe.moe_get_device_error(ws) == moe.MOE_DEVERR_NONE   # read clears the word
+    w = SMALL["switch-small"]
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp)
+    f, _ = _ref_all(w, inp, False)
+    _check_full(w, res, inp, f, None)
+
+
 # ------------------------------------------------------------------ full sizes, sampled outputs
 @pytest.mark.parametrize("name", ["switch-base-top1", "gshard-top2-zipf", "dropless-top8-swiglu"])
 def test_full_size_forward_sampled(name):
