@@ -220,6 +220,39 @@ def moe_selftest_bounded_wait(ws, stream=None) -> None:
     _check(lib().moe_selftest_bounded_wait(_ptr(ws), _stream(stream)), "moe_selftest_bounded_wait")
 
 
+# ---------------------------------------------------------------- logging figures
+def _host(a):
+    """A torch tensor (any device) or array-like as a float64 numpy array."""
+    import numpy as np
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def balance_stats(importance, load, kept, T: int, k: int, alpha: float = 0.01) -> dict:
+    """Load-balance figures of one routed batch, for logging, from the router's per-expert importance
+    (sum over tokens of the routing probability) and load (top-k assignments), and the dispatch's kept counts:
+
+    - drop_rate = 1 - sum(kept) / (T k), the share of assignments over capacity;
+    - max_over_mean_load = max(load) / mean(load);
+    - cv2_importance, cv2_load: squared coefficients of variation (population variance / mean^2);
+    - aux = alpha E sum_e f_e P_e with f_e = load_e / (T k) and P_e = importance_e / T, the
+      load-balancing loss the router also returns ("Mixture of Experts (MoE) を1から解説 — Switch
+      Transformerのルーティングと負荷分散", eq. (4))."""
+    imp, ld, kp = _host(importance), _host(load), _host(kept)
+    E = ld.shape[0]
+    mean_ld = ld.mean()
+    f = ld / (T * k)
+    P = imp / T
+    return {
+        "drop_rate": 1.0 - kp.sum() / (T * k),
+        "max_over_mean_load": float(ld.max() / mean_ld) if mean_ld > 0 else 0.0,
+        "cv2_importance": float(imp.var() / imp.mean() ** 2) if imp.mean() > 0 else 0.0,
+        "cv2_load": float(ld.var() / mean_ld ** 2) if mean_ld > 0 else 0.0,
+        "aux": float(alpha * E * (f * P).sum()),
+    }
+
+
 # ---------------------------------------------------------------- convenience wrapper
 class MoELayer:
     """Buffers for one layer shape, and the forward/backward call sequences."""
@@ -285,6 +318,13 @@ class MoELayer:
         dw2 = dw2 if dw2 is not None else torch.empty(c.n_experts, c.d_model, c.d_ff, dtype=self.dt, device=dev)
         moe_backward(c, self._saved, dy, dx, dw_r, dw1, dw2, self.ws, self.stream)
         return dx, dw_r, dw1, dw2
+
+    def balance_stats(self) -> dict:
+        """balance_stats() of the last routed batch (synchronises the device first)."""
+        import torch
+        torch.cuda.synchronize()
+        c = self.cfg
+        return balance_stats(self.importance, self.load, self.kept, c.T, c.top_k, c.aux_alpha)
 
     def device_error(self) -> int:
         return moe_get_device_error(self.ws, self.stream)

@@ -23,6 +23,8 @@
 //     error word is private to the library, so they are not reported.
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -66,7 +68,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace moe
 
-extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+static moe_status dispatch_noalloc_impl(const moe_config *cfg, const void *x, const int32_t *topk_idx,
                                            int32_t *slot, int32_t *kept, int32_t *expert_offsets,
                                            int32_t *row_token, void *x_perm, moe_stream_t stream) {
   using namespace moe;
@@ -92,4 +94,13 @@ extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x,
   if (e != cudaSuccess) return report_cuda(e);
   return report_cuda(launch_dispatch_with_scratch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm,
                                                   nullptr, counts, bases, counter, status, (cudaStream_t)stream));
+}
+
+extern "C" moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int32_t *topk_idx,
+                                           int32_t *slot, int32_t *kept, int32_t *expert_offsets,
+                                           int32_t *row_token, void *x_perm, moe_stream_t stream) {
+  nvtxRangePushA("moe_dispatch_noalloc");  // NVTX range over the call (a no-op without a tool attached)
+  const moe_status s = dispatch_noalloc_impl(cfg, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, stream);
+  nvtxRangePop();
+  return s;
 }

@@ -6,6 +6,8 @@
 #include <cstdio>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -98,6 +100,16 @@ moe_status report_cuda(cudaError_t e) { return cuda_status(e); }
 
 using namespace moe;
 
+// NVTX range over one ABI call, named after it (shown on Nsight timelines;
+// without a tool attached the push and pop do nothing).
+struct NvtxRange {
+  explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange &) = delete;
+  NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define MOE_NVTX(name) NvtxRange moe_nvtx_range_(name)
+
 #define MOE_CHECK(expr)                 \
   do {                                  \
     moe_status _s = (expr);             \
@@ -149,6 +161,7 @@ moe_status moe_workspace_init(const moe_config *cfg, void *ws, moe_stream_t stre
 moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
                       float *probs, int32_t *topk_idx, float *topk_gate, float *importance, int32_t *load,
                       float *aux_loss, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_router");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance); MOE_PTR(load);
@@ -161,6 +174,7 @@ moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, co
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx, int32_t *slot,
                         int32_t *kept, int32_t *expert_offsets, int32_t *row_token, void *x_perm, void *ws,
                         moe_stream_t stream) {
+  MOE_NVTX("moe_dispatch");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(x); MOE_PTR(topk_idx); MOE_PTR(slot); MOE_PTR(kept); MOE_PTR(expert_offsets); MOE_PTR(row_token);
@@ -172,6 +186,7 @@ moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *top
 moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm, const int32_t *expert_offsets,
                            const void *w1, const void *w2, void *pre_act, void *h, void *y_perm, void *ws,
                            moe_stream_t stream) {
+  MOE_NVTX("moe_expert_gemm");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(x_perm); MOE_PTR(expert_offsets); MOE_PTR(w1); MOE_PTR(w2); MOE_PTR(h); MOE_PTR(y_perm); MOE_PTR(ws);
@@ -189,6 +204,7 @@ moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm, const int3
 moe_status moe_combine(const moe_config *cfg, const void *x, const void *y_perm, const int32_t *topk_idx,
                        const float *topk_gate, const int32_t *slot, const int32_t *expert_offsets, void *out,
                        moe_stream_t stream) {
+  MOE_NVTX("moe_combine");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_PTR(x); MOE_PTR(y_perm); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(slot); MOE_PTR(expert_offsets);
@@ -203,6 +219,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r, c
                        float *importance, int32_t *load, float *aux_loss, int32_t *slot, int32_t *kept,
                        int32_t *expert_offsets, int32_t *row_token, void *x_perm, void *h, void *y_perm, void *out,
                        void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_forward");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_REQUIRE(sh.dtype == MOE_BF16, MOE_ERR_UNSUPPORTED);
@@ -227,6 +244,7 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r, c
 
 moe_status moe_backward(const moe_config *cfg, const moe_saved *sv, const void *dy, void *dx, float *dw_r,
                         void *dw1, void *dw2, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_backward");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
   MOE_REQUIRE(sv != nullptr, MOE_ERR_INVALID_ARG);

@@ -283,6 +283,9 @@ def test_full_size_dropless_backward_sampled():
     dx, dw_r, dw1, dw2 = L.backward(dy)
     torch.cuda.synchronize()
     assert L.device_error() == 0
+    st = L.balance_stats()                        # logging figures from the layer's own statistics
+    assert st["drop_rate"] == 0.0                 # dropless
+    assert st["aux"] == pytest.approx(float(L.aux.item()), rel=1e-5)
     rng = np.random.default_rng(11)
     toks = sorted(rng.choice(w.T, 48, replace=False).tolist())
     exps = sorted(rng.choice(w.E, 3, replace=False).tolist())
