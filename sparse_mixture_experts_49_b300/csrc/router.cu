@@ -57,11 +57,6 @@ template <> __device__ __forceinline__ void load4<float>(const float *p, float *
   float4 v = *reinterpret_cast<const float4 *>(p);
   o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
 }
-template <> __device__ __forceinline__ void load4<bf16>(const bf16 *p, float *o) {
-  uint2 u = *reinterpret_cast<const uint2 *>(p);
-  o[0] = __uint_as_float(u.x << 16); o[1] = __uint_as_float(u.x & 0xFFFF0000u);
-  o[2] = __uint_as_float(u.y << 16); o[3] = __uint_as_float(u.y & 0xFFFF0000u);
-}
 
 // Order key of a logit: a larger float gives a larger key (-0.0 counts as
 // +0.0, so equal logits have equal keys); every key is above 0.
