@@ -1,14 +1,23 @@
 """Benchmark of the MoE FFN layer on B300.
 
 One step = one pass of the whole layer over one batch. By default that is
-the forward pass (router -> dispatch -> expert grouped GEMM -> combine, as
-the single moe_forward call) of the Switch-Base-like top-1 workload: T = 8192 tokens (16 x 512), d_model 768,
-128 experts, ReLU FFN 768 -> 3072 -> 768, capacity factor 1.25, bf16
-activations and experts with an fp32 router. `--workload` picks another of
-the bf16 workloads and `--pass fwdbwd` adds the backward pass (moe_backward)
-to every step. Inputs are seeded synthetic data of the workload's shape,
-resident in HBM before timing. The L2 cache is flushed (a 256 MiB write)
-before every timed step, outside the step's CUDA events.
+the forward and backward pass (moe_router -> moe_dispatch -> moe_expert_gemm
+-> moe_combine -> moe_backward) of the large fine-grained training layer:
+T = 4096 tokens, d_model 7168, 256 experts, top-8, SwiGLU FFN
+7168 -> 2048 -> 7168, capacity factor 1.25, bf16 experts with an fp32
+router and the alpha = 0.01 load-balancing loss in the backward pass.
+`--workload` picks another bf16 workload; `--pass fwd` times the forward
+alone, as the single moe_forward call. Inputs (tokens, router weights, every
+expert's weights, the upstream gradient) are the seeded synthetic draws of
+moe_synth, the same the parity tests give the oracle; they are resident in
+HBM before timing. The L2 cache is flushed (a 256 MiB write) before every
+timed step, outside the step's CUDA events.
+
+Besides the step time the JSON line carries, per kernel of the step, its
+launch duration measured with CUDA events by replaying that kernel's node of
+the captured step graph alone (after an L2 flush), its algorithmic bytes and
+FLOPs, and the fraction of the measured HBM or bf16 peak they reach; the
+`roofline` object is the step's longest launch.
 
 Prints one JSON line. `--impl reference` times the CPU oracle instead (the
 reference arm of this build: a plain fp64 restatement of the layer).
@@ -18,9 +27,10 @@ parallel replicas, no collective on the data path); time = max over ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
-import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -33,18 +43,10 @@ sys.path.insert(0, ROOT)
 
 import moe_synth as syn  # noqa: E402
 
-WORKLOAD = "switch-base-top1"
+WORKLOAD = "large-top8-swiglu"
 METRIC = "MoE-layer tokens/s fwd & fwd+bwd; grouped-GEMM % bf16 peak; dispatch % HBM BW"
 L2_FLUSH_BYTES = 256 << 20
-# kernels of the library per call of the bf16 layer: router (W_r split, tensor-core logits, selection +
-# statistics) 3, dispatch (count + scan, slots + row copy) 2, grouped GEMM 2, combine 1. moe_forward runs
-# the same, but top-1 layers combine inside the second grouped-GEMM launch.
-def forward_launches(w, fused_call: bool) -> int:
-    combine = 0 if (fused_call and w.k == 1) else 1
-    return 3 + 2 + 2 + combine
-# moe_backward of the bf16 layer: combine backward 1, grouped GEMMs 4, router logit gradient 1, W_r split 1,
-# router gradient GEMMs 2, dW_r part sum 1, unpermute-reduce 1
-LAUNCHES_BACKWARD = 11
+CSRC = os.path.join(ROOT, "sparse_mixture_experts_49_b300", "csrc")
 
 
 def load_peaks():
@@ -87,7 +89,6 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -96,9 +97,6 @@ class ClockSampler:
                  "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
-
-    def mark(self, which):
-        setattr(self, which, time.time())
 
     def stop(self):
         if self.proc is None:
@@ -116,28 +114,9 @@ class ClockSampler:
                 "samples": len(sm), "reasons": reasons}
 
 
-# ---------------------------------------------------------------- measured DRAM traffic (from an ncu capture)
-def gemm_source_hash() -> str:
-    import hashlib
-    h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "common.cuh"):
-        h.update(open(os.path.join(ROOT, "sparse_mixture_experts_49_b300", "csrc", f), "rb").read())
-    return h.hexdigest()[:16]
-
-
-def gemm_traffic(workload):
-    """dram read+write bytes per moe_expert_gemm call, from profiles/traffic.json, or None when the
-    counters were taken on a different version of the GEMM kernel source."""
-    try:
-        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[workload]
-        return t["gemm_bytes_per_call"] if t.get("source_hash") == gemm_source_hash() else None
-    except Exception:
-        return None
-
-
 # ---------------------------------------------------------------- algorithmic traffic and flops
 def algorithmic(w, K_a: int, E_used: int):
-    """Bytes / FLOPs each call must move or do (kept assignments only; the weights of the E_used experts
+    """Bytes / FLOPs each ABI call must move or do (kept assignments only; the weights of the E_used experts
     that keep at least one token, read once; the expert-gradient outputs cover all E experts)."""
     s = 2  # bf16
     d, F, E, T, k, R1 = w.d, w.F, w.E, w.T, w.k, w.R1
@@ -159,36 +138,199 @@ def algorithmic(w, K_a: int, E_used: int):
                 backward=backward_b, backward_flops=backward_flops, bwd_gemm_flops=2 * gemm_flops)
 
 
+def gemm_launch_algorithmic(role: str, w, K_a: int, E_used: int, training: bool):
+    """(bytes, FLOPs) one grouped-GEMM launch must move / do: the weights of the experts that keep tokens read
+    once (weight-gradient outputs: every expert's written once), the packed activation rows it reads and
+    writes once, kept rows only."""
+    s = 2
+    d, F, E, R1 = w.d, w.F, w.E, w.R1
+    swiglu = w.act == "swiglu"
+    if role == "gemm1":       # x_perm W1^T -> h (+ SwiGLU pre-activations when training)
+        b = E_used * R1 * d * s + K_a * d * s + K_a * F * s + (K_a * 2 * F * s if swiglu and training else 0)
+        return b, 2 * K_a * R1 * d
+    if role == "gemm2":       # h W2^T -> y_perm
+        return E_used * d * F * s + K_a * F * s + K_a * d * s, 2 * K_a * d * F
+    if role == "gemm2_combine":   # h W2^T, gated residual sum into out (kept rows: x read, out written)
+        return E_used * d * F * s + K_a * F * s + 2 * K_a * d * s, 2 * K_a * d * F
+    if role == "dH":          # dYp W2 -> activation backward -> dA (reads the saved pre-activations or h)
+        saved = K_a * 2 * F * s if swiglu else K_a * F * s
+        return E_used * d * F * s + K_a * d * s + saved + K_a * R1 * s, 2 * K_a * d * F
+    if role == "dW2":         # dYp^T h per expert -> dW2 (all E written)
+        return E * d * F * s + K_a * d * s + K_a * F * s, 2 * K_a * d * F
+    if role == "dXp":         # dA W1 -> dXp
+        return E_used * R1 * d * s + K_a * R1 * s + K_a * d * s, 2 * K_a * R1 * d
+    if role == "dW1":         # dA^T x_perm per expert -> dW1 (all E written)
+        return E * R1 * d * s + K_a * R1 * s + K_a * d * s, 2 * K_a * R1 * d
+    raise ValueError(role)
+
+
+# ---------------------------------------------------------------- kernel roles from their names
+_GEMM_ARGS = re.compile(r"grouped_gemm_kernel<(\d+), (\d+), (\d+), (\d+), (\d+)>")
+# the ABI call each library kernel belongs to (kernel name -> call)
+_CALL_OF = [("router_dh", "backward"), ("router_wsplit6", "backward"), ("router_dwr_sum", "backward"),
+            ("router", "router"), ("dispatch", "dispatch"), ("combine_backward", "backward"),
+            ("unpermute", "backward"), ("combine", "combine")]
+
+
+def demangle(names):
+    """C++ names of mangled kernel symbols (c++filt; the names unchanged when it is missing)."""
+    try:
+        r = subprocess.run(["c++filt"], input="\n".join(names), capture_output=True, text=True, timeout=30)
+        out = r.stdout.splitlines()
+        if r.returncode == 0 and len(out) == len(names):
+            return out
+    except Exception:
+        pass
+    return list(names)
+
+
+def kernel_roles(names):
+    """(role, ABI call) of each launch of one step, in launch order, from the demangled kernel names:
+    grouped-GEMM launches by their template arguments (PAIR, GROUP_K, A_MN, B_MN, EPI) and position (the first
+    grouped-K launch of the backward pass is dW2, the second dW1), every other kernel by its own name."""
+    roles, gk = [], 0
+    for n in names:
+        m = _GEMM_ARGS.search(n)
+        if m:
+            _, group_k, _, b_mn, epi = (int(v) for v in m.groups())
+            if epi == 5:
+                roles.append(("router_grad_dW_r" if group_k else "router_grad_dX_r", "backward"))
+            elif group_k:
+                roles.append(("dW2" if gk == 0 else "dW1", "backward"))
+                gk += 1
+            elif epi in (1, 2):
+                roles.append(("gemm1", "gemm"))
+            elif epi == 6:
+                roles.append(("gemm2_combine", "gemm"))
+            elif epi in (3, 4):
+                roles.append(("dH", "backward"))
+            elif b_mn:
+                roles.append(("dXp", "backward"))
+            else:
+                roles.append(("gemm2", "gemm"))
+            continue
+        head = re.split(r"[<(]", n.replace("(anonymous namespace)", "anon").replace("void ", "", 1), maxsplit=1)[0]
+        ident = head.split("::")[-1].strip()
+        call = next((c for key, c in _CALL_OF if key in ident), "other")
+        roles.append((ident, call))
+    return roles
+
+
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# the sources each kernel role is built from (a measured traffic figure holds while they are unchanged)
+def role_sources(role: str):
+    if role.startswith(("gemm", "dH", "dW", "dXp", "router_grad")):
+        return ("gemm_tc.cu", "common.cuh")
+    if role.startswith("router"):
+        return ("router.cu", "common.cuh") if "dh" not in role and "split6" not in role and "dwr" not in role \
+            else ("backward.cu", "common.cuh")
+    if role.startswith("dispatch"):
+        return ("dispatch.cu", "common.cuh")
+    return ("combine.cu", "common.cuh")
+
+
+def measured_traffic(workload: str, role: str):
+    """dram read + write bytes per launch of `role` from profiles/traffic.json, or None when the counters were
+    taken on a different version of the kernel's source (or not at all)."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[workload][role]
+        return t["dram_bytes_per_launch"] if t.get("source_hash") == source_hash(role_sources(role)) else None
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------- per-kernel times by replaying graph nodes
+def _drv_ok(res):
+    from cuda.bindings import driver as drv
+    err = res[0] if isinstance(res, tuple) else res
+    if err != drv.CUresult.CUDA_SUCCESS:
+        raise RuntimeError(f"CUDA driver call failed: {err}")
+    return res[1:] if isinstance(res, tuple) else None
+
+
+def replay_kernels_alone(step, stream, flush, reps: int):
+    """Captures `step` into a CUDA graph, then launches each of its kernel nodes alone (a one-node graph with
+    the node's parameters and launch attributes), `reps` times, each after an L2 flush, between two CUDA
+    events on `stream`. Returns [(mangled name, mean ms)] in launch order. Every library kernel overwrites
+    its outputs from its inputs, so replaying one kernel of the step alone repeats the same work."""
+    import torch
+    from cuda.bindings import driver as drv
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = drv.CUgraph(g.raw_cuda_graph())
+    n = _drv_ok(drv.cuGraphGetRootNodes(graph, 0))[1]
+    roots = _drv_ok(drv.cuGraphGetRootNodes(graph, n))[0]
+    order, frontier, seen = [], list(roots), set()
+    while frontier:                              # stream capture of one stream: a chain
+        node = frontier.pop(0)
+        key = int(node)
+        if key in seen:
+            continue
+        seen.add(key)
+        order.append(node)
+        m = _drv_ok(drv.cuGraphNodeGetDependentNodes(node, 0))[1]
+        if m:
+            frontier.extend(_drv_ok(drv.cuGraphNodeGetDependentNodes(node, m))[0])
+    s_handle = drv.CUstream(stream.cuda_stream)
+    out = []
+    for node in order:
+        if _drv_ok(drv.cuGraphNodeGetType(node))[0] != drv.CUgraphNodeType.CU_GRAPH_NODE_TYPE_KERNEL:
+            continue
+        params = _drv_ok(drv.cuGraphKernelNodeGetParams(node))[0]
+        func = params.func
+        if not int(func):
+            func = _drv_ok(drv.cuKernelGetFunction(params.kern))[0]
+        name = _drv_ok(drv.cuFuncGetName(func))[0]
+        name = name.decode() if isinstance(name, bytes) else str(name)
+        g1 = _drv_ok(drv.cuGraphCreate(0))[0]
+        n1 = _drv_ok(drv.cuGraphAddKernelNode(g1, None, 0, params))[0]
+        _drv_ok(drv.cuGraphKernelNodeCopyAttributes(n1, node))
+        ex = _drv_ok(drv.cuGraphInstantiate(g1, 0))[0]
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for _ in range(2):                       # warm-up launches
+            _drv_ok(drv.cuGraphLaunch(ex, s_handle))
+        for a, b in evs:
+            flush.zero_()
+            a.record(stream)
+            _drv_ok(drv.cuGraphLaunch(ex, s_handle))
+            b.record(stream)
+        torch.cuda.synchronize()
+        out.append((name, statistics.mean(a.elapsed_time(b) for a, b in evs)))
+        _drv_ok(drv.cuGraphExecDestroy(ex))
+        _drv_ok(drv.cuGraphDestroy(g1))
+    del g
+    return out
+
+
 # ---------------------------------------------------------------- inputs on the device
-DEVICE_DRAW_BYTES = 8 << 30   # expert weights above this size are drawn on the GPU (host draws take minutes)
-
-
 def device_inputs(w, want_dy: bool):
-    """x, W_r, bias (and dY) from moe_synth (margin-conditioned); expert weights per expert from moe_synth,
-    or, for the largest workloads, from torch's seeded Philox generator on the GPU with the same
-    distribution N(0, 0.1 / sqrt(fan_in)), rounded to bf16."""
+    """x, W_r, bias (and dY) from moe_synth (margin-conditioned), and every expert's weights from moe_synth's
+    per-expert draws (threaded), uploaded as bf16."""
     import torch
     bf = torch.bfloat16
     inp = syn.make_inputs(w, experts=False, dy=want_dy)
     dev = {"x": torch.from_numpy(inp["x"]).cuda().to(bf), "w_r": torch.from_numpy(inp["w_r"]).cuda(),
            "bias": None if inp["bias"] is None else torch.from_numpy(inp["bias"]).cuda(),
            "dy": torch.from_numpy(inp["dy"]).cuda().to(bf) if want_dy else None}
-    w1 = torch.empty(w.E, w.R1, w.d, dtype=bf, device="cuda")
-    w2 = torch.empty(w.E, w.d, w.F, dtype=bf, device="cuda")
-    host_draw = w.E * (w.R1 * w.d + w.d * w.F) * 2 <= DEVICE_DRAW_BYTES
-    if host_draw:
-        for e in range(w.E):
-            a, b = syn.expert_weights(w, e)
-            w1[e].copy_(torch.from_numpy(a).to(bf))
-            w2[e].copy_(torch.from_numpy(b).to(bf))
-    else:
-        g = torch.Generator(device="cuda")
-        for e in range(w.E):
-            g.manual_seed(w.seed * 1000003 + e)
-            w1[e].copy_(torch.randn(w.R1, w.d, generator=g, device="cuda") * (w.expert_scale / math.sqrt(w.d)))
-            w2[e].copy_(torch.randn(w.d, w.F, generator=g, device="cuda") * (w.expert_scale / math.sqrt(w.F)))
-    dev["w1"], dev["w2"] = w1, w2
-    dev["weights"] = "moe_synth (host, per expert)" if host_draw else "torch Philox on the GPU, seeded per expert"
+    t0 = time.perf_counter()
+    b1, b2 = syn.expert_weight_bits(w)
+    t_draw = time.perf_counter() - t0
+    dev["w1"] = torch.from_numpy(b1).view(bf).cuda()
+    dev["w2"] = torch.from_numpy(b2).view(bf).cuda()
+    del b1, b2
+    dev["weights"] = f"moe_synth per-expert draws (host, {t_draw:.1f} s on {min(32, os.cpu_count() or 1)} threads)"
     return inp, dev
 
 
@@ -267,17 +409,6 @@ def run_ours(args):
     K_a = int(L.offsets[-1].item())
     E_used = int((L.kept > 0).sum().item())   # experts whose weights the GEMMs read
 
-    # per-call breakdown (eager launches, CUDA events between the ABI calls)
-    n_eager = min(args.steps, 200)
-    nc = len(calls)
-    marks = [[ev() for _ in range(nc + 1)] for _ in range(n_eager)]
-    for i in range(n_eager):
-        flush.zero_()
-        step(marks[i])
-    torch.cuda.synchronize()
-    per_call = {c: [m[j].elapsed_time(m[j + 1]) for m in marks] for j, c in enumerate(calls)}
-    eager_ms = statistics.mean(m[0].elapsed_time(m[nc]) for m in marks)
-
     def capture(fn):
         g = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
@@ -294,40 +425,39 @@ def run_ours(args):
         return g
 
     # per-call times inside a CUDA graph of the separate calls, with timing events between the calls (no host
-    # launch gaps); the eager figures above are the fallback
-    per_call_source = "eager"
+    # launch gaps); eager launches with events between the calls are the fallback
+    nc = len(calls)
+    n_rep = max(3, min(args.steps, 100))
+    per_call_source = "graph"
     try:
         gm = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nc + 1)]
         g_m = capture(lambda: step(gm))
         reps = []
-        for _ in range(min(args.steps, 100)):
+        for _ in range(n_rep):
             flush.zero_()
             g_m.replay()
             torch.cuda.synchronize()
             reps.append([gm[j].elapsed_time(gm[j + 1]) for j in range(nc)])
         per_call = {c: [r[j] for r in reps] for j, c in enumerate(calls)}
-        per_call_source = "graph"
         del g_m
-    except Exception as exc:  # events inside captured graphs not available: keep the eager figures
+    except Exception as exc:  # events inside captured graphs not available
         per_call_source = f"eager ({type(exc).__name__})"
-
-    # the separate ABI calls as one graph (reported beside the timed step for forward-only workloads)
-    unfused_ms = None
-    if not bwd:
-        g_sep = capture(step)
-        ue = [(ev(), ev()) for _ in range(n_eager)]
-        for a_, b_ in ue:
+        marks = [[ev() for _ in range(nc + 1)] for _ in range(n_rep)]
+        for i in range(n_rep):
             flush.zero_()
-            a_.record(stream)
-            g_sep.replay()
-            b_.record(stream)
+            step(marks[i])
         torch.cuda.synchronize()
-        unfused_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ue)
-        del g_sep
+        per_call = {c: [m[j].elapsed_time(m[j + 1]) for m in marks] for j, c in enumerate(calls)}
+
+    # per-kernel launch times: each kernel node of the timed step replayed alone
+    try:
+        launches = replay_kernels_alone(timed_step, stream, flush, reps=max(3, min(args.steps, 20)))
+        launch_error = None
+    except Exception as exc:
+        launches, launch_error = [], f"{type(exc).__name__}: {exc}"[:300]
 
     # the timed steps: the whole step captured once in a CUDA graph, replayed
     graph = capture(timed_step)
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -429,25 +559,56 @@ def run_ours(args):
     if bwd:
         btf = alg["bwd_gemm_flops"] / (mean_call["backward"] * 1e-3) / 1e12
         kernels["backward"].update({"gemm_TFLOP/s": round(btf, 1), "frac_bf16_peak": round(btf / tflops, 4)})
-    gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
-    # the binding roof of the forward grouped GEMM: max(FLOPs / tensor peak, bytes / HBM peak)
-    tensor_bound = alg["gemm_flops"] / (tflops * 1e12) > alg["gemm"] / (hbm * 1e9)
-    traffic = gemm_traffic(w.name)
-    if tensor_bound:
-        # a contraction timed inside a long step under the power cap is held to the sustained bf16 peak; one that
-        # ran at full clock, to the burst peak
-        capped = "sw_power_cap" in (clk.get("reasons") or []) and tflops_sus > 0
-        peak_t = tflops_sus if capped else tflops
-        roof = {"bound": "tensor", "achieved": round(gemm_tf, 1), "peak": peak_t, "unit": "TFLOP/s",
-                "frac": round(gemm_tf / peak_t, 4), "peak_kind": "sustained (power cap active)" if capped else "burst",
-                "frac_of_burst_peak": round(gemm_tf / tflops, 4)}
-    else:
+
+    # per launch: the grouped GEMMs against max(FLOPs / tensor peak, bytes / HBM peak); the token kernels'
+    # launch times are summed per call and set against the call's algorithmic bytes
+    table, call_launch_ms = [], {}
+    names = demangle([n for n, _ in launches])
+    roles = kernel_roles(names)
+    for (_, ms), name, (role, call) in zip(launches, names, roles):
+        row = {"kernel": role, "call": call, "ms": round(ms, 5)}
+        if role in ("gemm1", "gemm2", "gemm2_combine", "dH", "dW2", "dXp", "dW1"):
+            b, f = gemm_launch_algorithmic(role, w, K_a, E_used, bwd)
+            t_hbm, t_tc = b / (hbm * 1e9), f / (tflops * 1e12)
+            row.update({"bytes": b, "flops": f, "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                        "TFLOP/s": round(f / (ms * 1e-3) / 1e12, 1), "bound": "tensor" if t_tc > t_hbm else "hbm",
+                        "frac_of_bound": round(max(t_hbm, t_tc) * 1e3 / ms, 4),
+                        "frac_bf16_peak": round(f / (ms * 1e-3) / 1e12 / tflops, 4),
+                        "traffic": measured_traffic(w.name, role)})
+        else:
+            call_launch_ms[call] = call_launch_ms.get(call, 0.0) + ms
+            row["traffic"] = measured_traffic(w.name, role)
+        row["name"] = name[:120]
+        table.append(row)
+    for c in ("router", "dispatch", "combine"):
+        if c in call_launch_ms and call_launch_ms[c] > 0:
+            gbs = alg[c] / (call_launch_ms[c] * 1e-3) / 1e9
+            kernels[c].update({"launches_ms": round(call_launch_ms[c], 5), "launches_GB/s": round(gbs, 1),
+                               "launches_frac_hbm": round(gbs / hbm, 4)})
+
+    gemm_rows = [r for r in table if "bytes" in r]
+    if gemm_rows:
+        top = max(gemm_rows, key=lambda r: r["ms"])
+        if top["bound"] == "tensor":
+            roof = {"bound": "tensor", "achieved": top["TFLOP/s"], "peak": tflops, "unit": "TFLOP/s",
+                    "frac": round(top["TFLOP/s"] / tflops, 4), "peak_kind": "burst (kernel timed alone)"}
+        else:
+            roof = {"bound": "hbm", "achieved": top["GB/s"], "peak": hbm, "unit": "GB/s",
+                    "frac": round(top["GB/s"] / hbm, 4)}
+        roof.update({"traffic": top["traffic"], "kernel": f"{top['kernel']} ({top['name']})",
+                     "launch_ms": top["ms"], "algorithmic_bytes_per_launch": top["bytes"],
+                     "algorithmic_flops_per_launch": top["flops"], "peak_source": peak_src,
+                     "timing": "the launch replayed alone from the step graph, CUDA events, L2 flushed before each"})
+    else:   # per-launch replay unavailable: the forward grouped-GEMM call (two launches) from the per-call events
+        gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(gemm_gbs / hbm, 4)}
-    roof.update({"kernel": "moe_expert_gemm (forward grouped GEMM, 2 launches)", "traffic": traffic,
-                 "peak_source": peak_src, "algorithmic_bytes_per_call": alg["gemm"],
-                 "algorithmic_flops_per_call": alg["gemm_flops"]})
-    launches = forward_launches(w, not bwd) + (LAUNCHES_BACKWARD if bwd else 0)
+                "frac": round(gemm_gbs / hbm, 4), "traffic": None, "peak_source": peak_src,
+                "kernel": "moe_expert_gemm (forward grouped GEMM call, 2 launches)",
+                "algorithmic_bytes_per_call": alg["gemm"]}
+    # the whole step against the HBM time of its algorithmic bytes
+    step_bytes = alg["router"] + alg["dispatch"] + alg["gemm"] + alg["combine"] + (alg["backward"] if bwd else 0)
+    step_floor_ms = step_bytes / (hbm * 1e9) * 1e3
+    n_launch = len(launches) if launches else None
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -456,28 +617,32 @@ def run_ours(args):
                    "top_k": w.k, "d_ff": w.F, "act": w.act, "renormalize": w.renormalize,
                    "capacity_factor": None if w.cf is None else f"{w.cf[0]}/{w.cf[1]}", "capacity": cap,
                    "capacity_reading": "floor(k*T*cf/E)" if w.cf is not None else "none (dropless)",
-                   "kept_assignments": K_a, "experts_with_tokens": E_used, "expert_weights": dv["weights"],
+                   "aux_alpha": w.alpha, "kept_assignments": K_a, "experts_with_tokens": E_used,
+                   "expert_weights": dv["weights"],
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed before every timed step (256 MiB write, outside the step's events)"},
         "roofline": roof,
+        "step_roofline": {"algorithmic_bytes": step_bytes, "hbm_floor_ms": round(step_floor_ms, 4),
+                          "frac": round(step_floor_ms / ms_step, 4), "peak": hbm, "unit": "GB/s"},
         "kernels": kernels,
+        "launches": table if table else {"error": launch_error},
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes, "call": "moe_forward" if not bwd else "separate calls + moe_backward",
                 "overlap": "uploads and downloads on their own streams, double-buffered, overlapping compute"},
-        "gpu_launches": launches * args.steps,
-        "eager_ms_per_step": round(eager_ms, 5),
+        "gpu_launches": n_launch * args.steps if n_launch else None,
+        "gpu_launches_per_step": n_launch,
         "step_call": "moe_forward (one call: router, dispatch, expert GEMMs, combine fused into the second GEMM "
                      "for top-1)" if not bwd else
                      "moe_router, moe_dispatch, moe_expert_gemm, moe_combine, moe_backward",
-        "separate_calls_graph_ms_per_step": None if unfused_ms is None else round(unfused_ms, 5),
         "timing": "step replayed as one CUDA graph; per-call figures from the separate ABI calls with events "
-                  "between them, replayed as a CUDA graph (per_call_source)",
+                  "between them, replayed as a CUDA graph (per_call_source); per-launch figures from each kernel "
+                  "node of the step graph replayed alone",
         "per_call_source": per_call_source,
         "clocks": clk,
         "wall_s_timed_region": round(t_wall1 - t_wall0, 3),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w, inp, bwd)
+        res["cpu_baseline"] = cpu_baseline(w, bwd)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
@@ -495,14 +660,44 @@ def _oracle_threads():
         return os.cpu_count()
 
 
-HOST_F64_WEIGHTS_MAX = 16 << 30   # the oracle's fp64 copy of the expert weights must fit in host RAM
+HOST_F64_WEIGHTS_MAX = 8 << 30   # the oracle's fp64 copy of a sample's expert weights
 
 
-def _oracle_weights(w):
-    if w.E * (w.R1 * w.d + w.d * w.F) * 8 > HOST_F64_WEIGHTS_MAX:
-        return None
-    w1, w2 = syn.all_expert_weights(w)
-    return w1.astype(np.float64), w2.astype(np.float64)
+def _f64_weight_bytes(w) -> int:
+    return w.E * (w.R1 * w.d + w.d * w.F) * 8
+
+
+def oracle_sample(w):
+    """The workload the oracle is timed on, and how it stands for w.
+
+    When the fp64 expert weights fit HOST_F64_WEIGHTS_MAX, w itself (a batch of its first tokens, chosen by
+    time). Otherwise the same layer with fewer experts: E' = E / 2^j experts and T' = T E' / E tokens (its
+    own seeded draws), so every expert's GEMM shape, the capacity, k and the rows per expert are w's, and
+    the per-token work is w's (the router's E-dependent share aside)."""
+    if _f64_weight_bytes(w) <= HOST_F64_WEIGHTS_MAX:
+        return w, None
+    E = w.E
+    while E > 1 and _f64_weight_bytes(w.with_(E=E)) > HOST_F64_WEIGHTS_MAX:
+        E //= 2
+    T = max(1, w.T * E // w.E)
+    ws = w.with_(name=f"{w.name}-T{T}-E{E}", T=T, E=E)
+    return ws, (f"the same layer with {E} of the {w.E} experts and {T} of the {w.T} tokens (T E'/E; its own "
+                f"seeded draws): every expert GEMM shape, k, the capacity ({_capacity(ws)}) and the rows per "
+                "expert are the full layer's, so its tokens/s stands for the full layer's; the oracle runs it "
+                "expert by expert through its callable expert source")
+
+
+def _capacity(w):
+    from oracle import moe_oracle as O
+    return O.capacity(w.T, w.E, w.k, w.cf, w.count_assignments)
+
+
+def _oracle_inputs(ws, bwd):
+    inp = syn.make_inputs(ws, experts=False, dy=bwd)
+    w1, w2 = syn.all_expert_weights(ws)
+    weights = (w1.astype(np.float64), w2.astype(np.float64))
+    del w1, w2
+    return inp, weights
 
 
 def _oracle_step(w, inp, Ts, weights, bwd):
@@ -510,9 +705,10 @@ def _oracle_step(w, inp, Ts, weights, bwd):
     kw = dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments, renormalize=w.renormalize,
               alpha=w.alpha)
     x = inp["x"][:Ts]
-    O.forward(x, inp["w_r"], inp["bias"], weights, **kw)
+    experts = lambda e: (weights[0][e], weights[1][e])    # one expert at a time, already fp64
+    O.forward(x, inp["w_r"], inp["bias"], experts, **kw)
     if bwd:
-        O.backward(x, inp["w_r"], inp["bias"], weights, inp["dy"][:Ts], **kw)
+        O.backward(x, inp["w_r"], inp["bias"], experts, inp["dy"][:Ts], **kw)
 
 
 def _oracle_batch(w, inp, weights, bwd, budget_s):
@@ -527,30 +723,28 @@ def _oracle_batch(w, inp, weights, bwd, budget_s):
     return Ts
 
 
-def _sample_text(w, Ts, bwd):
+def _sample_text(ws, Ts, bwd, how):
     what = "forward + backward" if bwd else "forward"
-    part = f"the full batch (T={w.T})" if Ts == w.T else f"the first {Ts} of the {w.T} tokens as one batch " \
-                                                          "(same capacity factor)"
-    return f"one {what} of {part} of {w.name}, fp64 numpy oracle, expert weights widened to fp64 before timing"
+    part = f"the full batch (T={ws.T})" if Ts == ws.T else f"the first {Ts} of the {ws.T} tokens as one batch " \
+                                                           "(same capacity factor)"
+    text = f"one {what} of {part} of {ws.name}, fp64 numpy oracle, expert weights widened to fp64 before timing"
+    return text + (f"; {how}" if how else "")
 
 
-def cpu_baseline(w, inp, bwd):
-    weights = _oracle_weights(w)
-    if weights is None:
-        return {"value": None, "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
-                "sample": f"not run: the oracle's fp64 expert weights of {w.name} exceed {HOST_F64_WEIGHTS_MAX >> 30} GiB "
-                          "of host memory"}
-    Ts = _oracle_batch(w, inp, weights, bwd, 20.0)
+def cpu_baseline(w, bwd):
+    ws, how = oracle_sample(w)
+    inp, weights = _oracle_inputs(ws, bwd)
+    Ts = _oracle_batch(ws, inp, weights, bwd, 20.0)
     # the sampled batch, repeated until at least 10 s of CPU work have been timed
     reps, t0 = 0, time.perf_counter()
     while True:
-        _oracle_step(w.with_(T=Ts), inp, Ts, weights, bwd)
+        _oracle_step(ws.with_(T=Ts), inp, Ts, weights, bwd)
         reps += 1
         dt = time.perf_counter() - t0
         if dt >= 10.0:
             break
     return {"value": round(Ts * reps / dt, 1), "unit": "tokens/s", "cores": _oracle_threads(), "kind": "oracle",
-            "sample": _sample_text(w, Ts, bwd) + f", {reps} time(s); {dt:.2f} s"}
+            "sample": _sample_text(ws, Ts, bwd, how) + f", {reps} time(s); {dt:.2f} s"}
 
 
 def run_reference(args):
@@ -559,28 +753,24 @@ def run_reference(args):
         return
     w = bench_workload(args)
     bwd = args.pass_ == "fwdbwd"
-    inp = syn.make_inputs(w, experts=False, dy=bwd)
-    weights = _oracle_weights(w)
-    if weights is None:
-        print(json.dumps({"impl": "reference", "unavailable": f"the oracle's fp64 expert weights of {w.name} do not "
-                                                              "fit in host memory"}), flush=True)
-        return
+    ws, how = oracle_sample(w)
+    inp, weights = _oracle_inputs(ws, bwd)
     budget = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    Ts = _oracle_batch(w, inp, weights, bwd, budget)
-    ws = w.with_(T=Ts)
+    Ts = _oracle_batch(ws, inp, weights, bwd, budget)
+    wt = ws.with_(T=Ts)
     for _ in range(args.warmup):
-        _oracle_step(ws, inp, Ts, weights, bwd)
+        _oracle_step(wt, inp, Ts, weights, bwd)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(ws, inp, Ts, weights, bwd)
+        _oracle_step(wt, inp, Ts, weights, bwd)
     dt = time.perf_counter() - t0
     value = Ts * args.steps / dt
     res = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": w.name, "pass": args.pass_, "T_sample": Ts},
+           "config": {"workload": w.name, "pass": args.pass_, "sample_workload": ws.name, "T_sample": Ts},
            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": _oracle_threads(),
-                            "kind": "oracle", "sample": "each step: " + _sample_text(w, Ts, bwd)},
+                            "kind": "oracle", "sample": "each step: " + _sample_text(ws, Ts, bwd, how)},
            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
 
@@ -591,8 +781,8 @@ BENCH_WORKLOADS = [n for n, w in syn.WORKLOADS.items() if w.dtype == "bf16"]
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=BENCH_WORKLOADS, default=WORKLOAD)
     ap.add_argument("--pass", dest="pass_", choices=["fwd", "fwdbwd"], default=None,

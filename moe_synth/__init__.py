@@ -191,6 +191,30 @@ def all_expert_weights(w: Workload) -> Tuple[np.ndarray, np.ndarray]:
     return w1, w2
 
 
+def expert_weight_bits(w: Workload, threads: Optional[int] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Every expert's (W1, W2) of a bf16 workload as bf16 bit patterns, uint16
+    [E, R1, d] and [E, d, F] (half the memory of float32), drawn expert by
+    expert on a thread pool. The values are exactly expert_weights(w, e):
+    each expert has its own generator, so the order the threads run in does
+    not matter. from_bf16_bits() widens one expert back to float32."""
+    if w.dtype != "bf16":
+        raise ValueError("expert_weight_bits is for bf16 workloads")
+    import concurrent.futures
+    import os
+    b1 = np.empty((w.E, w.R1, w.d), np.uint16)
+    b2 = np.empty((w.E, w.d, w.F), np.uint16)
+
+    def one(e):
+        a, b = expert_weights(w, e)
+        b1[e] = bf16_bits(a)
+        b2[e] = bf16_bits(b)
+
+    n = threads or min(32, os.cpu_count() or 1)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=n) as ex:
+        list(ex.map(one, range(w.E)))
+    return b1, b2
+
+
 def upstream_grad(w: Workload) -> np.ndarray:
     """dY [T, d] ~ N(0, 1), the gradient of the loss w.r.t. the layer output."""
     return _cast(w, _normal(rng_for(w, "dy"), (w.T, w.d), 1.0))

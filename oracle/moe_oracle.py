@@ -284,13 +284,16 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
 def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequence[int],
                      experts_sampled: Sequence[int], k: int, act: str, cf: Optional[Tuple[int, int]],
                      count_assignments: bool = True, renormalize: bool = False, alpha: float = 0.01) -> dict:
-    """The gradients of `backward` for a few tokens (dx rows) and a few experts
-    (dw1, dw2), without evaluating every expert on every token: the same chain
-    rule through eqs. (1), (2) and (4), taken token by token for dx (each
-    token's kept experts, its gate gradients, its softmax Jacobian, the aux
-    term that depends on the batch only through f) and expert by expert for
-    the weight gradients (the rows the expert kept). Routing and capacity
-    always cover the whole batch."""
+    """The gradients of `backward` for a few tokens (dx, dg and dh rows) and a
+    few experts (dw1, dw2), without evaluating every expert on every token:
+    the same chain rule through eqs. (1), (2) and (4). Each expert the
+    sampled tokens keep, or that is sampled itself, is fetched once; it gives
+    the sampled tokens' gate gradients and expert-path dx terms, and, for a
+    sampled expert, the weight gradients over every row it kept. Then, token
+    by token, the gate gradients go through the renormalisation and the
+    softmax Jacobian (plus the aux term, which depends on the batch only
+    through f) to dh and the router's dx term. Routing and capacity always
+    cover the whole batch."""
     x64, dy64 = _f64(x), _f64(dy)
     T, d = x64.shape
     wr64 = _f64(w_r)
@@ -298,10 +301,11 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
     r = route(x64, wr64, bias, k, renormalize, alpha)
     C = capacity(T, E, k, cf, count_assignments)
     s = assign_slots(r["idx"], E, C)
-    p, idx, gate = r["p"], r["idx"], r["gate"]
+    p, idx, gate, slot = r["p"], r["idx"], r["gate"], s["slot"]
+    toks = [int(t) for t in tokens]
+    sampled = set(int(e) for e in experts_sampled)
 
-    def expert_grads(z, dyv, g, e):
-        w1, w2 = _expert(experts, e)
+    def expert_grads(z, dyv, g, w1, w2):
         fw = expert_ffn(z, w1, w2, act)
         dyp = g[:, None] * dyv
         dhid = dyp @ w2
@@ -310,39 +314,46 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
         else:
             sg = 1.0 / (1.0 + np.exp(-fw["g"]))
             da = np.concatenate([dhid * fw["u"] * (sg * (1.0 + fw["g"] * (1.0 - sg))), dhid * silu(fw["g"])], axis=1)
-        return fw, dyp, da, w1
+        return fw, dyp, da
 
-    dx = {}
-    for t in (int(t) for t in tokens):
-        acc = dy64[t].copy()
-        dg = np.zeros(k)
+    acc = {t: dy64[t].copy() for t in toks}          # residual path
+    dg = {t: np.zeros(k) for t in toks}
+    pairs = {}                                        # expert -> the sampled tokens' kept pairs (t, j)
+    for t in toks:
         for j in range(k):
-            if s["slot"][t, j] < 0:
+            if slot[t, j] >= 0:
+                pairs.setdefault(int(idx[t, j]), []).append((t, j))
+    dw1, dw2 = {}, {}
+    for e in sorted(set(pairs) | sampled):
+        w1, w2 = _expert(experts, e)
+        if e in pairs:
+            tt = np.array([t for t, _ in pairs[e]])
+            jj = np.array([j for _, j in pairs[e]])
+            fw, _, da = expert_grads(x64[tt], dy64[tt], gate[tt, jj], w1, w2)
+            dz = da @ w1
+            for n, (t, j) in enumerate(pairs[e]):
+                dg[t][j] = float(np.dot(dy64[t], fw["y"][n]))
+                acc[t] += dz[n]
+        if e in sampled:
+            tt, jj = np.nonzero((idx == e) & (slot >= 0))
+            if len(tt) == 0:
+                dw1[e], dw2[e] = np.zeros_like(w1), np.zeros_like(w2)
                 continue
-            e = int(idx[t, j])
-            fw, dyp, da, w1 = expert_grads(x64[t][None, :], dy64[t][None, :], np.array([gate[t, j]]), e)
-            dg[j] = float(np.dot(dy64[t], fw["y"][0]))
-            acc += (da @ w1)[0]
+            fw, dyp, da = expert_grads(x64[tt], dy64[tt], gate[tt, jj], w1, w2)
+            dw2[e] = dyp.T @ fw["hid"]
+            dw1[e] = da.T @ x64[tt]
+    dx, dh = {}, {}
+    for t in toks:
         dp = np.zeros(E)
         if renormalize:
             psel = p[t, idx[t]]
-            dp[idx[t]] = (dg - np.dot(dg, gate[t])) / psel.sum()
+            dp[idx[t]] = (dg[t] - np.dot(dg[t], gate[t])) / psel.sum()
         else:
-            dp[idx[t]] = dg
+            dp[idx[t]] = dg[t]
         dp += alpha * E * r["f"] / float(T)
-        dh = p[t] * (dp - np.dot(p[t], dp))
-        dx[t] = acc + dh @ wr64
-    dw1, dw2 = {}, {}
-    for e in (int(e) for e in experts_sampled):
-        tt, jj = np.nonzero((idx == e) & (s["slot"] >= 0))
-        w1, w2 = _expert(experts, e)
-        if len(tt) == 0:
-            dw1[e], dw2[e] = np.zeros_like(w1), np.zeros_like(w2)
-            continue
-        fw, dyp, da, _ = expert_grads(x64[tt], dy64[tt], gate[tt, jj], e)
-        dw2[e] = dyp.T @ fw["hid"]
-        dw1[e] = da.T @ x64[tt]
-    return dict(dx=dx, dw1=dw1, dw2=dw2, route=r, slots=s)
+        dh[t] = p[t] * (dp - np.dot(p[t], dp))
+        dx[t] = acc[t] + dh[t] @ wr64
+    return dict(dx=dx, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r, slots=s)
 
 
 def loss(x, w_r, bias, experts: ExpertSource, dy, **kw) -> float:

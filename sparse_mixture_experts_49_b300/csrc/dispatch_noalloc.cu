@@ -14,9 +14,9 @@
 //   - the array has a fixed size: T <= MOE_NOALLOC_MAX_TOKENS (32768) tokens
 //     and E <= 256 experts, about 256 KB, and every GPU that loads the library
 //     holds it until the process exits;
-//   - the first call on a device looks the array's address up with
-//     cudaGetSymbolAddress; that first call should come before any stream
-//     capture;
+//   - the first call on a device (and the first after a device reset) looks
+//     the array's address up with cudaGetSymbolAddress; that first call
+//     should come before any stream capture;
 //   - all calls share the array and it keeps the last call's contents: two
 //     calls whose work can overlap on the GPU race with each other;
 //   - bad or repeated expert indices are still treated as dropped, but the
@@ -44,19 +44,56 @@ static __device__ __align__(256) int32_t g_dispatch_scratch[kScratchInts];
 
 std::mutex g_mutex;
 int32_t *g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};  // unique id of the context the address belongs to
 
-// Device address of g_dispatch_scratch on the current device, looked up once per device.
+// Unique id of the calling thread's current CUDA context (0 if it cannot be
+// read). A device reset destroys the primary context and the module loaded in
+// it; the context created after it has a new id, so a cached address is never
+// reused across a reset. Driver entry points are looked up at run time, so the
+// library needs no link-time dependency on libcuda.
+unsigned long long current_context_id() {
+  typedef CUresult (*GetCurrentFn)(CUcontext *);
+  typedef CUresult (*GetIdFn)(CUcontext, unsigned long long *);
+  static GetCurrentFn get_current = nullptr;
+  static GetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *a = nullptr, *b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) == cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess &&
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) == cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess) {
+      get_current = reinterpret_cast<GetCurrentFn>(a);
+      get_id = reinterpret_cast<GetIdFn>(b);
+    }
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+      get_id(ctx, &id) == CUDA_SUCCESS)
+    return id;
+  return 0;
+}
+
+// Device address of g_dispatch_scratch on the current device, looked up once
+// per device and context (set-up work: the first call on a device, or the
+// first after a device reset, calls cudaGetSymbolAddress).
 cudaError_t scratch_on_current_device(int32_t **out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // 0 when no context is current yet: then the lookup below creates the
+  // device's primary context, and the id is read again after it.
+  unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || ctx == 0 || g_scratch_ctx[dev] != ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dispatch_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<int32_t *>(p);
+    g_scratch_ctx[dev] = current_context_id();
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;

@@ -74,12 +74,8 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False):
     if backward:
         dy = to_dev(torch, inp["dy"], dt)
         dx, dw_r, dw1, dw2 = layer.backward(dy)
-        inter = moe.moe_backward_intermediates(cfg, layer.ws)
-        torch.cuda.synchronize()
-        base = layer.ws.data_ptr()
-        dg = layer.ws[inter["dg"] - base: inter["dg"] - base + w.T * w.k * 4].view(torch.float32).view(w.T, w.k)
-        dh = layer.ws[inter["dh"] - base: inter["dh"] - base + w.T * w.E * 4].view(torch.float32).view(w.T, w.E)
-        res.update(dx=np64(dx), dw_r=np64(dw_r), dw1=np64(dw1), dw2=np64(dw2), dg=np64(dg), dh=np64(dh))
+        dg, dh = backward_intermediates(torch, moe, cfg, layer, w.T, w.k, w.E)
+        res.update(dx=np64(dx), dw_r=np64(dw_r), dw1=np64(dw1), dw2=np64(dw2), dg=dg, dh=dh)
     torch.cuda.synchronize()
     res.update(out=np64(layer.out), probs=np64(layer.probs), idx=np64(layer.topk_idx), gate=np64(layer.topk_gate),
                importance=np64(layer.importance), load=np64(layer.load), aux=float(layer.aux.item()),
@@ -99,12 +95,27 @@ def oracle_kw(w):
 
 
 def assert_close(got, ref, tol, what):
+    """max|got - ref| <= tol * max|ref|; returns the measured ratio max|err| / max|ref| (printed, so that a run
+    with -rP records the margin each check had)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, f"{what}: shape {got.shape} vs {ref.shape}"
     err = float(np.max(np.abs(got - ref))) if got.size else 0.0
     scale = float(np.max(np.abs(ref))) if ref.size else 0.0
     assert err <= tol * scale + 1e-30, f"{what}: max|err| {err:.3e} > {tol} x max|ref| {scale:.3e}"
+    ratio = err / scale if scale > 0 else 0.0
+    print(f"[tol] {what}: max|err|/max|ref| = {ratio:.3e} (bound {tol:g})")
+    return ratio
+
+
+def backward_intermediates(torch, moe, cfg, layer, T, k, E):
+    """dg [T, k] and dh [T, E] (fp32) of the last moe_backward, read from the layer's workspace."""
+    inter = moe.moe_backward_intermediates(cfg, layer.ws)
+    torch.cuda.synchronize()
+    base = layer.ws.data_ptr()
+    dg = layer.ws[inter["dg"] - base: inter["dg"] - base + T * k * 4].view(torch.float32).view(T, k)
+    dh = layer.ws[inter["dh"] - base: inter["dh"] - base + T * E * 4].view(torch.float32).view(T, E)
+    return np64(dg), np64(dh)
 
 
 def check_routing(res, ref, w):

@@ -51,12 +51,61 @@ def test_skewed_layer_counts_only_experts_that_keep_tokens():
     assert all_experts - used == 9 * 2 * 4096 * 1024 * 2    # the weights of the 9 empty experts
 
 
-def test_launch_counts():
+def test_grouped_gemm_launch_bytes_large_training():
+    """Per-launch algorithmic bytes of the large training layer's six grouped-GEMM launches, element by element:
+    together they are the forward call's and the backward GEMMs' bytes."""
     b = _bench()
-    top1 = syn.WORKLOADS["switch-base-top1"]
-    top8 = syn.WORKLOADS["dropless-top8-swiglu"]
-    # router 3 (split, logits, selection), dispatch 2, grouped GEMM 2, combine 1 unless fused into GEMM 2 (top-1)
-    assert b.forward_launches(top1, True) == 7
-    assert b.forward_launches(top1, False) == 8
-    assert b.forward_launches(top8, True) == 8
-    assert b.LAUNCHES_BACKWARD == 11
+    w = syn.WORKLOADS["large-top8-swiglu"]         # d 7168, F 2048, E 256, SwiGLU (R1 = 4096)
+    K_a, E_used, d, F, R1, E = 32749, 256, 7168, 2048, 4096, 256
+    g = {r: b.gemm_launch_algorithmic(r, w, K_a, E_used, True) for r in ("gemm1", "gemm2", "dH", "dW2", "dXp", "dW1")}
+    assert g["gemm1"] == (E_used * R1 * d * 2 + K_a * d * 2 + K_a * F * 2 + K_a * 2 * F * 2, 2 * K_a * R1 * d)
+    assert g["gemm2"] == (E_used * d * F * 2 + K_a * F * 2 + K_a * d * 2, 2 * K_a * d * F)
+    assert g["dW1"] == (E * R1 * d * 2 + K_a * R1 * 2 + K_a * d * 2, 2 * K_a * R1 * d)
+    assert g["dW2"] == (E * d * F * 2 + K_a * d * 2 + K_a * F * 2, 2 * K_a * d * F)
+    assert g["dH"][0] == E_used * d * F * 2 + K_a * d * 2 + K_a * 2 * F * 2 + K_a * R1 * 2
+    assert g["dXp"][0] == E_used * R1 * d * 2 + K_a * R1 * 2 + K_a * d * 2
+    a = b.algorithmic(w, K_a, E_used)
+    assert g["gemm1"][0] + g["gemm2"][0] == a["gemm"]           # the forward call's two launches
+    assert g["gemm1"][1] + g["gemm2"][1] == a["gemm_flops"]
+    assert sum(g[r][1] for r in ("dH", "dW2", "dXp", "dW1")) == a["bwd_gemm_flops"]
+
+
+def test_kernel_roles_from_demangled_names():
+    b = _bench()
+    gemm = "void moe::tc::grouped_gemm_kernel<{}>(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, moe::tc::Args)"
+    names = [
+        "moe::(anonymous namespace)::router_split_kernel(float const*, int, int, int, __nv_bfloat16*)",
+        "void moe::(anonymous namespace)::rt::router_tc_kernel<256>(CUtensorMap_st, CUtensorMap_st, moe::(anonymous namespace)::rt::Args)",
+        "void moe::(anonymous namespace)::router_select_kernel<8>(float const*, int, moe::(anonymous namespace)::RouterArgs)",
+        "void moe::(anonymous namespace)::dispatch_count_kernel<8>(int const*, int, int, int, long)",
+        "void moe::(anonymous namespace)::dispatch_place_kernel<__nv_bfloat16, 8>(__nv_bfloat16 const*)",
+        gemm.format("0, 0, 0, 0, 2"), gemm.format("0, 0, 0, 0, 0"),
+        "void moe::(anonymous namespace)::combine_kernel<__nv_bfloat16, 8>(__nv_bfloat16 const*)",
+        "void moe::(anonymous namespace)::combine_backward_kernel<__nv_bfloat16, 8>(__nv_bfloat16 const*)",
+        gemm.format("0, 0, 0, 1, 4"), gemm.format("0, 1, 1, 1, 0"), gemm.format("0, 0, 0, 1, 0"),
+        gemm.format("0, 1, 1, 1, 0"),
+        "void moe::(anonymous namespace)::router_dh_kernel<8>(float const*)",
+        "moe::(anonymous namespace)::router_wsplit6_kernel(float const*, int, int, int, __nv_bfloat16*)",
+        gemm.format("0, 0, 0, 1, 5"), gemm.format("0, 1, 1, 1, 5"),
+        "moe::(anonymous namespace)::router_dwr_sum_kernel(float const*, int, int, int, int, float*)",
+        "void moe::(anonymous namespace)::unpermute_kernel<__nv_bfloat16, 8>(__nv_bfloat16 const*)",
+    ]
+    roles = b.kernel_roles(names)
+    assert [r for r, _ in roles] == [
+        "router_split_kernel", "router_tc_kernel", "router_select_kernel", "dispatch_count_kernel",
+        "dispatch_place_kernel", "gemm1", "gemm2", "combine_kernel", "combine_backward_kernel", "dH", "dW2", "dXp",
+        "dW1", "router_dh_kernel", "router_wsplit6_kernel", "router_grad_dX_r", "router_grad_dW_r",
+        "router_dwr_sum_kernel", "unpermute_kernel"]
+    assert [c for _, c in roles] == ["router"] * 3 + ["dispatch"] * 2 + ["gemm"] * 2 + ["combine"] + ["backward"] * 11
+    assert b.kernel_roles([gemm.format("0, 0, 0, 0, 6")]) == [("gemm2_combine", "gemm")]
+
+
+def test_oracle_sample_of_the_large_layer_keeps_every_per_expert_shape():
+    b = _bench()
+    w = syn.WORKLOADS["large-top8-swiglu"]
+    ws, how = b.oracle_sample(w)
+    assert how and ws.E == 16 and ws.T == 256 and (ws.d, ws.F, ws.k, ws.act, ws.cf) == (w.d, w.F, w.k, w.act, w.cf)
+    assert b._capacity(ws) == b._capacity(w) == 160                  # C = floor(k T cf / E) is unchanged
+    assert b._f64_weight_bytes(ws) <= b.HOST_F64_WEIGHTS_MAX
+    small = syn.WORKLOADS["switch-base-top1"]
+    assert b.oracle_sample(small) == (small, None)

@@ -354,6 +354,46 @@ def test_sampled_backward_matches_full_backward(wl):
                              experts_sampled=exps, **kw)
     for t in toks:
         np.testing.assert_allclose(smp["dx"][t], full["dx"][t], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(smp["dg"][t], full["dg"][t], rtol=1e-11, atol=1e-13)
+        np.testing.assert_allclose(smp["dh"][t], full["dh"][t], rtol=1e-11, atol=1e-15)
     for e in exps:
         np.testing.assert_allclose(smp["dw1"][e], full["dw1"][e], rtol=1e-11, atol=1e-13)
         np.testing.assert_allclose(smp["dw2"][e], full["dw2"][e], rtol=1e-11, atol=1e-13)
+
+
+# ------------------------------------------------------------------ sampled forward
+@pytest.mark.parametrize("wl", [
+    syn.Workload("fwd-sampled-drops", T=120, d=16, E=6, k=2, F=12, act="relu", dtype="f32", cf=(1, 2),
+                 zipf_s=1.2, router_std=0.4),
+    syn.Workload("fwd-sampled-renorm", T=90, d=12, E=7, k=3, F=10, act="swiglu", dtype="f32", cf=(3, 4),
+                 renormalize=True, router_std=0.4),
+    syn.Workload("fwd-sampled-top1", T=64, d=8, E=4, k=1, F=6, act="relu", dtype="f32", cf=(1, 1)),
+])
+def test_sampled_forward_matches_full_forward(wl):
+    """forward(tokens=S) is the full forward restricted to S: its out rows equal
+    forward()["out"][S] (the experts' GEMMs run on a subset of rows, so equal
+    up to the BLAS's summation order), and routing, slots and statistics are
+    the whole batch's. The cases drop tokens (capacity below the load,
+    Zipf-skewed logits), take k > 1 and renormalise, and the sample holds
+    tokens in any order, repeats none, and includes fully dropped tokens."""
+    inp = syn.make_inputs(wl)
+    kw = dict(k=wl.k, act=wl.act, cf=wl.cf, count_assignments=wl.count_assignments, renormalize=wl.renormalize,
+              alpha=wl.alpha)
+    experts = (inp["w1"], inp["w2"])
+    full = O.forward(inp["x"], inp["w_r"], inp["bias"], experts, **kw)
+    dropped = np.nonzero(np.all(full["slot"] < 0, axis=1))[0]
+    assert (full["slot"] < 0).any()
+    rng = np.random.default_rng(wl.T)
+    S = [int(t) for t in dropped[:2]] + [int(t) for t in rng.choice(wl.T, wl.T // 3, replace=False)]
+    S = list(dict.fromkeys(S))                                 # no repeats, arbitrary order
+    assert any(t in S for t in dropped)
+    part = O.forward(inp["x"], inp["w_r"], inp["bias"], experts, tokens=S, **kw)
+    np.testing.assert_array_equal(part["tokens"], S)
+    np.testing.assert_allclose(part["out"], full["out"][S], rtol=1e-13, atol=1e-15)
+    for t in dropped:
+        if t in S:
+            assert np.array_equal(part["out"][S.index(int(t))], inp["x"][t].astype(np.float64))
+    for key in ("idx", "slot", "kept", "offsets", "row_token", "load"):
+        np.testing.assert_array_equal(part[key], full[key])
+    np.testing.assert_allclose(part["gate"], full["gate"], rtol=0, atol=0)
+    assert part["aux"] == full["aux"]

@@ -11,8 +11,8 @@ import pytest
 
 import moe_synth as syn
 from oracle import moe_oracle as O
-from moe_cases import (SMALL, TOL_BF16, TOL_F32, assert_close, check_router_values, check_routing,
-                             expert_reference, oracle_kw, run_gpu)
+from moe_cases import (SMALL, TOL_BF16, TOL_F32, TOL_ROUTER_BF16, assert_close, backward_intermediates,
+                       check_router_values, check_routing, config_for, expert_reference, np64, oracle_kw, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -298,3 +298,56 @@ def test_full_size_dropless_backward_sampled():
     for e in exps:
         assert_close(dw1[e].float().cpu().numpy(), ref["dw1"][e], TOL_BF16, f"dw1[{e}]")
         assert_close(dw2[e].float().cpu().numpy(), ref["dw2"][e], TOL_BF16, f"dw2[{e}]")
+    dg, dh = backward_intermediates(torch, moe, cfg, L, w.T, w.k, w.E)
+    assert_close(dg[toks], np.stack([ref["dg"][t] for t in toks]), TOL_BF16, "dg (sampled tokens)")
+    assert_close(dh[toks], np.stack([ref["dh"][t] for t in toks]), TOL_BF16, "dh (sampled tokens)")
+    # dW_r = dh^T x over the whole batch, from the layer's own dh, in fp64
+    assert_close(np64(dw_r), dh.T @ inp["x"].astype(np.float64), TOL_ROUTER_BF16, "dw_r vs dh^T x (fp64)")
+
+
+def test_full_size_large_training_sampled():
+    """The large fine-grained training layer at its full size (T 4096, d 7168, 256 experts, top-8, SwiGLU
+    7168 -> 2048 -> 7168, capacity factor 1.25, alpha 0.01), forward + backward as the benchmark runs it, on
+    the same moe_synth draws the benchmark times: routing bit-exact over the whole batch (the K-split router
+    over 112 K blocks), the router's values, out, dX, dg and dh on 256 sampled tokens, dW1 and dW2 on 4
+    sampled experts (grouped-K GEMMs over ~128 rows per expert), and dW_r equal to dh^T x in fp64 over the
+    whole batch (the router gradient's token-range split)."""
+    import sparse_mixture_experts_49_b300 as moe
+    w = syn.WORKLOADS["large-top8-swiglu"]
+    inp = syn.make_inputs(w, experts=False, dy=True)
+    b1, b2 = syn.expert_weight_bits(w)
+    cfg = config_for(moe, w)
+    bf = torch.bfloat16
+    dev = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a, np.float32)).cuda().to(dt)
+    L = moe.MoELayer(cfg)
+    x, w_r, dy = dev(inp["x"], bf), dev(inp["w_r"], torch.float32), dev(inp["dy"], bf)
+    w1 = torch.from_numpy(b1).view(bf).cuda()
+    w2 = torch.from_numpy(b2).view(bf).cuda()
+    L.forward(x, w_r, w1, w2)
+    dx, dw_r, dw1, dw2 = L.backward(dy)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    experts = lambda e: (syn.from_bf16_bits(b1[e]), syn.from_bf16_bits(b2[e]))
+    rng = np.random.default_rng(5)
+    toks = sorted(rng.choice(w.T, 256, replace=False).tolist())
+    exps = sorted(rng.choice(w.E, 4, replace=False).tolist())
+    kw = oracle_kw(w)
+    f = O.forward(inp["x"], inp["w_r"], inp["bias"], experts, tokens=toks, **kw)
+    n = int(L.offsets[-1].item())
+    res = dict(idx=np64(L.topk_idx), load=np64(L.load), slot=np64(L.slot), kept=np64(L.kept),
+               offsets=np64(L.offsets), row_token=np64(L.row_token[:n]), probs=np64(L.probs),
+               gate=np64(L.topk_gate), importance=np64(L.importance), aux=float(L.aux.item()))
+    check_routing(res, f, w)
+    assert (f["slot"] < 0).any() and f["C"] == 160
+    check_router_values(res, f, w.dtype)
+    assert_close(np64(L.out)[toks], f["out"], TOL_BF16, "out (sampled tokens)")
+    ref = O.backward_sampled(inp["x"], inp["w_r"], inp["bias"], experts, inp["dy"], tokens=toks,
+                             experts_sampled=exps, **kw)
+    assert_close(np64(dx)[toks], np.stack([ref["dx"][t] for t in toks]), TOL_BF16, "dx (sampled tokens)")
+    dg, dh = backward_intermediates(torch, moe, cfg, L, w.T, w.k, w.E)
+    assert_close(dg[toks], np.stack([ref["dg"][t] for t in toks]), TOL_BF16, "dg (sampled tokens)")
+    assert_close(dh[toks], np.stack([ref["dh"][t] for t in toks]), TOL_BF16, "dh (sampled tokens)")
+    for e in exps:
+        assert_close(np64(dw1[e]), ref["dw1"][e], TOL_BF16, f"dw1[{e}]")
+        assert_close(np64(dw2[e]), ref["dw2"][e], TOL_BF16, f"dw2[{e}]")
+    assert_close(np64(dw_r), dh.T @ inp["x"].astype(np.float64), TOL_ROUTER_BF16, "dw_r vs dh^T x (fp64)")

@@ -41,7 +41,7 @@ def test_max_over_ranks_two_gloo_ranks(tmp_path):
 def test_reference_arm_under_torchrun_prints_once():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
-           "--gpus", "2", "--steps", "1", "--warmup", "3", "--tokens", "256"]
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--workload", "switch-base-top1", "--tokens", "256"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]

@@ -50,3 +50,12 @@ def test_zipf_bias_is_a_log_distribution():
     assert abs(np.exp(b).sum() - 1.0) < 1e-6
     assert np.all(np.diff(b) < 0)
     assert abs((b[0] - b[1]) - 1.2 * np.log(2.0)) < 1e-5
+
+
+def test_threaded_bit_draws_equal_the_per_expert_draws():
+    w = syn.WORKLOADS["large-top8-swiglu"].with_(name="bits-small", E=6, d=64, F=32)
+    b1, b2 = syn.expert_weight_bits(w, threads=3)
+    assert b1.dtype == np.uint16 and b1.shape == (6, 64, 64) and b2.shape == (6, 64, 32)
+    for e in range(w.E):
+        a, b = syn.expert_weights(w, e)
+        assert np.array_equal(syn.from_bf16_bits(b1[e]), a) and np.array_equal(syn.from_bf16_bits(b2[e]), b)

@@ -2,7 +2,7 @@
 memory at all (no workspace to pass), against the workspace-based
 moe_dispatch on the same inputs.
 
-The new entry point keeps its scratch in a fixed array inside the library,
+The entry point keeps its scratch in a fixed array inside the library,
 shared by every call, so it is checked on two calls in a row whose routings
 differ: the second call must not see anything the first one left behind.
 Dispatch is integer and copy work, so the comparison is bit for bit.
@@ -33,6 +33,9 @@ def test_noalloc_dispatch_matches_workspace_dispatch_on_two_calls():
     cases = [
         syn.Workload("noalloc-a", T=3000, d=256, E=32, k=2, F=256, act="relu", dtype="bf16", cf=(5, 4)),
         syn.Workload("noalloc-b", T=1100, d=320, E=16, k=4, F=256, act="relu", dtype="bf16", cf=(1, 1)),
+        # the fixed array's exact bound: T = MOE_NOALLOC_MAX_TOKENS tokens over 256 experts
+        syn.Workload("noalloc-max", T=moe.MOE_NOALLOC_MAX_TOKENS, d=128, E=256, k=2, F=256, act="relu",
+                     dtype="bf16", cf=(5, 4)),
     ]
     for w in cases:
         cfg = config_for(moe, w)
