@@ -270,9 +270,16 @@ def replay_kernels_alone(step, stream, flush, reps: int):
     stream.wait_stream(side)
     torch.cuda.synchronize()
     graph = drv.CUgraph(g.raw_cuda_graph())
-    n = _drv_ok(drv.cuGraphGetRootNodes(graph, 0))[1]
-    roots = _drv_ok(drv.cuGraphGetRootNodes(graph, n))[0]
-    order, frontier, seen = [], list(roots), set()
+
+    def listing(fn, *head):
+        # (nodes, count) of a driver query, whichever of its signatures the bindings expose (some also return
+        # edge data): the first list in the result is the nodes, the last integer the count
+        n = [v for v in _drv_ok(fn(*head, 0)) if isinstance(v, int)][-1]
+        if n == 0:
+            return []
+        return next(v for v in _drv_ok(fn(*head, n)) if isinstance(v, (list, tuple)))
+
+    order, frontier, seen = [], list(listing(drv.cuGraphGetRootNodes, graph)), set()
     while frontier:                              # stream capture of one stream: a chain
         node = frontier.pop(0)
         key = int(node)
@@ -280,9 +287,9 @@ def replay_kernels_alone(step, stream, flush, reps: int):
             continue
         seen.add(key)
         order.append(node)
-        m = _drv_ok(drv.cuGraphNodeGetDependentNodes(node, 0))[1]
-        if m:
-            frontier.extend(_drv_ok(drv.cuGraphNodeGetDependentNodes(node, m))[0])
+        frontier.extend(listing(drv.cuGraphNodeGetDependentNodes, node))
+    if len(order) != len(listing(drv.cuGraphGetNodes, graph)):
+        raise RuntimeError("the captured step graph is not one chain of nodes")
     s_handle = drv.CUstream(stream.cuda_stream)
     out = []
     for node in order:

@@ -36,8 +36,8 @@
  *     R1 = F (ReLU) or 2F (SwiGLU: gate rows then up rows),
  *     rows = moe_max_rows(cfg) = min(T*k, E*C) (T*k without a capacity).
  *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 1; d and F are
- *     multiples of 64 for MOE_BF16 and of 4 for MOE_F32 (MOE_ERR_ALIGNMENT
- *     otherwise).
+ *     multiples of 8 for MOE_BF16 and of 4 for MOE_F32, so that every row is
+ *     a whole number of 16-byte vectors (MOE_ERR_ALIGNMENT otherwise).
  */
 #ifndef MOE_H
 #define MOE_H
@@ -55,13 +55,19 @@ typedef enum moe_status {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1, /* null pointer, bad size, k > E, ... */
   MOE_ERR_UNSUPPORTED = 2, /* outside the limits above */
-  MOE_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned, or d/F not a multiple of 64 for bf16 */
+  MOE_ERR_ALIGNMENT = 3,   /* pointer not 16-byte aligned, or d/F not a multiple of 8 (bf16) or 4 (fp32) */
   MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed (see moe_last_cuda_error) */
   MOE_ERR_DEVICE = 5       /* a kernel recorded an error (see moe_get_device_error) */
 } moe_status;
 
 enum { MOE_ACT_RELU = 0, MOE_ACT_SWIGLU = 1 };
 enum { MOE_F32 = 0, MOE_BF16 = 1 };
+/* Router score functions. MOE_SCORE_SOFTMAX is [Switch] eq. (1); the two
+ * elementwise scores are the variants [Wiki] section 横断的知見 names (sigmoid
+ * gating without the softmax's zero-sum coupling, and sqrt(Softplus(h))):
+ *   sigmoid:       s_e = 1 / (1 + exp(-h_e))
+ *   sqrt_softplus: s_e = sqrt(log(1 + exp(h_e))) */
+enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1, MOE_SCORE_SQRT_SOFTPLUS = 2 };
 
 /* Codes a kernel can record in the workspace's error word. */
 enum {
@@ -82,6 +88,11 @@ typedef struct moe_config {
   int32_t act;         /* MOE_ACT_RELU: W2 relu(W1 z); MOE_ACT_SWIGLU: W2 (silu(Wg z) * Wu z) */
   int32_t dtype;       /* MOE_BF16 or MOE_F32 */
   int32_t renormalize; /* 1: gates renormalised over the k selected experts */
+  int32_t add_residual; /* 1: out = x + MoE(x) and a fully dropped token returns x ([Switch]
+                           section エキスパートには「定員」がある: overflow passes through the
+                           residual); 0: out = MoE(x), zeros for a fully dropped token (the
+                           caller adds the residual), and dX carries no dY term */
+  int32_t score;       /* MOE_SCORE_*: the router's score function (softmax by default) */
   int64_t capacity;    /* expert capacity C per expert; < 0: no limit (dropless) */
   float aux_alpha;     /* alpha of eq. (4) */
   int32_t reserved;    /* must be 0 */
@@ -130,6 +141,40 @@ moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r,
                       const float *logit_bias, float *probs, int32_t *topk_idx,
                       float *topk_gate, float *importance, int32_t *load, float *aux_loss,
                       void *ws, moe_stream_t stream);
+
+/*
+ * Router with a selection-only correction bias: the auxiliary-loss-free load
+ * balancing that [Wiki] "Mixture-of-Experts", section 横断的知見, describes
+ * (each expert's bias is added to the routing scores when the experts are
+ * chosen; the gates stay the scores). Everything as in moe_router, with
+ * cfg->score choosing the score s (softmax, sigmoid or sqrt(softplus)):
+ *   probs       [T, E] fp32 out (or NULL): the scores s
+ *   select_bias [E]    fp32: the k largest s + b per token are chosen
+ *                      (descending, ties to the lower index)
+ *   topk_gate   [T, k] fp32 out: s of the chosen experts (divided by their
+ *                      sum when cfg->renormalize); the bias is not in them
+ *   importance  [E]    fp32 out: sum_t s[t, e]
+ * Without a bias (moe_router, any cfg->score) the choice is the top-k of h,
+ * which is the order of every score function here. MOE_BF16 layers only
+ * (MOE_ERR_UNSUPPORTED otherwise). moe_backward differentiates the gates
+ * through cfg->score; the bias and the choice carry no gradient.
+ */
+moe_status moe_router_biased(const moe_config *cfg, const void *x, const float *w_r,
+                             const float *logit_bias, const float *select_bias, float *probs,
+                             int32_t *topk_idx, float *topk_gate, float *importance, int32_t *load,
+                             float *aux_loss, void *ws, moe_stream_t stream);
+
+/*
+ * The correction bias's update after a batch, the sign rule of the
+ * auxiliary-loss-free method [Wiki] section 横断的知見 cites:
+ *   select_bias[e] += gamma * sign(mean_e'(load) - load[e])
+ * so overloaded experts move down and underloaded ones up (no change at the
+ * mean). The sign is decided in integers, as sign(sum(load) - E load[e]).
+ *   load        [E] int32 (moe_router_biased's output)
+ *   select_bias [E] fp32, updated in place
+ */
+moe_status moe_select_bias_update(const moe_config *cfg, const int32_t *load, float *select_bias,
+                                  float gamma, moe_stream_t stream);
 
 /*
  * Dispatch ([Switch] eq. (3) and its dropped-token rule; [LRMoE] compaction
@@ -216,7 +261,8 @@ moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm,
  *   out[t] = x[t] + sum over j with slot[t, j] >= 0 of
  *            topk_gate[t, j] * y_perm[expert_offsets[e] + slot[t, j]]
  * summed in fp32 and rounded once. A token with every assignment dropped
- * gets x[t] bit for bit.
+ * gets x[t] bit for bit. With cfg->add_residual == 0 the x[t] term is left
+ * out (a fully dropped token gets zeros).
  *
  *   out [T, d] x dtype out (may not alias x or y_perm)
  */
@@ -276,7 +322,8 @@ typedef struct moe_saved {
  * carries no gradient; P does, through eq. (1)).
  *
  *   dy   [T, d]      x dtype
- *   dx   [T, d]      x dtype out: dY (residual) + expert path + router path
+ *   dx   [T, d]      x dtype out: dY (residual; only when cfg->add_residual) +
+ *                    expert path + router path
  *   dw_r [E, d]      fp32 out
  *   dw1  [E, R1, d]  x dtype out
  *   dw2  [E, d, F]   x dtype out

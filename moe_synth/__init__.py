@@ -58,6 +58,8 @@ class Workload:
     expert_scale: float = 0.1   # expert std = expert_scale / sqrt(fan_in)
     zipf_s: Optional[float] = None
     alpha: float = 0.01         # load-balancing loss coefficient
+    add_residual: bool = True   # out = x + MoE(x) (True) or MoE(x)
+    score: str = "softmax"      # router score function: softmax | sigmoid | sqrt_softplus
     backward: bool = False      # the workload includes the backward pass
     seed: int = 49
 

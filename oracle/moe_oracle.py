@@ -31,13 +31,19 @@ project's design notes):
 * Within an expert, assignments are ranked in ascending token order; rank < C
   is kept (slot = rank), the rest are dropped (slot = -1).
 * out = x + sum over kept selected experts of g * E_i(x); a token whose
-  assignments are all dropped returns x unchanged.
+  assignments are all dropped returns x unchanged. With add_residual off the
+  layer returns the gated sum alone (zeros for such a token): the residual
+  connection is the caller's.
 * f_e = load_e / (T*k) counted before capacity, P_e = importance_e / T,
   aux = alpha * E * sum_e f_e P_e.
 * Experts have no biases. ReLU: W2 relu(W1 z). SwiGLU: W2 (silu(Wg z) * (Wu z)),
   W1 = [Wg; Wu] stacked by rows, silu(u) = u / (1 + exp(-u)).
 * Backward of L = <dY, out> + aux with top-k sets, capacity masks and f held
   constant.
+* Router variants (score = sigmoid or sqrt_softplus, a selection-only
+  correction bias): p is the score, importance sums it, the gates are p of
+  the chosen experts, the choice is on p + b (on h without a bias); see
+  router_variants.py.
 
 Parity status: every function here is pinned by the oracle tests (invariants,
 closed forms, brute force on tiny inputs, finite differences); none is
@@ -48,6 +54,8 @@ from __future__ import annotations
 from typing import Callable, Optional, Sequence, Tuple, Union
 
 import numpy as np
+
+from . import router_variants as RV
 
 ExpertSource = Union[Tuple[np.ndarray, np.ndarray], Callable[[int], Tuple[np.ndarray, np.ndarray]]]
 
@@ -82,6 +90,19 @@ def softmax(h: np.ndarray) -> np.ndarray:
     return z / z.sum(axis=1, keepdims=True)
 
 
+def score_grad(h: np.ndarray, p: np.ndarray, dp: np.ndarray, score: str) -> np.ndarray:
+    """dL/dh from dL/dp through the score function: the softmax Jacobian of eq. (1),
+    p (dp - <p, dp>); elementwise scores multiply by their derivative,
+    sigmoid' = p (1 - p) and sqrt(softplus)'(h) = sigmoid(h) / (2 sqrt(softplus(h)))."""
+    if score == "softmax":
+        return p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    if score == "sigmoid":
+        return p * (1.0 - p) * dp
+    if score == "sqrt_softplus":
+        return (1.0 / (1.0 + np.exp(-h))) / (2.0 * p) * dp
+    raise ValueError(score)
+
+
 def top_k(h: np.ndarray, k: int) -> np.ndarray:
     """Indices of the k largest logits per token, largest first, ties to the
     lower index ([Switch] section 仕組み(1): "上位k個を選び"; k = 1 is the
@@ -90,17 +111,24 @@ def top_k(h: np.ndarray, k: int) -> np.ndarray:
     return order[:, :k].astype(np.int64)
 
 
-def route(x, w_r, bias, k: int, renormalize: bool, alpha: float) -> dict:
+def route(x, w_r, bias, k: int, renormalize: bool, alpha: float, score: str = "softmax",
+          sel_bias=None) -> dict:
     """Router, gates and balance statistics for one batch of T tokens.
 
     [Switch] eqs. (1), (2), (4) and the numpy sketch of section 負荷分散損失:
     probs -> expert choice -> gate -> f (fraction of assignments per expert)
     -> P (mean probability) -> aux = alpha * N * sum f_i P_i.
+
+    `score` and `sel_bias` are the router variants of [Wiki] section 横断的知見
+    (router_variants.py states them): p is then the elementwise score, and
+    with a correction bias the experts are chosen on p + b while the gates
+    stay p. Without a bias the choice is the top-k of h, which is the order
+    of p for the softmax and for every strictly increasing score.
     """
     h = router_logits(x, w_r, bias)
     T, E = h.shape
-    p = softmax(h)
-    idx = top_k(h, k)
+    p = softmax(h) if score == "softmax" else RV.scores(h, score)
+    idx = top_k(h, k) if sel_bias is None else RV.select(p, k, sel_bias)
     gate = np.take_along_axis(p, idx, axis=1)
     if renormalize:
         gate = gate / gate.sum(axis=1, keepdims=True)
@@ -178,9 +206,12 @@ def expert_ffn(z: np.ndarray, w1: np.ndarray, w2: np.ndarray, act: str) -> dict:
 def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
             cf: Optional[Tuple[int, int]], count_assignments: bool = True,
             renormalize: bool = False, alpha: float = 0.01,
-            tokens: Optional[Sequence[int]] = None) -> dict:
+            tokens: Optional[Sequence[int]] = None, add_residual: bool = True, score: str = "softmax",
+            sel_bias=None) -> dict:
     """out = x + sum_{i in T, kept} g_i E_i(x) ([Switch] eq. (2) with the
-    residual passthrough of dropped tokens).
+    residual passthrough of dropped tokens); without the residual
+    (add_residual=False) out is the gated sum alone, and a token whose
+    assignments are all dropped gets zeros.
 
     `tokens` restricts the expert evaluation (and `out`) to a subset of
     tokens; routing, slots and statistics always cover the whole batch,
@@ -189,11 +220,11 @@ def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
     x64 = _f64(x)
     T, d = x64.shape
     E = np.asarray(w_r).shape[0]
-    r = route(x64, w_r, bias, k, renormalize, alpha)
+    r = route(x64, w_r, bias, k, renormalize, alpha, score, sel_bias)
     C = capacity(T, E, k, cf, count_assignments)
     s = assign_slots(r["idx"], E, C)
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
-    out = x64[sel].copy()
+    out = x64[sel].copy() if add_residual else np.zeros((len(sel), d))
     where = {int(t): i for i, t in enumerate(sel)}
     for e in range(E):
         tt, jj = np.nonzero((r["idx"] == e) & (s["slot"] >= 0))
@@ -214,7 +245,8 @@ def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
 def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
              cf: Optional[Tuple[int, int]], count_assignments: bool = True,
              renormalize: bool = False, alpha: float = 0.01,
-             experts_needed: Optional[Sequence[int]] = None) -> dict:
+             experts_needed: Optional[Sequence[int]] = None, add_residual: bool = True,
+             score: str = "softmax", sel_bias=None) -> dict:
     """Gradients of L = <dY, out> + aux (chain rule through eqs. (1), (2), (4)).
 
     Top-k sets, capacity masks and f are constants ([Switch] section
@@ -226,10 +258,10 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
     T, d = x64.shape
     wr64 = _f64(w_r)
     E = wr64.shape[0]
-    r = route(x64, wr64, bias, k, renormalize, alpha)
+    r = route(x64, wr64, bias, k, renormalize, alpha, score, sel_bias)
     C = capacity(T, E, k, cf, count_assignments)
     s = assign_slots(r["idx"], E, C)
-    dx = dy64.copy()                       # residual path
+    dx = dy64.copy() if add_residual else np.zeros_like(dy64)   # residual path
     dg = np.zeros((T, k))
     dw1, dw2 = {}, {}
     need = set(range(E)) if experts_needed is None else set(int(e) for e in experts_needed)
@@ -274,8 +306,8 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
         np.put_along_axis(dp, idx, dg, axis=1)
     # eq. (4): d aux / d p_{t,e} = alpha * E * f_e / T
     dp += alpha * E * r["f"][None, :] / float(T)
-    # eq. (1): softmax Jacobian
-    dh = p * (dp - np.sum(p * dp, axis=1, keepdims=True))
+    # eq. (1): softmax Jacobian (or the elementwise score's derivative)
+    dh = score_grad(r["h"], p, dp, score)
     dw_r = dh.T @ x64
     dx += dh @ wr64
     return dict(dx=dx, dw_r=dw_r, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r, slots=s)
@@ -283,7 +315,8 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
 
 def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequence[int],
                      experts_sampled: Sequence[int], k: int, act: str, cf: Optional[Tuple[int, int]],
-                     count_assignments: bool = True, renormalize: bool = False, alpha: float = 0.01) -> dict:
+                     count_assignments: bool = True, renormalize: bool = False, alpha: float = 0.01,
+                     add_residual: bool = True, score: str = "softmax", sel_bias=None) -> dict:
     """The gradients of `backward` for a few tokens (dx, dg and dh rows) and a
     few experts (dw1, dw2), without evaluating every expert on every token:
     the same chain rule through eqs. (1), (2) and (4). Each expert the
@@ -298,7 +331,7 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
     T, d = x64.shape
     wr64 = _f64(w_r)
     E = wr64.shape[0]
-    r = route(x64, wr64, bias, k, renormalize, alpha)
+    r = route(x64, wr64, bias, k, renormalize, alpha, score, sel_bias)
     C = capacity(T, E, k, cf, count_assignments)
     s = assign_slots(r["idx"], E, C)
     p, idx, gate, slot = r["p"], r["idx"], r["gate"], s["slot"]
@@ -316,7 +349,7 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
             da = np.concatenate([dhid * fw["u"] * (sg * (1.0 + fw["g"] * (1.0 - sg))), dhid * silu(fw["g"])], axis=1)
         return fw, dyp, da
 
-    acc = {t: dy64[t].copy() for t in toks}          # residual path
+    acc = {t: dy64[t].copy() if add_residual else np.zeros(d) for t in toks}   # residual path
     dg = {t: np.zeros(k) for t in toks}
     pairs = {}                                        # expert -> the sampled tokens' kept pairs (t, j)
     for t in toks:
@@ -351,7 +384,7 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
         else:
             dp[idx[t]] = dg[t]
         dp += alpha * E * r["f"] / float(T)
-        dh[t] = p[t] * (dp - np.dot(p[t], dp))
+        dh[t] = score_grad(r["h"][t:t + 1], p[t:t + 1], dp[None, :], score)[0]
         dx[t] = acc[t] + dh[t] @ wr64
     return dict(dx=dx, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r, slots=s)
 

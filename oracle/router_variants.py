@@ -1,8 +1,8 @@
 """CPU oracle for router variants of the same layer (test infrastructure).
 
-Like moe_oracle, this is plain fp64 numpy that only the tests may use; no
-CUDA kernel implements these variants yet. It fixes what they compute before
-any kernel does.
+Like moe_oracle, this is plain fp64 numpy that only the tests may use. The
+layer oracle (moe_oracle.route / forward / backward) takes its score
+functions and selection from here.
 
 Page followed: [Wiki] "Mixture-of-Experts" (notes.yuuk.io), section 横断的知見,
 which names three changes to the router without giving formulas:

@@ -21,11 +21,14 @@ LIB_PATH = os.path.join(HERE, "libmoe.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_ALIGNMENT, MOE_ERR_CUDA, MOE_ERR_DEVICE = range(6)
 MOE_ACT_RELU, MOE_ACT_SWIGLU = 0, 1
 MOE_F32, MOE_BF16 = 0, 1
+MOE_SCORE_SOFTMAX, MOE_SCORE_SIGMOID, MOE_SCORE_SQRT_SOFTPLUS = 0, 1, 2
+SCORES = {"softmax": MOE_SCORE_SOFTMAX, "sigmoid": MOE_SCORE_SIGMOID, "sqrt_softplus": MOE_SCORE_SQRT_SOFTPLUS}
 MOE_DEVERR_NONE, MOE_DEVERR_BAD_EXPERT, MOE_DEVERR_DUP_EXPERT, MOE_DEVERR_TIMEOUT = range(4)
 MOE_NOALLOC_MAX_TOKENS = 32768
 
 EXPORTED = [
     "moe_capacity", "moe_max_rows", "moe_workspace_size", "moe_workspace_init", "moe_router",
+    "moe_router_biased", "moe_select_bias_update",
     "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_forward", "moe_backward",
     "moe_backward_intermediates",
     "moe_get_device_error", "moe_selftest_bounded_wait", "moe_status_string", "moe_last_cuda_error",
@@ -42,8 +45,9 @@ class moe_config(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("n_experts", ctypes.c_int32),
         ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32),
-        ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("capacity", ctypes.c_int64),
-        ("aux_alpha", ctypes.c_float), ("reserved", ctypes.c_int32),
+        ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("add_residual", ctypes.c_int32),
+        ("score", ctypes.c_int32), ("capacity", ctypes.c_int64), ("aux_alpha", ctypes.c_float),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -72,6 +76,8 @@ def lib() -> ctypes.CDLL:
             "moe_workspace_size": (ctypes.c_int, [C, ctypes.POINTER(SZ)]),
             "moe_workspace_init": (ctypes.c_int, [C, P, P]),
             "moe_router": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P]),
+            "moe_router_biased": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P, P]),
+            "moe_select_bias_update": (ctypes.c_int, [C, P, P, ctypes.c_float, P]),
             "moe_dispatch": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
             "moe_dispatch_noalloc": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
             "moe_expert_gemm": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
@@ -123,10 +129,11 @@ def _stream(stream) -> Optional[int]:
 
 def make_config(T: int, d_model: int, n_experts: int, top_k: int, d_ff: int, act: str = "relu",
                 dtype: str = "bf16", renormalize: bool = False, capacity: int = -1,
-                aux_alpha: float = 0.01) -> moe_config:
+                aux_alpha: float = 0.01, add_residual: bool = True, score: str = "softmax") -> moe_config:
     return moe_config(T=T, d_model=d_model, n_experts=n_experts, top_k=top_k, d_ff=d_ff,
                       act=MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_RELU,
                       dtype=MOE_BF16 if dtype == "bf16" else MOE_F32, renormalize=int(renormalize),
+                      add_residual=int(add_residual), score=SCORES[score],
                       capacity=-1 if capacity is None else int(capacity), aux_alpha=float(aux_alpha),
                       reserved=0)
 
@@ -157,6 +164,21 @@ def moe_router(cfg, x, w_r, logit_bias, probs, topk_idx, topk_gate, importance, 
     _check(lib().moe_router(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_bias), _ptr(probs), _ptr(topk_idx),
                             _ptr(topk_gate), _ptr(importance), _ptr(load), _ptr(aux_loss), _ptr(ws),
                             _stream(stream)), "moe_router")
+
+
+def moe_router_biased(cfg, x, w_r, logit_bias, select_bias, probs, topk_idx, topk_gate, importance, load, aux_loss,
+                      ws, stream=None):
+    """moe_router with a selection-only correction bias (the experts are chosen on score + bias; the gates are
+    the scores)."""
+    _check(lib().moe_router_biased(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_bias), _ptr(select_bias),
+                                   _ptr(probs), _ptr(topk_idx), _ptr(topk_gate), _ptr(importance), _ptr(load),
+                                   _ptr(aux_loss), _ptr(ws), _stream(stream)), "moe_router_biased")
+
+
+def moe_select_bias_update(cfg, load, select_bias, gamma: float, stream=None):
+    """select_bias[e] += gamma * sign(mean(load) - load[e]), in place."""
+    _check(lib().moe_select_bias_update(ctypes.byref(cfg), _ptr(load), _ptr(select_bias), float(gamma),
+                                        _stream(stream)), "moe_select_bias_update")
 
 
 def moe_dispatch(cfg, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, ws, stream=None):
@@ -286,11 +308,16 @@ class MoELayer:
         self.R1 = R1
         moe_workspace_init(cfg, self.ws, stream)
 
-    def forward(self, x, w_r, w1, w2, logit_bias=None, topk_idx=None):
-        """out = x + MoE(x). If topk_idx is given, the router's choice is replaced by it (replay)."""
+    def forward(self, x, w_r, w1, w2, logit_bias=None, topk_idx=None, select_bias=None):
+        """out = x + MoE(x) (MoE(x) alone without the residual). If topk_idx is given, the router's choice is
+        replaced by it (replay); select_bias is the selection-only correction bias (moe_router_biased)."""
         c, s = self.cfg, self.stream
-        moe_router(c, x, w_r, logit_bias, self.probs, self.topk_idx, self.topk_gate, self.importance, self.load,
-                   self.aux, self.ws, s)
+        if select_bias is None:
+            moe_router(c, x, w_r, logit_bias, self.probs, self.topk_idx, self.topk_gate, self.importance,
+                       self.load, self.aux, self.ws, s)
+        else:
+            moe_router_biased(c, x, w_r, logit_bias, select_bias, self.probs, self.topk_idx, self.topk_gate,
+                              self.importance, self.load, self.aux, self.ws, s)
         idx = self.topk_idx if topk_idx is None else topk_idx
         moe_dispatch(c, x, idx, self.slot, self.kept, self.offsets, self.row_token, self.x_perm, self.ws, s)
         moe_expert_gemm(c, self.x_perm, self.offsets, w1, w2, self.pre_act, self.h, self.y_perm, self.ws, s)

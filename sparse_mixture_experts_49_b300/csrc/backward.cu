@@ -10,7 +10,8 @@
 // the router receives a gradient; eq. (4) adds alpha N sum_i f_i P_i, where f
 // comes from the argmax (no gradient) and P_i = mean_t p_i (gradient
 // alpha N f_i / T on every p_{t,i}); eq. (1) is the softmax whose Jacobian
-// maps dp to dh = p * (dp - <p, dp>).
+// maps dp to dh = p * (dp - <p, dp>). With the router variants' elementwise
+// scores ([Wiki] "Mixture-of-Experts", section 横断的知見) dh = s'(h) dp.
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -48,8 +49,8 @@ __constant__ int kPartB[6] = {0, 1, 0, 2, 1, 0};
 template <int EPT>
 __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, const int32_t *idx, const float *gate,
                                                         const int32_t *load, const float *dg, int T, int E, int k,
-                                                        int renorm, float alpha, float *dh, bf16 *a6, int EP,
-                                                        int32_t *offs2, int G) {
+                                                        int renorm, float alpha, int score, float *dh, bf16 *a6,
+                                                        int EP, int32_t *offs2, int G) {
   if (a6 && blockIdx.x == 0) {
     if (threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
     if (threadIdx.x <= G) {
@@ -102,14 +103,24 @@ __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, cons
         if (lane + 32 * q == ej) dp[q] += add;
     }
     float s = 0.0f;
+    if (score == MOE_SCORE_SOFTMAX) {
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) s = fmaf(p[j], dp[j], s);
+      for (int j = 0; j < EPT; ++j) s = fmaf(p[j], dp[j], s);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    }
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
       const int e = lane + 32 * j;
-      const float v = p[j] * (dp[j] - s);
+      float v;
+      if (score == MOE_SCORE_SOFTMAX) {
+        v = p[j] * (dp[j] - s);                       // softmax Jacobian
+      } else if (score == MOE_SCORE_SIGMOID) {
+        v = p[j] * (1.0f - p[j]) * dp[j];             // sigmoid' = s (1 - s)
+      } else {
+        // sqrt(softplus)'(h) = sigmoid(h) / (2 s), and sigmoid(h) = 1 - exp(-softplus(h)) = 1 - exp(-s^2)
+        v = p[j] > 0.0f ? (-expm1f(-p[j] * p[j])) / (2.0f * p[j]) * dp[j] : 0.0f;
+      }
       if (e < E) dh[(int64_t)t * E + e] = v;
       if (a6 && e < EP) {
         const Parts3 q = split3(e < E ? v : 0.0f);
@@ -176,7 +187,7 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   cudaError_t err;
 #define MOE_DH(EPT)                                                                                            \
   err = launch_kernel(router_dh_kernel<EPT>, dim3(grid), dim3(256), 0, stream, probs, idx, gate, load, dg, sh.T, sh.E, \
-                   sh.k, sh.renorm, sh.alpha, dh, a6, EP, offs2, G)
+                   sh.k, sh.renorm, sh.alpha, sh.score, dh, a6, EP, offs2, G)
   if (sh.E <= 32) MOE_DH(1);
   else if (sh.E <= 64) MOE_DH(2);
   else if (sh.E <= 128) MOE_DH(4);

@@ -6,6 +6,8 @@
 // passes through the residual connection. The layer output is
 // out = x + sum over kept (t, j) of g[t, j] * y_perm[row(t, j)], accumulated in
 // fp32 and rounded once; a token with nothing kept returns x bit for bit.
+// Without the residual (add_residual = 0) the sum starts from zero, and the
+// backward's dX from zero instead of dY.
 //
 // All three kernels give one warp to a token and stream its rows with
 // 16-byte vector accesses, so they run at HBM speed.
@@ -42,7 +44,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, 
                                                       const int32_t *__restrict__ idx, const float *__restrict__ gate,
                                                       const int32_t *__restrict__ slot,
                                                       const int32_t *__restrict__ offsets, int T, int d, int k,
-                                                      XT *__restrict__ out) {
+                                                      int residual, XT *__restrict__ out) {
   constexpr int V = Vec16<XT>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
@@ -54,7 +56,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, 
     XT *orow = out + (int64_t)t * d;
     for (int v = lane; v < nvec; v += 32) {
       uint4 raw[KMAX + 1];
-      raw[0] = *reinterpret_cast<const uint4 *>(xr + v * V);
+      raw[0] = residual ? *reinterpret_cast<const uint4 *>(xr + v * V) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
         if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(y_perm + (int64_t)row[j] * d + v * V);
@@ -133,7 +135,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const XT *__restrict__ d
                                                         const float *__restrict__ dxr, const int32_t *__restrict__ idx,
                                                         const int32_t *__restrict__ slot,
                                                         const int32_t *__restrict__ offsets, int T, int d, int k,
-                                                        XT *__restrict__ dx) {
+                                                        int residual, XT *__restrict__ dx) {
   constexpr int V = Vec16<XT>::N;
   const int lane = threadIdx.x & 31;
   const int nvec = d / V;
@@ -143,7 +145,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const XT *__restrict__ d
     token_rows<KMAX>(t, k, idx, slot, offsets, nullptr, row, g);
     for (int v = lane; v < nvec; v += 32) {
       uint4 raw[KMAX + 1];
-      raw[0] = *reinterpret_cast<const uint4 *>(dy + (int64_t)t * d + v * V);
+      raw[0] = residual ? *reinterpret_cast<const uint4 *>(dy + (int64_t)t * d + v * V) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
         if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(dxp + (int64_t)row[j] * d + v * V);
@@ -184,7 +186,7 @@ template <typename XT, int KMAX>
 cudaError_t run_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx, const float *gate,
                         const int32_t *slot, const int32_t *offsets, void *out, cudaStream_t stream) {
   return launch_kernel(combine_kernel<XT, KMAX>, dim3(token_grid(sh.T)), dim3(256), 0, stream, (const XT *)x,
-                    (const XT *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, (XT *)out);
+                    (const XT *)y_perm, idx, gate, slot, offsets, sh.T, sh.d, sh.k, sh.residual, (XT *)out);
 }
 
 template <typename XT>
@@ -233,7 +235,7 @@ template <typename XT, int KMAX>
 cudaError_t run_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr, const int32_t *idx,
                           const int32_t *slot, const int32_t *offsets, void *dx, cudaStream_t stream) {
   return launch_kernel(unpermute_kernel<XT, KMAX>, dim3(token_grid(sh.T)), dim3(256), 0, stream, (const XT *)dy,
-                       (const XT *)dxp, dxr, idx, slot, offsets, sh.T, sh.d, sh.k, (XT *)dx);
+                       (const XT *)dxp, dxr, idx, slot, offsets, sh.T, sh.d, sh.k, sh.residual, (XT *)dx);
 }
 
 template <typename XT>

@@ -163,13 +163,14 @@ __global__ void __launch_bounds__(DT) dispatch_count_kernel(const int32_t *__res
 // rank if rank < C else -1) and writes the kept pair's row owner. Units of
 // other chunks may read either form and derive the same row, offsets[e] +
 // slot. The chunk goes to each kept row of x_perm (if given), or to
-// out_dropped (if given) when the token kept none. KMAX >= k bounds the
+// out_dropped (if given) when the token kept none (zeros instead of the
+// chunk when zero_dropped: the layer without its residual). KMAX >= k bounds the
 // unrolled row stores.
 template <typename XT, int KMAX>
 __global__ void __launch_bounds__(256) dispatch_place_kernel(
     const XT *__restrict__ x, const int32_t *__restrict__ idx, int T, int d, int E, int k, int64_t C,
     const int32_t *__restrict__ block_base, const int32_t *__restrict__ offsets, int32_t *slot,
-    int32_t *__restrict__ row_token, XT *__restrict__ x_perm, XT *__restrict__ out_dropped) {
+    int32_t *__restrict__ row_token, XT *__restrict__ x_perm, XT *__restrict__ out_dropped, int zero_dropped) {
   constexpr int V = Vec16<XT>::N;
   constexpr int U = 4;  // units in flight per warp
   const int lane = threadIdx.x & 31;
@@ -227,7 +228,8 @@ __global__ void __launch_bounds__(256) dispatch_place_kernel(
         if (lv && r >= 0 && x_perm) *reinterpret_cast<uint4 *>(x_perm + (int64_t)r * d + (int64_t)vv[b] * V) = val[b];
       }
       if (lv && !kept_any && out_dropped)
-        *reinterpret_cast<uint4 *>(out_dropped + (int64_t)tok[b] * d + (int64_t)vv[b] * V) = val[b];
+        *reinterpret_cast<uint4 *>(out_dropped + (int64_t)tok[b] * d + (int64_t)vv[b] * V) =
+            zero_dropped ? make_uint4(0u, 0u, 0u, 0u) : val[b];
     }
   }
 }
@@ -294,7 +296,7 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
   if (sh.dtype == MOE_BF16) {
 #define MOE_PLACE(KM)                                                                                            \
   return launch_kernel(dispatch_place_kernel<bf16, KM>, grid, dim3(256), 0, stream, (const bf16 *)x, idx, sh.T,   \
-                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped)
+                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (bf16 *)x_perm, (bf16 *)out_dropped, sh.residual ? 0 : 1)
     if (sh.k == 1) MOE_PLACE(1);
     if (sh.k == 2) MOE_PLACE(2);
     if (sh.k <= 4) MOE_PLACE(4);
@@ -302,7 +304,7 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
 #undef MOE_PLACE
   }
   return launch_kernel(dispatch_place_kernel<float, 8>, grid, dim3(256), 0, stream, (const float *)x, idx, sh.T,
-                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm, (float *)out_dropped);
+                       sh.d, sh.E, sh.k, sh.C, base, offsets, slot, row_token, (float *)x_perm, (float *)out_dropped, sh.residual ? 0 : 1);
 }
 
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,

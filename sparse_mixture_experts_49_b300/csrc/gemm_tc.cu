@@ -59,6 +59,10 @@ template <int PAIR> constexpr int b_bytes() { return (PAIR ? BN / 2 : BN) * BK *
 template <int PAIR> constexpr int stage_bytes() { return A_BYTES + b_bytes<PAIR>(); }
 
 // Grouped-K: every group has the same tiles, so no prefix array is kept.
+// Tile queue of the dynamic scheduler: the producer warp takes tile indices
+// from a global counter and passes each to the MMA warp and the eight
+// epilogue warps through TQ slots.
+constexpr int TQ = 8;
 template <bool GK, int NST> struct __align__(8) SmemT {
   uint64_t full[NST];       // this CTA's TMA bytes of the stage have landed
   uint64_t empty[NST];      // the MMAs reading the stage have completed
@@ -66,8 +70,11 @@ template <bool GK, int NST> struct __align__(8) SmemT {
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t drain;
+  uint64_t tq_full[TQ];     // dynamic tiles: slot written by the producer
+  uint64_t tq_empty[TQ];    // dynamic tiles: slot read by the MMA warp and every epilogue warp
   uint32_t tmem_base;
   int abort_flag;
+  int tile_q[TQ];           // dynamic tiles: the tile of each slot (-1: no more tiles)
   int tile_start[GK ? 1 : MAX_E + 1];  // grouped-M: tiles of the groups before e
 };
 // Plain-store epilogues (EPI_STORE, EPI_STORE_F32) stage each warp's 32-row
@@ -112,6 +119,8 @@ struct Args {
   int64_t ldaux;
   const int32_t *a_rows;   // EPI_COMBINE: token of each packed row (row_token)
   const float *gate;       // EPI_COMBINE: gate of each token (top-1)
+  int residual;            // EPI_COMBINE: out = x + g y (1) or g y (0)
+  unsigned int *sched;     // {next tile, finished CTAs}, zero at launch: dynamic tile order (null: static)
   DeviceStatus *st;
 };
 
@@ -136,7 +145,7 @@ template <int PAIR, int GROUP_K, int A_MN, int B_MN, int EPI>
 __global__ void __launch_bounds__(THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
-                        const Args p) {
+                        const __grid_constant__ CUtensorMap tmE, const Args p) {
   constexpr bool TMA_STORE = tma_store_epi<EPI>();
   constexpr bool STAGED = staged_epi<EPI>();
   constexpr int NST = n_stages<PAIR, EPI>();
@@ -174,7 +183,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
       if (STAGED) prefetch_tmap(&tmC);
-      if (SWIGLU_FWD) prefetch_tmap(&tmD);
+      if (SWIGLU_FWD || EPI == EPI_SWIGLU_BWD) prefetch_tmap(&tmD);
+      if (SWIGLU_FWD) prefetch_tmap(&tmE);
       for (int i = 0; i < NST; ++i) {
         mbar_init(&s.full[i], 1);
         mbar_init(&s.empty[i], 1);
@@ -183,6 +193,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       // pair tiles: the even CTA's acc_empty collects the epilogue warps of both CTAs
       for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], PAIR ? 16 : 8); }
       mbar_init(&s.drain, 1);
+      for (int i = 0; i < TQ; ++i) { mbar_init(&s.tq_full[i], 1); mbar_init(&s.tq_empty[i], 1 + EPI_WARPS); }
       s.abort_flag = 0;
       fence_barrier_init();
     }
@@ -275,6 +286,32 @@ __global__ void __launch_bounds__(THREADS, 1)
     return nkk;
   };
 
+  // Tile order. Static: unit, unit + units, ... Dynamic (one CTA per tile,
+  // p.sched given): the producer takes the next index from the global
+  // counter as it starts each tile (one fetch ahead) and publishes it in the
+  // tile queue; the MMA and epilogue warps read the same sequence from the
+  // queue. A CTA whose producer has fetched past the end counts itself
+  // finished; the last one resets both counters for the next launch.
+  const bool dyn = !PAIR && p.sched != nullptr;
+  struct TileIter {
+    int next, q;
+    uint32_t ph;
+  };
+  // consumers (MMA warp, epilogue warps): the next tile, -1 when there are no more, -2 on abort
+  auto consumer_next = [&](TileIter &it) -> int {
+    if (!dyn) {
+      const int t = it.next;
+      it.next += units;
+      return t < total_tiles ? t : -1;
+    }
+    if (!mbar_wait_bounded(&s.tq_full[it.q], it.ph, abort_flag, p.st)) return -2;
+    const int t = *reinterpret_cast<volatile int *>(&s.tile_q[it.q]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s.tq_empty[it.q]);
+    if (++it.q == TQ) { it.q = 0; it.ph ^= 1; }
+    return t;
+  };
+
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer
     // Lane 0 waits for free stages and issues this CTA's tile loads.
@@ -288,7 +325,30 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t phase = 0;
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
-    for (int tile = unit0; ok && tile < total_tiles; tile += units) {
+    TileIter it{unit0, 0, 0};
+    int fetched = 0;   // dynamic: lane 0's prefetched index
+    if (dyn && lane == 0) fetched = (int)atomicAdd(p.sched, 1u);
+    while (ok) {
+      int tile;
+      if (dyn) {
+        tile = __shfl_sync(0xffffffffu, fetched, 0);
+        int pub = 1;
+        if (lane == 0) {
+          pub = mbar_wait_bounded(&s.tq_empty[it.q], it.ph ^ 1, abort_flag, p.st) ? 1 : 0;
+          if (pub) {
+            s.tile_q[it.q] = tile < total_tiles ? tile : -1;
+            mbar_arrive(&s.tq_full[it.q]);
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, pub, 0)) { ok = false; break; }
+        if (++it.q == TQ) { it.q = 0; it.ph ^= 1; }
+        if (tile >= total_tiles) break;
+        if (lane == 0) fetched = (int)atomicAdd(p.sched, 1u);   // the next tile, fetched ahead of its use
+      } else {
+        tile = it.next;
+        it.next += units;
+        if (tile >= total_tiles) break;
+      }
       int e, mt, nt;
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
@@ -348,6 +408,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (++stage == NST) { stage = 0; phase ^= 1; }
       }
     }
+    // dynamic tiles: the last CTA whose producer is done resets the counters
+    if (dyn && ok && lane == 0 && atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      p.sched[0] = 0u;
+      p.sched[1] = 0u;
+    }
     // (DIRECT, odd CTA: its bytes complete on the even CTA's barriers, which
     // that CTA drains)
     if (lane == 0 && *abort_flag && !(DIRECT && crank)) {
@@ -363,7 +428,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = unit0; ok && tile < total_tiles; tile += units) {
+    TileIter it{unit0, 0, 0};
+    while (ok) {
+      const int tile = consumer_next(it);
+      if (tile < 0) { ok = tile == -1; break; }
       int e, mt, nt;
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
@@ -451,7 +519,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(&s.acc_empty[0]), 0) : 0u;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = unit0; tile < total_tiles; tile += units) {
+    TileIter it{unit0, 0, 0};
+    while (true) {
+      const int tile = consumer_next(it);
+      if (tile < 0) break;
       int e, mt, nt;
       decode(tile, e, mt, nt);
       if (!mbar_wait_bounded<PAIR != 0>(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
@@ -511,11 +582,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (F32) {
               float *cp = static_cast<float *>(p.C) + row * p.ldc + col;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, x + 4 * i);
+              for (int i = 0; i < 8; ++i)
+                if (col + 4 * i < p.N) Vec16<float>::store(cp + 4 * i, x + 4 * i);
             } else {
               bf16 *cp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) Vec16<bf16>::store(cp + 8 * i, x + 8 * i);
+              for (int i = 0; i < 8; ++i)
+                if (col + 8 * i < p.N) Vec16<bf16>::store(cp + 8 * i, x + 8 * i);
             }
           }
         }
@@ -562,7 +635,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               __syncwarp();
               if (lane == 0) {
                 if (o == 0) tma_store_2d(&tmC, stg, col0, r0);
-                else tma_store_2d(&tmD, stg, (o - 1) * p.F + col0, r0);
+                else tma_store_2d(o == 1 ? &tmD : &tmE, stg, col0, r0);
                 bulk_commit();
               }
             }
@@ -578,12 +651,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int i = 0; i < 32; ++i) hv[i] = silu_f(v[i]) * w[i];
                 bf16 *hp = static_cast<bf16 *>(p.C) + row * p.ldc + col;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
+                for (int i = 0; i < 4; ++i)
+                  if (col + 8 * i < p.N) Vec16<bf16>::store(hp + 8 * i, hv + 8 * i);
                 if (p.C2) {
                   bf16 *gp = p.C2 + row * p.ldc2 + col;
                   bf16 *up = gp + p.F;
 #pragma unroll
                   for (int i = 0; i < 4; ++i) {
+                    if (col + 8 * i >= p.N) continue;
                     Vec16<bf16>::store(gp + 8 * i, v + 8 * i);
                     Vec16<bf16>::store(up + 8 * i, w + 8 * i);
                   }
@@ -640,11 +715,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             {
               uint4 lg[8], lu[8];
 #pragma unroll
+              const bool in_f = col0 + piece * 8 < p.F;   // columns past F: zeros (stores clip there)
               for (int i = 0; i < 8; ++i) {
                 const int rr = 4 * i + (lane >> 3);
                 const bf16 *src = p.aux + (rbase + rr) * p.ldaux + col0 + piece * 8;
-                lg[i] = *reinterpret_cast<const uint4 *>(src);
-                lu[i] = *reinterpret_cast<const uint4 *>(src + p.F);
+                lg[i] = in_f ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
+                lu[i] = in_f ? *reinterpret_cast<const uint4 *>(src + p.F) : make_uint4(0u, 0u, 0u, 0u);
               }
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
@@ -678,8 +754,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, bg, col0, (int)rbase);
-              tma_store_2d(&tmC, bu, p.F + col0, (int)rbase);
+              tma_store_2d(&tmC, bg, col0, (int)rbase);   // dG half of dA
+              tma_store_2d(&tmD, bu, col0, (int)rbase);   // dU half of dA
               bulk_commit();
             }
           }
@@ -705,11 +781,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (valid && col < p.N) {
                   const bf16 *ap = p.aux + orow * p.ldaux + col;
 #pragma unroll
-                  for (int i = 0; i < 4; ++i) aux[g * NAUX + i] = *reinterpret_cast<const uint4 *>(ap + 8 * i);
+                  for (int i = 0; i < 4; ++i)
+                    aux[g * NAUX + i] = col + 8 * i < p.N ? *reinterpret_cast<const uint4 *>(ap + 8 * i)
+                                                          : make_uint4(0u, 0u, 0u, 0u);
                   if (EPI == EPI_SWIGLU_BWD) {
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                      aux[g * NAUX + 4 + i] = *reinterpret_cast<const uint4 *>(ap + p.F + 8 * i);
+                      aux[g * NAUX + 4 + i] = col + 8 * i < p.N ? *reinterpret_cast<const uint4 *>(ap + p.F + 8 * i)
+                                                                : make_uint4(0u, 0u, 0u, 0u);
                   }
                 }
               }
@@ -726,7 +805,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Vec16<bf16>::unpack(aux[g * NAUX + i], w + 8 * i);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = fmaf(gt, v[i], w[i]);   // out = x + g * y, rounded once
+                for (int i = 0; i < 32; ++i) v[i] = p.residual ? fmaf(gt, v[i], w[i]) : gt * v[i];   // out = x + g y
               } else if (EPI == EPI_RELU_BWD) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) Vec16<bf16>::unpack(aux[g * NAUX + i], w + 8 * i);
@@ -746,17 +825,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     du[j] = dh * gg[j] * sg;                                      // dU = dH * silu(G)
                     v[8 * i + j] = dh * uu[j] * (sg * (1.0f + gg[j] * (1.0f - sg)));  // dG = dH * U * silu'(G)
                   }
-                  Vec16<bf16>::store(dp2 + 8 * i, du);
+                  if (col + 8 * i < p.N) Vec16<bf16>::store(dp2 + 8 * i, du);
                 }
               }
               if (EPI == EPI_STORE_F32) {
                 float *cp = static_cast<float *>(p.C) + row * p.ldc + col;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, v + 4 * i);
+                for (int i = 0; i < 8; ++i)
+                  if (col + 4 * i < p.N) Vec16<float>::store(cp + 4 * i, v + 4 * i);
               } else {
                 bf16 *cp = static_cast<bf16 *>(p.C) + orow * p.ldc + col;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+                for (int i = 0; i < 4; ++i)
+                  if (col + 8 * i < p.N) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
               }
             }
           }
@@ -777,11 +858,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (EPI == EPI_STORE_F32) {
               float *cp = static_cast<float *>(p.C) + cofs + col;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) Vec16<float>::store(cp + 4 * i, v + 4 * i);
+              for (int i = 0; i < 8; ++i)
+                if (col + 4 * i < p.N) Vec16<float>::store(cp + 4 * i, v + 4 * i);
             } else {
               bf16 *cp = static_cast<bf16 *>(p.C) + cofs + col;
 #pragma unroll
-              for (int i = 0; i < 4; ++i) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
+              for (int i = 0; i < 4; ++i)
+                if (col + 8 * i < p.N) Vec16<bf16>::store(cp + 8 * i, v + 8 * i);
             }
           }
         }
@@ -842,31 +925,49 @@ static int grid_size() {
 // mc is the output's tile map for the plain-store epilogues (ignored otherwise).
 // pair: CTA-pair tiles when a cluster of two fits, one CTA per tile otherwise.
 // md: the second output map (SwiGLU forward: the pre-activations).
+// Tile order of one-CTA-per-tile launches: dynamic (a counter in the
+// workspace hands out tiles as CTAs free up) unless MOE_GEMM_SCHED=static
+// (read at every call) selects the fixed stride.
+static unsigned int *tile_counters(DeviceStatus *st) {
+  const char *v = getenv("MOE_GEMM_SCHED");
+  if (v && v[0] == 's') return nullptr;
+  return reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(st) + kGemmSchedOffset);
+}
+
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
-                          const CUtensorMap &md, const Args &a, cudaStream_t stream) {
+                          const CUtensorMap &md, const CUtensorMap &me, const Args &a, cudaStream_t stream) {
+  Args args = a;
   if (pair) {
     const int g = grid_size<1, GROUP_K, A_MN, B_MN, EPI>();
+    args.sched = nullptr;   // pair tiles keep the fixed order
     if (g > 0)
       return launch_kernel_cluster(grouped_gemm_kernel<1, GROUP_K, A_MN, B_MN, EPI>, 2, dim3(g), dim3(THREADS),
-                                   smem_bytes<1, GROUP_K, EPI>(), stream, ma, mb, mc, md, a);
+                                   smem_bytes<1, GROUP_K, EPI>(), stream, ma, mb, mc, md, me, args);
   }
   const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
   if (g <= 0) return cudaErrorInvalidConfiguration;
+  args.sched = tile_counters(a.st);
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
-                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, md, a);
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, md, me, args);
+}
+template <int GROUP_K, int A_MN, int B_MN, int EPI>
+static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
+                          const CUtensorMap &md, const Args &a, cudaStream_t stream) {
+  static_assert(EPI != EPI_SWIGLU, "the SwiGLU forward epilogue needs the G and U maps");
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, mc, md, md, a, stream);
 }
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const CUtensorMap &mc,
                           const Args &a, cudaStream_t stream) {
-  static_assert(EPI != EPI_SWIGLU, "the SwiGLU forward epilogue needs the pre-activation map");
-  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, mc, mc, a, stream);
+  static_assert(EPI != EPI_SWIGLU && EPI != EPI_SWIGLU_BWD, "the SwiGLU epilogues need their second map");
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, mc, mc, mc, a, stream);
 }
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
 static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &mb, const Args &a,
                           cudaStream_t stream) {
   static_assert(!staged_epi<EPI>(), "staged epilogues need the output map");
-  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, ma, ma, a, stream);
+  return launch<GROUP_K, A_MN, B_MN, EPI>(pair, ma, mb, ma, ma, ma, a, stream);
 }
 // One CTA per tile only (shapes whose M is not a multiple of a pair tile).
 template <int GROUP_K, int A_MN, int B_MN, int EPI>
@@ -874,8 +975,10 @@ static cudaError_t launch_single(const CUtensorMap &ma, const CUtensorMap &mb, c
                                  const Args &a, cudaStream_t stream) {
   const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
   if (g <= 0) return cudaErrorInvalidConfiguration;
+  Args args = a;
+  args.sched = tile_counters(a.st);
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
-                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, mc, a);
+                       smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, mc, mc, args);
 }
 
 }  // namespace tc
@@ -907,15 +1010,19 @@ static int weights_read_once(const Shape &sh, bool pair) {
 static cudaError_t gemm1_act(const Shape &sh, bool pair, const CUtensorMap &ma, const CUtensorMap &mb,
                              const tc::Args &a, uint64_t rows, cudaStream_t stream) {
   using namespace tc;
-  CUtensorMap mc, md;
+  CUtensorMap mc, md, me;
   if (!make_map_2d(&mc, a.C, sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
   if (sh.act != MOE_ACT_SWIGLU) return launch<0, 0, 0, EPI_RELU>(pair, ma, mb, mc, a, stream);
   if (a.C2 != nullptr) {
-    if (!make_map_2d(&md, a.C2, 2 * (uint64_t)sh.F, rows, 64, 32)) return cudaErrorInvalidValue;
+    // G and U, each F wide, in the two halves of each 2F-wide pre-activation row
+    const uint64_t stride = 2 * (uint64_t)sh.F * 2;
+    if (!make_map_2d_strided(&md, a.C2, sh.F, rows, stride, 64, 32) ||
+        !make_map_2d_strided(&me, a.C2 + sh.F, sh.F, rows, stride, 64, 32))
+      return cudaErrorInvalidValue;
   } else {
-    md = mc;
+    md = me = mc;
   }
-  return launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, mc, md, a, stream);
+  return launch<0, 0, 0, EPI_SWIGLU>(pair, ma, mb, mc, md, me, a, stream);
 }
 
 cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t *offsets, const void *w1,
@@ -1016,6 +1123,7 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   b.ldaux = sh.d;
   b.a_rows = row_token;
   b.gate = gate;
+  b.residual = sh.residual;
   return launch<0, 0, 0, EPI_COMBINE>(pair, ma, mb, b, stream);
 }
 
@@ -1040,9 +1148,13 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
       return cudaErrorInvalidValue;
     if (swiglu) {
       a.aux = (const bf16 *)pre_act; a.ldaux = 2 * (int64_t)sh.F;
-      CUtensorMap mc;  // dA [rows, 2F], 64-column x 32-row store boxes
-      if (!make_map_2d(&mc, da, sh.R1, rows, 64, 32)) return cudaErrorInvalidValue;
-      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, mc, a, stream);
+      // dA [rows, 2F] = [dG | dU]: one map per F-wide half, 64-column x 32-row store boxes
+      CUtensorMap mc, md;
+      const uint64_t stride = 2 * (uint64_t)sh.F * 2;
+      if (!make_map_2d_strided(&mc, da, sh.F, rows, stride, 64, 32) ||
+          !make_map_2d_strided(&md, static_cast<bf16 *>(da) + sh.F, sh.F, rows, stride, 64, 32))
+        return cudaErrorInvalidValue;
+      err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, mc, md, a, stream);
     } else {
       a.aux = (const bf16 *)h; a.ldaux = sh.F;
       err = launch<0, 0, 1, EPI_RELU_BWD>(pair, ma, mb, a, stream);

@@ -13,6 +13,8 @@ struct DeviceStatus;
 // moe_config after validation, with derived sizes.
 struct Shape {
   int T, d, E, k, F, R1, act, dtype, renorm;
+  int residual;   // add_residual
+  int score;      // MOE_SCORE_*
   int64_t C;      // capacity, < 0 = none
   float alpha;
   int64_t rows;   // rows of the packed buffers
@@ -23,16 +25,17 @@ enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU
        EPI_COMBINE = 6 };
 
 // Workspace carve-up (byte offsets from the workspace base). The first 256
-// bytes hold the error word (offset 0), the router's completion counter (64)
-// and the dispatch's completion counter (128); the router's statistics
+// bytes hold the error word (offset 0), the router's completion counter (64),
+// the dispatch's completion counter (128) and the grouped GEMM's tile
+// counters (192: next tile, 196: CTAs done); the router's statistics
 // accumulators follow. All of [0, zeroed) starts at zero (moe_workspace_init)
 // and every call leaves it at zero again.
+constexpr size_t kGemmSchedOffset = 192;
 struct WsLayout {
   size_t status;                 // DeviceStatus
   size_t router_acc;               // [E] u64 importance (units of 2^-32), then [E] int32 load
   size_t zeroed;                   // end of the region that must start at zero
   size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
-  size_t router_partial;           // [splits, T, EP] fp32 partial logits (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
   size_t dg, dh, dxr;              // backward: [T, k], [T, E], [T, d] fp32
@@ -47,20 +50,22 @@ constexpr int DISPATCH_TOKENS = 256;  // tokens per dispatch block
 
 int router_blocks(const Shape &sh);
 
-// How the router runs for a shape: tensor cores for bf16 x (logits of 128
-// tokens x EP padded experts per CTA, K split into `splits` ranges so that
-// about kRouterTargetCtas CTAs run), CUDA cores for fp32 x.
-constexpr int kRouterTargetCtas = 148;
+// How the router runs for a shape: tensor cores for bf16 x (one fused kernel
+// per 128-token tile, the ep padded expert columns split over a cluster of
+// `cluster` CTAs of nc columns each), CUDA cores for fp32 x.
 struct RouterPlan {
   bool tensor_cores;
-  int ep, m_tiles, splits, kb_per_split;
+  int ep, m_tiles, cluster, nc;
 };
 RouterPlan router_plan(const Shape &sh);
 int dispatch_blocks(const Shape &sh);
 
-cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, float *probs,
-                          int32_t *idx, float *gate, float *importance, int32_t *load, float *aux, void *ws,
-                          cudaStream_t stream);
+// sel_bias: the selection-only correction bias (bf16 layers), or null.
+cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, const float *sel_bias,
+                          float *probs, int32_t *idx, float *gate, float *importance, int32_t *load, float *aux,
+                          void *ws, cudaStream_t stream);
+cudaError_t launch_select_bias_update(const Shape &sh, const int32_t *load, float gamma, float *sel_bias,
+                                      cudaStream_t stream);
 
 // x_perm may be null (rows are not copied); out_dropped, when given, gets
 // x[t] for every token with no kept assignment.

@@ -31,10 +31,14 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   if (c->act != MOE_ACT_RELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
   if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
   if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
+  if (c->add_residual != 0 && c->add_residual != 1) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID && c->score != MOE_SCORE_SQRT_SOFTPLUS)
+    return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (c->reserved != 0 || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
   if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
   if (c->n_experts > 256 || c->top_k > 8) return MOE_ERR_UNSUPPORTED;
-  const int mult = c->dtype == MOE_BF16 ? 64 : 4;
+  const int mult = c->dtype == MOE_BF16 ? 8 : 4;   // 16-byte rows for TMA and the vector accesses
   if (c->d_model % mult != 0 || c->d_ff % mult != 0) return MOE_ERR_ALIGNMENT;
   const int64_t Tk = (int64_t)c->T * c->top_k;
   if (Tk > (int64_t)1 << 30 || (int64_t)c->d_model * c->d_ff * 2 > ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
@@ -47,6 +51,8 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   sh->act = c->act;
   sh->dtype = c->dtype;
   sh->renorm = c->renormalize;
+  sh->residual = c->add_residual;
+  sh->score = c->score;
   sh->C = c->capacity < 0 ? -1 : c->capacity;
   sh->alpha = c->aux_alpha;
   int64_t rows = Tk;
@@ -70,7 +76,6 @@ WsLayout ws_layout(const Shape &sh) {
   L.zeroed = o;
   const RouterPlan rp = router_plan(sh);
   L.router_parts = take(rp.tensor_cores ? (size_t)3 * rp.ep * sh.d * 2 : 0);
-  L.router_partial = take(rp.tensor_cores ? (size_t)rp.splits * sh.T * rp.ep * 4 : 0);
   L.disp_counts = take(db * sh.E * 4);
   L.disp_base = take(db * sh.E * 4);
   const size_t rows = (size_t)(sh.rows > 0 ? sh.rows : 1);
@@ -167,8 +172,32 @@ moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, co
   MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance); MOE_PTR(load);
   MOE_PTR(ws);
   MOE_OPT_PTR(logit_bias); MOE_OPT_PTR(probs); MOE_OPT_PTR(aux_loss);
-  return cuda_status(launch_router(sh, x, w_r, logit_bias, probs, topk_idx, topk_gate, importance, load, aux_loss,
-                                   ws, (cudaStream_t)stream));
+  return cuda_status(launch_router(sh, x, w_r, logit_bias, nullptr, probs, topk_idx, topk_gate, importance, load,
+                                   aux_loss, ws, (cudaStream_t)stream));
+}
+
+moe_status moe_router_biased(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
+                             const float *select_bias, float *probs, int32_t *topk_idx, float *topk_gate,
+                             float *importance, int32_t *load, float *aux_loss, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_router_biased");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.dtype == MOE_BF16, MOE_ERR_UNSUPPORTED);
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(select_bias); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance);
+  MOE_PTR(load); MOE_PTR(ws);
+  MOE_OPT_PTR(logit_bias); MOE_OPT_PTR(probs); MOE_OPT_PTR(aux_loss);
+  return cuda_status(launch_router(sh, x, w_r, logit_bias, select_bias, probs, topk_idx, topk_gate, importance, load,
+                                   aux_loss, ws, (cudaStream_t)stream));
+}
+
+moe_status moe_select_bias_update(const moe_config *cfg, const int32_t *load, float *select_bias, float gamma,
+                                  moe_stream_t stream) {
+  MOE_NVTX("moe_select_bias_update");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_PTR(load); MOE_PTR(select_bias);
+  MOE_REQUIRE(std::isfinite(gamma), MOE_ERR_INVALID_ARG);
+  return cuda_status(launch_select_bias_update(sh, load, gamma, select_bias, (cudaStream_t)stream));
 }
 
 moe_status moe_dispatch(const moe_config *cfg, const void *x, const int32_t *topk_idx, int32_t *slot,
@@ -230,7 +259,8 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r, c
   if (sh.k > 1) MOE_PTR(y_perm);
   MOE_REQUIRE(out != x, MOE_ERR_INVALID_ARG);
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = launch_router(sh, x, w_r, logit_bias, probs, topk_idx, topk_gate, importance, load, aux_loss, ws, s);
+  cudaError_t e =
+      launch_router(sh, x, w_r, logit_bias, nullptr, probs, topk_idx, topk_gate, importance, load, aux_loss, ws, s);
   if (e != cudaSuccess) return cuda_status(e);
   e = launch_dispatch(sh, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, sh.k == 1 ? out : nullptr, ws,
                       s);

@@ -12,21 +12,22 @@
 // carry its 24-bit significand; x is already bf16, so every product
 // x_i * part_e,i is exact in the fp32 accumulator, and h = x W_hi^T +
 // x W_mid^T + x W_lo^T is the fp32 dot product up to the order of the fp32
-// additions. A tcgen05 kernel (128 tokens x all experts per CTA, K split
-// across CTAs when there are few token tiles) writes fp32 partial logits;
-// a selection kernel sums the partials in a fixed order and does softmax and
-// top-k. fp32 layers use a register-tiled CUDA-core kernel instead.
+// additions. One fused tcgen05 kernel per 128-token tile computes the logits
+// into TMEM and, in its epilogue, one thread per token does softmax, top-k
+// and the statistics straight from TMEM. When there are few token tiles, the
+// experts' columns are split over a cluster of up to four CTAs, which swap
+// only per-token records (local maximum, local sum of exponentials, top-k
+// candidates) through distributed shared memory. fp32 layers use a
+// register-tiled CUDA-core kernel, one warp per token for the selection.
 //
-// Selection: one warp per token, softmax in fp32 with the row maximum
-// subtracted, then k rounds of a warp arg-max (descending logit, ties to the
-// lower index: a max reduction over order keys of the logits, then a min
-// reduction over the expert indices holding the maximum). Importance and load are summed per block in a fixed order;
-// each block then adds its sums into per-expert accumulators in the
-// workspace: the loads as 32-bit integers, the importance as 64-bit fixed
-// point (units of 2^-32). Integer addition is associative, so the totals do
-// not depend on the order in which blocks arrive and the statistics are
-// bitwise reproducible. The last block to finish converts the totals, forms
-// the aux loss with a fixed-shape tree and clears the accumulators.
+// Ties in the top-k go to the lower expert index (descending logit order
+// keys, then ascending index). Importance and load are summed per CTA in a
+// fixed order, then added into per-expert accumulators in the workspace: the
+// loads as 32-bit integers, the importance as 64-bit fixed point (units of
+// 2^-32). Integer addition is associative, so the totals do not depend on
+// the order in which CTAs arrive and the statistics are bitwise
+// reproducible. The last CTA to finish converts the totals, forms the aux
+// loss with a fixed-shape tree and clears the accumulators.
 #include <cfloat>
 
 #include "common.cuh"
@@ -348,30 +349,107 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float *w_r, int
   }
 }
 
-namespace rt {
-constexpr int BM = 128;
-constexpr int BK = 64;
-template <int EP> struct Geo {
-  static constexpr int A_BYTES = BM * BK * 2;
-  static constexpr int B_BYTES = EP * BK * 2;  // one part
+namespace rf {
+constexpr int BM = 128;        // tokens per CTA (TMEM lanes)
+constexpr int BK = 64;         // K per stage (one 128-byte swizzled row of bf16)
+constexpr int THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 one token row per thread
+constexpr int KMAX = 8;        // top-k candidates kept per row
+constexpr int SMAX = 4;        // CTAs per cluster (expert-column split)
+constexpr int MAX_STAGES = 8;
+constexpr int SMEM_LIMIT = 232448;
+
+template <int NC> struct Geo {
+  static constexpr int A_BYTES = BM * BK * 2;      // x tile
+  static constexpr int B_BYTES = NC * BK * 2;      // one bf16 part of this CTA's W_r rows
   static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
-  static constexpr int STAGES = EP >= 256 ? 2 : (EP >= 128 ? 3 : 4);
-  static constexpr int TMEM_COLS = EP < 32 ? 32 : EP;
-  static constexpr size_t SMEM = 1024 + (size_t)STAGES * STAGE_BYTES + 256;
+  static constexpr int TMEM_COLS = NC;             // NC >= 32, a power of two
+};
+
+// One row as one CTA of a cluster sees it (its NC expert columns): the k
+// best (selection key, expert) pairs, packed so that a larger value is the
+// larger key, ties to the lower expert; the score of each; the local max m
+// and sum of exp(h - m) z (softmax scores).
+struct Cand {
+  unsigned long long c[KMAX];
+  float sc[KMAX];
+  float m, z;
 };
 struct __align__(8) Bars {
-  uint64_t full[4];
-  uint64_t empty[4];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t acc_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int last;          // this CTA finished last
 };
+
 struct Args {
-  int T, E, kb_per_split, KB;
-  float *partial;   // [splits, T, EP]
+  int T, E, EP, k, renorm, S, nk, stages, score;
+  const float *bias;              // [E] added to h (or null)
+  const float *sel_bias;          // [E] added to the scores for the choice only (or null)
+  float *probs;                   // [T, E] scores, or null
+  int32_t *idx;                   // [T, k]
+  float *gate;                    // [T, k]
+  unsigned long long *acc_imp;    // [E] importance in units of 2^-32
+  int32_t *acc_load;              // [E]
+  float alpha;
+  float *importance;
+  int32_t *load;
+  float *aux;
+  unsigned int *counter;
   DeviceStatus *st;
 };
+
+__host__ __device__ constexpr size_t recv_bytes(int S) { return S > 1 ? (size_t)S * BM * sizeof(Cand) : 0; }
+template <int NC> size_t smem_bytes(int S, int stages) {
+  return 1024 + (size_t)stages * Geo<NC>::STAGE_BYTES + recv_bytes(S) + sizeof(Bars);
+}
+
+__device__ __forceinline__ unsigned long long pack_cand(float key, int e) {
+  return ((unsigned long long)logit_key(key) << 32) | (unsigned)(0xFFFF - e);
+}
+__device__ __forceinline__ int cand_expert(unsigned long long c) { return 0xFFFF - (int)(c & 0xFFFFu); }
+// Inverse of logit_key (a -0.0 key comes back as +0.0).
+__device__ __forceinline__ float cand_key(unsigned long long c) {
+  const uint32_t key = (uint32_t)(c >> 32);
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+// p = exp(h - M) / Z: the one expression both the probabilities and the gates use.
+__device__ __forceinline__ float prob_of(float h, float M, float Z) { return expf(h - M) / Z; }
+// The elementwise scores: sigmoid, and sqrt(softplus) with
+// softplus(h) = max(h, 0) + log1p(exp(-|h|)) (no overflow for large h).
+__device__ __forceinline__ float elem_score(float h, int score) {
+  if (score == MOE_SCORE_SIGMOID) return 1.0f / (1.0f + expf(-h));
+  return sqrtf(fmaxf(h, 0.0f) + log1pf(expf(-fabsf(h))));
+}
+
+// Keeps (c, sc)[0..k) sorted by c, descending: (v, vs) goes in at its place
+// when v beats c[k - 1] (held by the caller in `last`, which this updates),
+// the rest shift down. Unrolled over KMAX with the runtime k as a predicate.
+__device__ __forceinline__ void insert_cand(unsigned long long (&c)[KMAX], float (&sc)[KMAX], unsigned long long &last,
+                                            unsigned long long v, float vs, int k) {
+  if (v <= last) return;
+#pragma unroll
+  for (int j = KMAX - 1; j > 0; --j) {
+    if (j < k && v > c[j - 1]) { c[j] = c[j - 1]; sc[j] = sc[j - 1]; }
+    else if (j < k && v > c[j]) { c[j] = v; sc[j] = vs; }
+  }
+  if (v > c[0]) { c[0] = v; sc[0] = vs; }
+  last = c[0];
+#pragma unroll
+  for (int j = 1; j < KMAX; ++j)
+    if (j == k - 1) last = c[j];
+}
+
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Named barrier of the four epilogue warps.
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -380,24 +458,97 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 200000000ull) break;
 }
 
-// Partial logits of 128 tokens x all experts over the CTA's K range. Warp 0
-// loads (x tile once, then the hi/mid/lo parts of W_r), warp 1 issues
-// 3 x 4 MMAs per 64-deep K step into one TMEM accumulator, warps 2-5 store it.
-template <int EP>
-__global__ void __launch_bounds__(192, 1)
-    router_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Args a) {
-  using G = Geo<EP>;
+// This row's record (candidates, their scores, m, z) into slot [rank][r] of
+// every CTA of the cluster.
+__device__ __forceinline__ void send_record(Cand *recv, int rank, int r, int S, const unsigned long long (&c)[KMAX],
+                                            const float (&sc)[KMAX], float m, float z) {
+  const uint32_t mine = smem_u32(&recv[rank * BM + r]);
+  for (int dst = 0; dst < S; ++dst) {
+    const uint32_t ra = mapa_shared(mine, (uint32_t)dst);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) st_cluster_u64(ra + 8u * j, c[j]);
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) st_cluster_f32(ra + 8u * KMAX + 4u * j, sc[j]);
+    st_cluster_f32(ra + 12u * KMAX, m);
+    st_cluster_f32(ra + 12u * KMAX + 4u, z);
+  }
+}
+// The k best of the S sorted lists of row r (distinct experts: no equal
+// values); heads holds each list's next position, 8 bits per list.
+__device__ __forceinline__ void merge_records(const Cand *recv, int r, int S, int k, unsigned long long (&c)[KMAX],
+                                              float (&sc)[KMAX]) {
+  uint32_t heads = 0;
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
+    unsigned long long best = 0ull;
+    float bs = 0.0f;
+    int from = 0;
+#pragma unroll
+    for (int s = 0; s < SMAX; ++s) {
+      const int hd = (int)((heads >> (8 * s)) & 0xFFu);
+      const bool ok = j < k && s < S && hd < k;
+      const unsigned long long v = ok ? recv[s * BM + r].c[hd] : 0ull;
+      if (v > best) { best = v; bs = recv[s * BM + r].sc[hd]; from = s; }
+    }
+    c[j] = best;
+    sc[j] = bs;
+    heads += 1u << (8 * from);
+  }
+}
+
+// Logits, scores, top-k and statistics of 128 tokens, with the experts'
+// columns split over the S CTAs of a cluster (NC = EP / S each).
+//   warp 0: TMA of the x tile and of the hi/mid/lo parts of this CTA's W_r
+//           rows, one 64-deep K step per stage;
+//   warp 1: 3 x 4 tcgen05 MMAs (M 128, N NC, K 16) per stage into one fp32
+//           TMEM accumulator;
+//   warps 2-5: one token row per thread, read from TMEM. Softmax scores:
+//           pass 1 the local maximum (and, without a correction bias, the
+//           top-k candidates by logit), pass 2 the sum of exp(h - m); the
+//           cluster's CTAs swap these per-row records over distributed shared
+//           memory, each forms M = max m and Z = sum z exp(m - M) in CTA order
+//           and merges the candidates. Elementwise scores: pass 1 the
+//           candidates by logit (by score + bias with a correction bias) with
+//           their scores. Pass 3 writes the scores of its columns (staged
+//           through shared memory so each store instruction covers one
+//           128-byte row piece), sums them per expert, and, for softmax scores
+//           with a correction bias, forms the candidates by p + b and swaps
+//           them in a second exchange. The row's experts and gates come from
+//           the merged candidates (CTA `rank` writes the rows r with
+//           r % S == rank).
+template <int NC>
+__global__ void __launch_bounds__(THREADS, 1)
+    router_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                        const Args a) {
+  using G = Geo<NC>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  Bars &b = *reinterpret_cast<Bars *>(tiles + (size_t)G::STAGES * G::STAGE_BYTES);
+  const int S = a.S;
+  Cand *recv = reinterpret_cast<Cand *>(tiles + (size_t)a.stages * G::STAGE_BYTES);   // [S][BM]
+  Bars &b = *reinterpret_cast<Bars *>(reinterpret_cast<uint8_t *>(recv) + recv_bytes(S));
   volatile int *abort_flag = &b.abort_flag;
+  // Used only after this CTA's MMAs have completed, in the then idle ring:
+  float *stage_out = reinterpret_cast<float *>(tiles);                       // [4 warps][32 rows][32]
+  float *imp_w = stage_out + 4 * 32 * 32;                                    // [4 row quarters][NC]
+  int *cnt = reinterpret_cast<int *>(imp_w + 4 * NC);                        // [EP]
+  float *term = reinterpret_cast<float *>(cnt + 256);                        // [256]
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = S > 1 ? (int)cluster_ctarank() : 0;
+  const int m0 = blockIdx.y * BM;
+  const int col0 = rank * NC;
+  const int E = a.E, k = a.k;
+  const bool softmax = a.score == MOE_SCORE_SOFTMAX;
+  // softmax scores with a correction bias choose on p + b, known only after
+  // the first exchange: a second one follows pass 3
+  const bool late_choice = softmax && a.sel_bias != nullptr;
+  const int cluster_syncs = S > 1 ? (late_choice ? 3 : 1) : 0;
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
     prefetch_tmap(&tmW);
-    for (int i = 0; i < G::STAGES; ++i) { mbar_init(&b.full[i], 1); mbar_init(&b.empty[i], 1); }
+    for (int i = 0; i < a.stages; ++i) { mbar_init(&b.full[i], 1); mbar_init(&b.empty[i], 1); }
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.drain, 1);
     b.abort_flag = 0;
@@ -410,10 +561,6 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = b.tmem_base;
-  const int m0 = blockIdx.x * BM;
-  const int kb0 = blockIdx.y * a.kb_per_split;
-  const int kb1 = min(a.KB, kb0 + a.kb_per_split);
-  const int nk = max(0, kb1 - kb0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -421,30 +568,31 @@ __global__ void __launch_bounds__(192, 1)
       const uint64_t pol_w = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_parity = 0;
-      for (int ks = 0; ks < nk; ++ks) {
+      for (int ks = 0; ks < a.nk; ++ks) {
         if (!mbar_wait_bounded(&b.empty[stage], phase ^ 1, abort_flag, a.st)) break;
         uint8_t *a_s = tiles + (size_t)stage * G::STAGE_BYTES;
         mbar_arrive_expect_tx(&b.full[stage], G::STAGE_BYTES);
-        const int k0 = (kb0 + ks) * BK;
+        const int k0 = ks * BK;
         tma_load_2d(a_s, &tmX, &b.full[stage], k0, m0, pol_x);
 #pragma unroll
         for (int part = 0; part < 3; ++part)
-          tma_load_2d(a_s + G::A_BYTES + part * G::B_BYTES, &tmW, &b.full[stage], k0, part * EP, pol_w);
+          tma_load_2d(a_s + G::A_BYTES + part * G::B_BYTES, &tmW, &b.full[stage], k0, part * a.EP + col0, pol_w);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == G::STAGES) { stage = 0; phase ^= 1; }
+        if (++stage == a.stages) { stage = 0; phase ^= 1; }
       }
       if (*abort_flag)
-        for (int i = 0; i < G::STAGES; ++i)
+        for (int i = 0; i < a.stages; ++i)
           if (issued & (1u << i)) drain_wait(&b.full[i], (issued_parity >> i) & 1);
     }
     __syncwarp();
+    for (int i = 0; i < cluster_syncs; ++i) cluster_sync_all();
   } else if (warp == 1) {
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, EP, 0, 0);
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, NC, 0, 0);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int ks = 0; ks < nk; ++ks) {
+    for (int ks = 0; ks < a.nk; ++ks) {
       if (!mbar_wait_bounded(&b.full[stage], phase, abort_flag, a.st)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
@@ -460,7 +608,7 @@ __global__ void __launch_bounds__(192, 1)
         tc_commit(&b.empty[stage]);
       }
       __syncwarp();
-      if (++stage == G::STAGES) { stage = 0; phase ^= 1; }
+      if (++stage == a.stages) { stage = 0; phase ^= 1; }
     }
     if (ok && lane == 0) tc_commit(&b.acc_full);
     __syncwarp();
@@ -469,29 +617,190 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       drain_wait(&b.drain, 0);
     }
+    for (int i = 0; i < cluster_syncs; ++i) cluster_sync_all();
   } else {
-    // Each warp owns 32 rows. TMEM gives a thread one row; a 32 x 33 shared
-    // transpose (in the now idle stage buffers) turns that into 128-byte
-    // coalesced row stores. Partial rows have stride EP (padding columns are 0).
     const int q = warp & 3;
-    if (nk > 0 && mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st)) {
-      tc_fence_after();
-      float *tr = reinterpret_cast<float *>(tiles) + q * (32 * 33);
-      float v[32];
-      const int row0 = m0 + q * 32;
-      float *dst = a.partial + ((int64_t)blockIdx.y * a.T + row0) * EP;
-#pragma unroll 1
-      for (int c = 0; c < EP / 32; ++c) {
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c * 32, v);
+    const int r = q * 32 + lane;
+    const int t = m0 + r;
+    const bool live = t < a.T;
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    float m = -FLT_MAX, z = 0.0f;
+    unsigned long long cand[KMAX];
+    float csc[KMAX];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) tr[lane * 33 + i] = v[i];
-        __syncwarp();
-#pragma unroll 8
-        for (int r = 0; r < 32; ++r)
-          if (row0 + r < a.T) dst[(int64_t)r * EP + c * 32 + lane] = tr[r * 33 + lane];
-        __syncwarp();
+    for (int j = 0; j < KMAX; ++j) { cand[j] = 0ull; csc[j] = 0.0f; }
+    unsigned long long last = 0ull;   // cand[k - 1]
+    // warp-uniform: the TMEM loads below are warp-collective
+    const bool acc_ok =
+        __all_sync(0xffffffffu, mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st) ? 1 : 0) != 0;
+    float v[32];
+    if (acc_ok) {
+      tc_fence_after();
+      // pass 1: maximum (softmax) and the candidates that need no global statistics
+#pragma unroll 1
+      for (int c = 0; c < NC / 32; ++c) {
+        tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = col0 + c * 32 + i;
+          if (e < E) {
+            const float h = v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f);
+            if (softmax) {
+              m = fmaxf(m, h);
+              if (!late_choice) insert_cand(cand, csc, last, pack_cand(h, e), 0.0f, k);
+            } else {
+              const float sv = elem_score(h, a.score);
+              const float key = a.sel_bias ? sv + __ldg(a.sel_bias + e) : h;
+              insert_cand(cand, csc, last, pack_cand(key, e), sv, k);
+            }
+          }
+        }
       }
-      tc_fence_before();
+      // pass 2 (softmax): sum of exp(h - m)
+      if (softmax) {
+#pragma unroll 1
+        for (int c = 0; c < NC / 32; ++c) {
+          tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int e = col0 + c * 32 + i;
+            if (e < E) z += expf(v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f) - m);
+          }
+        }
+      }
+    }
+    float M = m, Z = z;
+    if (S > 1) {
+      send_record(recv, rank, r, S, cand, csc, m, z);
+      cluster_sync_all();   // every CTA's records are in
+      if (softmax) {
+        M = -FLT_MAX;
+        for (int s = 0; s < S; ++s) M = fmaxf(M, recv[s * BM + r].m);
+        Z = 0.0f;
+        for (int s = 0; s < S; ++s) Z += recv[s * BM + r].z * expf(recv[s * BM + r].m - M);
+      }
+      if (!late_choice) merge_records(recv, r, S, k, cand, csc);
+    }
+    for (int e = threadIdx.x - 64; e < a.EP; e += 128) cnt[e] = 0;
+    epilogue_sync();
+    // pass 3: the scores of this CTA's columns; per 32 x 32 block, each lane
+    // writes its row into the warp's 128-byte swizzled staging rows, then
+    // lane j takes column j row by row: one coalesced 128-byte store per row
+    // and the column's sum over the block's live rows.
+    float *stg = stage_out + (warp - 2) * 32 * 32;
+#pragma unroll 1
+    for (int c = 0; c < NC / 32; ++c) {
+      if (acc_ok) tmem_ld32(t_row + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = col0 + c * 32 + i;
+        float sv = 0.0f;
+        if (acc_ok && live && e < E) {
+          const float h = v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f);
+          sv = softmax ? prob_of(h, M, Z) : elem_score(h, a.score);
+          if (late_choice) insert_cand(cand, csc, last, pack_cand(sv + __ldg(a.sel_bias + e), e), sv, k);
+        }
+        v[i] = sv;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4 *>(stg + lane * 32 + ((j ^ (lane & 7)) << 2)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      __syncwarp();
+      const int e = col0 + c * 32 + lane;
+      float colsum = 0.0f;
+#pragma unroll 4
+      for (int rr = 0; rr < 32; ++rr) {
+        const float pv = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+        const int tt = m0 + q * 32 + rr;
+        if (tt < a.T) {
+          colsum += pv;
+          if (a.probs && e < E) a.probs[(int64_t)tt * E + e] = pv;
+        }
+      }
+      imp_w[q * NC + c * 32 + lane] = colsum;
+      __syncwarp();
+    }
+    if (late_choice && S > 1) {
+      cluster_sync_all();   // every CTA has read the first records
+      send_record(recv, rank, r, S, cand, csc, M, Z);
+      cluster_sync_all();   // the second records are in
+      merge_records(recv, r, S, k, cand, csc);
+    }
+    // the row's experts and gates
+    if (acc_ok && live && (r % S) == rank) {
+      float gv[KMAX];
+      float psum = 0.0f;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        gv[j] = 0.0f;
+        if (j < k) {
+          // softmax scores chosen by logit: p from the logit the key carries
+          gv[j] = (softmax && !late_choice) ? prob_of(cand_key(cand[j]), M, Z) : csc[j];
+          psum += gv[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const int e = cand_expert(cand[j]);
+          a.idx[(int64_t)t * k + j] = e;
+          a.gate[(int64_t)t * k + j] = a.renorm ? gv[j] / psum : gv[j];
+          atomicAdd(&cnt[e], 1);
+        }
+      }
+    }
+    epilogue_sync();
+    // this CTA's per-expert sums: importance over its 128 rows (row quarters
+    // in a fixed order) and loads, added as integers into the accumulators
+    for (int c = threadIdx.x - 64; c < NC; c += 128) {
+      const int e = col0 + c;
+      if (e < E) {
+        const float sm = imp_w[c] + imp_w[NC + c] + imp_w[2 * NC + c] + imp_w[3 * NC + c];
+        // sm <= 128 rows x a score <= 1 (softmax, sigmoid) or <= 2^64 (sqrt softplus of an
+        // fp32 logit): llrint of sm * 2^32 is exact to 2^-33 while sm < 2^31
+        const unsigned long long qv = (unsigned long long)llrint((double)sm * 4294967296.0);
+        if (qv) atomicAdd(a.acc_imp + e, qv);
+      }
+    }
+    for (int e = threadIdx.x - 64; e < E; e += 128)
+      if (cnt[e]) atomicAdd(a.acc_load + e, cnt[e]);
+    tc_fence_before();   // this warp's TMEM loads are ordered before the release below
+  }
+
+  // The last CTA to finish converts the accumulated importance and load,
+  // sums the aux terms as a fixed-shape tree over 256 slots, and clears the
+  // accumulators and the counter for the next call.
+  {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) b.last = atomicAdd(a.counter, 1u) == gridDim.x * gridDim.y - 1;
+    __syncthreads();
+    if (b.last) {
+      __threadfence();
+      for (int e = threadIdx.x; e < 256; e += THREADS) {
+        float v = 0.0f;
+        if (e < E) {
+          const unsigned long long qv = __ldcg(a.acc_imp + e);
+          const int c = __ldcg(a.acc_load + e);
+          const float sm = (float)((double)qv * (1.0 / 4294967296.0));
+          a.acc_imp[e] = 0ull;
+          a.acc_load[e] = 0;
+          a.importance[e] = sm;
+          a.load[e] = c;
+          v = ((float)c / ((float)a.T * (float)k)) * (sm / (float)a.T);
+        }
+        term[e] = v;
+      }
+      __syncthreads();
+      for (int w = 128; w > 0; w >>= 1) {
+        for (int e = threadIdx.x; e < w; e += THREADS) term[e] += term[e + w];
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) {
+        if (a.aux) *a.aux = a.alpha * (float)E * term[0];
+        *a.counter = 0u;
+      }
     }
   }
   __syncthreads();
@@ -500,54 +809,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_dealloc(tmem, G::TMEM_COLS);
   }
 }
-}  // namespace rt
-
-// Logits = sum of the split partials in split order (+ bias), then selection
-// of 32 tokens per block. Partial rows have stride EP; every thread loads its
-// float4 chunks of all splits before adding, so the loads overlap.
-constexpr int RT_TC = 32;  // tokens per selection block (measured: 32 beats 64 and 128; 16 is faster
-                           // for 16384 tokens but slower for the 8192-token switch-base layer)
-template <int EPT>
-__global__ void __launch_bounds__(256) router_select_kernel(const float *partial, int splits, const RouterArgs a,
-                                                            const StatsOut so) {
-  constexpr int EP = 32 * EPT;
-  constexpr int Q = EP / 4;              // float4 per row
-  constexpr int CH = RT_TC * Q / 256;    // float4 chunks per thread
-  extern __shared__ float sm[];
-  float *lg = sm;                      // [RT_TC][EP + 1]
-  float *impw = lg + RT_TC * (EP + 1); // [8][EP]
-  int *cnt = reinterpret_cast<int *>(impw + 8 * EP);
-  const int t0 = blockIdx.x * RT_TC;
-  const int E = a.E;
-  float4 acc[CH];
-#pragma unroll
-  for (int c = 0; c < CH; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < splits; ++s) {
-    float4 v[CH];
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      const int i = threadIdx.x + 256 * c, tl = i / Q, e4 = i - tl * Q, t = t0 + tl;
-      v[c] = (t < a.T) ? __ldcs(reinterpret_cast<const float4 *>(partial + ((int64_t)s * a.T + t) * EP) + e4)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      acc[c].x += v[c].x; acc[c].y += v[c].y; acc[c].z += v[c].z; acc[c].w += v[c].w;
-    }
-  }
-#pragma unroll
-  for (int c = 0; c < CH; ++c) {
-    const int i = threadIdx.x + 256 * c, tl = i / Q, e = (i - tl * Q) * 4;
-    const float vv[4] = {acc[c].x, acc[c].y, acc[c].z, acc[c].w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      lg[tl * (EP + 1) + e + u] = vv[u] + ((a.bias != nullptr && e + u < E) ? a.bias[e + u] : 0.0f);
-  }
-  for (int e = threadIdx.x; e < EP; e += 256) cnt[e] = 0;
-  __syncthreads();
-  select_block<EPT, RT_TC / 8>(lg, impw, cnt, a, t0);
-  finish_if_last(a, so.alpha, so.importance, so.load, so.aux, so.counter);
-}
+}  // namespace rf
 
 template <typename K>
 cudaError_t set_smem(K kern, size_t bytes) {
@@ -562,64 +824,89 @@ cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStre
   return launch_kernel(router_simt_kernel<XT, EPT>, dim3(nblk), dim3(256), smem, stream, a, so);
 }
 
-template <int EPT>
-cudaError_t run_select(const float *partial, int splits, const RouterArgs &a, const StatsOut &so, int nblk,
-                       cudaStream_t stream) {
-  constexpr size_t smem = select_smem_bytes<EPT, RT_TC>();
-  static cudaError_t attr = set_smem(router_select_kernel<EPT>, smem);
+template <int NC>
+cudaError_t run_fused(const CUtensorMap &mx, const CUtensorMap &mw, const rf::Args &ra, int m_tiles,
+                      cudaStream_t stream) {
+  static cudaError_t attr = set_smem(rf::router_fused_kernel<NC>, rf::SMEM_LIMIT);
   if (attr != cudaSuccess) return attr;
-  return launch_kernel(router_select_kernel<EPT>, dim3(nblk), dim3(256), smem, stream, partial, splits, a, so);
-}
-
-template <int EP>
-cudaError_t run_tc(const CUtensorMap &mx, const CUtensorMap &mw, const rt::Args &ta, int m_tiles, int splits,
-                   cudaStream_t stream) {
-  static cudaError_t attr = set_smem(rt::router_tc_kernel<EP>, rt::Geo<EP>::SMEM);
-  if (attr != cudaSuccess) return attr;
-  return launch_kernel(rt::router_tc_kernel<EP>, dim3(m_tiles, splits), dim3(192), rt::Geo<EP>::SMEM, stream, mx, mw,
-                    ta);
+  const size_t smem = rf::smem_bytes<NC>(ra.S, ra.stages);
+  if (ra.S > 1)
+    return launch_kernel_cluster(rf::router_fused_kernel<NC>, ra.S, dim3(ra.S, m_tiles), dim3(rf::THREADS), smem,
+                                 stream, mx, mw, ra);
+  return launch_kernel(rf::router_fused_kernel<NC>, dim3(1, m_tiles), dim3(rf::THREADS), smem, stream, mx, mw, ra);
 }
 
 int epad_of(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
 
+template <int NC> int fused_stages(int S) {
+  const size_t fixed = 1024 + rf::recv_bytes(S) + sizeof(rf::Bars);
+  int st = (int)((rf::SMEM_LIMIT - fixed) / rf::Geo<NC>::STAGE_BYTES);
+  return st > rf::MAX_STAGES ? rf::MAX_STAGES : st;
+}
+
 }  // namespace
 
-int router_blocks(const Shape &sh) {
-  const int per = sh.dtype == MOE_BF16 ? RT_TC : RT;
-  return (sh.T + per - 1) / per;
-}
+int router_blocks(const Shape &sh) { return (sh.T + RT - 1) / RT; }
 
 RouterPlan router_plan(const Shape &sh) {
   RouterPlan p;
   p.tensor_cores = sh.dtype == MOE_BF16;
   p.ep = epad_of(sh.E);
-  p.m_tiles = (sh.T + rt::BM - 1) / rt::BM;
-  const int KB = (sh.d + rt::BK - 1) / rt::BK;
-  int splits = kRouterTargetCtas / p.m_tiles;
-  if (splits < 1) splits = 1;
-  if (splits > KB) splits = KB;
-  p.kb_per_split = (KB + splits - 1) / splits;
-  p.splits = (KB + p.kb_per_split - 1) / p.kb_per_split;
+  p.m_tiles = (sh.T + rf::BM - 1) / rf::BM;
+  // expert columns split over a cluster of S CTAs while the grid stays
+  // within one wave and every CTA keeps at least 32 columns
+  int S = 1;
+  while (2 * S <= rf::SMAX && p.m_tiles * 2 * S <= sm_count() && p.ep / (2 * S) >= 32) S *= 2;
+  p.cluster = S;
+  p.nc = p.ep / S;
   return p;
 }
 
-cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, float *probs,
-                          int32_t *idx, float *gate, float *importance, int32_t *load, float *aux, void *ws,
-                          cudaStream_t stream) {
+// b_e += gamma * sign(mean(load) - load_e), decided in integers:
+// sign(sum(load) - E load_e) (the mean is sum / E). One block.
+__global__ void __launch_bounds__(256) select_bias_update_kernel(const int32_t *load, int E, float gamma,
+                                                                 float *sel_bias) {
+  __shared__ long long part[256];
+  long long sum = 0;
+  for (int e = threadIdx.x; e < E; e += 256) sum += load[e];
+  part[threadIdx.x] = sum;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+    __syncthreads();
+  }
+  const long long total = part[0];
+  for (int e = threadIdx.x; e < E; e += 256) {
+    const long long diff = total - (long long)E * load[e];
+    const float step = diff > 0 ? gamma : (diff < 0 ? -gamma : 0.0f);
+    sel_bias[e] = sel_bias[e] + step;
+  }
+}
+
+cudaError_t launch_select_bias_update(const Shape &sh, const int32_t *load, float gamma, float *sel_bias,
+                                      cudaStream_t stream) {
+  return launch_kernel(select_bias_update_kernel, dim3(1), dim3(256), 0, stream, load, sh.E, gamma, sel_bias);
+}
+
+cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, const float *bias, const float *sel_bias,
+                          float *probs, int32_t *idx, float *gate, float *importance, int32_t *load, float *aux,
+                          void *ws, cudaStream_t stream) {
   const WsLayout L = ws_layout(sh);
   uint8_t *w = static_cast<uint8_t *>(ws);
-  RouterArgs a;
-  a.x = x; a.w_r = w_r; a.bias = bias; a.probs = probs; a.idx = idx; a.gate = gate;
-  a.acc_imp = reinterpret_cast<unsigned long long *>(w + L.router_acc);
-  a.acc_load = reinterpret_cast<int32_t *>(w + L.router_acc + 8 * (size_t)sh.E);
-  a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
-  const int nblk = router_blocks(sh);
+  unsigned long long *acc_imp = reinterpret_cast<unsigned long long *>(w + L.router_acc);
+  int32_t *acc_load = reinterpret_cast<int32_t *>(w + L.router_acc + 8 * (size_t)sh.E);
+  unsigned int *counter = reinterpret_cast<unsigned int *>(w + L.status + 64);
   const RouterPlan plan = router_plan(sh);
-  StatsOut so;
-  so.alpha = sh.alpha; so.importance = importance; so.load = load; so.aux = aux;
-  so.counter = reinterpret_cast<unsigned int *>(w + L.status + 64);
   cudaError_t e;
   if (!plan.tensor_cores) {
+    RouterArgs a;
+    a.x = x; a.w_r = w_r; a.bias = bias; a.probs = probs; a.idx = idx; a.gate = gate;
+    a.acc_imp = acc_imp;
+    a.acc_load = acc_load;
+    a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
+    StatsOut so;
+    so.alpha = sh.alpha; so.importance = importance; so.load = load; so.aux = aux; so.counter = counter;
+    const int nblk = router_blocks(sh);
     if (sh.E <= 32) e = run_simt<float, 1>(a, so, nblk, stream);
     else if (sh.E <= 64) e = run_simt<float, 2>(a, so, nblk, stream);
     else if (sh.E <= 128) e = run_simt<float, 4>(a, so, nblk, stream);
@@ -627,30 +914,28 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
     return e;
   }
   bf16 *parts = reinterpret_cast<bf16 *>(w + L.router_parts);
-  float *partial = reinterpret_cast<float *>(w + L.router_partial);
   const int64_t n = (int64_t)plan.ep * sh.d;
   int sgrid = (int)((n + 255) / 256);
   if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
   e = launch_kernel(router_split_kernel, dim3(sgrid), dim3(256), 0, stream, w_r, sh.E, plan.ep, sh.d, parts);
   if (e != cudaSuccess) return e;
   CUtensorMap mx, mw;
-  if (!make_map_2d(&mx, x, sh.d, sh.T, 64, 128) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
+  if (!make_map_2d(&mx, x, sh.d, sh.T, 64, rf::BM) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.nc))
     return cudaErrorInvalidValue;
-  rt::Args ta;
-  ta.T = sh.T; ta.E = sh.E; ta.kb_per_split = plan.kb_per_split; ta.KB = (sh.d + rt::BK - 1) / rt::BK;
-  ta.partial = partial;
-  ta.st = reinterpret_cast<DeviceStatus *>(w + L.status);
-  switch (plan.ep) {
-    case 32: e = run_tc<32>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-    case 64: e = run_tc<64>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-    case 128: e = run_tc<128>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
-    default: e = run_tc<256>(mx, mw, ta, plan.m_tiles, plan.splits, stream); break;
+  rf::Args ra;
+  ra.T = sh.T; ra.E = sh.E; ra.EP = plan.ep; ra.k = sh.k; ra.renorm = sh.renorm; ra.S = plan.cluster;
+  ra.nk = (sh.d + rf::BK - 1) / rf::BK;
+  ra.score = sh.score;
+  ra.bias = bias; ra.sel_bias = sel_bias; ra.probs = probs; ra.idx = idx; ra.gate = gate;
+  ra.acc_imp = acc_imp; ra.acc_load = acc_load;
+  ra.alpha = sh.alpha; ra.importance = importance; ra.load = load; ra.aux = aux; ra.counter = counter;
+  ra.st = reinterpret_cast<DeviceStatus *>(w + L.status);
+  switch (plan.nc) {
+    case 32: ra.stages = fused_stages<32>(ra.S); return run_fused<32>(mx, mw, ra, plan.m_tiles, stream);
+    case 64: ra.stages = fused_stages<64>(ra.S); return run_fused<64>(mx, mw, ra, plan.m_tiles, stream);
+    case 128: ra.stages = fused_stages<128>(ra.S); return run_fused<128>(mx, mw, ra, plan.m_tiles, stream);
+    default: ra.stages = fused_stages<256>(ra.S); return run_fused<256>(mx, mw, ra, plan.m_tiles, stream);
   }
-  if (e != cudaSuccess) return e;
-  if (sh.E <= 32) return run_select<1>(partial, plan.splits, a, so, nblk, stream);
-  if (sh.E <= 64) return run_select<2>(partial, plan.splits, a, so, nblk, stream);
-  if (sh.E <= 128) return run_select<4>(partial, plan.splits, a, so, nblk, stream);
-  return run_select<8>(partial, plan.splits, a, so, nblk, stream);
 }
 
 }  // namespace moe

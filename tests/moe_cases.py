@@ -40,7 +40,8 @@ def abi_capacity(moe, w) -> int:
 
 def config_for(moe, w):
     return moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=w.k, d_ff=w.F, act=w.act, dtype=w.dtype,
-                           renormalize=w.renormalize, capacity=abi_capacity(moe, w), aux_alpha=w.alpha)
+                           renormalize=w.renormalize, capacity=abi_capacity(moe, w), aux_alpha=w.alpha,
+                           add_residual=w.add_residual, score=w.score)
 
 
 def to_dev(torch, a, dtype):
@@ -54,7 +55,7 @@ def np64(t):
         else t.cpu().numpy().astype(np.int64)
 
 
-def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False):
+def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False, select_bias=None):
     import torch
     import sparse_mixture_experts_49_b300 as moe
     cfg = config_for(moe, w)
@@ -66,10 +67,11 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False):
     w1 = to_dev(torch, inp["w1"], dt)
     w2 = to_dev(torch, inp["w2"], dt)
     idx_t = None if topk_idx is None else torch.from_numpy(np.asarray(topk_idx, np.int32)).cuda()
+    sel = None if select_bias is None else to_dev(torch, select_bias, torch.float32)
     if fused:
         layer.infer(x, w_r, w1, w2, bias)
     else:
-        layer.forward(x, w_r, w1, w2, bias, idx_t)
+        layer.forward(x, w_r, w1, w2, bias, idx_t, select_bias=sel)
     res = {}
     if backward:
         dy = to_dev(torch, inp["dy"], dt)
@@ -91,7 +93,7 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False):
 
 def oracle_kw(w):
     return dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments, renormalize=w.renormalize,
-                alpha=w.alpha)
+                alpha=w.alpha, add_residual=w.add_residual, score=w.score)
 
 
 def assert_close(got, ref, tol, what):

@@ -62,7 +62,7 @@ def test_rows_and_workspace_size():
     (dict(top_k=17), moe.MOE_ERR_INVALID_ARG),          # k > E
     (dict(n_experts=300, top_k=2), moe.MOE_ERR_UNSUPPORTED),
     (dict(top_k=9, n_experts=16), moe.MOE_ERR_UNSUPPORTED),
-    (dict(d_model=200), moe.MOE_ERR_ALIGNMENT),          # bf16 needs multiples of 64
+    (dict(d_model=204), moe.MOE_ERR_ALIGNMENT),          # bf16 needs multiples of 8 (16-byte rows)
     (dict(d_ff=100), moe.MOE_ERR_ALIGNMENT),
     (dict(dtype="f32", d_model=66), moe.MOE_ERR_ALIGNMENT),
     (dict(T=0), moe.MOE_ERR_INVALID_ARG),
@@ -73,11 +73,26 @@ def test_config_validation(kw, status):
     assert e.value.status == status
 
 
+def test_bf16_sizes_multiple_of_8_are_accepted():
+    for d, F in [(136, 200), (8, 8), (4104, 1000)]:
+        assert moe.moe_workspace_size(cfg(d_model=d, d_ff=F)) > 0
+        assert moe.moe_workspace_size(cfg(d_model=d, d_ff=F, act="swiglu")) > 0
+
+
 def test_config_bad_fields():
     c = cfg()
     c.act = 7
     with pytest.raises(moe.MoEError):
         moe.moe_workspace_size(c)
+    for field, bad in (("add_residual", 2), ("score", 3), ("renormalize", -1)):
+        c = cfg()
+        setattr(c, field, bad)
+        with pytest.raises(moe.MoEError) as e:
+            moe.moe_workspace_size(c)
+        assert e.value.status == moe.MOE_ERR_INVALID_ARG
+    with pytest.raises(moe.MoEError) as e:                     # router variants: bf16 layers only
+        moe.moe_workspace_size(cfg(dtype="f32", score="sigmoid"))
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
     c = cfg()
     c.reserved = 1
     with pytest.raises(moe.MoEError):

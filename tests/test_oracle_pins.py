@@ -254,7 +254,7 @@ def _relu_pattern(pp, base, w):
     return out
 
 
-def _fd_check(w, n_coords=60, eps=1e-4, seed=0):
+def _fd_check(w, n_coords=60, eps=1e-4, seed=0, add_residual=True, score="softmax", sel_bias=None):
     """Central differences of L = <dY, out> + aux against the oracle's backward.
 
     eps = 1e-4: at 1e-6 the fp64 rounding of L divided by 2 eps already
@@ -263,7 +263,8 @@ def _fd_check(w, n_coords=60, eps=1e-4, seed=0):
     """
     inp = syn.make_inputs(w, dy=True)
     kw = dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments,
-              renormalize=w.renormalize, alpha=w.alpha)
+              renormalize=w.renormalize, alpha=w.alpha, add_residual=add_residual, score=score,
+              sel_bias=sel_bias)
     x = inp["x"].astype(np.float64)
     w_r = inp["w_r"].astype(np.float64)
     w1 = inp["w1"].astype(np.float64)
@@ -397,3 +398,76 @@ def test_sampled_forward_matches_full_forward(wl):
         np.testing.assert_array_equal(part[key], full[key])
     np.testing.assert_allclose(part["gate"], full["gate"], rtol=0, atol=0)
     assert part["aux"] == full["aux"]
+
+
+# ------------------------------------------------------------------ without the residual
+def test_without_residual_single_expert_is_plain_ffn():
+    """E = 1, k = 1, add_residual off: p = 1, so the layer is FFN(x) alone (textbook loops)."""
+    rng = np.random.default_rng(16)
+    T, d, F = 6, 5, 4
+    x = rng.standard_normal((T, d))
+    w1 = rng.standard_normal((1, 2 * F, d))
+    w2 = rng.standard_normal((1, d, F))
+    f = O.forward(x, rng.standard_normal((1, d)), None, (w1, w2), k=1, act="swiglu", cf=None, add_residual=False)
+    np.testing.assert_allclose(f["out"], _ffn_loops(x, w1[0], w2[0], "swiglu"), rtol=1e-12, atol=1e-13)
+
+
+def test_without_residual_dense_masked_and_dropped_tokens_are_zero():
+    """No residual: out = sum over kept top-k of g_i E_i(x) from every expert evaluated densely (brute-force
+    top-k mask, token-order capacity from the brute-force slots); fully dropped tokens give zeros."""
+    w = syn.Workload("pin-nores", T=30, d=8, E=5, k=2, F=6, act="relu", dtype="f32", cf=(1, 2), router_std=0.5)
+    inp = syn.make_inputs(w)
+    f = O.forward(inp["x"], inp["w_r"], None, (inp["w1"], inp["w2"]), k=2, act="relu", cf=(1, 2),
+                  add_residual=False)
+    x = inp["x"].astype(np.float64)
+    h = x @ inp["w_r"].astype(np.float64).T
+    p = scipy.special.softmax(h, axis=1)
+    top = _brute_topk(h, 2)
+    slot = _brute_slots(top, w.E, O.capacity(w.T, w.E, 2, (1, 2)))
+    ref = np.zeros_like(x)
+    for t in range(w.T):
+        for j in range(2):
+            if slot[t, j] >= 0:
+                e = top[t, j]
+                y = _ffn_loops(x[t:t + 1], inp["w1"][e].astype(np.float64), inp["w2"][e].astype(np.float64), "relu")
+                ref[t] += p[t, e] * y[0]
+    assert (slot < 0).all(axis=1).any()
+    np.testing.assert_allclose(f["out"], ref, rtol=1e-11, atol=1e-12)
+    assert np.all(f["out"][(slot < 0).all(axis=1)] == 0.0)
+
+
+def test_gradients_finite_differences_without_residual():
+    w = syn.Workload("fd-nores", T=40, d=10, E=5, k=2, F=8, act="swiglu", dtype="f32", cf=(3, 4),
+                     renormalize=True, router_std=0.4, backward=True)
+    checked, skipped = _fd_check(w, n_coords=30, add_residual=False)
+    assert checked >= 100 and skipped <= checked // 10
+
+
+# ------------------------------------------------------------------ router variants in the layer
+@pytest.mark.parametrize("score,biased", [("sigmoid", False), ("sigmoid", True), ("sqrt_softplus", False),
+                                          ("sqrt_softplus", True), ("softmax", True)])
+def test_gradients_finite_differences_router_variants(score, biased):
+    """The layer's gradients with an elementwise score (its own derivative in place of the softmax Jacobian)
+    and with a selection-only correction bias (constant choice, gates without the bias) against central
+    differences of L = <dY, out> + aux."""
+    w = syn.Workload(f"fd-{score}-{biased}", T=40, d=10, E=6, k=2, F=8, act="swiglu", dtype="f32", cf=(3, 4),
+                     renormalize=biased, router_std=0.4, backward=True)
+    b = np.random.default_rng(3).standard_normal(w.E) * 0.05 if biased else None
+    checked, skipped = _fd_check(w, n_coords=25, score=score, sel_bias=b)
+    assert checked >= 80 and skipped <= checked // 10
+
+
+def test_route_with_variants_follows_the_variant_oracle():
+    """moe_oracle.route with a score function and a correction bias chooses, gates and counts as
+    router_variants.route_variant does on the same logits; the statistics sum the scores."""
+    rng = np.random.default_rng(9)
+    x, w_r = rng.standard_normal((50, 12)), rng.standard_normal((7, 12)) / 3.0
+    b = rng.standard_normal(7) * 0.2
+    from oracle import router_variants as RV
+    for score in RV.SCORES:
+        for sel in (None, b):
+            r = O.route(x, w_r, None, 3, True, 0.01, score, sel)
+            v = RV.route_variant(O.router_logits(x, w_r), 3, score, sel_bias=sel, renormalize=True)
+            assert np.array_equal(r["idx"], v["idx"]) and np.array_equal(r["load"], v["load"])
+            np.testing.assert_allclose(r["gate"], v["gate"], rtol=1e-15)
+            np.testing.assert_allclose(r["importance"], v["s"].sum(axis=0), rtol=1e-13)

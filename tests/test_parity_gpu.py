@@ -27,8 +27,8 @@ def _gpu():
     moe.lib()   # fails loudly if the library is not built
 
 
-def _ref_all(w, inp, backward):
-    kw = oracle_kw(w)
+def _ref_all(w, inp, backward, sel_bias=None):
+    kw = dict(oracle_kw(w), sel_bias=sel_bias)
     experts = (inp["w1"], inp["w2"])
     f = O.forward(inp["x"], inp["w_r"], inp["bias"], experts, **kw)
     b = O.backward(inp["x"], inp["w_r"], inp["bias"], experts, inp["dy"], **kw) if backward else None
@@ -46,7 +46,8 @@ def _check_full(w, res, inp, f, b):
     assert_close(res["y_perm"], y_ref, tol, "y_perm")
     assert_close(res["out"], f["out"], tol, "out")
     dropped = np.all(f["slot"] < 0, axis=1)
-    assert np.array_equal(res["out"][dropped], inp["x"].astype(np.float64)[dropped]), "dropped tokens must return x"
+    passthrough = inp["x"].astype(np.float64)[dropped] if w.add_residual else np.zeros((int(dropped.sum()), w.d))
+    assert np.array_equal(res["out"][dropped], passthrough), "dropped tokens must return x (zeros without residual)"
     if b is not None:
         assert_close(res["dg"], b["dg"], tol, "dg")
         assert_close(res["dh"], b["dh"], tol, "dh")
@@ -93,6 +94,26 @@ def test_router_expert_counts_and_many_tiles(E, k):
     res = run_gpu(w, inp)
     f, _ = _ref_all(w, inp, False)
     _check_full(w, res, inp, f, None)
+
+
+@pytest.mark.parametrize("T,E,k,renorm", [(200, 256, 8, False), (130, 130, 3, True), (96, 64, 2, False),
+                                          (1000, 128, 1, False), (4000, 48, 4, True)])
+def test_router_cluster_splits(T, E, k, renorm):
+    """The fused tensor-core router with its expert columns split over 4, 2 or 1 CTAs of a cluster (few or
+    many 128-token tiles; a partial last tile; 130 experts, where the last CTA's columns hold no expert):
+    routing bit-exact, values against the oracle, and every gate equal to the probability the same kernel
+    wrote for its expert, bit for bit (the gates are not renormalised)."""
+    w = syn.Workload(f"router-split-{T}-{E}-{k}", T=T, d=256, E=E, k=k, F=128, act="relu", dtype="bf16",
+                     cf=(5, 4), renormalize=renorm, router_std=1 / 16)
+    inp = syn.make_inputs(w, dy=False)
+    res = run_gpu(w, inp)
+    f, _ = _ref_all(w, inp, False)
+    check_routing(res, f, w)
+    check_router_values(res, f, w.dtype)
+    assert res["device_error"] == 0
+    if not renorm:
+        assert np.array_equal(res["gate"], np.take_along_axis(res["probs"], res["idx"], axis=1))
+    assert np.all(np.abs(res["probs"].sum(axis=1) - 1.0) <= 1e-5)
 
 
 @pytest.mark.parametrize("name", ["switch-small", "gshard-small", "dropless-small", "top1-many-tiles"])
@@ -351,3 +372,97 @@ def test_full_size_large_training_sampled():
         assert_close(np64(dw1[e]), ref["dw1"][e], TOL_BF16, f"dw1[{e}]")
         assert_close(np64(dw2[e]), ref["dw2"][e], TOL_BF16, f"dw2[{e}]")
     assert_close(np64(dw_r), dh.T @ inp["x"].astype(np.float64), TOL_ROUTER_BF16, "dw_r vs dh^T x (fp64)")
+
+
+# ------------------------------------------------------------------ the layer without its residual
+@pytest.mark.parametrize("name", ["switch-small", "gshard-small", "dropless-small"])
+def test_without_residual(name):
+    """add_residual = 0: out = MoE(x) (zeros for fully dropped tokens), dX without the dY term, on the
+    separate calls and on moe_forward (top-1: the dispatch writes the zeros, the second GEMM's epilogue the
+    gated sums)."""
+    w = SMALL[name].with_(add_residual=False, backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+    fused = run_gpu(w, inp, fused=True)
+    assert_close(fused["out"], f["out"], TOL_BF16, "out (moe_forward)")
+    dropped = np.all(f["slot"] < 0, axis=1)
+    assert np.all(fused["out"][dropped] == 0.0)
+
+
+# ------------------------------------------------------------------ router variants
+def _variant_inputs(w, sel_bias):
+    """Inputs whose variant selection keys (score + correction bias, fp64) keep every consecutive gap among
+    the k + 1 largest at least the generator's margin, so that the choice and its order are unique: the
+    first T of 3T margin-conditioned tokens that pass."""
+    from oracle import router_variants as RV
+    big = syn.make_inputs(w.with_(T=3 * w.T), dy=True)
+    if sel_bias is None:
+        keep = np.arange(w.T)
+    else:
+        h = O.router_logits(big["x"], big["w_r"], big["bias"])
+        key = (O.softmax(h) if w.score == "softmax" else RV.scores(h, w.score)) + sel_bias[None, :]
+        top = -np.sort(-key, axis=1)[:, : w.k + 1]
+        keep = np.nonzero((top[:, :-1] - top[:, 1:]).min(axis=1) >= syn.MARGIN)[0][: w.T]
+        assert len(keep) == w.T
+    big["x"], big["dy"] = big["x"][keep], big["dy"][keep]
+    return big
+
+
+@pytest.mark.parametrize("score,biased", [("sigmoid", False), ("sigmoid", True), ("sqrt_softplus", False),
+                                          ("sqrt_softplus", True), ("softmax", True)])
+def test_router_variants(score, biased):
+    """Sigmoid and sqrt(softplus) scores and the selection-only correction bias ([Wiki] "Mixture-of-Experts",
+    section 横断的知見) through the whole layer, forward and backward, against the oracle: routing bit-exact,
+    the scores within the router's tolerance, every gate the score of its expert, layer outputs and gradients
+    within the bf16 tolerance. Cluster-split router (E 64 over 2 CTAs) and a single-CTA one (E 32)."""
+    for E in (64, 32):
+        w = syn.Workload(f"variant-{score}-{biased}-{E}", T=1500, d=256, E=E, k=4, F=192, act="swiglu",
+                         dtype="bf16", cf=(5, 4), renormalize=biased, router_std=1 / 16, score=score, backward=True)
+        sel = (np.random.default_rng(E).standard_normal(E) * 0.02).astype(np.float32) if biased else None
+        inp = _variant_inputs(w, sel)
+        res = run_gpu(w, inp, backward=True, select_bias=sel)
+        f, b = _ref_all(w, inp, True, sel_bias=sel)
+        _check_full(w, res, inp, f, b)
+        if not w.renormalize:
+            assert np.array_equal(res["gate"], np.take_along_axis(res["probs"], res["idx"], axis=1))
+
+
+def test_select_bias_update_sign_rule():
+    """b_e += gamma sign(mean(load) - load_e) on the GPU, bit for bit against the oracle's update rounded to
+    fp32 (a correctly rounded fp32 sum), including experts exactly at the mean."""
+    import sparse_mixture_experts_49_b300 as moe
+    from oracle import router_variants as RV
+    rng = np.random.default_rng(21)
+    for E, T, k in [(64, 1000, 4), (256, 4096, 8), (7, 10, 3)]:
+        cfg = moe.make_config(T=T, d_model=64, n_experts=E, top_k=k, d_ff=64)
+        load = rng.multinomial(T * k, np.ones(E) / E).astype(np.int32)
+        if E == 7:
+            load = np.array([4, 5, 3, 6, 4, 4, 4], np.int32)      # mean 30 / 7: no expert at the mean
+        if E == 64:                                              # 8 experts exactly at the mean 62: no change
+            load = np.concatenate([np.full(8, 62), rng.multinomial(56 * 62, np.ones(56) / 56)]).astype(np.int32)
+            assert load.sum() == 64 * 62
+        b = (rng.standard_normal(E) * 0.01).astype(np.float32)
+        bd = torch.from_numpy(b).cuda()
+        moe.moe_select_bias_update(cfg, torch.from_numpy(load).cuda(), bd, 0.001)
+        torch.cuda.synchronize()
+        ref = RV.update_bias(b.astype(np.float64), load, np.float64(np.float32(0.001))).astype(np.float32)
+        assert np.array_equal(bd.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ sizes that are not tile multiples
+@pytest.mark.parametrize("act,k", [("relu", 1), ("swiglu", 2), ("relu", 3)])
+def test_dims_multiple_of_8(act, k):
+    """d_model 136 and d_ff 200 (multiples of 8, not of the 64-wide K step or the 128/256-wide N tiles):
+    K tails come from the tensor maps' zero fill, N tails are clipped by the tile stores and masked in 8-column
+    vectors elsewhere (the SwiGLU halves have a map each). Forward + backward on the separate calls, and
+    moe_forward (top-1: the combine epilogue)."""
+    w = syn.Workload(f"dims8-{act}-{k}", T=700, d=136, E=12, k=k, F=200, act=act, dtype="bf16", cf=(5, 4),
+                     router_std=1 / np.sqrt(136), backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, res, inp, f, b)
+    fused = run_gpu(w, inp, fused=True)
+    assert_close(fused["out"], f["out"], TOL_BF16, "out (moe_forward)")
