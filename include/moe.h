@@ -34,7 +34,9 @@
  *     section 学習を安定させる3つの工夫: the router stays in float32).
  *   - Sizes: T tokens, d = d_model, E experts, k = top_k, F = d_ff,
  *     R1 = F (ReLU) or 2F (SwiGLU: gate rows then up rows),
- *     rows = moe_max_rows(cfg) = min(T*k, E*C) (T*k without a capacity).
+ *     rows = moe_max_rows(cfg) = min(T*k, E*C) (T*k without a capacity;
+ *     min(T, E*C) with cfg->reroute). "k columns" below are 2 with
+ *     cfg->reroute (see moe_config), else k.
  *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 1; d and F are
  *     multiples of 8 for MOE_BF16 and of 4 for MOE_F32, so that every row is
  *     a whole number of 16-byte vectors (MOE_ERR_ALIGNMENT otherwise).
@@ -95,7 +97,13 @@ typedef struct moe_config {
   int32_t score;       /* MOE_SCORE_*: the router's score function (softmax by default) */
   int64_t capacity;    /* expert capacity C per expert; < 0: no limit (dropless) */
   float aux_alpha;     /* alpha of eq. (4) */
-  int32_t reserved;    /* must be 0 */
+  int32_t reroute;     /* 1: No-Token-Left-Behind ([Switch] section 論文の限界と、まだ分かって
+                          いないこと: overflow goes to the token's second candidate). Top-1 layers
+                          with E >= 2 and no renormalisation only. topk_idx, topk_gate and slot
+                          then have 2 columns: the first choice, and the second-best expert that a
+                          token dropped by its first choice's capacity is offered to in a second
+                          round (token order, into the room each expert has left; slot -1 where
+                          not kept). Load and f count first choices. 0: plain top-k. */
 } moe_config;
 
 /* Expert capacity, [Switch] eq. (3): floor(n * cf_num / (E * cf_den)) with
@@ -245,10 +253,12 @@ moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int3
  *   y_perm  [rows, d]      x dtype out
  * Rows past expert_offsets[E] are not written.
  *
- * bf16 layers run on tcgen05 tiles of 128 rows, one CTA each. With the
- * environment variable MOE_GEMM_PAIR=1 (read at every call) the expert GEMMs
- * of this call and of moe_forward / moe_backward run on CTA-pair tiles
- * instead (two CTAs of a cluster share an MMA of 256 rows); results agree to
+ * bf16 layers run on tcgen05 tiles of 128 rows, one CTA each, in a fixed
+ * order (CTA u takes tiles u, u + grid, ...). Two environment variables,
+ * read at every call, change that for this call and for moe_forward /
+ * moe_backward: MOE_GEMM_PAIR=1 runs CTA-pair tiles (two CTAs of a cluster
+ * share an MMA of 256 rows); MOE_GEMM_SCHED=dynamic hands the one-CTA tiles
+ * out from a counter in the workspace as CTAs free up. Results agree to
  * fp32 accumulation order.
  */
 moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm,

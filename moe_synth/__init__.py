@@ -60,6 +60,7 @@ class Workload:
     alpha: float = 0.01         # load-balancing loss coefficient
     add_residual: bool = True   # out = x + MoE(x) (True) or MoE(x)
     score: str = "softmax"      # router score function: softmax | sigmoid | sqrt_softplus
+    reroute: bool = False       # No-Token-Left-Behind: a top-1 token dropped by capacity tries its 2nd choice
     backward: bool = False      # the workload includes the backward pass
     seed: int = 49
 
@@ -163,9 +164,11 @@ def _token_margin(x: np.ndarray, w_r: np.ndarray, b: Optional[np.ndarray], k: in
 
 def tokens(w: Workload, w_r: np.ndarray, b: Optional[np.ndarray],
            margin: float = MARGIN, max_attempts: int = 1000) -> np.ndarray:
-    """x [T, d] with every token margin-conditioned against (w_r, b)."""
+    """x [T, d] with every token margin-conditioned against (w_r, b) (over the k + 1 largest logits; k = 2
+    when the second choice matters too, with rerouting)."""
+    kk = 2 if w.reroute else w.k
     x = _cast(w, _normal(rng_for(w, "x"), (w.T, w.d), 1.0))
-    bad = np.nonzero(_token_margin(x, w_r, b, w.k) < margin)[0]
+    bad = np.nonzero(_token_margin(x, w_r, b, kk) < margin)[0]
     attempt = 0
     while bad.size:
         attempt += 1
@@ -173,7 +176,7 @@ def tokens(w: Workload, w_r: np.ndarray, b: Optional[np.ndarray],
             raise RuntimeError(f"{w.name}: margin conditioning did not converge")
         for t in bad:
             x[t] = _cast(w, _normal(rng_for(w, "x-redraw", int(t), attempt), (w.d,), 1.0))
-        still = _token_margin(x[bad], w_r, b, w.k) < margin
+        still = _token_margin(x[bad], w_r, b, kk) < margin
         bad = bad[still]
     return x
 

@@ -112,7 +112,7 @@ def top_k(h: np.ndarray, k: int) -> np.ndarray:
 
 
 def route(x, w_r, bias, k: int, renormalize: bool, alpha: float, score: str = "softmax",
-          sel_bias=None) -> dict:
+          sel_bias=None, reroute: bool = False) -> dict:
     """Router, gates and balance statistics for one batch of T tokens.
 
     [Switch] eqs. (1), (2), (4) and the numpy sketch of section 負荷分散損失:
@@ -124,15 +124,23 @@ def route(x, w_r, bias, k: int, renormalize: bool, alpha: float, score: str = "s
     with a correction bias the experts are chosen on p + b while the gates
     stay p. Without a bias the choice is the top-k of h, which is the order
     of p for the softmax and for every strictly increasing score.
+
+    With `reroute` (No-Token-Left-Behind, top-1 layers only) the two best
+    experts of each token are kept, idx [T, 2] and gates [T, 2] (the second
+    the token's candidate when its first choice overflows); the load and f
+    still count the first choices, the layer's routing decision.
     """
     h = router_logits(x, w_r, bias)
     T, E = h.shape
     p = softmax(h) if score == "softmax" else RV.scores(h, score)
-    idx = top_k(h, k) if sel_bias is None else RV.select(p, k, sel_bias)
+    if reroute and (k != 1 or renormalize or E < 2):
+        raise ValueError("No-Token-Left-Behind rerouting is defined for top-1 layers of two or more experts")
+    kk = 2 if reroute else k
+    idx = top_k(h, kk) if sel_bias is None else RV.select(p, kk, sel_bias)
     gate = np.take_along_axis(p, idx, axis=1)
     if renormalize:
         gate = gate / gate.sum(axis=1, keepdims=True)
-    load = np.bincount(idx.ravel(), minlength=E).astype(np.int64)
+    load = np.bincount((idx[:, 0] if reroute else idx).ravel(), minlength=E).astype(np.int64)
     importance = p.sum(axis=0)
     f = load / float(T * k)
     P = importance / float(T)
@@ -183,6 +191,54 @@ def assign_slots(idx: np.ndarray, E: int, C: Optional[int]) -> dict:
     return dict(slot=slot, kept=kept, offsets=offsets, row_token=row_token)
 
 
+def assign_slots_reroute(idx2: np.ndarray, E: int, C: Optional[int]) -> dict:
+    """No-Token-Left-Behind ([Switch] section 論文の限界と、まだ分かっていないこと:
+    overflow goes to the token's second candidate), read for top-1 layers.
+
+    Round 1 is the dropped-token rule on the first choices: each expert takes
+    its tokens in ascending token order and keeps the first C. Round 2: every
+    token dropped in round 1 offers its second-choice expert, in ascending
+    token order, the room that expert has left; slots continue after the
+    round-1 ones. slot[t, 0] is the round-1 slot, slot[t, 1] the round-2 one
+    (-1 where the assignment is not kept); a token keeps at most one.
+    """
+    T = idx2.shape[0]
+    slot = np.full((T, 2), -1, dtype=np.int64)
+    count = np.zeros(E, dtype=np.int64)
+    for t in range(T):
+        e = int(idx2[t, 0])
+        if C is None or count[e] < C:
+            slot[t, 0] = count[e]
+        count[e] += 1
+    fill = count.copy() if C is None else np.minimum(count, C)
+    for t in range(T):
+        if slot[t, 0] >= 0:
+            continue
+        e = int(idx2[t, 1])
+        if C is None or fill[e] < C:
+            slot[t, 1] = fill[e]
+            fill[e] += 1
+    kept = fill
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    offsets[1:] = np.cumsum(kept)
+    row_token = np.full(int(offsets[-1]), -1, dtype=np.int64)
+    for t in range(T):
+        for j in range(2):
+            if slot[t, j] >= 0:
+                row_token[offsets[idx2[t, j]] + slot[t, j]] = t
+    return dict(slot=slot, kept=kept, offsets=offsets, row_token=row_token)
+
+
+def _routing(x64, w_r, bias, k, renormalize, alpha, score, sel_bias, reroute, cf, count_assignments):
+    """Route, capacity and slots of one batch, as forward and backward share them."""
+    r = route(x64, w_r, bias, k, renormalize, alpha, score, sel_bias, reroute)
+    T = x64.shape[0]
+    E = r["p"].shape[1]
+    C = capacity(T, E, k, cf, count_assignments)
+    s = assign_slots_reroute(r["idx"], E, C) if reroute else assign_slots(r["idx"], E, C)
+    return r, C, s
+
+
 # ------------------------------------------------------------------ experts
 def silu(u):
     return u / (1.0 + np.exp(-u))
@@ -207,7 +263,7 @@ def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
             cf: Optional[Tuple[int, int]], count_assignments: bool = True,
             renormalize: bool = False, alpha: float = 0.01,
             tokens: Optional[Sequence[int]] = None, add_residual: bool = True, score: str = "softmax",
-            sel_bias=None) -> dict:
+            sel_bias=None, reroute: bool = False) -> dict:
     """out = x + sum_{i in T, kept} g_i E_i(x) ([Switch] eq. (2) with the
     residual passthrough of dropped tokens); without the residual
     (add_residual=False) out is the gated sum alone, and a token whose
@@ -220,9 +276,7 @@ def forward(x, w_r, bias, experts: ExpertSource, *, k: int, act: str,
     x64 = _f64(x)
     T, d = x64.shape
     E = np.asarray(w_r).shape[0]
-    r = route(x64, w_r, bias, k, renormalize, alpha, score, sel_bias)
-    C = capacity(T, E, k, cf, count_assignments)
-    s = assign_slots(r["idx"], E, C)
+    r, C, s = _routing(x64, w_r, bias, k, renormalize, alpha, score, sel_bias, reroute, cf, count_assignments)
     sel = np.arange(T) if tokens is None else np.asarray(tokens, dtype=np.int64)
     out = x64[sel].copy() if add_residual else np.zeros((len(sel), d))
     where = {int(t): i for i, t in enumerate(sel)}
@@ -246,7 +300,7 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
              cf: Optional[Tuple[int, int]], count_assignments: bool = True,
              renormalize: bool = False, alpha: float = 0.01,
              experts_needed: Optional[Sequence[int]] = None, add_residual: bool = True,
-             score: str = "softmax", sel_bias=None) -> dict:
+             score: str = "softmax", sel_bias=None, reroute: bool = False) -> dict:
     """Gradients of L = <dY, out> + aux (chain rule through eqs. (1), (2), (4)).
 
     Top-k sets, capacity masks and f are constants ([Switch] section
@@ -258,11 +312,9 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
     T, d = x64.shape
     wr64 = _f64(w_r)
     E = wr64.shape[0]
-    r = route(x64, wr64, bias, k, renormalize, alpha, score, sel_bias)
-    C = capacity(T, E, k, cf, count_assignments)
-    s = assign_slots(r["idx"], E, C)
+    r, C, s = _routing(x64, wr64, bias, k, renormalize, alpha, score, sel_bias, reroute, cf, count_assignments)
     dx = dy64.copy() if add_residual else np.zeros_like(dy64)   # residual path
-    dg = np.zeros((T, k))
+    dg = np.zeros(r["idx"].shape)         # [T, k] ([T, 2] with rerouting)
     dw1, dw2 = {}, {}
     need = set(range(E)) if experts_needed is None else set(int(e) for e in experts_needed)
     for e in range(E):
@@ -316,7 +368,8 @@ def backward(x, w_r, bias, experts: ExpertSource, dy, *, k: int, act: str,
 def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequence[int],
                      experts_sampled: Sequence[int], k: int, act: str, cf: Optional[Tuple[int, int]],
                      count_assignments: bool = True, renormalize: bool = False, alpha: float = 0.01,
-                     add_residual: bool = True, score: str = "softmax", sel_bias=None) -> dict:
+                     add_residual: bool = True, score: str = "softmax", sel_bias=None,
+                     reroute: bool = False) -> dict:
     """The gradients of `backward` for a few tokens (dx, dg and dh rows) and a
     few experts (dw1, dw2), without evaluating every expert on every token:
     the same chain rule through eqs. (1), (2) and (4). Each expert the
@@ -331,9 +384,7 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
     T, d = x64.shape
     wr64 = _f64(w_r)
     E = wr64.shape[0]
-    r = route(x64, wr64, bias, k, renormalize, alpha, score, sel_bias)
-    C = capacity(T, E, k, cf, count_assignments)
-    s = assign_slots(r["idx"], E, C)
+    r, C, s = _routing(x64, wr64, bias, k, renormalize, alpha, score, sel_bias, reroute, cf, count_assignments)
     p, idx, gate, slot = r["p"], r["idx"], r["gate"], s["slot"]
     toks = [int(t) for t in tokens]
     sampled = set(int(e) for e in experts_sampled)
@@ -350,10 +401,11 @@ def backward_sampled(x, w_r, bias, experts: ExpertSource, dy, *, tokens: Sequenc
         return fw, dyp, da
 
     acc = {t: dy64[t].copy() if add_residual else np.zeros(d) for t in toks}   # residual path
-    dg = {t: np.zeros(k) for t in toks}
+    kc = idx.shape[1]                                 # k columns (2 with rerouting)
+    dg = {t: np.zeros(kc) for t in toks}
     pairs = {}                                        # expert -> the sampled tokens' kept pairs (t, j)
     for t in toks:
-        for j in range(k):
+        for j in range(kc):
             if slot[t, j] >= 0:
                 pairs.setdefault(int(idx[t, j]), []).append((t, j))
     dw1, dw2 = {}, {}

@@ -47,7 +47,7 @@ class moe_config(ctypes.Structure):
         ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("add_residual", ctypes.c_int32),
         ("score", ctypes.c_int32), ("capacity", ctypes.c_int64), ("aux_alpha", ctypes.c_float),
-        ("reserved", ctypes.c_int32),
+        ("reroute", ctypes.c_int32),
     ]
 
 
@@ -129,13 +129,14 @@ def _stream(stream) -> Optional[int]:
 
 def make_config(T: int, d_model: int, n_experts: int, top_k: int, d_ff: int, act: str = "relu",
                 dtype: str = "bf16", renormalize: bool = False, capacity: int = -1,
-                aux_alpha: float = 0.01, add_residual: bool = True, score: str = "softmax") -> moe_config:
+                aux_alpha: float = 0.01, add_residual: bool = True, score: str = "softmax",
+                reroute: bool = False) -> moe_config:
     return moe_config(T=T, d_model=d_model, n_experts=n_experts, top_k=top_k, d_ff=d_ff,
                       act=MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_RELU,
                       dtype=MOE_BF16 if dtype == "bf16" else MOE_F32, renormalize=int(renormalize),
                       add_residual=int(add_residual), score=SCORES[score],
                       capacity=-1 if capacity is None else int(capacity), aux_alpha=float(aux_alpha),
-                      reserved=0)
+                      reroute=int(reroute))
 
 
 # ---------------------------------------------------------------- entry points (same names as the C ABI)
@@ -285,6 +286,8 @@ class MoELayer:
         self.stream = stream
         self.dt = torch.bfloat16 if cfg.dtype == MOE_BF16 else torch.float32
         T, d, E, k, F = cfg.T, cfg.d_model, cfg.n_experts, cfg.top_k, cfg.d_ff
+        if cfg.reroute:
+            k = 2   # columns: first choice, second candidate
         R1 = 2 * F if cfg.act == MOE_ACT_SWIGLU else F
         self.rows = moe_max_rows(cfg)
         dev = torch.device(device)
@@ -332,7 +335,7 @@ class MoELayer:
         c = self.cfg
         moe_forward(c, x, w_r, logit_bias, w1, w2, self.probs, self.topk_idx, self.topk_gate, self.importance,
                     self.load, self.aux, self.slot, self.kept, self.offsets, self.row_token, self.x_perm, self.h,
-                    self.y_perm if c.top_k > 1 else None, self.out, self.ws, self.stream)
+                    self.y_perm if (c.top_k > 1 or c.reroute) else None, self.out, self.ws, self.stream)
         return self.out
 
     def backward(self, dy, dx=None, dw_r=None, dw1=None, dw2=None):

@@ -49,8 +49,8 @@ __constant__ int kPartB[6] = {0, 1, 0, 2, 1, 0};
 template <int EPT>
 __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, const int32_t *idx, const float *gate,
                                                         const int32_t *load, const float *dg, int T, int E, int k,
-                                                        int renorm, float alpha, int score, float *dh, bf16 *a6,
-                                                        int EP, int32_t *offs2, int G) {
+                                                        int renorm, float alpha, int score, int k_route, float *dh,
+                                                        bf16 *a6, int EP, int32_t *offs2, int G) {
   if (a6 && blockIdx.x == 0) {
     if (threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
     if (threadIdx.x <= G) {
@@ -59,7 +59,8 @@ __global__ void __launch_bounds__(256) router_dh_kernel(const float *probs, cons
     }
   }
   const int lane = threadIdx.x & 31;
-  const float aux_scale = alpha * (float)E / ((float)T * (float)T * (float)k);  // alpha E f_e / T = this * load_e
+  // alpha E f_e / T = this * load_e (f counts the k_route routing columns: 1 with rerouting)
+  const float aux_scale = alpha * (float)E / ((float)T * (float)T * (float)k_route);
   float base[EPT];
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
@@ -187,7 +188,7 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   cudaError_t err;
 #define MOE_DH(EPT)                                                                                            \
   err = launch_kernel(router_dh_kernel<EPT>, dim3(grid), dim3(256), 0, stream, probs, idx, gate, load, dg, sh.T, sh.E, \
-                   sh.k, sh.renorm, sh.alpha, sh.score, dh, a6, EP, offs2, G)
+                   sh.k, sh.renorm, sh.alpha, sh.score, sh.k_route, dh, a6, EP, offs2, G)
   if (sh.E <= 32) MOE_DH(1);
   else if (sh.E <= 64) MOE_DH(2);
   else if (sh.E <= 128) MOE_DH(4);

@@ -54,22 +54,34 @@ __global__ void __launch_bounds__(256) combine_kernel(const XT *__restrict__ x, 
     token_rows<KMAX>(t, k, idx, slot, offsets, gate, row, g);
     const XT *xr = x + (int64_t)t * d;
     XT *orow = out + (int64_t)t * d;
-    for (int v = lane; v < nvec; v += 32) {
-      uint4 raw[KMAX + 1];
-      raw[0] = residual ? *reinterpret_cast<const uint4 *>(xr + v * V) : make_uint4(0u, 0u, 0u, 0u);
+    // NB vectors per lane per pass, all their loads issued before any is used
+    constexpr int NB = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+    for (int v0 = lane; v0 < nvec; v0 += 32 * NB) {
+      uint4 raw[NB][KMAX + 1];
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j)
-        if (row[j] >= 0) raw[j + 1] = *reinterpret_cast<const uint4 *>(y_perm + (int64_t)row[j] * d + v * V);
-      float acc[V], y[V];
-      Vec16<XT>::unpack(raw[0], acc);
+      for (int q = 0; q < NB; ++q) {
+        const int v = v0 + 32 * q;
+        if (v >= nvec) break;
+        raw[q][0] = residual ? *reinterpret_cast<const uint4 *>(xr + v * V) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (row[j] < 0) continue;
-        Vec16<XT>::unpack(raw[j + 1], y);
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], y[i], acc[i]);
+        for (int j = 0; j < KMAX; ++j)
+          if (row[j] >= 0) raw[q][j + 1] = *reinterpret_cast<const uint4 *>(y_perm + (int64_t)row[j] * d + v * V);
       }
-      Vec16<XT>::store(orow + v * V, acc);
+#pragma unroll
+      for (int q = 0; q < NB; ++q) {
+        const int v = v0 + 32 * q;
+        if (v >= nvec) break;
+        float acc[V], y[V];
+        Vec16<XT>::unpack(raw[q][0], acc);
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          if (row[j] < 0) continue;
+          Vec16<XT>::unpack(raw[q][j + 1], y);
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i] = fmaf(g[j], y[i], acc[i]);
+        }
+        Vec16<XT>::store(orow + v * V, acc);
+      }
     }
   }
 }

@@ -117,7 +117,7 @@ static moe_status dispatch_noalloc_impl(const moe_config *cfg, const void *x, co
     if (p == nullptr) return MOE_ERR_INVALID_ARG;
     if (!aligned16(p)) return MOE_ERR_ALIGNMENT;
   }
-  if (sh.T > MOE_NOALLOC_MAX_TOKENS || sh.E > kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (sh.T > MOE_NOALLOC_MAX_TOKENS || sh.E > kMaxExperts || sh.reroute) return MOE_ERR_UNSUPPORTED;
   int32_t *base = nullptr;
   cudaError_t e = scratch_on_current_device(&base);
   if (e != cudaSuccess) return report_cuda(e);

@@ -925,12 +925,17 @@ static int grid_size() {
 // mc is the output's tile map for the plain-store epilogues (ignored otherwise).
 // pair: CTA-pair tiles when a cluster of two fits, one CTA per tile otherwise.
 // md: the second output map (SwiGLU forward: the pre-activations).
-// Tile order of one-CTA-per-tile launches: dynamic (a counter in the
-// workspace hands out tiles as CTAs free up) unless MOE_GEMM_SCHED=static
-// (read at every call) selects the fixed stride.
+// Tile order of one-CTA-per-tile launches: the fixed stride (CTA u takes
+// tiles u, u + grid, ...), or, with MOE_GEMM_SCHED=dynamic in the
+// environment (read at every call), tiles handed out by a counter in the
+// workspace as CTAs free up. Measured on the B300 (bench.py, static and
+// dynamic back to back): no faster on any workload (the skewed GShard-style
+// layer's GEMMs are held back by their last partial wave of tiles, not by
+// uneven tile costs), and the short weight-gradient tiles of the large layer
+// slower by the queue handshake, so the fixed stride is the default.
 static unsigned int *tile_counters(DeviceStatus *st) {
   const char *v = getenv("MOE_GEMM_SCHED");
-  if (v && v[0] == 's') return nullptr;
+  if (!(v && v[0] == 'd')) return nullptr;
   return reinterpret_cast<unsigned int *>(reinterpret_cast<uint8_t *>(st) + kGemmSchedOffset);
 }
 

@@ -15,6 +15,8 @@ struct Shape {
   int T, d, E, k, F, R1, act, dtype, renorm;
   int residual;   // add_residual
   int score;      // MOE_SCORE_*
+  int reroute;    // No-Token-Left-Behind: k = 2 columns (first choice, second candidate)
+  int k_route;    // top_k of the config: the columns load and f count (1 with reroute)
   int64_t C;      // capacity, < 0 = none
   float alpha;
   int64_t rows;   // rows of the packed buffers
@@ -26,9 +28,9 @@ enum { EPI_STORE = 0, EPI_RELU = 1, EPI_SWIGLU = 2, EPI_RELU_BWD = 3, EPI_SWIGLU
 
 // Workspace carve-up (byte offsets from the workspace base). The first 256
 // bytes hold the error word (offset 0), the router's completion counter (64),
-// the dispatch's completion counter (128) and the grouped GEMM's tile
-// counters (192: next tile, 196: CTAs done); the router's statistics
-// accumulators follow. All of [0, zeroed) starts at zero (moe_workspace_init)
+// the dispatch's completion counters (128; 160 for rerouting's second round)
+// and the grouped GEMM's tile counters (192: next tile, 196: CTAs done); the
+// router's statistics accumulators follow. All of [0, zeroed) starts at zero (moe_workspace_init)
 // and every call leaves it at zero again.
 constexpr size_t kGemmSchedOffset = 192;
 struct WsLayout {
@@ -37,6 +39,7 @@ struct WsLayout {
   size_t zeroed;                   // end of the region that must start at zero
   size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
+  size_t disp_counts2, disp_base2, disp_kept1;  // rerouting's second round: [blocks, E], [blocks, E], [E]
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
   size_t dg, dh, dxr;              // backward: [T, k], [T, E], [T, d] fp32
   size_t rg_a6, rg_b6, rg_c3, rg_offs;  // bf16 router gradient: [T, 6EP], [6EP, d] bf16; [G, 3EP, d] fp32;
@@ -68,15 +71,22 @@ cudaError_t launch_select_bias_update(const Shape &sh, const int32_t *load, floa
                                       cudaStream_t stream);
 
 // x_perm may be null (rows are not copied); out_dropped, when given, gets
-// x[t] for every token with no kept assignment.
+// x[t] for every token with no kept assignment. With sh.reroute the second
+// round runs too (scratch in the workspace's rerouting regions).
 cudaError_t launch_dispatch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot, int32_t *kept,
                             int32_t *offsets, int32_t *row_token, void *x_perm, void *out_dropped, void *ws,
                             cudaStream_t stream);
 
+// Scratch of rerouting's second round: per-block counts and bases [blocks, E],
+// the first round's kept counts [E], a zero-initialised completion counter.
+struct RerouteScratch {
+  int32_t *counts2, *base2, *kept1;
+  unsigned int *counter2;
+};
 cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const int32_t *idx, int32_t *slot,
                                          int32_t *kept, int32_t *offsets, int32_t *row_token, void *x_perm,
                                          void *out_dropped, int32_t *counts, int32_t *base, unsigned int *counter,
-                                         DeviceStatus *st, cudaStream_t stream);
+                                         DeviceStatus *st, cudaStream_t stream, const RerouteScratch *rr = nullptr);
 moe_status dispatch_shape(const moe_config *cfg, Shape *sh);
 moe_status report_cuda(cudaError_t e);
 

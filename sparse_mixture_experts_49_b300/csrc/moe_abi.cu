@@ -35,7 +35,8 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID && c->score != MOE_SCORE_SQRT_SOFTPLUS)
     return MOE_ERR_INVALID_ARG;
   if (c->score != MOE_SCORE_SOFTMAX && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
-  if (c->reserved != 0 || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if ((c->reroute != 0 && c->reroute != 1) || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if (c->reroute && (c->top_k != 1 || c->n_experts < 2 || c->renormalize)) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
   if (c->n_experts > 256 || c->top_k > 8) return MOE_ERR_UNSUPPORTED;
   const int mult = c->dtype == MOE_BF16 ? 8 : 4;   // 16-byte rows for TMA and the vector accesses
@@ -53,9 +54,12 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   sh->renorm = c->renormalize;
   sh->residual = c->add_residual;
   sh->score = c->score;
+  sh->reroute = c->reroute;
+  sh->k_route = c->top_k;
+  if (c->reroute) sh->k = 2;   // columns: first choice, second candidate
   sh->C = c->capacity < 0 ? -1 : c->capacity;
   sh->alpha = c->aux_alpha;
-  int64_t rows = Tk;
+  int64_t rows = c->reroute ? (int64_t)c->T : Tk;   // rerouting keeps at most one assignment per token
   if (sh->C >= 0 && sh->C * sh->E < rows) rows = sh->C * sh->E;
   sh->rows = rows;
   sh->elt = c->dtype == MOE_BF16 ? 2 : 4;
@@ -78,6 +82,9 @@ WsLayout ws_layout(const Shape &sh) {
   L.router_parts = take(rp.tensor_cores ? (size_t)3 * rp.ep * sh.d * 2 : 0);
   L.disp_counts = take(db * sh.E * 4);
   L.disp_base = take(db * sh.E * 4);
+  L.disp_counts2 = take(sh.reroute ? db * sh.E * 4 : 0);
+  L.disp_base2 = take(sh.reroute ? db * sh.E * 4 : 0);
+  L.disp_kept1 = take(sh.reroute ? (size_t)sh.E * 4 : 0);
   const size_t rows = (size_t)(sh.rows > 0 ? sh.rows : 1);
   L.dyp = take(rows * sh.d * sh.elt);
   L.da = take(rows * sh.R1 * sh.elt);

@@ -51,6 +51,7 @@ struct RouterArgs {
   unsigned long long *acc_imp;  // [E] importance in units of 2^-32
   int32_t *acc_load;             // [E]
   int T, d, E, k, renorm;
+  int k_route;                   // columns the load and f count (k; 1 with rerouting)
 };
 
 template <typename XT> __device__ __forceinline__ void load4(const XT *p, float *o);
@@ -198,7 +199,7 @@ __device__ __forceinline__ void select_block(const float *lg, float *impw, int *
       if (live[g] && lane < a.k) {
         a.idx[(int64_t)tt[g] * a.k + lane] = my_e[g];
         a.gate[(int64_t)tt[g] * a.k + lane] = a.renorm ? my_p[g] / psum[g] : my_p[g];
-        atomicAdd(&cnt[my_e[g]], 1);
+        if (lane < a.k_route) atomicAdd(&cnt[my_e[g]], 1);
       }
     }
   }
@@ -240,7 +241,7 @@ __device__ __forceinline__ void finish_if_last(const RouterArgs &a, float alpha,
     a.acc_load[e] = 0;
     importance[e] = s;
     load[e] = c;
-    v = ((float)c / ((float)a.T * (float)a.k)) * (s / (float)a.T);
+    v = ((float)c / ((float)a.T * (float)a.k_route)) * (s / (float)a.T);
   }
   term[e] = v;
   __syncthreads();
@@ -386,6 +387,7 @@ struct __align__(8) Bars {
 
 struct Args {
   int T, E, EP, k, renorm, S, nk, stages, score;
+  int k_route;                    // columns the load and f count (k; 1 with rerouting)
   const float *bias;              // [E] added to h (or null)
   const float *sel_bias;          // [E] added to the scores for the choice only (or null)
   float *probs;                   // [T, E] scores, or null
@@ -411,7 +413,7 @@ __device__ __forceinline__ unsigned long long pack_cand(float key, int e) {
 }
 __device__ __forceinline__ int cand_expert(unsigned long long c) { return 0xFFFF - (int)(c & 0xFFFFu); }
 // Inverse of logit_key (a -0.0 key comes back as +0.0).
-__device__ __forceinline__ float cand_key(unsigned long long c) {
+__device__ __forceinline__ float cand_key_value(unsigned long long c) {
   const uint32_t key = (uint32_t)(c >> 32);
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
@@ -422,24 +424,6 @@ __device__ __forceinline__ float prob_of(float h, float M, float Z) { return exp
 __device__ __forceinline__ float elem_score(float h, int score) {
   if (score == MOE_SCORE_SIGMOID) return 1.0f / (1.0f + expf(-h));
   return sqrtf(fmaxf(h, 0.0f) + log1pf(expf(-fabsf(h))));
-}
-
-// Keeps (c, sc)[0..k) sorted by c, descending: (v, vs) goes in at its place
-// when v beats c[k - 1] (held by the caller in `last`, which this updates),
-// the rest shift down. Unrolled over KMAX with the runtime k as a predicate.
-__device__ __forceinline__ void insert_cand(unsigned long long (&c)[KMAX], float (&sc)[KMAX], unsigned long long &last,
-                                            unsigned long long v, float vs, int k) {
-  if (v <= last) return;
-#pragma unroll
-  for (int j = KMAX - 1; j > 0; --j) {
-    if (j < k && v > c[j - 1]) { c[j] = c[j - 1]; sc[j] = sc[j - 1]; }
-    else if (j < k && v > c[j]) { c[j] = v; sc[j] = vs; }
-  }
-  if (v > c[0]) { c[0] = v; sc[0] = vs; }
-  last = c[0];
-#pragma unroll
-  for (int j = 1; j < KMAX; ++j)
-    if (j == k - 1) last = c[j];
 }
 
 __device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
@@ -458,42 +442,67 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 200000000ull) break;
 }
 
+// One token row's candidate list, kept by its thread in shared memory with
+// the rows interleaved (entry j of row r at j * BM + r, so a warp's accesses
+// fall in distinct banks): the k best selection keys, descending, and the
+// score of each.
+struct CandList {
+  unsigned long long *key;   // [KMAX][BM]
+  float *sc;                 // [KMAX][BM]
+  int r, k;
+  unsigned long long last;   // key[k - 1]: a new key enters only when it beats this
+  __device__ __forceinline__ void clear() {
+    for (int j = 0; j < k; ++j) { key[j * BM + r] = 0ull; sc[j * BM + r] = 0.0f; }
+    last = 0ull;
+  }
+  __device__ __forceinline__ void offer(unsigned long long v, float vs) {
+    if (v <= last) return;
+    int j = k - 1;
+    while (j > 0 && key[(j - 1) * BM + r] < v) {
+      key[j * BM + r] = key[(j - 1) * BM + r];
+      sc[j * BM + r] = sc[(j - 1) * BM + r];
+      --j;
+    }
+    key[j * BM + r] = v;
+    sc[j * BM + r] = vs;
+    last = key[(k - 1) * BM + r];
+  }
+};
+
 // This row's record (candidates, their scores, m, z) into slot [rank][r] of
 // every CTA of the cluster.
-__device__ __forceinline__ void send_record(Cand *recv, int rank, int r, int S, const unsigned long long (&c)[KMAX],
-                                            const float (&sc)[KMAX], float m, float z) {
-  const uint32_t mine = smem_u32(&recv[rank * BM + r]);
+__device__ __forceinline__ void send_record(Cand *recv, int rank, int S, const CandList &cl, float m, float z) {
+  const uint32_t mine = smem_u32(&recv[rank * BM + cl.r]);
   for (int dst = 0; dst < S; ++dst) {
     const uint32_t ra = mapa_shared(mine, (uint32_t)dst);
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) st_cluster_u64(ra + 8u * j, c[j]);
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) st_cluster_f32(ra + 8u * KMAX + 4u * j, sc[j]);
+    for (int j = 0; j < KMAX; ++j) {
+      st_cluster_u64(ra + 8u * j, j < cl.k ? cl.key[j * BM + cl.r] : 0ull);
+      st_cluster_f32(ra + 8u * KMAX + 4u * j, j < cl.k ? cl.sc[j * BM + cl.r] : 0.0f);
+    }
     st_cluster_f32(ra + 12u * KMAX, m);
     st_cluster_f32(ra + 12u * KMAX + 4u, z);
   }
 }
-// The k best of the S sorted lists of row r (distinct experts: no equal
-// values); heads holds each list's next position, 8 bits per list.
-__device__ __forceinline__ void merge_records(const Cand *recv, int r, int S, int k, unsigned long long (&c)[KMAX],
-                                              float (&sc)[KMAX]) {
+// The k best of the S sorted lists of row r into cl (distinct experts: no
+// equal keys); heads holds each list's next position, 8 bits per list.
+__device__ __forceinline__ void merge_records(const Cand *recv, int S, CandList &cl) {
   uint32_t heads = 0;
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
+  for (int j = 0; j < cl.k; ++j) {
     unsigned long long best = 0ull;
     float bs = 0.0f;
     int from = 0;
-#pragma unroll
-    for (int s = 0; s < SMAX; ++s) {
+    for (int s = 0; s < S; ++s) {
       const int hd = (int)((heads >> (8 * s)) & 0xFFu);
-      const bool ok = j < k && s < S && hd < k;
-      const unsigned long long v = ok ? recv[s * BM + r].c[hd] : 0ull;
-      if (v > best) { best = v; bs = recv[s * BM + r].sc[hd]; from = s; }
+      if (hd < cl.k) {
+        const unsigned long long v = recv[s * BM + cl.r].c[hd];
+        if (v > best) { best = v; bs = recv[s * BM + cl.r].sc[hd]; from = s; }
+      }
     }
-    c[j] = best;
-    sc[j] = bs;
+    cl.key[j * BM + cl.r] = best;
+    cl.sc[j * BM + cl.r] = bs;
     heads += 1u << (8 * from);
   }
+  cl.last = cl.key[(cl.k - 1) * BM + cl.r];
 }
 
 // Logits, scores, top-k and statistics of 128 tokens, with the experts'
@@ -533,6 +542,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   float *imp_w = stage_out + 4 * 32 * 32;                                    // [4 row quarters][NC]
   int *cnt = reinterpret_cast<int *>(imp_w + 4 * NC);                        // [EP]
   float *term = reinterpret_cast<float *>(cnt + 256);                        // [256]
+  unsigned long long *cand_key = reinterpret_cast<unsigned long long *>(term + 256);   // [KMAX][BM]
+  float *cand_sc = reinterpret_cast<float *>(cand_key + KMAX * BM);                      // [KMAX][BM]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = S > 1 ? (int)cluster_ctarank() : 0;
@@ -624,54 +635,61 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int t = m0 + r;
     const bool live = t < a.T;
     const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const float *bias = a.bias, *sel_bias = a.sel_bias;
     float m = -FLT_MAX, z = 0.0f;
-    unsigned long long cand[KMAX];
-    float csc[KMAX];
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) { cand[j] = 0ull; csc[j] = 0.0f; }
-    unsigned long long last = 0ull;   // cand[k - 1]
+    CandList cl{cand_key, cand_sc, r, k, 0ull};
     // warp-uniform: the TMEM loads below are warp-collective
     const bool acc_ok =
         __all_sync(0xffffffffu, mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st) ? 1 : 0) != 0;
-    float v[32];
+    float v[8];
+    // (the ring is idle once this CTA's MMAs have completed: the lists live there)
+    cl.clear();
     if (acc_ok) {
       tc_fence_after();
-      // pass 1: maximum (softmax) and the candidates that need no global statistics
+      // pass 1: the maximum (softmax) and the candidates that need no global statistics
+      if (softmax) {
 #pragma unroll 1
-      for (int c = 0; c < NC / 32; ++c) {
-        tmem_ld32(t_row + c * 32, v);
+        for (int c = 0; c < NC / 8; ++c) {
+          tmem_ld8(t_row + c * 8, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int e = col0 + c * 32 + i;
-          if (e < E) {
-            const float h = v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f);
-            if (softmax) {
+          for (int i = 0; i < 8; ++i) {
+            const int e = col0 + c * 8 + i;
+            if (e < E) {
+              const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
               m = fmaxf(m, h);
-              if (!late_choice) insert_cand(cand, csc, last, pack_cand(h, e), 0.0f, k);
-            } else {
-              const float sv = elem_score(h, a.score);
-              const float key = a.sel_bias ? sv + __ldg(a.sel_bias + e) : h;
-              insert_cand(cand, csc, last, pack_cand(key, e), sv, k);
+              if (!late_choice) cl.offer(pack_cand(h, e), 0.0f);
             }
           }
         }
-      }
-      // pass 2 (softmax): sum of exp(h - m)
-      if (softmax) {
+        // pass 2: sum of exp(h - m)
 #pragma unroll 1
-        for (int c = 0; c < NC / 32; ++c) {
-          tmem_ld32(t_row + c * 32, v);
+        for (int c = 0; c < NC / 8; ++c) {
+          tmem_ld8(t_row + c * 8, v);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int e = col0 + c * 32 + i;
-            if (e < E) z += expf(v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f) - m);
+          for (int i = 0; i < 8; ++i) {
+            const int e = col0 + c * 8 + i;
+            if (e < E) z += expf(v[i] + (bias ? __ldg(bias + e) : 0.0f) - m);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < NC / 8; ++c) {
+          tmem_ld8(t_row + c * 8, v);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int e = col0 + c * 8 + i;
+            if (e < E) {
+              const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
+              const float sv = elem_score(h, a.score);
+              cl.offer(pack_cand(sel_bias ? sv + __ldg(sel_bias + e) : h, e), sv);
+            }
           }
         }
       }
     }
     float M = m, Z = z;
     if (S > 1) {
-      send_record(recv, rank, r, S, cand, csc, m, z);
+      send_record(recv, rank, S, cl, m, z);
       cluster_sync_all();   // every CTA's records are in
       if (softmax) {
         M = -FLT_MAX;
@@ -679,33 +697,37 @@ __global__ void __launch_bounds__(THREADS, 1)
         Z = 0.0f;
         for (int s = 0; s < S; ++s) Z += recv[s * BM + r].z * expf(recv[s * BM + r].m - M);
       }
-      if (!late_choice) merge_records(recv, r, S, k, cand, csc);
+      if (!late_choice) merge_records(recv, S, cl);
     }
     for (int e = threadIdx.x - 64; e < a.EP; e += 128) cnt[e] = 0;
     epilogue_sync();
     // pass 3: the scores of this CTA's columns; per 32 x 32 block, each lane
-    // writes its row into the warp's 128-byte swizzled staging rows, then
-    // lane j takes column j row by row: one coalesced 128-byte store per row
-    // and the column's sum over the block's live rows.
+    // writes its row into the warp's 128-byte swizzled staging rows (8
+    // columns at a time), then lane j takes column j row by row: one
+    // coalesced 128-byte store per row and the column's sum over the block's
+    // live rows.
     float *stg = stage_out + (warp - 2) * 32 * 32;
 #pragma unroll 1
     for (int c = 0; c < NC / 32; ++c) {
-      if (acc_ok) tmem_ld32(t_row + c * 32, v);
+#pragma unroll 1
+      for (int sub = 0; sub < 4; ++sub) {
+        if (acc_ok) tmem_ld8(t_row + c * 32 + sub * 8, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int e = col0 + c * 32 + i;
-        float sv = 0.0f;
-        if (acc_ok && live && e < E) {
-          const float h = v[i] + (a.bias ? __ldg(a.bias + e) : 0.0f);
-          sv = softmax ? prob_of(h, M, Z) : elem_score(h, a.score);
-          if (late_choice) insert_cand(cand, csc, last, pack_cand(sv + __ldg(a.sel_bias + e), e), sv, k);
+        for (int i = 0; i < 8; ++i) {
+          const int e = col0 + c * 32 + sub * 8 + i;
+          float sv = 0.0f;
+          if (acc_ok && live && e < E) {
+            const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
+            sv = softmax ? prob_of(h, M, Z) : elem_score(h, a.score);
+            if (late_choice) cl.offer(pack_cand(sv + __ldg(sel_bias + e), e), sv);
+          }
+          v[i] = sv;
         }
-        v[i] = sv;
+        *reinterpret_cast<float4 *>(stg + lane * 32 + (((2 * sub) ^ (lane & 7)) << 2)) =
+            make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4 *>(stg + lane * 32 + (((2 * sub + 1) ^ (lane & 7)) << 2)) =
+            make_float4(v[4], v[5], v[6], v[7]);
       }
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        *reinterpret_cast<float4 *>(stg + lane * 32 + ((j ^ (lane & 7)) << 2)) =
-            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       __syncwarp();
       const int e = col0 + c * 32 + lane;
       float colsum = 0.0f;
@@ -723,31 +745,26 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     if (late_choice && S > 1) {
       cluster_sync_all();   // every CTA has read the first records
-      send_record(recv, rank, r, S, cand, csc, M, Z);
+      send_record(recv, rank, S, cl, M, Z);
       cluster_sync_all();   // the second records are in
-      merge_records(recv, r, S, k, cand, csc);
+      merge_records(recv, S, cl);
     }
     // the row's experts and gates
     if (acc_ok && live && (r % S) == rank) {
-      float gv[KMAX];
       float psum = 0.0f;
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        gv[j] = 0.0f;
-        if (j < k) {
-          // softmax scores chosen by logit: p from the logit the key carries
-          gv[j] = (softmax && !late_choice) ? prob_of(cand_key(cand[j]), M, Z) : csc[j];
-          psum += gv[j];
-        }
+      for (int j = 0; j < k; ++j) {
+        // softmax scores chosen by logit: p from the logit the key carries
+        const float g = (softmax && !late_choice) ? prob_of(cand_key_value(cl.key[j * BM + r]), M, Z)
+                                                  : cl.sc[j * BM + r];
+        cl.sc[j * BM + r] = g;
+        psum += g;
       }
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          const int e = cand_expert(cand[j]);
-          a.idx[(int64_t)t * k + j] = e;
-          a.gate[(int64_t)t * k + j] = a.renorm ? gv[j] / psum : gv[j];
-          atomicAdd(&cnt[e], 1);
-        }
+      for (int j = 0; j < k; ++j) {
+        const int e = cand_expert(cl.key[j * BM + r]);
+        const float g = cl.sc[j * BM + r];
+        a.idx[(int64_t)t * k + j] = e;
+        a.gate[(int64_t)t * k + j] = a.renorm ? g / psum : g;
+        if (j < a.k_route) atomicAdd(&cnt[e], 1);
       }
     }
     epilogue_sync();
@@ -788,7 +805,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           a.acc_load[e] = 0;
           a.importance[e] = sm;
           a.load[e] = c;
-          v = ((float)c / ((float)a.T * (float)k)) * (sm / (float)a.T);
+          v = ((float)c / ((float)a.T * (float)a.k_route)) * (sm / (float)a.T);
         }
         term[e] = v;
       }
@@ -903,7 +920,7 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
     a.x = x; a.w_r = w_r; a.bias = bias; a.probs = probs; a.idx = idx; a.gate = gate;
     a.acc_imp = acc_imp;
     a.acc_load = acc_load;
-    a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm;
+    a.T = sh.T; a.d = sh.d; a.E = sh.E; a.k = sh.k; a.renorm = sh.renorm; a.k_route = sh.k_route;
     StatsOut so;
     so.alpha = sh.alpha; so.importance = importance; so.load = load; so.aux = aux; so.counter = counter;
     const int nblk = router_blocks(sh);
@@ -924,6 +941,7 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
     return cudaErrorInvalidValue;
   rf::Args ra;
   ra.T = sh.T; ra.E = sh.E; ra.EP = plan.ep; ra.k = sh.k; ra.renorm = sh.renorm; ra.S = plan.cluster;
+  ra.k_route = sh.k_route;
   ra.nk = (sh.d + rf::BK - 1) / rf::BK;
   ra.score = sh.score;
   ra.bias = bias; ra.sel_bias = sel_bias; ra.probs = probs; ra.idx = idx; ra.gate = gate;

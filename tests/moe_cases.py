@@ -41,7 +41,7 @@ def abi_capacity(moe, w) -> int:
 def config_for(moe, w):
     return moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=w.k, d_ff=w.F, act=w.act, dtype=w.dtype,
                            renormalize=w.renormalize, capacity=abi_capacity(moe, w), aux_alpha=w.alpha,
-                           add_residual=w.add_residual, score=w.score)
+                           add_residual=w.add_residual, score=w.score, reroute=w.reroute)
 
 
 def to_dev(torch, a, dtype):
@@ -93,7 +93,7 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False, sele
 
 def oracle_kw(w):
     return dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments, renormalize=w.renormalize,
-                alpha=w.alpha, add_residual=w.add_residual, score=w.score)
+                alpha=w.alpha, add_residual=w.add_residual, score=w.score, reroute=w.reroute)
 
 
 def assert_close(got, ref, tol, what):

@@ -94,9 +94,14 @@ def test_config_bad_fields():
         moe.moe_workspace_size(cfg(dtype="f32", score="sigmoid"))
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
     c = cfg()
-    c.reserved = 1
+    c.reroute = 2
     with pytest.raises(moe.MoEError):
         moe.moe_workspace_size(c)
+    with pytest.raises(moe.MoEError) as e:                     # rerouting: top-1 layers only
+        moe.moe_workspace_size(cfg(reroute=True))               # (top_k 2)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    rr = cfg(top_k=1, reroute=True)
+    assert moe.moe_max_rows(rr) == min(1000, 16 * 250)          # at most one kept assignment per token
     c = cfg()
     c.aux_alpha = float("nan")
     with pytest.raises(moe.MoEError):

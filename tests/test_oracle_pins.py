@@ -254,7 +254,8 @@ def _relu_pattern(pp, base, w):
     return out
 
 
-def _fd_check(w, n_coords=60, eps=1e-4, seed=0, add_residual=True, score="softmax", sel_bias=None):
+def _fd_check(w, n_coords=60, eps=1e-4, seed=0, add_residual=True, score="softmax", sel_bias=None,
+              reroute=False):
     """Central differences of L = <dY, out> + aux against the oracle's backward.
 
     eps = 1e-4: at 1e-6 the fp64 rounding of L divided by 2 eps already
@@ -264,7 +265,7 @@ def _fd_check(w, n_coords=60, eps=1e-4, seed=0, add_residual=True, score="softma
     inp = syn.make_inputs(w, dy=True)
     kw = dict(k=w.k, act=w.act, cf=w.cf, count_assignments=w.count_assignments,
               renormalize=w.renormalize, alpha=w.alpha, add_residual=add_residual, score=score,
-              sel_bias=sel_bias)
+              sel_bias=sel_bias, reroute=reroute)
     x = inp["x"].astype(np.float64)
     w_r = inp["w_r"].astype(np.float64)
     w1 = inp["w1"].astype(np.float64)
@@ -471,3 +472,75 @@ def test_route_with_variants_follows_the_variant_oracle():
             assert np.array_equal(r["idx"], v["idx"]) and np.array_equal(r["load"], v["load"])
             np.testing.assert_allclose(r["gate"], v["gate"], rtol=1e-15)
             np.testing.assert_allclose(r["importance"], v["s"].sum(axis=0), rtol=1e-13)
+
+
+# ------------------------------------------------------------------ No-Token-Left-Behind
+def _brute_reroute(first, second, E, C):
+    """The two rounds spelled out with per-expert queues: round 1 keeps each expert's first C first-choice
+    tokens (token order); round 2 walks the round-1 dropouts in token order and admits each to its second
+    expert while that expert holds fewer than C."""
+    T = len(first)
+    slot = -np.ones((T, 2), dtype=np.int64)
+    held = {e: [] for e in range(E)}
+    for t in range(T):
+        if len(held[first[t]]) < C:
+            slot[t, 0] = len(held[first[t]])
+            held[first[t]].append(t)
+    for t in range(T):
+        if slot[t, 0] < 0 and len(held[second[t]]) < C:
+            slot[t, 1] = len(held[second[t]])
+            held[second[t]].append(t)
+    return slot, np.array([len(held[e]) for e in range(E)])
+
+
+@pytest.mark.parametrize("C", [0, 2, 5, 40])
+def test_reroute_slots_brute_force_and_invariants(C):
+    rng = np.random.default_rng(30 + C)
+    T, E = 60, 5
+    idx2 = np.stack([rng.permutation(E)[:2] for _ in range(T)])
+    idx2[:25, 0] = 1                                    # overload expert 1 so that round 2 has work
+    s = O.assign_slots_reroute(idx2, E, C)
+    slot, kept = _brute_reroute(idx2[:, 0], idx2[:, 1], E, C)
+    np.testing.assert_array_equal(s["slot"], slot)
+    np.testing.assert_array_equal(s["kept"], kept)
+    assert np.all(s["kept"] <= C) and np.all(((s["slot"] >= 0).sum(axis=1)) <= 1)
+    plain = O.assign_slots(idx2[:, :1], E, C)
+    np.testing.assert_array_equal(s["slot"][:, 0], plain["slot"][:, 0])   # round 1 is the plain rule
+    assert (s["slot"] >= 0).any(axis=1).sum() >= (plain["slot"] >= 0).sum()
+    for t in range(T):
+        for j in range(2):
+            if s["slot"][t, j] >= 0:
+                row = s["offsets"][idx2[t, j]] + s["slot"][t, j]
+                assert s["row_token"][row] == t
+
+
+def test_reroute_layer_gates_and_statistics():
+    """The second-choice expert's probability is the gate of a rerouted token; load and f count first choices;
+    a token is dropped for good only when both of its experts are full."""
+    w = syn.Workload("reroute-pin", T=80, d=8, E=6, k=1, F=6, act="relu", dtype="f32", cf=(1, 2), router_std=0.6,
+                     zipf_s=1.5)
+    inp = syn.make_inputs(w)
+    f = O.forward(inp["x"], inp["w_r"], inp["bias"], (inp["w1"], inp["w2"]), k=1, act="relu", cf=(1, 2),
+                  reroute=True)
+    base = O.forward(inp["x"], inp["w_r"], inp["bias"], (inp["w1"], inp["w2"]), k=1, act="relu", cf=(1, 2))
+    assert f["idx"].shape == (w.T, 2) and np.array_equal(f["idx"][:, 0], base["idx"][:, 0])
+    np.testing.assert_array_equal(f["load"], base["load"])
+    assert f["aux"] == base["aux"]
+    np.testing.assert_array_equal(f["gate"], np.take_along_axis(f["p"], f["idx"], axis=1))
+    rerouted = f["slot"][:, 1] >= 0
+    assert rerouted.any()
+    x = inp["x"].astype(np.float64)
+    for t in np.nonzero(rerouted)[0][:5]:
+        e = f["idx"][t, 1]
+        y = O.expert_ffn(x[t:t + 1], inp["w1"][e].astype(np.float64), inp["w2"][e].astype(np.float64), "relu")["y"]
+        np.testing.assert_allclose(f["out"][t], x[t] + f["p"][t, e] * y[0], rtol=1e-12)
+    C = f["C"]
+    for t in np.nonzero((f["slot"] < 0).all(axis=1))[0]:
+        assert f["kept"][f["idx"][t, 0]] == C and f["kept"][f["idx"][t, 1]] == C
+
+
+def test_gradients_finite_differences_reroute():
+    w = syn.Workload("fd-reroute", T=48, d=10, E=5, k=1, F=8, act="swiglu", dtype="f32", cf=(1, 2), router_std=0.5,
+                     zipf_s=1.2, backward=True)
+    checked, skipped = _fd_check(w, n_coords=30, reroute=True)
+    assert checked >= 100 and skipped <= checked // 10

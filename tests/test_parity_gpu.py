@@ -222,11 +222,26 @@ PAIR_CASES = {
 }
 
 
-@pytest.mark.parametrize("mode", ["1", "0"])
+@pytest.mark.parametrize("mode", ["1", "0", "dynamic"])
 @pytest.mark.parametrize("name", list(PAIR_CASES))
 def test_gemm_tile_modes(name, mode, monkeypatch):
-    """Every expert GEMM forced onto CTA-pair tiles (MOE_GEMM_PAIR=1) or onto
-    one CTA per tile (0), forward and backward, against the oracle."""
+    """Every expert GEMM forced onto CTA-pair tiles (MOE_GEMM_PAIR=1), onto
+    one CTA per tile in the fixed order (0), or one CTA per tile handed out by
+    the workspace's tile counter (MOE_GEMM_SCHED=dynamic), forward and
+    backward, against the oracle; twice in a row for the counter, which every
+    launch must leave at zero."""
+    if mode == "dynamic":
+        monkeypatch.setenv("MOE_GEMM_PAIR", "0")
+        monkeypatch.setenv("MOE_GEMM_SCHED", "dynamic")
+        w = PAIR_CASES[name]
+        inp = syn.make_inputs(w, dy=True)
+        import sparse_mixture_experts_49_b300 as moe
+        layer = moe.MoELayer(config_for(moe, w))
+        f, b = _ref_all(w, inp, True)
+        for _ in range(2):
+            res = run_gpu(w, inp, backward=True, layer=layer)
+            _check_full(w, res, inp, f, b)
+        return
     monkeypatch.setenv("MOE_GEMM_PAIR", mode)
     w = PAIR_CASES[name]
     inp = syn.make_inputs(w, dy=True)
@@ -465,4 +480,23 @@ def test_dims_multiple_of_8(act, k):
     f, b = _ref_all(w, inp, True)
     _check_full(w, res, inp, f, b)
     fused = run_gpu(w, inp, fused=True)
+    assert_close(fused["out"], f["out"], TOL_BF16, "out (moe_forward)")
+
+
+# ------------------------------------------------------------------ No-Token-Left-Behind
+@pytest.mark.parametrize("T,cf", [(1000, (3, 4)), (6200, (1, 2))])
+def test_reroute_second_choice(T, cf):
+    """Top-1 layers with rerouting ([Switch] section 論文の限界と、まだ分かっていないこと): the two-round
+    slots (first choices, then the round-1 dropouts' second choices into the room left) bit-exact against
+    the oracle over one and many dispatch blocks, forward and backward values within tolerance, and
+    moe_forward on the same layer."""
+    w = syn.Workload(f"reroute-{T}", T=T, d=256, E=16, k=1, F=256, act="relu", dtype="bf16", cf=cf, zipf_s=1.2,
+                     router_std=1 / 16, reroute=True, backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    res = run_gpu(w, inp, backward=True)
+    f, b = _ref_all(w, inp, True)
+    assert (f["slot"][:, 1] >= 0).any() and (f["slot"] < 0).all(axis=1).any()
+    _check_full(w, res, inp, f, b)
+    fused = run_gpu(w, inp, fused=True)
+    check_routing(fused, f, w)
     assert_close(fused["out"], f["out"], TOL_BF16, "out (moe_forward)")
