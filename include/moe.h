@@ -104,6 +104,11 @@ typedef struct moe_config {
                           token dropped by its first choice's capacity is offered to in a second
                           round (token order, into the room each expert has left; slot -1 where
                           not kept). Load and f count first choices. 0: plain top-k. */
+  int32_t expert_choice; /* 1: expert-choice routing (see moe_router_expert_choice): each expert
+                            takes the min(C, T) tokens with the largest scores; top_k must be 1
+                            (unused), capacity C >= 1, softmax scores, T <= 32768, no rerouting
+                            or renormalisation. 0: token-choice top-k. */
+  int32_t reserved;    /* must be 0 */
 } moe_config;
 
 /* Expert capacity, [Switch] eq. (3): floor(n * cf_num / (E * cf_den)) with
@@ -308,6 +313,36 @@ moe_status moe_forward(const moe_config *cfg, const void *x, const float *w_r,
                        int32_t *row_token, void *x_perm, void *h, void *y_perm, void *out, void *ws,
                        moe_stream_t stream);
 
+/*
+ * Expert-choice routing ([Wiki] "Mixture-of-Experts", section 横断的知見: the
+ * experts pick their top-k tokens instead of the tokens picking experts), for
+ * layers with cfg->expert_choice = 1. Read with the rest of the layer: the
+ * scores are eq. (1)'s softmax over the experts, p [T, E]; expert e takes the
+ * Ce = min(C, T) tokens with the largest p[:, e] (descending, ties to the
+ * lower token index) and keeps them in ascending token order as its group of
+ * rows e Ce .. e Ce + Ce - 1; a chosen (t, e)'s gate is p[t, e]; a token can
+ * be chosen by any number of experts, or none. rows = moe_max_rows(cfg) =
+ * E * Ce. The balance is built in: no auxiliary loss is formed.
+ *
+ * Router: probs [T, E] fp32 out (required), row_token [rows] int32 out (the
+ * token of each row), row_gate [rows] fp32 out (its gate), expert_offsets
+ * [E + 1] int32 out (e Ce), importance [E] fp32 out (sum_t p[t, e]).
+ * The expert FFNs are moe_expert_gemm with these offsets.
+ */
+moe_status moe_router_expert_choice(const moe_config *cfg, const void *x, const float *w_r,
+                                    const float *logit_bias, float *probs, int32_t *row_token,
+                                    float *row_gate, int32_t *expert_offsets, float *importance,
+                                    void *ws, moe_stream_t stream);
+/* x_perm [rows, d] out: x_perm[row] = x[row_token[row]]. */
+moe_status moe_dispatch_expert_choice(const moe_config *cfg, const void *x, const int32_t *row_token,
+                                      void *x_perm, moe_stream_t stream);
+/* out[t] = x[t] (only with cfg->add_residual) + sum over the rows whose token
+ * is t of row_gate[row] * y_perm[row], in expert order, summed in fp32 and
+ * rounded once. out [T, d] may not alias x or y_perm. */
+moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const void *y_perm,
+                                     const int32_t *row_token, const float *row_gate, void *out,
+                                     void *ws, moe_stream_t stream);
+
 /* Everything the forward pass produced that the backward pass reads. */
 typedef struct moe_saved {
   const void *x;                  /* [T, d] */
@@ -325,6 +360,28 @@ typedef struct moe_saved {
   const void *h;                  /* [rows, F] */
   const void *y_perm;             /* [rows, d] */
 } moe_saved;
+
+/* The expert-choice forward pass's saved tensors. */
+typedef struct moe_saved_expert_choice {
+  const void *x;                  /* [T, d] */
+  const float *w_r;               /* [E, d] */
+  const void *w1;                 /* [E, R1, d] */
+  const void *w2;                 /* [E, d, F] */
+  const float *probs;             /* [T, E] */
+  const int32_t *row_token;       /* [rows] */
+  const float *row_gate;          /* [rows] */
+  const int32_t *expert_offsets;  /* [E + 1] */
+  const void *x_perm;             /* [rows, d] */
+  const void *pre_act;            /* [rows, 2F] (SwiGLU) or NULL (ReLU) */
+  const void *h;                  /* [rows, F] */
+  const void *y_perm;             /* [rows, d] */
+} moe_saved_expert_choice;
+
+/* Backward of an expert-choice layer's L = <dY, out> (the choices held
+ * constant): dx, dw_r, dw1, dw2 as in moe_backward. */
+moe_status moe_backward_expert_choice(const moe_config *cfg, const moe_saved_expert_choice *saved,
+                                      const void *dy, void *dx, float *dw_r, void *dw1, void *dw2,
+                                      void *ws, moe_stream_t stream);
 
 /*
  * Backward of L = <dY, out> + aux, with the top-k sets, capacity masks and

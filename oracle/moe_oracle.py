@@ -445,3 +445,87 @@ def loss(x, w_r, bias, experts: ExpertSource, dy, **kw) -> float:
     """L = <dY, out> + aux, the scalar whose gradient `backward` returns."""
     f = forward(x, w_r, bias, experts, **kw)
     return float(np.sum(_f64(dy) * f["out"])) + f["aux"]
+
+
+# ------------------------------------------------------------------ expert-choice routing
+def route_expert_choice(x, w_r, bias, C: int) -> dict:
+    """Expert-choice routing ([Wiki] "Mixture-of-Experts", section 横断的知見: the
+    experts pick their top-k tokens instead of the tokens picking experts).
+
+    Read with the rest of the layer: the scores are eq. (1)'s softmax over the
+    experts, p [T, E]; expert e takes the min(C, T) tokens with the largest
+    p[:, e] (descending, ties to the lower token index), kept in ascending
+    token order as its group of rows; the gate of a chosen (t, e) is p[t, e].
+    A token can be chosen by any number of experts, or none. importance_e =
+    sum_t p[t, e]; load_e = the number chosen. The balance is built in, so no
+    auxiliary loss is formed.
+    """
+    h = router_logits(x, w_r, bias)
+    T, E = h.shape
+    p = softmax(h)
+    Ce = min(C, T)
+    chosen = np.zeros((E, Ce), dtype=np.int64)
+    for e in range(E):
+        order = sorted(range(T), key=lambda t: (-p[t, e], t))      # descending score, ties to the lower token
+        chosen[e] = np.sort(order[:Ce])
+    gate = np.take_along_axis(p.T, chosen, axis=1)                  # [E, Ce]
+    load = np.full(E, Ce, dtype=np.int64)
+    return dict(h=h, p=p, chosen=chosen, gate=gate, importance=p.sum(axis=0), load=load,
+                offsets=np.arange(E + 1, dtype=np.int64) * Ce, row_token=chosen.reshape(-1))
+
+
+def forward_expert_choice(x, w_r, bias, experts: ExpertSource, *, C: int, act: str,
+                          add_residual: bool = True) -> dict:
+    """out_t = x_t + sum over the experts e that chose t of p[t, e] E_e(x_t)."""
+    x64 = _f64(x)
+    r = route_expert_choice(x64, w_r, bias, C)
+    out = x64.copy() if add_residual else np.zeros_like(x64)
+    for e in range(r["p"].shape[1]):
+        tt = r["chosen"][e]
+        if len(tt) == 0:
+            continue
+        w1, w2 = _expert(experts, e)
+        y = expert_ffn(x64[tt], w1, w2, act)["y"]
+        out[tt] += r["gate"][e][:, None] * y              # tt has no repeats within one expert
+    res = dict(r)
+    res.update(out=out)
+    return res
+
+
+def backward_expert_choice(x, w_r, bias, experts: ExpertSource, dy, *, C: int, act: str,
+                           add_residual: bool = True) -> dict:
+    """Gradients of L = <dY, out> with the choices held constant: the chain rule
+    through each chosen pair's gate p[t, e] and expert, then eq. (1)'s softmax
+    Jacobian. dg [E, Ce] is the gradient at each chosen pair's gate."""
+    x64, dy64 = _f64(x), _f64(dy)
+    wr64 = _f64(w_r)
+    r = route_expert_choice(x64, wr64, bias, C)
+    T, E = r["p"].shape
+    dx = dy64.copy() if add_residual else np.zeros_like(dy64)
+    dg = np.zeros_like(r["gate"])
+    dp = np.zeros((T, E))
+    dw1, dw2 = {}, {}
+    for e in range(E):
+        tt = r["chosen"][e]
+        w1, w2 = _expert(experts, e)
+        if len(tt) == 0:
+            dw1[e], dw2[e] = np.zeros_like(w1), np.zeros_like(w2)
+            continue
+        z = x64[tt]
+        fw = expert_ffn(z, w1, w2, act)
+        g = r["gate"][e][:, None]
+        dg[e] = np.sum(dy64[tt] * fw["y"], axis=1)
+        dp[tt, e] = dg[e]
+        dyp = g * dy64[tt]
+        dhid = dyp @ w2
+        dw2[e] = dyp.T @ fw["hid"]
+        if act == "relu":
+            da = dhid * (fw["a"] > 0)
+        else:
+            sg = 1.0 / (1.0 + np.exp(-fw["g"]))
+            da = np.concatenate([dhid * fw["u"] * (sg * (1.0 + fw["g"] * (1.0 - sg))), dhid * silu(fw["g"])], axis=1)
+        dw1[e] = da.T @ z
+        dx[tt] += da @ w1
+    dh = score_grad(r["h"], r["p"], dp, "softmax")
+    dx += dh @ wr64
+    return dict(dx=dx, dw_r=dh.T @ x64, dg=dg, dh=dh, dw1=dw1, dw2=dw2, route=r)

@@ -28,7 +28,8 @@ MOE_NOALLOC_MAX_TOKENS = 32768
 
 EXPORTED = [
     "moe_capacity", "moe_max_rows", "moe_workspace_size", "moe_workspace_init", "moe_router",
-    "moe_router_biased", "moe_select_bias_update",
+    "moe_router_biased", "moe_select_bias_update", "moe_router_expert_choice", "moe_dispatch_expert_choice",
+    "moe_combine_expert_choice", "moe_backward_expert_choice",
     "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_gemm", "moe_combine", "moe_forward", "moe_backward",
     "moe_backward_intermediates",
     "moe_get_device_error", "moe_selftest_bounded_wait", "moe_status_string", "moe_last_cuda_error",
@@ -47,8 +48,14 @@ class moe_config(ctypes.Structure):
         ("top_k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("act", ctypes.c_int32),
         ("dtype", ctypes.c_int32), ("renormalize", ctypes.c_int32), ("add_residual", ctypes.c_int32),
         ("score", ctypes.c_int32), ("capacity", ctypes.c_int64), ("aux_alpha", ctypes.c_float),
-        ("reroute", ctypes.c_int32),
+        ("reroute", ctypes.c_int32), ("expert_choice", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
+
+
+class moe_saved_expert_choice(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "x", "w_r", "w1", "w2", "probs", "row_token", "row_gate", "expert_offsets", "x_perm", "pre_act", "h",
+        "y_perm")]
 
 
 class moe_saved(ctypes.Structure):
@@ -78,6 +85,11 @@ def lib() -> ctypes.CDLL:
             "moe_router": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P]),
             "moe_router_biased": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P, P]),
             "moe_select_bias_update": (ctypes.c_int, [C, P, P, ctypes.c_float, P]),
+            "moe_router_expert_choice": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P]),
+            "moe_dispatch_expert_choice": (ctypes.c_int, [C, P, P, P, P]),
+            "moe_combine_expert_choice": (ctypes.c_int, [C, P, P, P, P, P, P, P]),
+            "moe_backward_expert_choice": (ctypes.c_int, [C, ctypes.POINTER(moe_saved_expert_choice), P, P, P, P, P,
+                                                          P, P]),
             "moe_dispatch": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
             "moe_dispatch_noalloc": (ctypes.c_int, [C, P, P, P, P, P, P, P, P]),
             "moe_expert_gemm": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P]),
@@ -130,13 +142,13 @@ def _stream(stream) -> Optional[int]:
 def make_config(T: int, d_model: int, n_experts: int, top_k: int, d_ff: int, act: str = "relu",
                 dtype: str = "bf16", renormalize: bool = False, capacity: int = -1,
                 aux_alpha: float = 0.01, add_residual: bool = True, score: str = "softmax",
-                reroute: bool = False) -> moe_config:
+                reroute: bool = False, expert_choice: bool = False) -> moe_config:
     return moe_config(T=T, d_model=d_model, n_experts=n_experts, top_k=top_k, d_ff=d_ff,
                       act=MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_RELU,
                       dtype=MOE_BF16 if dtype == "bf16" else MOE_F32, renormalize=int(renormalize),
                       add_residual=int(add_residual), score=SCORES[score],
                       capacity=-1 if capacity is None else int(capacity), aux_alpha=float(aux_alpha),
-                      reroute=int(reroute))
+                      reroute=int(reroute), expert_choice=int(expert_choice), reserved=0)
 
 
 # ---------------------------------------------------------------- entry points (same names as the C ABI)
@@ -180,6 +192,31 @@ def moe_select_bias_update(cfg, load, select_bias, gamma: float, stream=None):
     """select_bias[e] += gamma * sign(mean(load) - load[e]), in place."""
     _check(lib().moe_select_bias_update(ctypes.byref(cfg), _ptr(load), _ptr(select_bias), float(gamma),
                                         _stream(stream)), "moe_select_bias_update")
+
+
+def moe_router_expert_choice(cfg, x, w_r, logit_bias, probs, row_token, row_gate, expert_offsets, importance, ws,
+                             stream=None):
+    """Expert-choice routing: each expert takes the min(C, T) tokens with the largest softmax scores."""
+    _check(lib().moe_router_expert_choice(ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(logit_bias), _ptr(probs),
+                                          _ptr(row_token), _ptr(row_gate), _ptr(expert_offsets), _ptr(importance),
+                                          _ptr(ws), _stream(stream)), "moe_router_expert_choice")
+
+
+def moe_dispatch_expert_choice(cfg, x, row_token, x_perm, stream=None):
+    _check(lib().moe_dispatch_expert_choice(ctypes.byref(cfg), _ptr(x), _ptr(row_token), _ptr(x_perm),
+                                            _stream(stream)), "moe_dispatch_expert_choice")
+
+
+def moe_combine_expert_choice(cfg, x, y_perm, row_token, row_gate, out, ws, stream=None):
+    _check(lib().moe_combine_expert_choice(ctypes.byref(cfg), _ptr(x), _ptr(y_perm), _ptr(row_token), _ptr(row_gate),
+                                           _ptr(out), _ptr(ws), _stream(stream)), "moe_combine_expert_choice")
+
+
+def moe_backward_expert_choice(cfg, saved: dict, dy, dx, dw_r, dw1, dw2, ws, stream=None):
+    sv = moe_saved_expert_choice(**{k: _ptr(saved.get(k)) for k, _ in moe_saved_expert_choice._fields_})
+    _check(lib().moe_backward_expert_choice(ctypes.byref(cfg), ctypes.byref(sv), _ptr(dy), _ptr(dx), _ptr(dw_r),
+                                            _ptr(dw1), _ptr(dw2), _ptr(ws), _stream(stream)),
+           "moe_backward_expert_choice")
 
 
 def moe_dispatch(cfg, x, topk_idx, slot, kept, expert_offsets, row_token, x_perm, ws, stream=None):
@@ -308,6 +345,7 @@ class MoELayer:
         self.h = z(max(self.rows, 1), F)
         self.y_perm = z(max(self.rows, 1), d)
         self.out = z(T, d)
+        self.row_gate = z(max(self.rows, 1), dtype=torch.float32) if cfg.expert_choice else None
         self.R1 = R1
         moe_workspace_init(cfg, self.ws, stream)
 
@@ -315,6 +353,17 @@ class MoELayer:
         """out = x + MoE(x) (MoE(x) alone without the residual). If topk_idx is given, the router's choice is
         replaced by it (replay); select_bias is the selection-only correction bias (moe_router_biased)."""
         c, s = self.cfg, self.stream
+        if c.expert_choice:
+            # expert-choice routing: the experts pick their tokens (groups of min(C, T) rows each)
+            moe_router_expert_choice(c, x, w_r, logit_bias, self.probs, self.row_token, self.row_gate, self.offsets,
+                                     self.importance, self.ws, s)
+            moe_dispatch_expert_choice(c, x, self.row_token, self.x_perm, s)
+            moe_expert_gemm(c, self.x_perm, self.offsets, w1, w2, self.pre_act, self.h, self.y_perm, self.ws, s)
+            moe_combine_expert_choice(c, x, self.y_perm, self.row_token, self.row_gate, self.out, self.ws, s)
+            self._saved = dict(x=x, w_r=w_r, w1=w1, w2=w2, probs=self.probs, row_token=self.row_token,
+                               row_gate=self.row_gate, expert_offsets=self.offsets, x_perm=self.x_perm,
+                               pre_act=self.pre_act, h=self.h, y_perm=self.y_perm)
+            return self.out
         if select_bias is None:
             moe_router(c, x, w_r, logit_bias, self.probs, self.topk_idx, self.topk_gate, self.importance,
                        self.load, self.aux, self.ws, s)
@@ -346,7 +395,10 @@ class MoELayer:
         dw_r = dw_r if dw_r is not None else torch.empty(c.n_experts, c.d_model, dtype=torch.float32, device=dev)
         dw1 = dw1 if dw1 is not None else torch.empty(c.n_experts, self.R1, c.d_model, dtype=self.dt, device=dev)
         dw2 = dw2 if dw2 is not None else torch.empty(c.n_experts, c.d_model, c.d_ff, dtype=self.dt, device=dev)
-        moe_backward(c, self._saved, dy, dx, dw_r, dw1, dw2, self.ws, self.stream)
+        if c.expert_choice:
+            moe_backward_expert_choice(c, self._saved, dy, dx, dw_r, dw1, dw2, self.ws, self.stream)
+        else:
+            moe_backward(c, self._saved, dy, dx, dw_r, dw1, dw2, self.ws, self.stream)
         return dx, dw_r, dw1, dw2
 
     def balance_stats(self) -> dict:

@@ -169,7 +169,111 @@ int grid_for(int64_t n) {
   return (int)(g < cap ? (g > 0 ? g : 1) : cap);
 }
 
+// Expert-choice routing's logit gradient (see expert_choice.cu): warp per
+// token; lane holds experts lane + 32 j. A chosen (t, e) carries the gradient
+// at its gate, dg_row of its row e C + (rank of t among expert e's chosen
+// tokens: membership bitmap word prefix + popcount below t); dh = p (dp -
+// <p, dp>) (eq. (1); no auxiliary term). Writes dh, and for bf16 layers its
+// six exact part blocks and the dW_r split bounds as router_dh_kernel does.
+template <int EPT>
+__global__ void __launch_bounds__(256) router_dh_ec_kernel(const float *probs, const uint32_t *bm,
+                                                           const int32_t *bm_prefix, const float *dg_row, int T, int E,
+                                                           int Ce, float *dh, bf16 *a6, int EP, int32_t *offs2, int G) {
+  if (a6 && blockIdx.x == 0) {
+    if (threadIdx.x < 2) offs2[threadIdx.x] = threadIdx.x ? T : 0;
+    if (threadIdx.x <= G) {
+      const int64_t b = ((int64_t)threadIdx.x * T / G + 63) / 64 * 64;
+      offs2[2 + threadIdx.x] = (int32_t)(b < T ? b : T);
+    }
+  }
+  const int lane = threadIdx.x & 31;
+  const int W = (T + 31) / 32;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += (gridDim.x * blockDim.x) >> 5) {
+    const int w = t >> 5;
+    const uint32_t below = (1u << (t & 31)) - 1u;
+    float p[EPT], dp[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = lane + 32 * j;
+      p[j] = 0.0f;
+      dp[j] = 0.0f;
+      if (e < E) {
+        p[j] = probs[(int64_t)t * E + e];
+        const uint32_t word = bm[(int64_t)e * W + w];
+        if ((word >> (t & 31)) & 1u) dp[j] = dg_row[(int64_t)e * Ce + bm_prefix[(int64_t)e * W + w] + __popc(word & below)];
+      }
+    }
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) s = fmaf(p[j], dp[j], s);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = lane + 32 * j;
+      const float v = p[j] * (dp[j] - s);
+      if (e < E) dh[(int64_t)t * E + e] = v;
+      if (a6 && e < EP) {
+        const Parts3 q = split3(e < E ? v : 0.0f);
+        bf16 *row = a6 + (int64_t)t * 6 * EP + e;
+#pragma unroll
+        for (int b = 0; b < 6; ++b) row[b * EP] = q.h[kPartA[b]];
+      }
+    }
+  }
+}
+
 }  // namespace
+
+// dW_r = dh^T x and dX_r = dh W_r from the logit gradient (and, for bf16
+// layers, its part blocks and split bounds the logit-gradient kernel wrote).
+static cudaError_t router_grads_from_dh(const Shape &sh, const void *x, const float *w_r, const float *dh,
+                                        float *dw_r, float *dxr, void *ws, cudaStream_t stream) {
+  const bool tc = sh.dtype == MOE_BF16;
+  if (!tc) return router_weight_grads(sh, dh, x, w_r, dw_r, dxr, stream);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  const int EP = router_plan(sh).ep;
+  bf16 *a6 = reinterpret_cast<bf16 *>(w + L.rg_a6);
+  bf16 *b6 = reinterpret_cast<bf16 *>(w + L.rg_b6);
+  float *c3 = reinterpret_cast<float *>(w + L.rg_c3);
+  int32_t *offs2 = reinterpret_cast<int32_t *>(w + L.rg_offs);
+  const int G = router_grad_splits(sh);
+  cudaError_t err = launch_kernel(router_wsplit6_kernel, dim3(grid_for((int64_t)EP * sh.d)), dim3(256), 0, stream, w_r,
+                                  sh.E, EP, sh.d, b6);
+  if (err != cudaSuccess) return err;
+  err = tc_router_grads(sh, EP, a6, b6, x, offs2, offs2 + 2, G, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status),
+                        stream);
+  if (err != cudaSuccess) return err;
+  return launch_kernel(router_dwr_sum_kernel, dim3(grid_for((int64_t)sh.E * sh.d / 4)), dim3(256), 0, stream, c3, sh.E,
+                       EP, sh.d, G, dw_r);
+}
+
+cudaError_t launch_router_backward_ec(const Shape &sh, const void *x, const float *w_r, const float *probs,
+                                      const uint32_t *bm, const int32_t *bm_prefix, const float *dg_row, float *dh,
+                                      float *dw_r, float *dxr, void *ws, cudaStream_t stream) {
+  const bool tc = sh.dtype == MOE_BF16;
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  const int EP = router_plan(sh).ep;
+  bf16 *a6 = tc ? reinterpret_cast<bf16 *>(w + L.rg_a6) : nullptr;
+  int32_t *offs2 = reinterpret_cast<int32_t *>(w + L.rg_offs);
+  const int G = tc ? router_grad_splits(sh) : 0;
+  int grid = (sh.T + 7) / 8;
+  if (grid > sm_count() * 8) grid = sm_count() * 8;
+  const int Ce = (int)(sh.rows / sh.E);
+  cudaError_t err;
+#define MOE_DH_EC(EPT)                                                                                                  \
+  err = launch_kernel(router_dh_ec_kernel<EPT>, dim3(grid), dim3(256), 0, stream, probs, bm, bm_prefix, dg_row, sh.T, sh.E, \
+                      Ce, dh, a6, EP, offs2, G)
+  if (sh.E <= 32) MOE_DH_EC(1);
+  else if (sh.E <= 64) MOE_DH_EC(2);
+  else if (sh.E <= 128) MOE_DH_EC(4);
+  else MOE_DH_EC(8);
+#undef MOE_DH_EC
+  if (err != cudaSuccess) return err;
+  return router_grads_from_dh(sh, x, w_r, dh, dw_r, dxr, ws, stream);
+}
 
 cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *w_r, const float *probs,
                                    const int32_t *idx, const float *gate, const int32_t *load, const float *dg,
@@ -195,15 +299,9 @@ cudaError_t launch_router_backward(const Shape &sh, const void *x, const float *
   else MOE_DH(8);
 #undef MOE_DH
   if (err != cudaSuccess) return err;
-  if (!tc) return router_weight_grads(sh, dh, x, w_r, dw_r, dxr, stream);
-  err = launch_kernel(router_wsplit6_kernel, dim3(grid_for((int64_t)EP * sh.d)), dim3(256), 0, stream, w_r, sh.E, EP,
-                   sh.d, b6);
-  if (err != cudaSuccess) return err;
-  err = tc_router_grads(sh, EP, a6, b6, x, offs2, offs2 + 2, G, dxr, c3, reinterpret_cast<DeviceStatus *>(w + L.status),
-                        stream);
-  if (err != cudaSuccess) return err;
-  return launch_kernel(router_dwr_sum_kernel, dim3(grid_for((int64_t)sh.E * sh.d / 4)), dim3(256), 0, stream, c3, sh.E,
-                       EP, sh.d, G, dw_r);
+  (void)b6;
+  (void)c3;
+  return router_grads_from_dh(sh, x, w_r, dh, dw_r, dxr, ws, stream);
 }
 
 }  // namespace moe

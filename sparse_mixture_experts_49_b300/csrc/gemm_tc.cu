@@ -530,6 +530,16 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       const int mrow0 = mt * TM + half_row;  // this CTA's first row of the tile (group- or M-relative)
       float v[32], w[32];
+      bool released = false;  // the accumulator handed back to the MMA warp
+      auto release_acc = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (PAIR) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)acc);
+          else mbar_arrive(&s.acc_empty[acc]);
+        }
+        released = true;
+      };
       if (TMA_STORE) {
         // This warp's 32-row slice: whole slices go through the staging buffer
         // and a TMA store; a slice cut by the end of its group (grouped-M) is
@@ -547,19 +557,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         } else {
           r0 = mrow0 + q * 32;
         }
-#pragma unroll 1
-        for (int c = 4 * half; c < 4 * half + 4; c += CPB) {
+        // the warp's four 32-column pieces in flight together, then the
+        // accumulator goes back to the MMA warp before any store
+        uint32_t xr[4][32];
+        if (!zero && nvalid > 0) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_ld32_issue(t_row + (4 * half + u) * 32, xr[u]);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) tmem_wait32(xr[u]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) xr[u][i] = 0u;
+        }
+        release_acc();
+#pragma unroll
+        for (int cu = 0; cu < 4; cu += CPB) {
+          const int c = 4 * half + cu;
           const int col = nt * BN + c * 32;
           if (nvalid == 0 || col >= p.N) continue;
           float x[32 * CPB];
 #pragma unroll
-          for (int u = 0; u < CPB; ++u) {
-            if (!zero) tmem_ld32(t_row + (c + u) * 32, x + 32 * u);
-            else {
+          for (int u = 0; u < CPB; ++u)
 #pragma unroll
-              for (int i = 0; i < 32; ++i) x[32 * u + i] = 0.0f;
-            }
-          }
+            for (int i = 0; i < 32; ++i) x[32 * u + i] = __uint_as_float(xr[cu + u][i]);
           if (nvalid == 32) {
             if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
             __syncwarp();
@@ -869,12 +891,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (PAIR) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)acc);
-        else mbar_arrive(&s.acc_empty[acc]);
-      }
+      if (!released) release_acc();
       if (++acc == 2) { acc = 0; acc_phase ^= 1; }
     }
     if (STAGED && lane == 0) bulk_wait_all();  // stores complete before the CTA exits

@@ -16,6 +16,7 @@ struct Shape {
   int residual;   // add_residual
   int score;      // MOE_SCORE_*
   int reroute;    // No-Token-Left-Behind: k = 2 columns (first choice, second candidate)
+  int ec;         // expert-choice routing: rows = E * min(C, T), groups of min(C, T) rows
   int k_route;    // top_k of the config: the columns load and f count (1 with reroute)
   int64_t C;      // capacity, < 0 = none
   float alpha;
@@ -40,6 +41,8 @@ struct WsLayout {
   size_t router_parts;             // [3, EP, d] bf16: hi/mid/lo split of W_r (tensor-core router)
   size_t disp_counts, disp_base;   // [dispatch blocks, E]
   size_t disp_counts2, disp_base2, disp_kept1;  // rerouting's second round: [blocks, E], [blocks, E], [E]
+  size_t ec_bm, ec_prefix;         // expert choice: membership bitmap [E, W] u32 and word prefixes [E, W]
+  size_t ec_idx, ec_gate, ec_load, ec_aux, ec_dg;  // expert choice: the router's top-1 outputs (unused), dg per row
   size_t dyp, da, dxp;             // backward: [rows, d], [rows, R1], [rows, d]
   size_t dg, dh, dxr;              // backward: [T, k], [T, E], [T, d] fp32
   size_t rg_a6, rg_b6, rg_c3, rg_offs;  // bf16 router gradient: [T, 6EP], [6EP, d] bf16; [G, 3EP, d] fp32;
@@ -89,6 +92,24 @@ cudaError_t launch_dispatch_with_scratch(const Shape &sh, const void *x, const i
                                          DeviceStatus *st, cudaStream_t stream, const RerouteScratch *rr = nullptr);
 moe_status dispatch_shape(const moe_config *cfg, Shape *sh);
 moe_status report_cuda(cudaError_t e);
+
+// Expert-choice routing (expert_choice.cu); T <= kExpertChoiceMaxTokens.
+constexpr int kExpertChoiceMaxTokens = 32768;
+cudaError_t launch_ec_select(const Shape &sh, const float *probs, int32_t *row_token, float *row_gate,
+                             int32_t *expert_offsets, uint32_t *bm, int32_t *prefix, cudaStream_t stream);
+cudaError_t launch_ec_membership(const Shape &sh, const int32_t *row_token, uint32_t *bm, int32_t *prefix,
+                                 cudaStream_t stream);
+cudaError_t launch_ec_gather(const Shape &sh, const void *x, const int32_t *row_token, void *x_perm,
+                             cudaStream_t stream);
+cudaError_t launch_ec_combine(const Shape &sh, const void *x, const void *y_perm, const float *row_gate,
+                              const uint32_t *bm, const int32_t *prefix, void *out, cudaStream_t stream);
+cudaError_t launch_ec_combine_backward(const Shape &sh, const void *dy, const void *y_perm, const int32_t *row_token,
+                                       const float *row_gate, void *dyp, float *dg_row, cudaStream_t stream);
+cudaError_t launch_ec_unpermute(const Shape &sh, const void *dy, const void *dxp, const float *dxr, const uint32_t *bm,
+                                const int32_t *prefix, void *dx, cudaStream_t stream);
+cudaError_t launch_router_backward_ec(const Shape &sh, const void *x, const float *w_r, const float *probs,
+                                      const uint32_t *bm, const int32_t *bm_prefix, const float *dg_row, float *dh,
+                                      float *dw_r, float *dxr, void *ws, cudaStream_t stream);
 
 cudaError_t launch_combine(const Shape &sh, const void *x, const void *y_perm, const int32_t *idx,
                            const float *gate, const int32_t *slot, const int32_t *offsets, void *out,

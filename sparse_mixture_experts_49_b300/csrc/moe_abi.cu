@@ -36,6 +36,10 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
     return MOE_ERR_INVALID_ARG;
   if (c->score != MOE_SCORE_SOFTMAX && c->dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if ((c->reroute != 0 && c->reroute != 1) || !std::isfinite(c->aux_alpha)) return MOE_ERR_INVALID_ARG;
+  if ((c->expert_choice != 0 && c->expert_choice != 1) || c->reserved != 0) return MOE_ERR_INVALID_ARG;
+  if (c->expert_choice && (c->top_k != 1 || c->reroute || c->renormalize || c->score != MOE_SCORE_SOFTMAX ||
+                           c->capacity < 1 || c->T > kExpertChoiceMaxTokens))
+    return MOE_ERR_UNSUPPORTED;
   if (c->reroute && (c->top_k != 1 || c->n_experts < 2 || c->renormalize)) return MOE_ERR_UNSUPPORTED;
   if (c->top_k > c->n_experts) return MOE_ERR_INVALID_ARG;
   if (c->n_experts > 256 || c->top_k > 8) return MOE_ERR_UNSUPPORTED;
@@ -55,12 +59,14 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   sh->residual = c->add_residual;
   sh->score = c->score;
   sh->reroute = c->reroute;
+  sh->ec = c->expert_choice;
   sh->k_route = c->top_k;
   if (c->reroute) sh->k = 2;   // columns: first choice, second candidate
   sh->C = c->capacity < 0 ? -1 : c->capacity;
   sh->alpha = c->aux_alpha;
   int64_t rows = c->reroute ? (int64_t)c->T : Tk;   // rerouting keeps at most one assignment per token
   if (sh->C >= 0 && sh->C * sh->E < rows) rows = sh->C * sh->E;
+  if (c->expert_choice) rows = (int64_t)c->n_experts * (c->capacity < c->T ? c->capacity : c->T);
   sh->rows = rows;
   sh->elt = c->dtype == MOE_BF16 ? 2 : 4;
   return MOE_OK;
@@ -85,6 +91,14 @@ WsLayout ws_layout(const Shape &sh) {
   L.disp_counts2 = take(sh.reroute ? db * sh.E * 4 : 0);
   L.disp_base2 = take(sh.reroute ? db * sh.E * 4 : 0);
   L.disp_kept1 = take(sh.reroute ? (size_t)sh.E * 4 : 0);
+  const size_t ecw = sh.ec ? (size_t)sh.E * ((sh.T + 31) / 32) * 4 : 0;
+  L.ec_bm = take(ecw);
+  L.ec_prefix = take(ecw);
+  L.ec_idx = take(sh.ec ? (size_t)sh.T * 4 : 0);
+  L.ec_gate = take(sh.ec ? (size_t)sh.T * 4 : 0);
+  L.ec_load = take(sh.ec ? (size_t)sh.E * 4 : 0);
+  L.ec_aux = take(sh.ec ? 4 : 0);
+  L.ec_dg = take(sh.ec ? (size_t)sh.rows * 4 : 0);
   const size_t rows = (size_t)(sh.rows > 0 ? sh.rows : 1);
   L.dyp = take(rows * sh.d * sh.elt);
   L.da = take(rows * sh.R1 * sh.elt);
@@ -176,6 +190,7 @@ moe_status moe_router(const moe_config *cfg, const void *x, const float *w_r, co
   MOE_NVTX("moe_router");
   Shape sh;
   MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(!sh.ec, MOE_ERR_INVALID_ARG);   // expert-choice layers route with moe_router_expert_choice
   MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(topk_idx); MOE_PTR(topk_gate); MOE_PTR(importance); MOE_PTR(load);
   MOE_PTR(ws);
   MOE_OPT_PTR(logit_bias); MOE_OPT_PTR(probs); MOE_OPT_PTR(aux_loss);
@@ -309,6 +324,91 @@ moe_status moe_backward(const moe_config *cfg, const moe_saved *sv, const void *
                              dxr, ws, s);
   if (e != cudaSuccess) return cuda_status(e);
   return cuda_status(launch_unpermute(sh, dy, dxp, dxr, sv->topk_idx, sv->slot, sv->expert_offsets, dx, s));
+}
+
+moe_status moe_router_expert_choice(const moe_config *cfg, const void *x, const float *w_r, const float *logit_bias,
+                                    float *probs, int32_t *row_token, float *row_gate, int32_t *expert_offsets,
+                                    float *importance, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_router_expert_choice");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.ec, MOE_ERR_INVALID_ARG);
+  MOE_PTR(x); MOE_PTR(w_r); MOE_PTR(probs); MOE_PTR(row_token); MOE_PTR(row_gate); MOE_PTR(expert_offsets);
+  MOE_PTR(importance); MOE_PTR(ws);
+  MOE_OPT_PTR(logit_bias);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  cudaStream_t s = (cudaStream_t)stream;
+  // the softmax scores and their column sums; the top-1 choice the router also makes is not used
+  cudaError_t e = launch_router(sh, x, w_r, logit_bias, nullptr, probs, reinterpret_cast<int32_t *>(w + L.ec_idx),
+                                reinterpret_cast<float *>(w + L.ec_gate), importance,
+                                reinterpret_cast<int32_t *>(w + L.ec_load), reinterpret_cast<float *>(w + L.ec_aux), ws,
+                                s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_ec_select(sh, probs, row_token, row_gate, expert_offsets,
+                                      reinterpret_cast<uint32_t *>(w + L.ec_bm),
+                                      reinterpret_cast<int32_t *>(w + L.ec_prefix), s));
+}
+
+moe_status moe_dispatch_expert_choice(const moe_config *cfg, const void *x, const int32_t *row_token, void *x_perm,
+                                      moe_stream_t stream) {
+  MOE_NVTX("moe_dispatch_expert_choice");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.ec, MOE_ERR_INVALID_ARG);
+  MOE_PTR(x); MOE_PTR(row_token); MOE_PTR(x_perm);
+  return cuda_status(launch_ec_gather(sh, x, row_token, x_perm, (cudaStream_t)stream));
+}
+
+moe_status moe_combine_expert_choice(const moe_config *cfg, const void *x, const void *y_perm, const int32_t *row_token,
+                                     const float *row_gate, void *out, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_combine_expert_choice");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.ec, MOE_ERR_INVALID_ARG);
+  MOE_PTR(x); MOE_PTR(y_perm); MOE_PTR(row_token); MOE_PTR(row_gate); MOE_PTR(out); MOE_PTR(ws);
+  MOE_REQUIRE(out != x && out != y_perm, MOE_ERR_INVALID_ARG);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  uint32_t *bm = reinterpret_cast<uint32_t *>(w + L.ec_bm);
+  int32_t *prefix = reinterpret_cast<int32_t *>(w + L.ec_prefix);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_ec_membership(sh, row_token, bm, prefix, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_ec_combine(sh, x, y_perm, row_gate, bm, prefix, out, s));
+}
+
+moe_status moe_backward_expert_choice(const moe_config *cfg, const moe_saved_expert_choice *sv, const void *dy,
+                                      void *dx, float *dw_r, void *dw1, void *dw2, void *ws, moe_stream_t stream) {
+  MOE_NVTX("moe_backward_expert_choice");
+  Shape sh;
+  MOE_CHECK(make_shape(cfg, &sh));
+  MOE_REQUIRE(sh.ec && sv != nullptr, MOE_ERR_INVALID_ARG);
+  MOE_PTR(sv->x); MOE_PTR(sv->w_r); MOE_PTR(sv->w1); MOE_PTR(sv->w2); MOE_PTR(sv->probs); MOE_PTR(sv->row_token);
+  MOE_PTR(sv->row_gate); MOE_PTR(sv->expert_offsets); MOE_PTR(sv->x_perm); MOE_PTR(sv->h); MOE_PTR(sv->y_perm);
+  if (sh.act == MOE_ACT_SWIGLU) MOE_PTR(sv->pre_act);
+  MOE_PTR(dy); MOE_PTR(dx); MOE_PTR(dw_r); MOE_PTR(dw1); MOE_PTR(dw2); MOE_PTR(ws);
+  const WsLayout L = ws_layout(sh);
+  uint8_t *w = static_cast<uint8_t *>(ws);
+  void *dyp = w + L.dyp, *da = w + L.da, *dxp = w + L.dxp;
+  float *dh = reinterpret_cast<float *>(w + L.dh);
+  float *dxr = reinterpret_cast<float *>(w + L.dxr);
+  float *dg_row = reinterpret_cast<float *>(w + L.ec_dg);
+  uint32_t *bm = reinterpret_cast<uint32_t *>(w + L.ec_bm);
+  int32_t *prefix = reinterpret_cast<int32_t *>(w + L.ec_prefix);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = launch_ec_membership(sh, sv->row_token, bm, prefix, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_ec_combine_backward(sh, dy, sv->y_perm, sv->row_token, sv->row_gate, dyp, dg_row, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = sh.dtype == MOE_BF16 ? tc_expert_backward(sh, sv->expert_offsets, sv->x_perm, sv->w1, sv->w2, sv->pre_act,
+                                                sv->h, dyp, da, dxp, dw1, dw2, status_of(ws), s)
+                           : simt_expert_backward(sh, sv->expert_offsets, sv->x_perm, sv->w1, sv->w2, sv->pre_act,
+                                                  sv->h, dyp, da, dxp, dw1, dw2, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  e = launch_router_backward_ec(sh, sv->x, sv->w_r, sv->probs, bm, prefix, dg_row, dh, dw_r, dxr, ws, s);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(launch_ec_unpermute(sh, dy, dxp, dxr, bm, prefix, dx, s));
 }
 
 moe_status moe_backward_intermediates(const moe_config *cfg, void *ws, void **dyp, void **da, void **dxp,

@@ -353,7 +353,8 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float *w_r, int
 namespace rf {
 constexpr int BM = 128;        // tokens per CTA (TMEM lanes)
 constexpr int BK = 64;         // K per stage (one 128-byte swizzled row of bf16)
-constexpr int THREADS = 192;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-5 one token row per thread
+constexpr int EPI_WARPS = 16;  // 4 per TMEM lane quarter, each on a quarter of the CTA's columns
+constexpr int THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-17 epilogue
 constexpr int KMAX = 8;        // top-k candidates kept per row
 constexpr int SMAX = 4;        // CTAs per cluster (expert-column split)
 constexpr int MAX_STAGES = 8;
@@ -433,7 +434,6 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 // Named barrier of the four epilogue warps.
-__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -442,68 +442,84 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > 200000000ull) break;
 }
 
-// One token row's candidate list, kept by its thread in shared memory with
-// the rows interleaved (entry j of row r at j * BM + r, so a warp's accesses
-// fall in distinct banks): the k best selection keys, descending, and the
-// score of each.
-struct CandList {
-  unsigned long long *key;   // [KMAX][BM]
-  float *sc;                 // [KMAX][BM]
-  int r, k;
-  unsigned long long last;   // key[k - 1]: a new key enters only when it beats this
+// A thread's candidate list in registers: the KMAX best selection keys seen
+// so far, descending, with the score of each. Branch-free insertion (the
+// same compare-and-swap chain for every lane, whatever its keys), so that a
+// warp never splits on which of its rows took a new candidate.
+struct RegList {
+  unsigned long long c[KMAX];
+  float s[KMAX];
   __device__ __forceinline__ void clear() {
-    for (int j = 0; j < k; ++j) { key[j * BM + r] = 0ull; sc[j * BM + r] = 0.0f; }
-    last = 0ull;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) { c[j] = 0ull; s[j] = 0.0f; }
   }
-  __device__ __forceinline__ void offer(unsigned long long v, float vs) {
-    if (v <= last) return;
-    int j = k - 1;
-    while (j > 0 && key[(j - 1) * BM + r] < v) {
-      key[j * BM + r] = key[(j - 1) * BM + r];
-      sc[j * BM + r] = sc[(j - 1) * BM + r];
-      --j;
+  __device__ __forceinline__ void offer(unsigned long long v, float vs, int k) {
+    if (k == 1) {   // uniform over the kernel: the maximum alone
+      if (v > c[0]) { c[0] = v; s[0] = vs; }
+      return;
     }
-    key[j * BM + r] = v;
-    sc[j * BM + r] = vs;
-    last = key[(k - 1) * BM + r];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const bool gt = v > c[j];
+      const unsigned long long cj = c[j];
+      const float sj = s[j];
+      c[j] = gt ? v : cj;
+      s[j] = gt ? vs : sj;
+      v = gt ? cj : v;
+      vs = gt ? sj : vs;
+    }
   }
 };
 
-// This row's record (candidates, their scores, m, z) into slot [rank][r] of
-// every CTA of the cluster.
-__device__ __forceinline__ void send_record(Cand *recv, int rank, int S, const CandList &cl, float m, float z) {
-  const uint32_t mine = smem_u32(&recv[rank * BM + cl.r]);
+__device__ __forceinline__ void put_record(Cand &rc, const RegList &l, float m, float z) {
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) { rc.c[j] = l.c[j]; rc.sc[j] = l.s[j]; }
+  rc.m = m;
+  rc.z = z;
+}
+// This row's record into slot [rank][r] of every CTA of the cluster.
+__device__ __forceinline__ void send_record(Cand *recv, int rank, int r, int S, const RegList &l, float m, float z) {
+  const uint32_t mine = smem_u32(&recv[rank * BM + r]);
   for (int dst = 0; dst < S; ++dst) {
     const uint32_t ra = mapa_shared(mine, (uint32_t)dst);
+#pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      st_cluster_u64(ra + 8u * j, j < cl.k ? cl.key[j * BM + cl.r] : 0ull);
-      st_cluster_f32(ra + 8u * KMAX + 4u * j, j < cl.k ? cl.sc[j * BM + cl.r] : 0.0f);
+      st_cluster_u64(ra + 8u * j, l.c[j]);
+      st_cluster_f32(ra + 8u * KMAX + 4u * j, l.s[j]);
     }
     st_cluster_f32(ra + 12u * KMAX, m);
     st_cluster_f32(ra + 12u * KMAX + 4u, z);
   }
 }
-// The k best of the S sorted lists of row r into cl (distinct experts: no
-// equal keys); heads holds each list's next position, 8 bits per list.
-__device__ __forceinline__ void merge_records(const Cand *recv, int S, CandList &cl) {
-  uint32_t heads = 0;
-  for (int j = 0; j < cl.k; ++j) {
+// The k best of n sorted records recs[i * stride] (distinct experts: no equal
+// keys) into l, and the softmax statistics they combine to: M = max m,
+// Z = sum z exp(m - M) in record order.
+__device__ __forceinline__ void merge_records(const Cand *recs, int stride, int n, int k, RegList &l, float &M,
+                                              float &Z) {
+  M = -FLT_MAX;
+  for (int i = 0; i < n; ++i) M = fmaxf(M, recs[i * stride].m);
+  Z = 0.0f;
+  for (int i = 0; i < n; ++i) Z += recs[i * stride].z * expf(recs[i * stride].m - M);
+  uint32_t heads = 0;   // each list's next position, 8 bits per list
+#pragma unroll
+  for (int j = 0; j < KMAX; ++j) {
     unsigned long long best = 0ull;
     float bs = 0.0f;
     int from = 0;
-    for (int s = 0; s < S; ++s) {
-      const int hd = (int)((heads >> (8 * s)) & 0xFFu);
-      if (hd < cl.k) {
-        const unsigned long long v = recv[s * BM + cl.r].c[hd];
-        if (v > best) { best = v; bs = recv[s * BM + cl.r].sc[hd]; from = s; }
+    for (int i = 0; i < n; ++i) {
+      const int hd = (int)((heads >> (8 * i)) & 0xFFu);
+      if (j < k && hd < k) {
+        const unsigned long long v = recs[i * stride].c[hd];
+        if (v > best) { best = v; bs = recs[i * stride].sc[hd]; from = i; }
       }
     }
-    cl.key[j * BM + cl.r] = best;
-    cl.sc[j * BM + cl.r] = bs;
+    l.c[j] = best;
+    l.s[j] = bs;
     heads += 1u << (8 * from);
   }
-  cl.last = cl.key[(cl.k - 1) * BM + cl.r];
 }
+// Named barrier of the sixteen epilogue warps.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory"); }
 
 // Logits, scores, top-k and statistics of 128 tokens, with the experts'
 // columns split over the S CTAs of a cluster (NC = EP / S each).
@@ -538,12 +554,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   Bars &b = *reinterpret_cast<Bars *>(reinterpret_cast<uint8_t *>(recv) + recv_bytes(S));
   volatile int *abort_flag = &b.abort_flag;
   // Used only after this CTA's MMAs have completed, in the then idle ring:
-  float *stage_out = reinterpret_cast<float *>(tiles);                       // [4 warps][32 rows][32]
-  float *imp_w = stage_out + 4 * 32 * 32;                                    // [4 row quarters][NC]
+  Cand *part_rec = reinterpret_cast<Cand *>(tiles);                          // [4 column parts][BM]
+  float *stage_out = reinterpret_cast<float *>(part_rec + 4 * BM);           // [16 warps][32 rows][32]
+  float *imp_w = stage_out + EPI_WARPS * 32 * 32;                            // [4 row quarters][NC]
   int *cnt = reinterpret_cast<int *>(imp_w + 4 * NC);                        // [EP]
   float *term = reinterpret_cast<float *>(cnt + 256);                        // [256]
-  unsigned long long *cand_key = reinterpret_cast<unsigned long long *>(term + 256);   // [KMAX][BM]
-  float *cand_sc = reinterpret_cast<float *>(cand_key + KMAX * BM);                      // [KMAX][BM]
+  float2 *fin = reinterpret_cast<float2 *>(term + 256);                      // [BM] the rows' M and Z
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = S > 1 ? (int)cluster_ctarank() : 0;
@@ -630,96 +646,112 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < cluster_syncs; ++i) cluster_sync_all();
   } else {
+    // Warp w reads TMEM lane quarter q = w % 4 (rows 32 q .. 32 q + 31, one
+    // per lane) and column part pp of the CTA's NC columns (CP wide).
+    constexpr int CP = NC / 4;
+    constexpr int SC = CP < 32 ? CP : 32;   // staging width of pass 3
     const int q = warp & 3;
+    const int pp = (warp - 2) >> 2;
     const int r = q * 32 + lane;
     const int t = m0 + r;
     const bool live = t < a.T;
-    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(pp * CP);
+    const int ecol0 = col0 + pp * CP;       // this thread's first expert
     const float *bias = a.bias, *sel_bias = a.sel_bias;
     float m = -FLT_MAX, z = 0.0f;
-    CandList cl{cand_key, cand_sc, r, k, 0ull};
+    RegList cl;
+    cl.clear();
     // warp-uniform: the TMEM loads below are warp-collective
     const bool acc_ok =
         __all_sync(0xffffffffu, mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st) ? 1 : 0) != 0;
     float v[8];
-    // (the ring is idle once this CTA's MMAs have completed: the lists live there)
-    cl.clear();
     if (acc_ok) {
       tc_fence_after();
       // pass 1: the maximum (softmax) and the candidates that need no global statistics
       if (softmax) {
 #pragma unroll 1
-        for (int c = 0; c < NC / 8; ++c) {
+        for (int c = 0; c < CP / 8; ++c) {
           tmem_ld8(t_row + c * 8, v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int e = col0 + c * 8 + i;
+            const int e = ecol0 + c * 8 + i;
             if (e < E) {
               const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
               m = fmaxf(m, h);
-              if (!late_choice) cl.offer(pack_cand(h, e), 0.0f);
+              if (!late_choice) cl.offer(pack_cand(h, e), 0.0f, k);
             }
           }
         }
         // pass 2: sum of exp(h - m)
 #pragma unroll 1
-        for (int c = 0; c < NC / 8; ++c) {
+        for (int c = 0; c < CP / 8; ++c) {
           tmem_ld8(t_row + c * 8, v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int e = col0 + c * 8 + i;
+            const int e = ecol0 + c * 8 + i;
             if (e < E) z += expf(v[i] + (bias ? __ldg(bias + e) : 0.0f) - m);
           }
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < NC / 8; ++c) {
+        for (int c = 0; c < CP / 8; ++c) {
           tmem_ld8(t_row + c * 8, v);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int e = col0 + c * 8 + i;
+            const int e = ecol0 + c * 8 + i;
             if (e < E) {
               const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
               const float sv = elem_score(h, a.score);
-              cl.offer(pack_cand(sel_bias ? sv + __ldg(sel_bias + e) : h, e), sv);
+              cl.offer(pack_cand(sel_bias ? sv + __ldg(sel_bias + e) : h, e), sv, k);
             }
           }
         }
       }
     }
-    float M = m, Z = z;
-    if (S > 1) {
-      send_record(recv, rank, S, cl, m, z);
-      cluster_sync_all();   // every CTA's records are in
-      if (softmax) {
-        M = -FLT_MAX;
-        for (int s = 0; s < S; ++s) M = fmaxf(M, recv[s * BM + r].m);
-        Z = 0.0f;
-        for (int s = 0; s < S; ++s) Z += recv[s * BM + r].z * expf(recv[s * BM + r].m - M);
-      }
-      if (!late_choice) merge_records(recv, S, cl);
+    // merge the four column parts of each row (warps of part 0, one thread per row), then the cluster's CTAs
+    put_record(part_rec[pp * BM + r], cl, m, z);
+    epi_sync();
+    float M = -FLT_MAX, Z = 0.0f;
+    if (pp == 0) {
+      merge_records(part_rec + r, BM, 4, k, cl, M, Z);
+      if (S > 1) send_record(recv, rank, r, S, cl, M, Z);
     }
-    for (int e = threadIdx.x - 64; e < a.EP; e += 128) cnt[e] = 0;
-    epilogue_sync();
-    // pass 3: the scores of this CTA's columns; per 32 x 32 block, each lane
-    // writes its row into the warp's 128-byte swizzled staging rows (8
-    // columns at a time), then lane j takes column j row by row: one
-    // coalesced 128-byte store per row and the column's sum over the block's
-    // live rows.
+    if (S > 1) {
+      cluster_sync_all();   // every CTA's records are in
+      if (pp == 0) {
+        RegList ml;
+        float M2, Z2;
+        merge_records(recv + r, BM, S, k, ml, M2, Z2);
+        if (!late_choice) cl = ml;
+        M = M2;
+        Z = Z2;
+      }
+    }
+    if (pp == 0) fin[r] = make_float2(M, Z);
+    for (int e = threadIdx.x - 64; e < a.EP; e += 32 * EPI_WARPS) cnt[e] = 0;
+    epi_sync();
+    M = fin[r].x;
+    Z = fin[r].y;
+    if (late_choice) cl.clear();
+    // pass 3: the scores of this thread's columns; per 32 x SC block, each
+    // lane writes its row into the warp's 128-byte swizzled staging rows (8
+    // columns at a time), then lane j < SC takes column j row by row: one
+    // coalesced store of the block's row piece per row, and the column's sum
+    // over the block's live rows.
     float *stg = stage_out + (warp - 2) * 32 * 32;
 #pragma unroll 1
-    for (int c = 0; c < NC / 32; ++c) {
+    for (int c = 0; c < CP / SC; ++c) {
 #pragma unroll 1
-      for (int sub = 0; sub < 4; ++sub) {
-        if (acc_ok) tmem_ld8(t_row + c * 32 + sub * 8, v);
+      for (int sub = 0; sub < SC / 8; ++sub) {
+        if (acc_ok) tmem_ld8(t_row + c * SC + sub * 8, v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int e = col0 + c * 32 + sub * 8 + i;
+          const int e = ecol0 + c * SC + sub * 8 + i;
           float sv = 0.0f;
           if (acc_ok && live && e < E) {
             const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
             sv = softmax ? prob_of(h, M, Z) : elem_score(h, a.score);
-            if (late_choice) cl.offer(pack_cand(sv + __ldg(sel_bias + e), e), sv);
+            if (late_choice) cl.offer(pack_cand(sv + __ldg(sel_bias + e), e), sv, k);
           }
           v[i] = sv;
         }
@@ -729,48 +761,68 @@ __global__ void __launch_bounds__(THREADS, 1)
             make_float4(v[4], v[5], v[6], v[7]);
       }
       __syncwarp();
-      const int e = col0 + c * 32 + lane;
-      float colsum = 0.0f;
+      if (lane < SC) {
+        const int e = ecol0 + c * SC + lane;
+        float colsum = 0.0f;
 #pragma unroll 4
-      for (int rr = 0; rr < 32; ++rr) {
-        const float pv = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-        const int tt = m0 + q * 32 + rr;
-        if (tt < a.T) {
-          colsum += pv;
-          if (a.probs && e < E) a.probs[(int64_t)tt * E + e] = pv;
+        for (int rr = 0; rr < 32; ++rr) {
+          const float pv = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
+          const int tt = m0 + q * 32 + rr;
+          if (tt < a.T) {
+            colsum += pv;
+            if (a.probs && e < E) a.probs[(int64_t)tt * E + e] = pv;
+          }
         }
+        imp_w[q * NC + pp * CP + c * SC + lane] = colsum;
       }
-      imp_w[q * NC + c * 32 + lane] = colsum;
       __syncwarp();
     }
-    if (late_choice && S > 1) {
-      cluster_sync_all();   // every CTA has read the first records
-      send_record(recv, rank, S, cl, M, Z);
-      cluster_sync_all();   // the second records are in
-      merge_records(recv, S, cl);
+    if (late_choice) {
+      // softmax scores with a correction bias: the candidates by p + b, merged over the parts and the cluster
+      epi_sync();   // every part's first records have been read
+      put_record(part_rec[pp * BM + r], cl, M, Z);
+      epi_sync();
+      if (pp == 0) {
+        float Mx, Zx;
+        merge_records(part_rec + r, BM, 4, k, cl, Mx, Zx);
+      }
+      if (S > 1) {
+        cluster_sync_all();   // every CTA has read the first records
+        if (pp == 0) send_record(recv, rank, r, S, cl, M, Z);
+        cluster_sync_all();   // the second records are in
+        if (pp == 0) {
+          float Mx, Zx;
+          merge_records(recv + r, BM, S, k, cl, Mx, Zx);
+        }
+      }
     }
     // the row's experts and gates
-    if (acc_ok && live && (r % S) == rank) {
+    if (pp == 0 && acc_ok && live && (r % S) == rank) {
+      float gv[KMAX];
       float psum = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        // softmax scores chosen by logit: p from the logit the key carries
-        const float g = (softmax && !late_choice) ? prob_of(cand_key_value(cl.key[j * BM + r]), M, Z)
-                                                  : cl.sc[j * BM + r];
-        cl.sc[j * BM + r] = g;
-        psum += g;
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        gv[j] = 0.0f;
+        if (j < k) {
+          // softmax scores chosen by logit: p from the logit the key carries
+          gv[j] = (softmax && !late_choice) ? prob_of(cand_key_value(cl.c[j]), M, Z) : cl.s[j];
+          psum += gv[j];
+        }
       }
-      for (int j = 0; j < k; ++j) {
-        const int e = cand_expert(cl.key[j * BM + r]);
-        const float g = cl.sc[j * BM + r];
-        a.idx[(int64_t)t * k + j] = e;
-        a.gate[(int64_t)t * k + j] = a.renorm ? g / psum : g;
-        if (j < a.k_route) atomicAdd(&cnt[e], 1);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          const int e = cand_expert(cl.c[j]);
+          a.idx[(int64_t)t * k + j] = e;
+          a.gate[(int64_t)t * k + j] = a.renorm ? gv[j] / psum : gv[j];
+          if (j < a.k_route) atomicAdd(&cnt[e], 1);
+        }
       }
     }
-    epilogue_sync();
+    epi_sync();
     // this CTA's per-expert sums: importance over its 128 rows (row quarters
     // in a fixed order) and loads, added as integers into the accumulators
-    for (int c = threadIdx.x - 64; c < NC; c += 128) {
+    for (int c = threadIdx.x - 64; c < NC; c += 32 * EPI_WARPS) {
       const int e = col0 + c;
       if (e < E) {
         const float sm = imp_w[c] + imp_w[NC + c] + imp_w[2 * NC + c] + imp_w[3 * NC + c];
@@ -780,7 +832,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (qv) atomicAdd(a.acc_imp + e, qv);
       }
     }
-    for (int e = threadIdx.x - 64; e < E; e += 128)
+    for (int e = threadIdx.x - 64; e < E; e += 32 * EPI_WARPS)
       if (cnt[e]) atomicAdd(a.acc_load + e, cnt[e]);
     tc_fence_before();   // this warp's TMEM loads are ordered before the release below
   }
@@ -841,9 +893,16 @@ cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStre
   return launch_kernel(router_simt_kernel<XT, EPT>, dim3(nblk), dim3(256), smem, stream, a, so);
 }
 
+// Shared memory the epilogue uses inside the idle ring: four column parts' records, sixteen warps' staging
+// blocks, the per-expert sums and counts, the aux tree and the rows' M and Z.
+template <int NC> constexpr size_t epilogue_ring_bytes() {
+  return 4 * rf::BM * sizeof(rf::Cand) + rf::EPI_WARPS * 32 * 32 * 4 + 4 * NC * 4 + 256 * 4 + 256 * 4 + rf::BM * 8;
+}
+
 template <int NC>
 cudaError_t run_fused(const CUtensorMap &mx, const CUtensorMap &mw, const rf::Args &ra, int m_tiles,
                       cudaStream_t stream) {
+  if ((size_t)ra.stages * rf::Geo<NC>::STAGE_BYTES < epilogue_ring_bytes<NC>()) return cudaErrorInvalidConfiguration;
   static cudaError_t attr = set_smem(rf::router_fused_kernel<NC>, rf::SMEM_LIMIT);
   if (attr != cudaSuccess) return attr;
   const size_t smem = rf::smem_bytes<NC>(ra.S, ra.stages);

@@ -76,7 +76,7 @@ def run_gpu(w, inp, backward=False, topk_idx=None, layer=None, fused=False, sele
     if backward:
         dy = to_dev(torch, inp["dy"], dt)
         dx, dw_r, dw1, dw2 = layer.backward(dy)
-        dg, dh = backward_intermediates(torch, moe, cfg, layer, w.T, w.k, w.E)
+        dg, dh = backward_intermediates(torch, moe, cfg, layer, w.T, 2 if w.reroute else w.k, w.E)
         res.update(dx=np64(dx), dw_r=np64(dw_r), dw1=np64(dw1), dw2=np64(dw2), dg=dg, dh=dh)
     torch.cuda.synchronize()
     res.update(out=np64(layer.out), probs=np64(layer.probs), idx=np64(layer.topk_idx), gate=np64(layer.topk_gate),

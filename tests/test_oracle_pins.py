@@ -544,3 +544,79 @@ def test_gradients_finite_differences_reroute():
                      zipf_s=1.2, backward=True)
     checked, skipped = _fd_check(w, n_coords=30, reroute=True)
     assert checked >= 100 and skipped <= checked // 10
+
+
+# ------------------------------------------------------------------ expert-choice routing
+def test_expert_choice_brute_force_choice_and_dense_sum():
+    """Each expert's chosen tokens by brute-force rank counting over its score column (ties to the lower
+    token: a tie planted on purpose), and the layer equal to x plus a dense evaluation of every expert
+    masked to the pairs chosen."""
+    w = syn.Workload("ec-pin", T=20, d=6, E=4, k=1, F=5, act="relu", dtype="f32", cf=None, router_std=0.6)
+    inp = syn.make_inputs(w)
+    x = inp["x"].astype(np.float64)
+    w_r = inp["w_r"].astype(np.float64)
+    w_r[3] = w_r[2]                                   # experts 2 and 3 score every token alike
+    C = 7
+    f = O.forward_expert_choice(x, w_r, None, (inp["w1"], inp["w2"]), C=C, act="relu")
+    p = scipy.special.softmax(x @ w_r.T, axis=1)
+    for e in range(w.E):
+        beats = lambda a, b: p[a, e] > p[b, e] or (p[a, e] == p[b, e] and a < b)
+        top = sorted(t for t in range(w.T) if sum(beats(u, t) for u in range(w.T) if u != t) < C)
+        assert f["chosen"][e].tolist() == top
+    assert f["chosen"][2].tolist() == f["chosen"][3].tolist()
+    ref = x.copy()
+    for t in range(w.T):
+        for e in range(w.E):
+            if t in f["chosen"][e]:
+                y = _ffn_loops(x[t:t + 1], inp["w1"][e].astype(np.float64), inp["w2"][e].astype(np.float64), "relu")
+                ref[t] += p[t, e] * y[0]
+    np.testing.assert_allclose(f["out"], ref, rtol=1e-12, atol=1e-13)
+    assert np.all(f["load"] == C) and f["offsets"][-1] == w.E * C
+
+
+def test_expert_choice_capacity_above_tokens_takes_every_token():
+    """C >= T: every expert takes every token, so out = x + sum over all experts of p E(x) (the dense mixture)."""
+    rng = np.random.default_rng(17)
+    T, d, E, F = 6, 4, 3, 5
+    x, w_r = rng.standard_normal((T, d)), rng.standard_normal((E, d))
+    w1, w2 = rng.standard_normal((E, F, d)), rng.standard_normal((E, d, F))
+    f = O.forward_expert_choice(x, w_r, None, (w1, w2), C=10, act="relu")
+    p = scipy.special.softmax(x @ w_r.T, axis=1)
+    ref = x + sum(p[:, e:e + 1] * _ffn_loops(x, w1[e], w2[e], "relu") for e in range(E))
+    np.testing.assert_allclose(f["out"], ref, rtol=1e-12, atol=1e-13)
+
+
+def test_expert_choice_gradients_finite_differences():
+    w = syn.Workload("fd-ec", T=30, d=8, E=5, k=1, F=6, act="swiglu", dtype="f32", cf=None, router_std=0.5,
+                     backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    x, w_r = inp["x"].astype(np.float64), inp["w_r"].astype(np.float64)
+    w1, w2, dy = inp["w1"].astype(np.float64), inp["w2"].astype(np.float64), inp["dy"].astype(np.float64)
+    C = 9
+    g = O.backward_expert_choice(x, w_r, None, (w1, w2), dy, C=C, act="swiglu")
+    base = O.route_expert_choice(x, w_r, None, C)["chosen"]
+
+    def L(xx, wr, a1, a2):
+        f = O.forward_expert_choice(xx, wr, None, (a1, a2), C=C, act="swiglu")
+        return float(np.sum(dy * f["out"])), np.array_equal(f["chosen"], base)
+
+    grads = {"x": g["dx"], "w_r": g["dw_r"], "w1": np.stack([g["dw1"][e] for e in range(w.E)]),
+             "w2": np.stack([g["dw2"][e] for e in range(w.E)])}
+    params = {"x": x, "w_r": w_r, "w1": w1, "w2": w2}
+    rng = np.random.default_rng(2)
+    eps, checked, skipped = 1e-4, 0, 0
+    for name, arr in params.items():
+        for _ in range(25):
+            v = np.zeros(arr.shape)
+            v[tuple(rng.integers(0, s) for s in arr.shape)] = 1.0
+            pp, mm = dict(params), dict(params)
+            pp[name], mm[name] = arr + eps * v, arr - eps * v
+            lp, sp = L(pp["x"], pp["w_r"], pp["w1"], pp["w2"])
+            lm, sm = L(mm["x"], mm["w_r"], mm["w1"], mm["w2"])
+            if not (sp and sm):
+                skipped += 1
+                continue
+            an = float(np.sum(grads[name] * v))
+            assert abs((lp - lm) / (2 * eps) - an) <= 1e-6 * max(1e-3, abs(an)), name
+            checked += 1
+    assert checked >= 80 and skipped <= checked // 10

@@ -500,3 +500,46 @@ def test_reroute_second_choice(T, cf):
     fused = run_gpu(w, inp, fused=True)
     check_routing(fused, f, w)
     assert_close(fused["out"], f["out"], TOL_BF16, "out (moe_forward)")
+
+
+# ------------------------------------------------------------------ expert-choice routing
+@pytest.mark.parametrize("T,E,C,act,dtype", [(1000, 16, 160, "swiglu", "bf16"), (700, 24, 50, "relu", "bf16"),
+                                              (300, 8, 400, "relu", "bf16"), (512, 8, 96, "relu", "f32")])
+def test_expert_choice(T, E, C, act, dtype):
+    """Expert-choice routing ([Wiki] "Mixture-of-Experts", section 横断的知見): each expert's chosen tokens
+    (its rows, in token order) bit-exact against the oracle, the gates and probabilities within the router's
+    tolerance, the layer output and every gradient within the layer's; C above T takes every token. The
+    inputs keep each expert's C-th and (C+1)-th scores at least 5e-5 apart (relative), far above fp32 error."""
+    import sparse_mixture_experts_49_b300 as moe
+    w = syn.Workload(f"ec-{T}-{E}-{C}", T=T, d=256 if dtype == "bf16" else 64, E=E, k=1, F=192 if dtype == "bf16" else 128,
+                     act=act, dtype=dtype, cf=None, router_std=1 / 16 if dtype == "bf16" else None, backward=True)
+    inp = syn.make_inputs(w, dy=True)
+    cfg = moe.make_config(T=w.T, d_model=w.d, n_experts=w.E, top_k=1, d_ff=w.F, act=act, dtype=dtype, capacity=C,
+                          expert_choice=True)
+    L = moe.MoELayer(cfg)
+    dt = L.dt
+    from moe_cases import to_dev
+    x, w_r = to_dev(torch, inp["x"], dt), to_dev(torch, inp["w_r"], torch.float32)
+    w1, w2, dy = to_dev(torch, inp["w1"], dt), to_dev(torch, inp["w2"], dt), to_dev(torch, inp["dy"], dt)
+    out = L.forward(x, w_r, w1, w2)
+    dx, dw_r, dw1, dw2 = L.backward(dy)
+    torch.cuda.synchronize()
+    assert L.device_error() == 0
+    f = O.forward_expert_choice(inp["x"], inp["w_r"], None, (inp["w1"], inp["w2"]), C=C, act=act)
+    b = O.backward_expert_choice(inp["x"], inp["w_r"], None, (inp["w1"], inp["w2"]), inp["dy"], C=C, act=act)
+    Ce = min(C, T)
+    rows = E * Ce
+    assert np.array_equal(np64(L.row_token[:rows]), f["row_token"])
+    assert np.array_equal(np64(L.offsets), f["offsets"])
+    tol_r = TOL_F32 if dtype == "f32" else TOL_ROUTER_BF16
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    assert_close(np64(L.probs), f["p"], tol_r, "probs")
+    assert_close(np64(L.row_gate[:rows]), f["gate"].reshape(-1), tol_r, "row gates")
+    assert_close(np64(L.importance), f["importance"], tol_r, "importance")
+    assert_close(np64(out), f["out"], tol, "out")
+    assert_close(np64(dx), b["dx"], tol, "dx")
+    assert_close(np64(dw_r), b["dw_r"], tol, "dw_r")
+    assert_close(np64(dw1), np.stack([b["dw1"][e] for e in range(E)]), tol, "dw1")
+    assert_close(np64(dw2), np.stack([b["dw2"][e] for e in range(E)]), tol, "dw2")
+    _, dh = backward_intermediates(torch, moe, cfg, L, T, 1, E)
+    assert_close(dh, b["dh"], tol, "dh")
