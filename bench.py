@@ -257,8 +257,12 @@ def _drv_ok(res):
 def replay_kernels_alone(step, stream, flush, reps: int):
     """Captures `step` into a CUDA graph, then launches each of its kernel nodes alone (a one-node graph with
     the node's parameters and launch attributes), `reps` times, each after an L2 flush, between two CUDA
-    events on `stream`. Returns [(mangled name, mean ms)] in launch order. Every library kernel overwrites
-    its outputs from its inputs, so replaying one kernel of the step alone repeats the same work."""
+    events on `stream`. Kernel nodes that the step could run side by side (consecutive in launch order, with
+    no path between them in the graph, as when a call forks onto a second stream) form a group, and each group
+    of two or more is also replayed as one graph of those nodes alone, side by side. Returns
+    ([(mangled name, mean ms, group)] in launch order, {group: mean ms of the group replayed together}).
+    Every library kernel overwrites its outputs from its inputs, so replaying kernels of the step alone
+    repeats the same work."""
     import torch
     from cuda.bindings import driver as drv
     g = torch.cuda.CUDAGraph(keep_graph=True)
@@ -279,31 +283,25 @@ def replay_kernels_alone(step, stream, flush, reps: int):
             return []
         return next(v for v in _drv_ok(fn(*head, n)) if isinstance(v, (list, tuple)))
 
-    order, frontier, seen = [], list(listing(drv.cuGraphGetRootNodes, graph)), set()
-    while frontier:                              # stream capture of one stream: a chain
-        node = frontier.pop(0)
-        key = int(node)
-        if key in seen:
-            continue
-        seen.add(key)
-        order.append(node)
-        frontier.extend(listing(drv.cuGraphNodeGetDependentNodes, node))
-    if len(order) != len(listing(drv.cuGraphGetNodes, graph)):
-        raise RuntimeError("the captured step graph is not one chain of nodes")
+    nodes = list(listing(drv.cuGraphGetNodes, graph))
+    by_key = {int(n): n for n in nodes}
+    pos = {int(n): i for i, n in enumerate(nodes)}          # creation order
+    deps = {int(n): [int(d) for d in listing(drv.cuGraphNodeGetDependencies, n)] for n in nodes}
+    order = topological_order(deps, pos)
+    anc = {}
+    for k in order:
+        anc[k] = set(deps[k]).union(*(anc[d] for d in deps[k])) if deps[k] else set()
+    kern = [k for k in order
+            if _drv_ok(drv.cuGraphNodeGetType(by_key[k]))[0] == drv.CUgraphNodeType.CU_GRAPH_NODE_TYPE_KERNEL]
+    group_of = concurrent_groups(kern, anc)
     s_handle = drv.CUstream(stream.cuda_stream)
-    out = []
-    for node in order:
-        if _drv_ok(drv.cuGraphNodeGetType(node))[0] != drv.CUgraphNodeType.CU_GRAPH_NODE_TYPE_KERNEL:
-            continue
-        params = _drv_ok(drv.cuGraphKernelNodeGetParams(node))[0]
-        func = params.func
-        if not int(func):
-            func = _drv_ok(drv.cuKernelGetFunction(params.kern))[0]
-        name = _drv_ok(drv.cuFuncGetName(func))[0]
-        name = name.decode() if isinstance(name, bytes) else str(name)
+
+    def time_nodes(members):
         g1 = _drv_ok(drv.cuGraphCreate(0))[0]
-        n1 = _drv_ok(drv.cuGraphAddKernelNode(g1, None, 0, params))[0]
-        _drv_ok(drv.cuGraphKernelNodeCopyAttributes(n1, node))
+        for k in members:
+            params = _drv_ok(drv.cuGraphKernelNodeGetParams(by_key[k]))[0]
+            n1 = _drv_ok(drv.cuGraphAddKernelNode(g1, None, 0, params))[0]
+            _drv_ok(drv.cuGraphKernelNodeCopyAttributes(n1, by_key[k]))
         ex = _drv_ok(drv.cuGraphInstantiate(g1, 0))[0]
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
         for _ in range(2):                       # warm-up launches
@@ -314,11 +312,63 @@ def replay_kernels_alone(step, stream, flush, reps: int):
             _drv_ok(drv.cuGraphLaunch(ex, s_handle))
             b.record(stream)
         torch.cuda.synchronize()
-        out.append((name, statistics.mean(a.elapsed_time(b) for a, b in evs)))
         _drv_ok(drv.cuGraphExecDestroy(ex))
         _drv_ok(drv.cuGraphDestroy(g1))
+        return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+    out = []
+    for k in kern:
+        params = _drv_ok(drv.cuGraphKernelNodeGetParams(by_key[k]))[0]
+        func = params.func
+        if not int(func):
+            func = _drv_ok(drv.cuKernelGetFunction(params.kern))[0]
+        name = _drv_ok(drv.cuFuncGetName(func))[0]
+        name = name.decode() if isinstance(name, bytes) else str(name)
+        out.append((name, time_nodes([k]), group_of[k]))
+    groups = {}
+    for gid in sorted(set(group_of.values())):
+        members = [k for k in kern if group_of[k] == gid]
+        if len(members) > 1:
+            groups[gid] = time_nodes(members)
     del g
-    return out
+    return out, groups
+
+
+def topological_order(deps, pos):
+    """Node keys in an order that puts every node after its dependencies, ready nodes taken in creation order
+    (`pos`); raises on a cycle."""
+    indeg = {k: len(v) for k, v in deps.items()}
+    children = {k: [] for k in deps}
+    for k, ds in deps.items():
+        for d in ds:
+            children[d].append(k)
+    ready = sorted((k for k, n in indeg.items() if n == 0), key=pos.get)
+    order = []
+    while ready:
+        k = ready.pop(0)
+        order.append(k)
+        for c in children[k]:
+            indeg[c] -= 1
+            if indeg[c] == 0:
+                ready.append(c)
+        ready.sort(key=pos.get)
+    if len(order) != len(deps):
+        raise RuntimeError("the captured step graph has a cycle")
+    return order
+
+
+def concurrent_groups(kern, anc):
+    """Group ids of kernel nodes (in launch order): a node joins the current group when no node of it is an
+    ancestor or a descendant of the node (they can run side by side), else it opens the next group."""
+    group_of, cur, gid = {}, [], 0
+    for k in kern:
+        if cur and all(c not in anc[k] and k not in anc[c] for c in cur):
+            cur.append(k)
+        else:
+            gid += 1 if cur else 0
+            cur = [k]
+        group_of[k] = gid
+    return group_of
 
 
 # ---------------------------------------------------------------- inputs on the device
@@ -458,10 +508,10 @@ def run_ours(args):
 
     # per-kernel launch times: each kernel node of the timed step replayed alone
     try:
-        launches = replay_kernels_alone(timed_step, stream, flush, reps=max(3, min(args.steps, 20)))
+        launches, group_ms = replay_kernels_alone(timed_step, stream, flush, reps=max(3, min(args.steps, 20)))
         launch_error = None
     except Exception as exc:
-        launches, launch_error = [], f"{type(exc).__name__}: {exc}"[:300]
+        launches, group_ms, launch_error = [], {}, f"{type(exc).__name__}: {exc}"[:300]
 
     # the timed steps: the whole step captured once in a CUDA graph, replayed
     graph = capture(timed_step)
@@ -570,30 +620,48 @@ def run_ours(args):
     # per launch: the grouped GEMMs against max(FLOPs / tensor peak, bytes / HBM peak); the token kernels'
     # launch times are summed per call and set against the call's algorithmic bytes
     table, call_launch_ms = [], {}
-    names = demangle([n for n, _ in launches])
+    names = demangle([n for n, _, _ in launches])
     roles = kernel_roles(names)
-    for (_, ms), name, (role, call) in zip(launches, names, roles):
+
+    def against_bound(row, b, f, ms):
+        t_hbm, t_tc = b / (hbm * 1e9), f / (tflops * 1e12)
+        row.update({"bytes": b, "flops": f, "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
+                    "TFLOP/s": round(f / (ms * 1e-3) / 1e12, 1), "bound": "tensor" if t_tc > t_hbm else "hbm",
+                    "frac_of_bound": round(max(t_hbm, t_tc) * 1e3 / ms, 4),
+                    "frac_bf16_peak": round(f / (ms * 1e-3) / 1e12 / tflops, 4)})
+        return row
+
+    for (_, ms, gid), name, (role, call) in zip(launches, names, roles):
         row = {"kernel": role, "call": call, "ms": round(ms, 5)}
+        if gid in group_ms:
+            row["group"] = gid
         if role in ("gemm1", "gemm2", "gemm2_combine", "dH", "dW2", "dXp", "dW1"):
-            b, f = gemm_launch_algorithmic(role, w, K_a, E_used, bwd)
-            t_hbm, t_tc = b / (hbm * 1e9), f / (tflops * 1e12)
-            row.update({"bytes": b, "flops": f, "GB/s": round(b / (ms * 1e-3) / 1e9, 1),
-                        "TFLOP/s": round(f / (ms * 1e-3) / 1e12, 1), "bound": "tensor" if t_tc > t_hbm else "hbm",
-                        "frac_of_bound": round(max(t_hbm, t_tc) * 1e3 / ms, 4),
-                        "frac_bf16_peak": round(f / (ms * 1e-3) / 1e12 / tflops, 4),
-                        "traffic": measured_traffic(w.name, role)})
+            against_bound(row, *gemm_launch_algorithmic(role, w, K_a, E_used, bwd), ms)
+            row["traffic"] = measured_traffic(w.name, role)
         else:
             call_launch_ms[call] = call_launch_ms.get(call, 0.0) + ms
             row["traffic"] = measured_traffic(w.name, role)
         row["name"] = name[:120]
         table.append(row)
+    # launches the step runs side by side, replayed together
+    concurrent = []
+    for gid, ms in group_ms.items():
+        rows = [r for r in table if r.get("group") == gid]
+        unit = {"kernels": [r["kernel"] for r in rows], "ms": round(ms, 5), "name": " + ".join(r["kernel"] for r in rows)}
+        if all("bytes" in r for r in rows):
+            against_bound(unit, sum(r["bytes"] for r in rows), sum(r["flops"] for r in rows), ms)
+            trs = [r["traffic"] for r in rows]
+            unit["traffic"] = sum(trs) if all(t is not None for t in trs) else None
+        concurrent.append(unit)
     for c in ("router", "dispatch", "combine"):
         if c in call_launch_ms and call_launch_ms[c] > 0:
             gbs = alg[c] / (call_launch_ms[c] * 1e-3) / 1e9
             kernels[c].update({"launches_ms": round(call_launch_ms[c], 5), "launches_GB/s": round(gbs, 1),
                                "launches_frac_hbm": round(gbs / hbm, 4)})
 
-    gemm_rows = [r for r in table if "bytes" in r]
+    # the dominant unit: the longest grouped-GEMM launch that runs alone, or the longest group of GEMM
+    # launches that run side by side (timed together)
+    gemm_rows = [r for r in table if "bytes" in r and "group" not in r] + [u for u in concurrent if "bytes" in u]
     if gemm_rows:
         top = max(gemm_rows, key=lambda r: r["ms"])
         if top["bound"] == "tensor":
@@ -602,10 +670,15 @@ def run_ours(args):
         else:
             roof = {"bound": "hbm", "achieved": top["GB/s"], "peak": hbm, "unit": "GB/s",
                     "frac": round(top["GB/s"] / hbm, 4)}
-        roof.update({"traffic": top["traffic"], "kernel": f"{top['kernel']} ({top['name']})",
+        side_by_side = "kernels" in top
+        roof.update({"traffic": top["traffic"],
+                     "kernel": (f"{top['name']} (launched side by side on two streams, each on its share of the "
+                                f"SMs)") if side_by_side else f"{top['kernel']} ({top['name']})",
                      "launch_ms": top["ms"], "algorithmic_bytes_per_launch": top["bytes"],
                      "algorithmic_flops_per_launch": top["flops"], "peak_source": peak_src,
-                     "timing": "the launch replayed alone from the step graph, CUDA events, L2 flushed before each"})
+                     "timing": ("the group's launches replayed together from the step graph" if side_by_side else
+                                "the launch replayed alone from the step graph") +
+                     ", CUDA events, L2 flushed before each"})
     else:   # per-launch replay unavailable: the forward grouped-GEMM call (two launches) from the per-call events
         gemm_gbs = alg["gemm"] / (mean_call["gemm"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(gemm_gbs, 1), "peak": hbm, "unit": "GB/s",
@@ -633,6 +706,7 @@ def run_ours(args):
                           "frac": round(step_floor_ms / ms_step, 4), "peak": hbm, "unit": "GB/s"},
         "kernels": kernels,
         "launches": table if table else {"error": launch_error},
+        "concurrent_launches": concurrent,
         "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                 "d2h_bytes_per_step": io_bytes, "call": "moe_forward" if not bwd else "separate calls + moe_backward",
                 "overlap": "uploads and downloads on their own streams, double-buffered, overlapping compute"},

@@ -736,8 +736,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             {
               uint4 lg[8], lu[8];
-#pragma unroll
               const bool in_f = col0 + piece * 8 < p.F;   // columns past F: zeros (stores clip there)
+#pragma unroll
               for (int i = 0; i < 8; ++i) {
                 const int rr = 4 * i + (lane >> 3);
                 const bf16 *src = p.aux + (rbase + rr) * p.ldaux + col0 + piece * 8;

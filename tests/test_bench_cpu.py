@@ -4,6 +4,8 @@ workload shapes, and the kernel-launch counts it reports."""
 import importlib.util
 import os
 
+import pytest
+
 import moe_synth as syn
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -109,3 +111,28 @@ def test_oracle_sample_of_the_large_layer_keeps_every_per_expert_shape():
     assert b._f64_weight_bytes(ws) <= b.HOST_F64_WEIGHTS_MAX
     small = syn.WORKLOADS["switch-base-top1"]
     assert b.oracle_sample(small) == (small, None)
+
+
+def test_step_graph_order_and_side_by_side_groups():
+    """The backward GEMMs on two streams: the main stream runs dH then dXp, the side stream dW2 then dW1 (after
+    dH). Launch order follows the dependencies; dH with dW2 and dXp with dW1 form the side-by-side groups."""
+    b = _bench()
+    # creation order: cb (combine backward), dH, dW2, dXp, dW1, dh (router), unp
+    deps = {"cb": [], "dH": ["cb"], "dW2": ["cb"], "dXp": ["dH"], "dW1": ["dW2", "dH"], "dh": ["dXp", "dW1"],
+            "unp": ["dh"]}
+    pos = {k: i for i, k in enumerate(deps)}
+    order = b.topological_order(deps, pos)
+    assert order == ["cb", "dH", "dW2", "dXp", "dW1", "dh", "unp"]
+    anc = {}
+    for k in order:
+        anc[k] = set(deps[k]).union(*(anc[d] for d in deps[k])) if deps[k] else set()
+    g = b.concurrent_groups(order, anc)
+    assert g["dH"] == g["dW2"] and g["dXp"] == g["dW1"]
+    assert len({g["cb"], g["dH"], g["dXp"], g["dh"], g["unp"]}) == 5
+    # a chain: every node its own group
+    chain = {"a": [], "b": ["a"], "c": ["b"]}
+    o = b.topological_order(chain, {"a": 0, "b": 1, "c": 2})
+    an = {"a": set(), "b": {"a"}, "c": {"a", "b"}}
+    assert sorted(b.concurrent_groups(o, an).values()) == [0, 1, 2]
+    with pytest.raises(RuntimeError):
+        b.topological_order({"a": ["b"], "b": ["a"]}, {"a": 0, "b": 1})
