@@ -37,7 +37,7 @@
  *     rows = moe_max_rows(cfg) = min(T*k, E*C) (T*k without a capacity;
  *     min(T, E*C) with cfg->reroute). "k columns" below are 2 with
  *     cfg->reroute (see moe_config), else k.
- *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 1; d and F are
+ *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), T >= 1, d <= 2^22; d and F are
  *     multiples of 8 for MOE_BF16 and of 4 for MOE_F32, so that every row is
  *     a whole number of 16-byte vectors (MOE_ERR_ALIGNMENT otherwise).
  */

@@ -57,11 +57,11 @@ constexpr int DISPATCH_TOKENS = 256;  // tokens per dispatch block
 int router_blocks(const Shape &sh);
 
 // How the router runs for a shape: tensor cores for bf16 x (one fused kernel
-// per 128-token tile, the ep padded expert columns split over a cluster of
-// `cluster` CTAs of nc columns each), CUDA cores for fp32 x.
+// per 128-token tile over all ep padded expert columns, d split over a
+// cluster of `cluster` CTAs), CUDA cores for fp32 x.
 struct RouterPlan {
   bool tensor_cores;
-  int ep, m_tiles, cluster, nc;
+  int ep, m_tiles, cluster;
 };
 RouterPlan router_plan(const Shape &sh);
 int dispatch_blocks(const Shape &sh);

@@ -46,7 +46,8 @@ static moe_status make_shape(const moe_config *c, Shape *sh) {
   const int mult = c->dtype == MOE_BF16 ? 8 : 4;   // 16-byte rows for TMA and the vector accesses
   if (c->d_model % mult != 0 || c->d_ff % mult != 0) return MOE_ERR_ALIGNMENT;
   const int64_t Tk = (int64_t)c->T * c->top_k;
-  if (Tk > (int64_t)1 << 30 || (int64_t)c->d_model * c->d_ff * 2 > ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (Tk > (int64_t)1 << 30 || (int64_t)c->d_model * c->d_ff * 2 > ((int64_t)1 << 31) || c->d_model > (1 << 22))
+    return MOE_ERR_UNSUPPORTED;
   sh->T = c->T;
   sh->d = c->d_model;
   sh->E = c->n_experts;

@@ -13,12 +13,12 @@
 // x_i * part_e,i is exact in the fp32 accumulator, and h = x W_hi^T +
 // x W_mid^T + x W_lo^T is the fp32 dot product up to the order of the fp32
 // additions. One fused tcgen05 kernel per 128-token tile computes the logits
-// into TMEM and, in its epilogue, one thread per token does softmax, top-k
-// and the statistics straight from TMEM. When there are few token tiles, the
-// experts' columns are split over a cluster of up to four CTAs, which swap
-// only per-token records (local maximum, local sum of exponentials, top-k
-// candidates) through distributed shared memory. fp32 layers use a
-// register-tiled CUDA-core kernel, one warp per token for the selection.
+// of all experts into TMEM; when there are few token tiles, d is split over a
+// cluster of up to eight CTAs, which add their partial logits in distributed
+// shared memory (each CTA finishes its share of the tile's rows). Softmax,
+// top-k and the statistics then run one warp per token on the summed logits,
+// which never leave the chip. fp32 layers use a register-tiled CUDA-core
+// kernel, one warp per token for the selection.
 //
 // Ties in the top-k go to the lower expert index (descending logit order
 // keys, then ascending index). Importance and load are summed per CTA in a
@@ -336,46 +336,51 @@ __global__ void __launch_bounds__(256) router_simt_kernel(const RouterArgs a, co
 // ---------------------------------------------------------------- tensor-core path (bf16 layers)
 // W_r [E, d] fp32 -> parts [3][EP][d] bf16 with W = hi + mid + lo (rows >= E are zero).
 __global__ void __launch_bounds__(256) router_split_kernel(const float *w_r, int E, int EP, int d, bf16 *parts) {
-  const int64_t n = (int64_t)EP * d;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int e = (int)(i / d);
-    const float w = (e < E) ? w_r[i] : 0.0f;
-    const bf16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);          // exact
-    const bf16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);        // exact
-    parts[i] = hi;
-    parts[n + i] = mid;
-    parts[2 * n + i] = __float2bfloat16_rn(r2);
+  // four consecutive weights per step (d is a multiple of 4: the row never changes inside one)
+  const uint32_t n4 = (uint32_t)EP * (uint32_t)d / 4u;
+  const size_t n = (size_t)EP * d;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += gridDim.x * blockDim.x) {
+    const uint32_t e = (4u * i) / (uint32_t)d;
+    float4 w = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if ((int)e < E) w = __ldg(reinterpret_cast<const float4 *>(w_r) + i);
+    const float wv[4] = {w.x, w.y, w.z, w.w};
+    bf16 hi[4], mid[4], lo[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      hi[j] = __float2bfloat16_rn(wv[j]);
+      const float r1 = wv[j] - __bfloat162float(hi[j]);   // exact
+      mid[j] = __float2bfloat16_rn(r1);
+      const float r2 = r1 - __bfloat162float(mid[j]);     // exact
+      lo[j] = __float2bfloat16_rn(r2);
+    }
+    *reinterpret_cast<uint2 *>(parts + 4 * (size_t)i) = *reinterpret_cast<const uint2 *>(hi);
+    *reinterpret_cast<uint2 *>(parts + n + 4 * (size_t)i) = *reinterpret_cast<const uint2 *>(mid);
+    *reinterpret_cast<uint2 *>(parts + 2 * n + 4 * (size_t)i) = *reinterpret_cast<const uint2 *>(lo);
   }
 }
 
 namespace rf {
-constexpr int BM = 128;        // tokens per CTA (TMEM lanes)
+constexpr int BM = 128;        // tokens per CTA tile (TMEM lanes)
 constexpr int BK = 64;         // K per stage (one 128-byte swizzled row of bf16)
-constexpr int EPI_WARPS = 16;  // 4 per TMEM lane quarter, each on a quarter of the CTA's columns
+constexpr int EPI_WARPS = 16;  // 4 per TMEM lane quarter, each on a quarter of the columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;   // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2-17 epilogue
-constexpr int KMAX = 8;        // top-k candidates kept per row
-constexpr int SMAX = 4;        // CTAs per cluster (expert-column split)
+constexpr int SMAX = 8;        // CTAs per cluster (K split)
 constexpr int MAX_STAGES = 8;
 constexpr int SMEM_LIMIT = 232448;
 
-template <int NC> struct Geo {
+template <int EP> struct Geo {
   static constexpr int A_BYTES = BM * BK * 2;      // x tile
-  static constexpr int B_BYTES = NC * BK * 2;      // one bf16 part of this CTA's W_r rows
+  static constexpr int B_BYTES = EP * BK * 2;      // one bf16 part of W_r
   static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
-  static constexpr int TMEM_COLS = NC;             // NC >= 32, a power of two
+  static constexpr int TMEM_COLS = EP;             // EP >= 32, a power of two
+  static constexpr int EPT = EP / 32;              // columns per lane in the row pass
+  // after the mainloop, inside the idle ring: the partial logits [S][BM / S][EP]
+  // (fp32, 16-byte units of each row permuted by the row's low three bits),
+  // the warps' per-expert sums [16][EP], the loads [256] and the aux tree [256]
+  static constexpr size_t SLAB_BYTES = (size_t)BM * EP * 4;
+  static constexpr size_t EPI_BYTES = SLAB_BYTES + (size_t)EPI_WARPS * EP * 4 + 256 * 4 + 256 * 4;
 };
 
-// One row as one CTA of a cluster sees it (its NC expert columns): the k
-// best (selection key, expert) pairs, packed so that a larger value is the
-// larger key, ties to the lower expert; the score of each; the local max m
-// and sum of exp(h - m) z (softmax scores).
-struct Cand {
-  unsigned long long c[KMAX];
-  float sc[KMAX];
-  float m, z;
-};
 struct __align__(8) Bars {
   uint64_t full[MAX_STAGES];
   uint64_t empty[MAX_STAGES];
@@ -387,7 +392,7 @@ struct __align__(8) Bars {
 };
 
 struct Args {
-  int T, E, EP, k, renorm, S, nk, stages, score;
+  int T, E, k, renorm, S, nk, stages, score;
   int k_route;                    // columns the load and f count (k; 1 with rerouting)
   const float *bias;              // [E] added to h (or null)
   const float *sel_bias;          // [E] added to the scores for the choice only (or null)
@@ -404,22 +409,15 @@ struct Args {
   DeviceStatus *st;
 };
 
-__host__ __device__ constexpr size_t recv_bytes(int S) { return S > 1 ? (size_t)S * BM * sizeof(Cand) : 0; }
-template <int NC> size_t smem_bytes(int S, int stages) {
-  return 1024 + (size_t)stages * Geo<NC>::STAGE_BYTES + recv_bytes(S) + sizeof(Bars);
+template <int EP> size_t smem_bytes(int stages) {
+  return 1024 + (size_t)stages * Geo<EP>::STAGE_BYTES + sizeof(Bars);
 }
 
-__device__ __forceinline__ unsigned long long pack_cand(float key, int e) {
-  return ((unsigned long long)logit_key(key) << 32) | (unsigned)(0xFFFF - e);
-}
-__device__ __forceinline__ int cand_expert(unsigned long long c) { return 0xFFFF - (int)(c & 0xFFFFu); }
-// Inverse of logit_key (a -0.0 key comes back as +0.0).
+// Inverse of logit_key on the high word (a -0.0 key comes back as +0.0).
 __device__ __forceinline__ float cand_key_value(unsigned long long c) {
   const uint32_t key = (uint32_t)(c >> 32);
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
-// p = exp(h - M) / Z: the one expression both the probabilities and the gates use.
-__device__ __forceinline__ float prob_of(float h, float M, float Z) { return expf(h - M) / Z; }
 // The elementwise scores: sigmoid, and sqrt(softplus) with
 // softplus(h) = max(h, 0) + log1p(exp(-|h|)) (no overflow for large h).
 __device__ __forceinline__ float elem_score(float h, int score) {
@@ -427,13 +425,10 @@ __device__ __forceinline__ float elem_score(float h, int score) {
   return sqrtf(fmaxf(h, 0.0f) + log1pf(expf(-fabsf(h))));
 }
 
-__device__ __forceinline__ void st_cluster_u64(uint32_t addr, unsigned long long v) {
-  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-// Named barrier of the four epilogue warps.
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -441,136 +436,56 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   while (!mbar_try_wait(a, parity))
     if (global_timer_ns() - t0 > 200000000ull) break;
 }
-
-// A thread's candidate list in registers: the KMAX best selection keys seen
-// so far, descending, with the score of each. Branch-free insertion (the
-// same compare-and-swap chain for every lane, whatever its keys), so that a
-// warp never splits on which of its rows took a new candidate.
-struct RegList {
-  unsigned long long c[KMAX];
-  float s[KMAX];
-  __device__ __forceinline__ void clear() {
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) { c[j] = 0ull; s[j] = 0.0f; }
-  }
-  __device__ __forceinline__ void offer(unsigned long long v, float vs, int k) {
-    if (k == 1) {   // uniform over the kernel: the maximum alone
-      if (v > c[0]) { c[0] = v; s[0] = vs; }
-      return;
-    }
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      const bool gt = v > c[j];
-      const unsigned long long cj = c[j];
-      const float sj = s[j];
-      c[j] = gt ? v : cj;
-      s[j] = gt ? vs : sj;
-      v = gt ? cj : v;
-      vs = gt ? sj : vs;
-    }
-  }
-};
-
-__device__ __forceinline__ void put_record(Cand &rc, const RegList &l, float m, float z) {
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) { rc.c[j] = l.c[j]; rc.sc[j] = l.s[j]; }
-  rc.m = m;
-  rc.z = z;
-}
-// This row's record into slot [rank][r] of every CTA of the cluster.
-__device__ __forceinline__ void send_record(Cand *recv, int rank, int r, int S, const RegList &l, float m, float z) {
-  const uint32_t mine = smem_u32(&recv[rank * BM + r]);
-  for (int dst = 0; dst < S; ++dst) {
-    const uint32_t ra = mapa_shared(mine, (uint32_t)dst);
-#pragma unroll
-    for (int j = 0; j < KMAX; ++j) {
-      st_cluster_u64(ra + 8u * j, l.c[j]);
-      st_cluster_f32(ra + 8u * KMAX + 4u * j, l.s[j]);
-    }
-    st_cluster_f32(ra + 12u * KMAX, m);
-    st_cluster_f32(ra + 12u * KMAX + 4u, z);
-  }
-}
-// The k best of n sorted records recs[i * stride] (distinct experts: no equal
-// keys) into l, and the softmax statistics they combine to: M = max m,
-// Z = sum z exp(m - M) in record order.
-__device__ __forceinline__ void merge_records(const Cand *recs, int stride, int n, int k, RegList &l, float &M,
-                                              float &Z) {
-  M = -FLT_MAX;
-  for (int i = 0; i < n; ++i) M = fmaxf(M, recs[i * stride].m);
-  Z = 0.0f;
-  for (int i = 0; i < n; ++i) Z += recs[i * stride].z * expf(recs[i * stride].m - M);
-  uint32_t heads = 0;   // each list's next position, 8 bits per list
-#pragma unroll
-  for (int j = 0; j < KMAX; ++j) {
-    unsigned long long best = 0ull;
-    float bs = 0.0f;
-    int from = 0;
-    for (int i = 0; i < n; ++i) {
-      const int hd = (int)((heads >> (8 * i)) & 0xFFu);
-      if (j < k && hd < k) {
-        const unsigned long long v = recs[i * stride].c[hd];
-        if (v > best) { best = v; bs = recs[i * stride].sc[hd]; from = i; }
-      }
-    }
-    l.c[j] = best;
-    l.s[j] = bs;
-    heads += 1u << (8 * from);
-  }
-}
 // Named barrier of the sixteen epilogue warps.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory"); }
 
-// Logits, scores, top-k and statistics of 128 tokens, with the experts'
-// columns split over the S CTAs of a cluster (NC = EP / S each).
-//   warp 0: TMA of the x tile and of the hi/mid/lo parts of this CTA's W_r
-//           rows, one 64-deep K step per stage;
-//   warp 1: 3 x 4 tcgen05 MMAs (M 128, N NC, K 16) per stage into one fp32
+// Float offset of column c of slab row `row` (rows EP floats apart; the 16-byte
+// units of a row permuted by the row's low three bits, so that 32 lanes
+// writing 32 rows, or reading 32 columns of one row, touch every bank once
+// per 128 bytes).
+template <int EP> __device__ __forceinline__ int slab_at(int row, int c) {
+  return row * EP + ((((c >> 2) ^ (row & 7))) << 2) + (c & 3);
+}
+
+// Logits, scores, top-k and statistics of 128 tokens. The S CTAs of a cluster
+// split d (each its share of the 64-deep K steps) and every CTA's MMAs cover
+// all EP expert columns, so each holds partial logits of all 128 rows; row r
+// belongs to CTA r / (128 / S), which receives the other CTAs' partials of
+// its rows through distributed shared memory and adds them in CTA order.
+//   warp 0: TMA of the x tile and of the hi/mid/lo parts of W_r, one K step
+//           per stage;
+//   warp 1: 3 x 4 tcgen05 MMAs (M 128, N EP, K 16) per stage into one fp32
 //           TMEM accumulator;
-//   warps 2-5: one token row per thread, read from TMEM. Softmax scores:
-//           pass 1 the local maximum (and, without a correction bias, the
-//           top-k candidates by logit), pass 2 the sum of exp(h - m); the
-//           cluster's CTAs swap these per-row records over distributed shared
-//           memory, each forms M = max m and Z = sum z exp(m - M) in CTA order
-//           and merges the candidates. Elementwise scores: pass 1 the
-//           candidates by logit (by score + bias with a correction bias) with
-//           their scores. Pass 3 writes the scores of its columns (staged
-//           through shared memory so each store instruction covers one
-//           128-byte row piece), sums them per expert, and, for softmax scores
-//           with a correction bias, forms the candidates by p + b and swaps
-//           them in a second exchange. The row's experts and gates come from
-//           the merged candidates (CTA `rank` writes the rows r with
-//           r % S == rank).
-template <int NC>
+//   warps 2-17: drain TMEM (thread per row, a quarter of the columns per
+//           warp) into the owners' shared memory; then one warp per row of
+//           this CTA's rows: the row's EP values spread over the lanes, warp
+//           reductions for the softmax maximum and sum, k rounds of a warp
+//           maximum over selection keys for the top-k, coalesced stores of
+//           the scores, per-expert sums of the scores and the loads.
+template <int EP>
 __global__ void __launch_bounds__(THREADS, 1)
     router_fused_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                         const Args a) {
-  using G = Geo<NC>;
+  using G = Geo<EP>;
+  constexpr int EPT = G::EPT;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *tiles = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  const int S = a.S;
-  Cand *recv = reinterpret_cast<Cand *>(tiles + (size_t)a.stages * G::STAGE_BYTES);   // [S][BM]
-  Bars &b = *reinterpret_cast<Bars *>(reinterpret_cast<uint8_t *>(recv) + recv_bytes(S));
+  Bars &b = *reinterpret_cast<Bars *>(tiles + (size_t)a.stages * G::STAGE_BYTES);
   volatile int *abort_flag = &b.abort_flag;
-  // Used only after this CTA's MMAs have completed, in the then idle ring:
-  Cand *part_rec = reinterpret_cast<Cand *>(tiles);                          // [4 column parts][BM]
-  float *stage_out = reinterpret_cast<float *>(part_rec + 4 * BM);           // [16 warps][32 rows][32]
-  float *imp_w = stage_out + EPI_WARPS * 32 * 32;                            // [4 row quarters][NC]
-  int *cnt = reinterpret_cast<int *>(imp_w + 4 * NC);                        // [EP]
-  float *term = reinterpret_cast<float *>(cnt + 256);                        // [256]
-  float2 *fin = reinterpret_cast<float2 *>(term + 256);                      // [BM] the rows' M and Z
+  // Used only after the mainloops of the cluster have completed, in the then idle ring:
+  float *slab = reinterpret_cast<float *>(tiles);                               // [S][rows][EP]
+  float *imp_w = reinterpret_cast<float *>(tiles + G::SLAB_BYTES);               // [16 warps][EP]
+  int *cnt = reinterpret_cast<int *>(imp_w + EPI_WARPS * EP);                    // [256]
+  float *term = reinterpret_cast<float *>(cnt + 256);                            // [256]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S;
   const int rank = S > 1 ? (int)cluster_ctarank() : 0;
+  const int rows = BM / S;                       // rows of the tile this CTA finishes
   const int m0 = blockIdx.y * BM;
-  const int col0 = rank * NC;
+  const int ks0 = (rank * a.nk) / S, ks1 = ((rank + 1) * a.nk) / S;
   const int E = a.E, k = a.k;
-  const bool softmax = a.score == MOE_SCORE_SOFTMAX;
-  // softmax scores with a correction bias choose on p + b, known only after
-  // the first exchange: a second one follows pass 3
-  const bool late_choice = softmax && a.sel_bias != nullptr;
-  const int cluster_syncs = S > 1 ? (late_choice ? 3 : 1) : 0;
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
@@ -595,7 +510,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint64_t pol_w = policy_evict_last();
       int stage = 0;
       uint32_t phase = 0, issued = 0, issued_parity = 0;
-      for (int ks = 0; ks < a.nk; ++ks) {
+      for (int ks = ks0; ks < ks1; ++ks) {
         if (!mbar_wait_bounded(&b.empty[stage], phase ^ 1, abort_flag, a.st)) break;
         uint8_t *a_s = tiles + (size_t)stage * G::STAGE_BYTES;
         mbar_arrive_expect_tx(&b.full[stage], G::STAGE_BYTES);
@@ -603,7 +518,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_load_2d(a_s, &tmX, &b.full[stage], k0, m0, pol_x);
 #pragma unroll
         for (int part = 0; part < 3; ++part)
-          tma_load_2d(a_s + G::A_BYTES + part * G::B_BYTES, &tmW, &b.full[stage], k0, part * a.EP + col0, pol_w);
+          tma_load_2d(a_s + G::A_BYTES + part * G::B_BYTES, &tmW, &b.full[stage], k0, part * EP, pol_w);
         issued |= 1u << stage;
         issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == a.stages) { stage = 0; phase ^= 1; }
@@ -613,13 +528,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (issued & (1u << i)) drain_wait(&b.full[i], (issued_parity >> i) & 1);
     }
     __syncwarp();
-    for (int i = 0; i < cluster_syncs; ++i) cluster_sync_all();
+    if (S > 1) { cluster_sync_all(); cluster_sync_all(); }
   } else if (warp == 1) {
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, NC, 0, 0);
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, EP, 0, 0);
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int ks = 0; ks < a.nk; ++ks) {
+    for (int ks = ks0; ks < ks1; ++ks) {
       if (!mbar_wait_bounded(&b.full[stage], phase, abort_flag, a.st)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
@@ -630,7 +545,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma_bf16(tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024), smem_desc_sw128(b0 + kk * 32, 16, 1024),
-                        IDESC, (ks > 0 || part > 0 || kk > 0) ? 1u : 0u);
+                        IDESC, (ks > ks0 || part > 0 || kk > 0) ? 1u : 0u);
         }
         tc_commit(&b.empty[stage]);
       }
@@ -644,197 +559,173 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       drain_wait(&b.drain, 0);
     }
-    for (int i = 0; i < cluster_syncs; ++i) cluster_sync_all();
+    if (S > 1) { cluster_sync_all(); cluster_sync_all(); }
   } else {
-    // Warp w reads TMEM lane quarter q = w % 4 (rows 32 q .. 32 q + 31, one
-    // per lane) and column part pp of the CTA's NC columns (CP wide).
-    constexpr int CP = NC / 4;
-    constexpr int SC = CP < 32 ? CP : 32;   // staging width of pass 3
-    const int q = warp & 3;
-    const int pp = (warp - 2) >> 2;
-    const int r = q * 32 + lane;
-    const int t = m0 + r;
-    const bool live = t < a.T;
-    const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(pp * CP);
-    const int ecol0 = col0 + pp * CP;       // this thread's first expert
-    const float *bias = a.bias, *sel_bias = a.sel_bias;
-    float m = -FLT_MAX, z = 0.0f;
-    RegList cl;
-    cl.clear();
+    const int ew = warp - 2;               // epilogue warp 0..15
+    const int q = warp & 3;                // TMEM lane quarter: rows 32 q .. 32 q + 31
+    const int pp = ew >> 2;                // column quarter
+    constexpr int CPW = EP / 4;            // columns a warp drains
     // warp-uniform: the TMEM loads below are warp-collective
     const bool acc_ok =
         __all_sync(0xffffffffu, mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st) ? 1 : 0) != 0;
-    float v[8];
-    if (acc_ok) {
-      tc_fence_after();
-      // pass 1: the maximum (softmax) and the candidates that need no global statistics
-      if (softmax) {
-#pragma unroll 1
-        for (int c = 0; c < CP / 8; ++c) {
-          tmem_ld8(t_row + c * 8, v);
+    tc_fence_after();
+    for (int e = threadIdx.x - 64; e < 256; e += 32 * EPI_WARPS) cnt[e] = 0;
+    if (S > 1) cluster_sync_all();         // every CTA's ring is idle: the partials may land
+    // drain: row r's partials go to slot `rank` of its owner's slab
+    {
+      const int r = q * 32 + lane;
+      const int owner = r / rows, lr = r - owner * rows;
+      const int drow = rank * rows + lr;
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(pp * CPW);
+      const uint32_t base = S > 1 ? mapa_shared(smem_u32(slab), (uint32_t)owner) : smem_u32(slab);
+      auto put4 = [&](int c, float v0, float v1, float v2, float v3) {
+        const uint32_t addr = base + 4u * (uint32_t)slab_at<EP>(drow, c);
+        if (S > 1) st_cluster_v4(addr, v0, v1, v2, v3);
+        else asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v0), "f"(v1), "f"(v2),
+                          "f"(v3) : "memory");
+      };
+      if constexpr (CPW >= 32) {
+        uint32_t v[CPW / 32][32];
+        if (acc_ok) {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = ecol0 + c * 8 + i;
-            if (e < E) {
-              const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
-              m = fmaxf(m, h);
-              if (!late_choice) cl.offer(pack_cand(h, e), 0.0f, k);
-            }
-          }
-        }
-        // pass 2: sum of exp(h - m)
-#pragma unroll 1
-        for (int c = 0; c < CP / 8; ++c) {
-          tmem_ld8(t_row + c * 8, v);
+          for (int c = 0; c < CPW / 32; ++c) tmem_ld32_issue(t_row + c * 32, v[c]);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = ecol0 + c * 8 + i;
-            if (e < E) z += expf(v[i] + (bias ? __ldg(bias + e) : 0.0f) - m);
-          }
+          for (int c = 0; c < CPW / 32; ++c) tmem_wait32(v[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < CPW / 32; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c][i] = 0u;
         }
+#pragma unroll
+        for (int c = 0; c < CPW / 32; ++c)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            put4(pp * CPW + c * 32 + 4 * j, __uint_as_float(v[c][4 * j]), __uint_as_float(v[c][4 * j + 1]),
+                 __uint_as_float(v[c][4 * j + 2]), __uint_as_float(v[c][4 * j + 3]));
       } else {
-#pragma unroll 1
-        for (int c = 0; c < CP / 8; ++c) {
-          tmem_ld8(t_row + c * 8, v);
+        float v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int e = ecol0 + c * 8 + i;
-            if (e < E) {
-              const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
-              const float sv = elem_score(h, a.score);
-              cl.offer(pack_cand(sel_bias ? sv + __ldg(sel_bias + e) : h, e), sv, k);
-            }
+        for (int c = 0; c < CPW / 8; ++c) {
+          if (acc_ok) tmem_ld8(t_row + c * 8, v);
+          else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
           }
+          put4(pp * CPW + c * 8, v[0], v[1], v[2], v[3]);
+          put4(pp * CPW + c * 8 + 4, v[4], v[5], v[6], v[7]);
         }
       }
     }
-    // merge the four column parts of each row (warps of part 0, one thread per row), then the cluster's CTAs
-    put_record(part_rec[pp * BM + r], cl, m, z);
-    epi_sync();
-    float M = -FLT_MAX, Z = 0.0f;
-    if (pp == 0) {
-      merge_records(part_rec + r, BM, 4, k, cl, M, Z);
-      if (S > 1) send_record(recv, rank, r, S, cl, M, Z);
-    }
-    if (S > 1) {
-      cluster_sync_all();   // every CTA's records are in
-      if (pp == 0) {
-        RegList ml;
-        float M2, Z2;
-        merge_records(recv + r, BM, S, k, ml, M2, Z2);
-        if (!late_choice) cl = ml;
-        M = M2;
-        Z = Z2;
-      }
-    }
-    if (pp == 0) fin[r] = make_float2(M, Z);
-    for (int e = threadIdx.x - 64; e < a.EP; e += 32 * EPI_WARPS) cnt[e] = 0;
-    epi_sync();
-    M = fin[r].x;
-    Z = fin[r].y;
-    if (late_choice) cl.clear();
-    // pass 3: the scores of this thread's columns; per 32 x SC block, each
-    // lane writes its row into the warp's 128-byte swizzled staging rows (8
-    // columns at a time), then lane j < SC takes column j row by row: one
-    // coalesced store of the block's row piece per row, and the column's sum
-    // over the block's live rows.
-    float *stg = stage_out + (warp - 2) * 32 * 32;
+    tc_fence_before();                     // this warp's TMEM loads are ordered before the release below
+    if (S > 1) cluster_sync_all();         // every partial of this CTA's rows has landed
+    else epi_sync();
+
+    // one warp per row: rows ew, ew + 16, ... of this CTA's `rows`
+    const bool softmax = a.score == MOE_SCORE_SOFTMAX;
+    const bool late_choice = softmax && a.sel_bias != nullptr;
+    float imp[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) imp[j] = 0.0f;
+    const int swz = lane >> 2, sub = lane & 3;
 #pragma unroll 1
-    for (int c = 0; c < CP / SC; ++c) {
+    for (int lr = ew; lr < rows; lr += EPI_WARPS) {
+      const int t = m0 + rank * rows + lr;
+      if (t >= a.T) break;                 // rows past T: the tile's ragged tail (warp-uniform)
+      float h[EPT], sc[EPT];
+      uint32_t key[EPT];
+      float m = -FLT_MAX;
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        const int e = lane + 32 * j;
+        float acc = 0.0f;
+        for (int src = 0; src < S; ++src) {
+          const int row = src * rows + lr;
+          acc += slab[row * EP + (((swz ^ (row & 7))) << 2) + sub + 32 * j];
+        }
+        h[j] = acc + ((a.bias && e < E) ? __ldg(a.bias + e) : 0.0f);
+        if (e < E) m = fmaxf(m, h[j]);
+      }
+      if (softmax) {
+        // M: the row maximum (a warp maximum over order-preserving keys); Z: the sum of exp(h - M), the lanes'
+        // sums in column order, then a butterfly (both lanes of a pair add the same two values, so every lane
+        // ends with the same Z)
+        const float M = cand_key_value((unsigned long long)__reduce_max_sync(0xffffffffu, logit_key(m)) << 32);
+        float z = 0.0f;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+          sc[j] = (lane + 32 * j < E) ? expf(h[j] - M) : 0.0f;
+          z += sc[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) sc[j] = sc[j] / z;   // p = exp(h - M) / Z
+      } else {
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) sc[j] = (lane + 32 * j < E) ? elem_score(h[j], a.score) : 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < EPT; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = 0u;
+        if (e < E) {
+          // softmax without a correction bias chooses by logit (the same order as by p, without p's rounding)
+          const float sel = a.sel_bias ? sc[j] + __ldg(a.sel_bias + e) : h[j];
+          key[j] = logit_key(late_choice || !softmax ? sel : h[j]);
+          imp[j] += sc[j];
+          if (a.probs) a.probs[(int64_t)t * E + e] = sc[j];
+        }
+      }
+      // k rounds: the warp's largest remaining key (one max reduction), the lowest expert holding it (one min
+      // reduction), taken out by its lane
+      int my_e = 0;
+      float my_g = 0.0f, psum = 0.0f;
 #pragma unroll 1
-      for (int sub = 0; sub < SC / 8; ++sub) {
-        if (acc_ok) tmem_ld8(t_row + c * SC + sub * 8, v);
+      for (int i = 0; i < k; ++i) {
+        uint32_t best = 0u;
+        int bj = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int e = ecol0 + c * SC + sub * 8 + i;
-          float sv = 0.0f;
-          if (acc_ok && live && e < E) {
-            const float h = v[i] + (bias ? __ldg(bias + e) : 0.0f);
-            sv = softmax ? prob_of(h, M, Z) : elem_score(h, a.score);
-            if (late_choice) cl.offer(pack_cand(sv + __ldg(sel_bias + e), e), sv, k);
-          }
-          v[i] = sv;
+        for (int j = 0; j < EPT; ++j)
+          if (key[j] > best) { best = key[j]; bj = j; }   // strict: equal keys keep the lower expert
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, best);
+        const uint32_t mine = (best == wmax && best != 0u) ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu;
+        const uint32_t e = __reduce_min_sync(0xffffffffu, mine);
+        const int ej = (int)(e >> 5);
+        float gv = sc[0];
+#pragma unroll
+        for (int j = 1; j < EPT; ++j)
+          if (j == ej) gv = sc[j];
+        const float g = __shfl_sync(0xffffffffu, gv, (int)(e & 31u));
+        if ((uint32_t)lane == (e & 31u)) {
+#pragma unroll
+          for (int j = 0; j < EPT; ++j)
+            if (j == ej) key[j] = 0u;
         }
-        *reinterpret_cast<float4 *>(stg + lane * 32 + (((2 * sub) ^ (lane & 7)) << 2)) =
-            make_float4(v[0], v[1], v[2], v[3]);
-        *reinterpret_cast<float4 *>(stg + lane * 32 + (((2 * sub + 1) ^ (lane & 7)) << 2)) =
-            make_float4(v[4], v[5], v[6], v[7]);
+        psum += g;
+        if (lane == i) { my_e = (int)e; my_g = g; }
+        if (lane == 0 && i < a.k_route) atomicAdd(&cnt[e], 1);
       }
-      __syncwarp();
-      if (lane < SC) {
-        const int e = ecol0 + c * SC + lane;
-        float colsum = 0.0f;
-#pragma unroll 4
-        for (int rr = 0; rr < 32; ++rr) {
-          const float pv = stg[rr * 32 + ((((lane >> 2) ^ (rr & 7))) << 2) + (lane & 3)];
-          const int tt = m0 + q * 32 + rr;
-          if (tt < a.T) {
-            colsum += pv;
-            if (a.probs && e < E) a.probs[(int64_t)tt * E + e] = pv;
-          }
-        }
-        imp_w[q * NC + pp * CP + c * SC + lane] = colsum;
-      }
-      __syncwarp();
-    }
-    if (late_choice) {
-      // softmax scores with a correction bias: the candidates by p + b, merged over the parts and the cluster
-      epi_sync();   // every part's first records have been read
-      put_record(part_rec[pp * BM + r], cl, M, Z);
-      epi_sync();
-      if (pp == 0) {
-        float Mx, Zx;
-        merge_records(part_rec + r, BM, 4, k, cl, Mx, Zx);
-      }
-      if (S > 1) {
-        cluster_sync_all();   // every CTA has read the first records
-        if (pp == 0) send_record(recv, rank, r, S, cl, M, Z);
-        cluster_sync_all();   // the second records are in
-        if (pp == 0) {
-          float Mx, Zx;
-          merge_records(recv + r, BM, S, k, cl, Mx, Zx);
-        }
+      if (lane < k) {
+        a.idx[(int64_t)t * k + lane] = my_e;
+        a.gate[(int64_t)t * k + lane] = a.renorm ? my_g / psum : my_g;
       }
     }
-    // the row's experts and gates
-    if (pp == 0 && acc_ok && live && (r % S) == rank) {
-      float gv[KMAX];
-      float psum = 0.0f;
+    // this CTA's per-expert sums: the warps' partial sums added in warp order, as integers into the accumulators
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        gv[j] = 0.0f;
-        if (j < k) {
-          // softmax scores chosen by logit: p from the logit the key carries
-          gv[j] = (softmax && !late_choice) ? prob_of(cand_key_value(cl.c[j]), M, Z) : cl.s[j];
-          psum += gv[j];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          const int e = cand_expert(cl.c[j]);
-          a.idx[(int64_t)t * k + j] = e;
-          a.gate[(int64_t)t * k + j] = a.renorm ? gv[j] / psum : gv[j];
-          if (j < a.k_route) atomicAdd(&cnt[e], 1);
-        }
-      }
-    }
+    for (int j = 0; j < EPT; ++j) imp_w[ew * EP + lane + 32 * j] = imp[j];
     epi_sync();
-    // this CTA's per-expert sums: importance over its 128 rows (row quarters
-    // in a fixed order) and loads, added as integers into the accumulators
-    for (int c = threadIdx.x - 64; c < NC; c += 32 * EPI_WARPS) {
-      const int e = col0 + c;
-      if (e < E) {
-        const float sm = imp_w[c] + imp_w[NC + c] + imp_w[2 * NC + c] + imp_w[3 * NC + c];
+    for (int c = threadIdx.x - 64; c < EP; c += 32 * EPI_WARPS) {
+      if (c < E) {
+        float sm = 0.0f;
+        for (int w2 = 0; w2 < EPI_WARPS; ++w2) sm += imp_w[w2 * EP + c];
         // sm <= 128 rows x a score <= 1 (softmax, sigmoid) or <= 2^64 (sqrt softplus of an
         // fp32 logit): llrint of sm * 2^32 is exact to 2^-33 while sm < 2^31
         const unsigned long long qv = (unsigned long long)llrint((double)sm * 4294967296.0);
-        if (qv) atomicAdd(a.acc_imp + e, qv);
+        if (qv) atomicAdd(a.acc_imp + c, qv);
+        if (cnt[c]) atomicAdd(a.acc_load + c, cnt[c]);
       }
     }
-    for (int e = threadIdx.x - 64; e < E; e += 32 * EPI_WARPS)
-      if (cnt[e]) atomicAdd(a.acc_load + e, cnt[e]);
-    tc_fence_before();   // this warp's TMEM loads are ordered before the release below
   }
 
   // The last CTA to finish converts the accumulated importance and load,
@@ -893,30 +784,24 @@ cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStre
   return launch_kernel(router_simt_kernel<XT, EPT>, dim3(nblk), dim3(256), smem, stream, a, so);
 }
 
-// Shared memory the epilogue uses inside the idle ring: four column parts' records, sixteen warps' staging
-// blocks, the per-expert sums and counts, the aux tree and the rows' M and Z.
-template <int NC> constexpr size_t epilogue_ring_bytes() {
-  return 4 * rf::BM * sizeof(rf::Cand) + rf::EPI_WARPS * 32 * 32 * 4 + 4 * NC * 4 + 256 * 4 + 256 * 4 + rf::BM * 8;
-}
-
-template <int NC>
+template <int EP>
 cudaError_t run_fused(const CUtensorMap &mx, const CUtensorMap &mw, const rf::Args &ra, int m_tiles,
                       cudaStream_t stream) {
-  if ((size_t)ra.stages * rf::Geo<NC>::STAGE_BYTES < epilogue_ring_bytes<NC>()) return cudaErrorInvalidConfiguration;
-  static cudaError_t attr = set_smem(rf::router_fused_kernel<NC>, rf::SMEM_LIMIT);
+  if ((size_t)ra.stages * rf::Geo<EP>::STAGE_BYTES < rf::Geo<EP>::EPI_BYTES) return cudaErrorInvalidConfiguration;
+  static cudaError_t attr = set_smem(rf::router_fused_kernel<EP>, rf::SMEM_LIMIT);
   if (attr != cudaSuccess) return attr;
-  const size_t smem = rf::smem_bytes<NC>(ra.S, ra.stages);
+  const size_t smem = rf::smem_bytes<EP>(ra.stages);
   if (ra.S > 1)
-    return launch_kernel_cluster(rf::router_fused_kernel<NC>, ra.S, dim3(ra.S, m_tiles), dim3(rf::THREADS), smem,
+    return launch_kernel_cluster(rf::router_fused_kernel<EP>, ra.S, dim3(ra.S, m_tiles), dim3(rf::THREADS), smem,
                                  stream, mx, mw, ra);
-  return launch_kernel(rf::router_fused_kernel<NC>, dim3(1, m_tiles), dim3(rf::THREADS), smem, stream, mx, mw, ra);
+  return launch_kernel(rf::router_fused_kernel<EP>, dim3(1, m_tiles), dim3(rf::THREADS), smem, stream, mx, mw, ra);
 }
 
 int epad_of(int E) { return E <= 32 ? 32 : E <= 64 ? 64 : E <= 128 ? 128 : 256; }
 
-template <int NC> int fused_stages(int S) {
-  const size_t fixed = 1024 + rf::recv_bytes(S) + sizeof(rf::Bars);
-  int st = (int)((rf::SMEM_LIMIT - fixed) / rf::Geo<NC>::STAGE_BYTES);
+template <int EP> int fused_stages() {
+  const size_t fixed = 1024 + sizeof(rf::Bars);
+  int st = (int)((rf::SMEM_LIMIT - fixed) / rf::Geo<EP>::STAGE_BYTES);
   return st > rf::MAX_STAGES ? rf::MAX_STAGES : st;
 }
 
@@ -929,12 +814,12 @@ RouterPlan router_plan(const Shape &sh) {
   p.tensor_cores = sh.dtype == MOE_BF16;
   p.ep = epad_of(sh.E);
   p.m_tiles = (sh.T + rf::BM - 1) / rf::BM;
-  // expert columns split over a cluster of S CTAs while the grid stays
-  // within one wave and every CTA keeps at least 32 columns
+  // d split over a cluster of S CTAs while the grid stays within one wave
+  // and every CTA keeps at least one 64-deep K step
+  const int nk = (sh.d + rf::BK - 1) / rf::BK;
   int S = 1;
-  while (2 * S <= rf::SMAX && p.m_tiles * 2 * S <= sm_count() && p.ep / (2 * S) >= 32) S *= 2;
+  while (2 * S <= rf::SMAX && p.m_tiles * 2 * S <= sm_count() && 2 * S <= nk) S *= 2;
   p.cluster = S;
-  p.nc = p.ep / S;
   return p;
 }
 
@@ -991,15 +876,15 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   }
   bf16 *parts = reinterpret_cast<bf16 *>(w + L.router_parts);
   const int64_t n = (int64_t)plan.ep * sh.d;
-  int sgrid = (int)((n + 255) / 256);
+  int sgrid = (int)((n / 4 + 255) / 256);
   if (sgrid > 4 * sm_count()) sgrid = 4 * sm_count();
   e = launch_kernel(router_split_kernel, dim3(sgrid), dim3(256), 0, stream, w_r, sh.E, plan.ep, sh.d, parts);
   if (e != cudaSuccess) return e;
   CUtensorMap mx, mw;
-  if (!make_map_2d(&mx, x, sh.d, sh.T, 64, rf::BM) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.nc))
+  if (!make_map_2d(&mx, x, sh.d, sh.T, 64, rf::BM) || !make_map_2d(&mw, parts, sh.d, 3 * plan.ep, 64, plan.ep))
     return cudaErrorInvalidValue;
   rf::Args ra;
-  ra.T = sh.T; ra.E = sh.E; ra.EP = plan.ep; ra.k = sh.k; ra.renorm = sh.renorm; ra.S = plan.cluster;
+  ra.T = sh.T; ra.E = sh.E; ra.k = sh.k; ra.renorm = sh.renorm; ra.S = plan.cluster;
   ra.k_route = sh.k_route;
   ra.nk = (sh.d + rf::BK - 1) / rf::BK;
   ra.score = sh.score;
@@ -1007,11 +892,11 @@ cudaError_t launch_router(const Shape &sh, const void *x, const float *w_r, cons
   ra.acc_imp = acc_imp; ra.acc_load = acc_load;
   ra.alpha = sh.alpha; ra.importance = importance; ra.load = load; ra.aux = aux; ra.counter = counter;
   ra.st = reinterpret_cast<DeviceStatus *>(w + L.status);
-  switch (plan.nc) {
-    case 32: ra.stages = fused_stages<32>(ra.S); return run_fused<32>(mx, mw, ra, plan.m_tiles, stream);
-    case 64: ra.stages = fused_stages<64>(ra.S); return run_fused<64>(mx, mw, ra, plan.m_tiles, stream);
-    case 128: ra.stages = fused_stages<128>(ra.S); return run_fused<128>(mx, mw, ra, plan.m_tiles, stream);
-    default: ra.stages = fused_stages<256>(ra.S); return run_fused<256>(mx, mw, ra, plan.m_tiles, stream);
+  switch (plan.ep) {
+    case 32: ra.stages = fused_stages<32>(); return run_fused<32>(mx, mw, ra, plan.m_tiles, stream);
+    case 64: ra.stages = fused_stages<64>(); return run_fused<64>(mx, mw, ra, plan.m_tiles, stream);
+    case 128: ra.stages = fused_stages<128>(); return run_fused<128>(mx, mw, ra, plan.m_tiles, stream);
+    default: ra.stages = fused_stages<256>(); return run_fused<256>(mx, mw, ra, plan.m_tiles, stream);
   }
 }
 

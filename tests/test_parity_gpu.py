@@ -96,15 +96,18 @@ def test_router_expert_counts_and_many_tiles(E, k):
     _check_full(w, res, inp, f, None)
 
 
-@pytest.mark.parametrize("T,E,k,renorm", [(200, 256, 8, False), (130, 130, 3, True), (96, 64, 2, False),
-                                          (1000, 128, 1, False), (4000, 48, 4, True)])
-def test_router_cluster_splits(T, E, k, renorm):
-    """The fused tensor-core router with its expert columns split over 4, 2 or 1 CTAs of a cluster (few or
-    many 128-token tiles; a partial last tile; 130 experts, where the last CTA's columns hold no expert):
-    routing bit-exact, values against the oracle, and every gate equal to the probability the same kernel
-    wrote for its expert, bit for bit (the gates are not renormalised)."""
-    w = syn.Workload(f"router-split-{T}-{E}-{k}", T=T, d=256, E=E, k=k, F=128, act="relu", dtype="bf16",
-                     cf=(5, 4), renormalize=renorm, router_std=1 / 16)
+@pytest.mark.parametrize("T,E,k,renorm,d", [(200, 256, 8, False, 256), (130, 130, 3, True, 256),
+                                            (96, 64, 2, False, 256), (1000, 128, 1, False, 256),
+                                            (4000, 48, 4, True, 256), (300, 256, 8, False, 640),
+                                            (2000, 100, 2, True, 520), (20000, 32, 1, False, 136)])
+def test_router_cluster_splits(T, E, k, renorm, d):
+    """The fused tensor-core router with d split over 8, 4, 2 or 1 CTAs of a cluster (few or many 128-token
+    tiles; a partial last tile; K steps that do not divide evenly over the CTAs, and a partial last K step;
+    130 and 100 experts in padded column ranges): routing bit-exact, values against the oracle, and every
+    gate equal to the probability the same kernel wrote for its expert, bit for bit (the gates are not
+    renormalised)."""
+    w = syn.Workload(f"router-split-{T}-{E}-{k}-{d}", T=T, d=d, E=E, k=k, F=128, act="relu", dtype="bf16",
+                     cf=(5, 4), renormalize=renorm, router_std=1 / np.sqrt(d))
     inp = syn.make_inputs(w, dy=False)
     res = run_gpu(w, inp)
     f, _ = _ref_all(w, inp, False)
