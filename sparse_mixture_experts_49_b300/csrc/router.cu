@@ -374,11 +374,17 @@ template <int EP> struct Geo {
   static constexpr int STAGE_BYTES = A_BYTES + 3 * B_BYTES;
   static constexpr int TMEM_COLS = EP;             // EP >= 32, a power of two
   static constexpr int EPT = EP / 32;              // columns per lane in the row pass
-  // after the mainloop, inside the idle ring: the partial logits [S][BM / S][EP]
-  // (fp32, 16-byte units of each row permuted by the row's low three bits),
-  // the warps' per-expert sums [16][EP], the loads [256] and the aux tree [256]
+  // after the mainloop, inside the idle ring: the partial logits of this CTA's
+  // rows from every CTA of the cluster [S][BM / S][EP] (fp32, 16-byte units of
+  // each row permuted by the row's low three bits), then the outgoing partials
+  // of the other CTAs' rows [S - 1][BM / S][EP]; once the rows are done, the
+  // warps' per-expert sums [16][EP] and the aux tree [256] reuse the first part
   static constexpr size_t SLAB_BYTES = (size_t)BM * EP * 4;
-  static constexpr size_t EPI_BYTES = SLAB_BYTES + (size_t)EPI_WARPS * EP * 4 + 256 * 4 + 256 * 4;
+  static size_t epi_bytes(int S) {
+    const size_t slabs = SLAB_BYTES + SLAB_BYTES / S * (S - 1);
+    const size_t sums = (size_t)EPI_WARPS * EP * 4 + 256 * 4;
+    return slabs > sums ? slabs : sums;
+  }
 };
 
 struct __align__(8) Bars {
@@ -386,9 +392,11 @@ struct __align__(8) Bars {
   uint64_t empty[MAX_STAGES];
   uint64_t acc_full;
   uint64_t drain;
+  uint64_t recv;     // the other CTAs' partials of this CTA's rows have landed
   uint32_t tmem_base;
   int abort_flag;
   int last;          // this CTA finished last
+  uint32_t cnt2[128];  // this CTA's loads, two 16-bit counts per word (at most 128 rows x 8 each)
 };
 
 struct Args {
@@ -425,9 +433,11 @@ __device__ __forceinline__ float elem_score(float h, int score) {
   return sqrtf(fmaxf(h, 0.0f) + log1pf(expf(-fabsf(h))));
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
+// Bulk copy of `bytes` from this CTA's shared memory to another CTA's of the
+// cluster, completing on that CTA's barrier (both addresses from mapa_shared).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "r"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
@@ -435,6 +445,39 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(a, parity))
     if (global_timer_ns() - t0 > 200000000ull) break;
+}
+// One compare-exchange of a descending sort: position a before b when its key
+// is larger, or equal with the lower expert.
+__device__ __forceinline__ void cas_desc(uint32_t &ka, float &sa, uint32_t &ea, uint32_t &kb, float &sb,
+                                         uint32_t &eb) {
+  const bool sw = kb > ka || (kb == ka && eb < ea);
+  const uint32_t k0 = sw ? kb : ka, k1 = sw ? ka : kb;
+  const float s0 = sw ? sb : sa, s1 = sw ? sa : sb;
+  const uint32_t e0 = sw ? eb : ea, e1 = sw ? ea : eb;
+  ka = k0; kb = k1; sa = s0; sb = s1; ea = e0; eb = e1;
+}
+// Sorting networks for 1, 2, 4 and 8 candidates (1, 5 and 19 exchanges).
+template <int N> __device__ __forceinline__ void sort_desc(uint32_t (&k)[N], float (&s)[N], uint32_t (&e)[N]) {
+#define CX(i, j) cas_desc(k[i], s[i], e[i], k[j], s[j], e[j])
+  if constexpr (N == 2) {
+    CX(0, 1);
+  } else if constexpr (N == 4) {
+    CX(0, 1); CX(2, 3); CX(0, 2); CX(1, 3); CX(1, 2);
+  } else if constexpr (N == 8) {
+    CX(0, 1); CX(2, 3); CX(4, 5); CX(6, 7);
+    CX(0, 2); CX(1, 3); CX(4, 6); CX(5, 7);
+    CX(1, 2); CX(5, 6);
+    CX(0, 4); CX(1, 5); CX(2, 6); CX(3, 7);
+    CX(2, 4); CX(3, 5);
+    CX(1, 2); CX(3, 4); CX(5, 6);
+  }
+#undef CX
+}
+// Drops the head of a sorted list (the last position becomes empty: key 0).
+template <int N> __device__ __forceinline__ void pop_front(uint32_t (&k)[N], float (&s)[N], uint32_t (&e)[N]) {
+#pragma unroll
+  for (int j = 0; j + 1 < N; ++j) { k[j] = k[j + 1]; s[j] = s[j + 1]; e[j] = e[j + 1]; }
+  k[N - 1] = 0u;
 }
 // Named barrier of the sixteen epilogue warps.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(32 * EPI_WARPS) : "memory"); }
@@ -475,9 +518,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int *abort_flag = &b.abort_flag;
   // Used only after the mainloops of the cluster have completed, in the then idle ring:
   float *slab = reinterpret_cast<float *>(tiles);                               // [S][rows][EP]
-  float *imp_w = reinterpret_cast<float *>(tiles + G::SLAB_BYTES);               // [16 warps][EP]
-  int *cnt = reinterpret_cast<int *>(imp_w + EPI_WARPS * EP);                    // [256]
-  float *term = reinterpret_cast<float *>(cnt + 256);                            // [256]
+  float *outgoing = reinterpret_cast<float *>(tiles + G::SLAB_BYTES);            // [S - 1][rows][EP]
+  float *imp_w = slab;                                                           // [16 warps][EP], after the rows
+  float *term = imp_w + EPI_WARPS * EP;                                          // [256]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.S;
@@ -493,6 +536,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < a.stages; ++i) { mbar_init(&b.full[i], 1); mbar_init(&b.empty[i], 1); }
     mbar_init(&b.acc_full, 1);
     mbar_init(&b.drain, 1);
+    mbar_init(&b.recv, 1);
+    // the S - 1 incoming blocks of this CTA's rows (their bytes may land before or after this)
+    if (S > 1) mbar_arrive_expect_tx(&b.recv, (uint32_t)((S - 1) * (BM / S) * EP * 4));
     b.abort_flag = 0;
     fence_barrier_init();
   } else if (warp == 1) {
@@ -500,6 +546,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
     tc_fence_before();
   }
+  for (int i = threadIdx.x; i < 128; i += THREADS) b.cnt2[i] = 0u;
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = b.tmem_base;
@@ -528,7 +575,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (issued & (1u << i)) drain_wait(&b.full[i], (issued_parity >> i) & 1);
     }
     __syncwarp();
-    if (S > 1) { cluster_sync_all(); cluster_sync_all(); }
+    if (S > 1) cluster_sync_all();
   } else if (warp == 1) {
     constexpr uint32_t IDESC = idesc_bf16_f32(BM, EP, 0, 0);
     int stage = 0;
@@ -559,7 +606,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       drain_wait(&b.drain, 0);
     }
-    if (S > 1) { cluster_sync_all(); cluster_sync_all(); }
+    if (S > 1) cluster_sync_all();
   } else {
     const int ew = warp - 2;               // epilogue warp 0..15
     const int q = warp & 3;                // TMEM lane quarter: rows 32 q .. 32 q + 31
@@ -569,20 +616,20 @@ __global__ void __launch_bounds__(THREADS, 1)
     const bool acc_ok =
         __all_sync(0xffffffffu, mbar_wait_bounded(&b.acc_full, 0, abort_flag, a.st) ? 1 : 0) != 0;
     tc_fence_after();
-    for (int e = threadIdx.x - 64; e < 256; e += 32 * EPI_WARPS) cnt[e] = 0;
     if (S > 1) cluster_sync_all();         // every CTA's ring is idle: the partials may land
-    // drain: row r's partials go to slot `rank` of its owner's slab
+    // drain: row r's partials go to slot `rank` of its owner's slab, directly for this CTA's own rows, through
+    // the outgoing block of the owner (sent whole below) for the other CTAs' rows
     {
       const int r = q * 32 + lane;
       const int owner = r / rows, lr = r - owner * rows;
-      const int drow = rank * rows + lr;
+      const int srow = owner == rank ? rank * rows + lr : (owner < rank ? owner : owner - 1) * rows + lr;
+      float *dst = owner == rank ? slab : outgoing;
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(pp * CPW);
-      const uint32_t base = S > 1 ? mapa_shared(smem_u32(slab), (uint32_t)owner) : smem_u32(slab);
+      const uint32_t base = smem_u32(dst);
       auto put4 = [&](int c, float v0, float v1, float v2, float v3) {
-        const uint32_t addr = base + 4u * (uint32_t)slab_at<EP>(drow, c);
-        if (S > 1) st_cluster_v4(addr, v0, v1, v2, v3);
-        else asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v0), "f"(v1), "f"(v2),
-                          "f"(v3) : "memory");
+        const uint32_t addr = base + 4u * (uint32_t)slab_at<EP>(srow, c);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
+                     : "memory");
       };
       if constexpr (CPW >= 32) {
         uint32_t v[CPW / 32][32];
@@ -618,100 +665,145 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
     tc_fence_before();                     // this warp's TMEM loads are ordered before the release below
-    if (S > 1) cluster_sync_all();         // every partial of this CTA's rows has landed
-    else epi_sync();
+    if (S > 1) fence_proxy_async_smem();   // the outgoing blocks are read by the copy engine
+    epi_sync();
+    if (S > 1) {
+      if (threadIdx.x == 64) {
+        const uint32_t blk = (uint32_t)(rows * EP * 4);
+        for (int o = 0; o < S; ++o) {
+          if (o == rank) continue;
+          const int so = o < rank ? o : o - 1;
+          bulk_copy_to_peer(mapa_shared(smem_u32(slab) + (uint32_t)rank * blk, (uint32_t)o),
+                            smem_u32(outgoing) + (uint32_t)so * blk, blk, mapa_shared(smem_u32(&b.recv), (uint32_t)o));
+        }
+      }
+      // every other CTA's partials of this CTA's rows
+      mbar_wait_bounded<true>(&b.recv, 0, abort_flag, a.st);
+    }
 
-    // one warp per row: rows ew, ew + 16, ... of this CTA's `rows`
+    // one warp per row: rows ew, ew + 16, ... of this CTA's `rows`, R at a time (independent chains of
+    // reductions side by side)
     const bool softmax = a.score == MOE_SCORE_SOFTMAX;
     const bool late_choice = softmax && a.sel_bias != nullptr;
-    float imp[EPT];
+    constexpr int R = EPT >= 8 ? 1 : 2;     // (two rows of 256 columns do not fit the registers)
+    constexpr float LOG2E = 1.4426950408889634f;
+    float imp[EPT], bias_j[EPT], sbias_j[EPT];
+    bool colv[EPT];
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) imp[j] = 0.0f;
+    for (int j = 0; j < EPT; ++j) {
+      const int e = lane + 32 * j;
+      imp[j] = 0.0f;
+      colv[j] = e < E;
+      bias_j[j] = (a.bias && colv[j]) ? __ldg(a.bias + e) : 0.0f;
+      sbias_j[j] = (a.sel_bias && colv[j]) ? __ldg(a.sel_bias + e) : 0.0f;
+    }
     const int swz = lane >> 2, sub = lane & 3;
 #pragma unroll 1
-    for (int lr = ew; lr < rows; lr += EPI_WARPS) {
-      const int t = m0 + rank * rows + lr;
-      if (t >= a.T) break;                 // rows past T: the tile's ragged tail (warp-uniform)
-      float h[EPT], sc[EPT];
-      uint32_t key[EPT];
-      float m = -FLT_MAX;
+    for (int base = ew; base < rows; base += EPI_WARPS * R) {
+      float h[R][EPT], sc[R][EPT];
+      uint32_t key[R][EPT], ex[R][EPT];
+      bool live[R];
+      int64_t tr[R];
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        const int e = lane + 32 * j;
-        float acc = 0.0f;
-        for (int src = 0; src < S; ++src) {
-          const int row = src * rows + lr;
-          acc += slab[row * EP + (((swz ^ (row & 7))) << 2) + sub + 32 * j];
-        }
-        h[j] = acc + ((a.bias && e < E) ? __ldg(a.bias + e) : 0.0f);
-        if (e < E) m = fmaxf(m, h[j]);
-      }
-      if (softmax) {
-        // M: the row maximum (a warp maximum over order-preserving keys); Z: the sum of exp(h - M), the lanes'
-        // sums in column order, then a butterfly (both lanes of a pair add the same two values, so every lane
-        // ends with the same Z)
-        const float M = cand_key_value((unsigned long long)__reduce_max_sync(0xffffffffu, logit_key(m)) << 32);
-        float z = 0.0f;
+      for (int r = 0; r < R; ++r) {
+        const int lr = base + EPI_WARPS * r;
+        const int lc = lr < rows ? lr : base;                 // a row past `rows` recomputes `base`, unstored
+        tr[r] = (int64_t)m0 + rank * rows + lr;
+        live[r] = lr < rows && tr[r] < a.T;                   // warp-uniform
+        // the S partials of this row: the same permutation in every slot (rows is a multiple of 8)
+        const float *rp = slab + lc * EP + ((swz ^ (lc & 7)) << 2) + sub;
+        float m = -FLT_MAX;
 #pragma unroll
         for (int j = 0; j < EPT; ++j) {
-          sc[j] = (lane + 32 * j < E) ? expf(h[j] - M) : 0.0f;
-          z += sc[j];
+          float acc = rp[32 * j];
+          for (int src = 1; src < S; ++src) acc += rp[src * rows * EP + 32 * j];
+          h[r][j] = acc + bias_j[j];
+          if (colv[j]) m = fmaxf(m, h[r][j]);
+        }
+        sc[r][0] = m;   // the lane's maximum, until the softmax below
+      }
+      if (softmax) {
+        // M: the row maximum (a warp maximum over order-preserving keys); p = 2^((h - M) log2 e) / Z with
+        // Z = the lanes' sums in column order, then a butterfly (both lanes of a pair add the same two
+        // values, so every lane ends with the same Z), and one correctly rounded reciprocal of Z
+        float M[R], z[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+          M[r] = cand_key_value((unsigned long long)__reduce_max_sync(0xffffffffu, logit_key(sc[r][0])) << 32);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          z[r] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) {
+            sc[r][j] = colv[j] ? exp2f((h[r][j] - M[r]) * LOG2E) : 0.0f;
+            z[r] += sc[r][j];
+          }
         }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int j = 0; j < EPT; ++j) sc[j] = sc[j] / z;   // p = exp(h - M) / Z
+          for (int r = 0; r < R; ++r) z[r] += __shfl_xor_sync(0xffffffffu, z[r], o);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float inv = __frcp_rn(z[r]);
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) sc[r][j] *= inv;
+        }
       } else {
 #pragma unroll
-        for (int j = 0; j < EPT; ++j) sc[j] = (lane + 32 * j < E) ? elem_score(h[j], a.score) : 0.0f;
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int j = 0; j < EPT; ++j) sc[r][j] = colv[j] ? elem_score(h[r][j], a.score) : 0.0f;
       }
 #pragma unroll
-      for (int j = 0; j < EPT; ++j) {
-        const int e = lane + 32 * j;
-        key[j] = 0u;
-        if (e < E) {
+      for (int r = 0; r < R; ++r) {
+        float *prow = a.probs ? a.probs + tr[r] * E : nullptr;
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
           // softmax without a correction bias chooses by logit (the same order as by p, without p's rounding)
-          const float sel = a.sel_bias ? sc[j] + __ldg(a.sel_bias + e) : h[j];
-          key[j] = logit_key(late_choice || !softmax ? sel : h[j]);
-          imp[j] += sc[j];
-          if (a.probs) a.probs[(int64_t)t * E + e] = sc[j];
+          const float sel = late_choice || !softmax ? (a.sel_bias ? sc[r][j] + sbias_j[j] : h[r][j]) : h[r][j];
+          key[r][j] = colv[j] ? logit_key(sel) : 0u;
+          ex[r][j] = (uint32_t)(lane + 32 * j);
+          if (live[r] && colv[j]) {
+            imp[j] += sc[r][j];
+            if (prow) prow[lane + 32 * j] = sc[r][j];
+          }
         }
+        // the lane's candidates sorted by key, descending, ties to the lower expert
+        sort_desc<EPT>(key[r], sc[r], ex[r]);
       }
-      // k rounds: the warp's largest remaining key (one max reduction), the lowest expert holding it (one min
-      // reduction), taken out by its lane
-      int my_e = 0;
-      float my_g = 0.0f, psum = 0.0f;
+      // k rounds over the lanes' list heads: the largest key (one max reduction), the lowest expert holding
+      // it (one min reduction); the lane that holds it moves to its next candidate
+      int my_e[R];
+      float my_g[R], psum[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) { my_e[r] = 0; my_g[r] = 0.0f; psum[r] = 0.0f; }
 #pragma unroll 1
       for (int i = 0; i < k; ++i) {
-        uint32_t best = 0u;
-        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < EPT; ++j)
-          if (key[j] > best) { best = key[j]; bj = j; }   // strict: equal keys keep the lower expert
-        const uint32_t wmax = __reduce_max_sync(0xffffffffu, best);
-        const uint32_t mine = (best == wmax && best != 0u) ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu;
-        const uint32_t e = __reduce_min_sync(0xffffffffu, mine);
-        const int ej = (int)(e >> 5);
-        float gv = sc[0];
-#pragma unroll
-        for (int j = 1; j < EPT; ++j)
-          if (j == ej) gv = sc[j];
-        const float g = __shfl_sync(0xffffffffu, gv, (int)(e & 31u));
-        if ((uint32_t)lane == (e & 31u)) {
-#pragma unroll
-          for (int j = 0; j < EPT; ++j)
-            if (j == ej) key[j] = 0u;
+        for (int r = 0; r < R; ++r) {
+          const uint32_t wmax = __reduce_max_sync(0xffffffffu, key[r][0]);
+          const uint32_t mine = (key[r][0] == wmax && wmax != 0u) ? ex[r][0] : 0xFFFFFFFFu;
+          const uint32_t em = __reduce_min_sync(0xffffffffu, mine);
+          // (no key left only if NaN logits emptied the lists: expert 0, gate 0, not counted)
+          const bool found = wmax != 0u;
+          const uint32_t e = found ? em : 0u;
+          const float g = found ? __shfl_sync(0xffffffffu, sc[r][0], (int)(e & 31u)) : 0.0f;
+          if (found && ex[r][0] == e) pop_front<EPT>(key[r], sc[r], ex[r]);
+          psum[r] += g;
+          if (lane == i) { my_e[r] = (int)e; my_g[r] = g; }
+          if (lane == 0 && found && live[r] && i < a.k_route) atomicAdd(&b.cnt2[e >> 1], (e & 1u) ? 65536u : 1u);
         }
-        psum += g;
-        if (lane == i) { my_e = (int)e; my_g = g; }
-        if (lane == 0 && i < a.k_route) atomicAdd(&cnt[e], 1);
       }
-      if (lane < k) {
-        a.idx[(int64_t)t * k + lane] = my_e;
-        a.gate[(int64_t)t * k + lane] = a.renorm ? my_g / psum : my_g;
-      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (live[r] && lane < k) {
+          a.idx[tr[r] * k + lane] = my_e[r];
+          a.gate[tr[r] * k + lane] = a.renorm ? my_g[r] / psum[r] : my_g[r];
+        }
     }
     // this CTA's per-expert sums: the warps' partial sums added in warp order, as integers into the accumulators
+    epi_sync();                            // every row has been read: the slab is free
 #pragma unroll
     for (int j = 0; j < EPT; ++j) imp_w[ew * EP + lane + 32 * j] = imp[j];
     epi_sync();
@@ -723,7 +815,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // fp32 logit): llrint of sm * 2^32 is exact to 2^-33 while sm < 2^31
         const unsigned long long qv = (unsigned long long)llrint((double)sm * 4294967296.0);
         if (qv) atomicAdd(a.acc_imp + c, qv);
-        if (cnt[c]) atomicAdd(a.acc_load + c, cnt[c]);
+        const int n = (int)((b.cnt2[c >> 1] >> (16 * (c & 1))) & 0xFFFFu);
+        if (n) atomicAdd(a.acc_load + c, n);
       }
     }
   }
@@ -764,6 +857,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   __syncthreads();
+  // no CTA leaves while a copy into or out of its shared memory may be in flight (every CTA has waited for
+  // its incoming blocks before this point)
+  if (S > 1) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, G::TMEM_COLS);
@@ -787,7 +883,7 @@ cudaError_t run_simt(const RouterArgs &a, const StatsOut &so, int nblk, cudaStre
 template <int EP>
 cudaError_t run_fused(const CUtensorMap &mx, const CUtensorMap &mw, const rf::Args &ra, int m_tiles,
                       cudaStream_t stream) {
-  if ((size_t)ra.stages * rf::Geo<EP>::STAGE_BYTES < rf::Geo<EP>::EPI_BYTES) return cudaErrorInvalidConfiguration;
+  if ((size_t)ra.stages * rf::Geo<EP>::STAGE_BYTES < rf::Geo<EP>::epi_bytes(ra.S)) return cudaErrorInvalidConfiguration;
   static cudaError_t attr = set_smem(rf::router_fused_kernel<EP>, rf::SMEM_LIMIT);
   if (attr != cudaSuccess) return attr;
   const size_t smem = rf::smem_bytes<EP>(ra.stages);
@@ -817,8 +913,10 @@ RouterPlan router_plan(const Shape &sh) {
   // d split over a cluster of S CTAs while the grid stays within one wave
   // and every CTA keeps at least one 64-deep K step
   const int nk = (sh.d + rf::BK - 1) / rf::BK;
+  // (for 256 expert columns the ring holds the incoming and outgoing partials of at most four CTAs)
+  const int smax = p.ep == 256 ? 4 : rf::SMAX;
   int S = 1;
-  while (2 * S <= rf::SMAX && p.m_tiles * 2 * S <= sm_count() && 2 * S <= nk) S *= 2;
+  while (2 * S <= smax && p.m_tiles * 2 * S <= sm_count() && 2 * S <= nk) S *= 2;
   p.cluster = S;
   return p;
 }
