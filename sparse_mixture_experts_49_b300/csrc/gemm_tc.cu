@@ -272,12 +272,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         zeroed = nrows > 0;
         if (nrows > 0) {
           constexpr int NBLK = SB / 8192;  // 64-wide blocks of A and B in the stage
-          const int chunks = nrows * 8;    // 16-byte chunks per block
-          for (int i = lane; i < NBLK * chunks; i += 32) {
-            const int blk = i / chunks, rem = i - blk * chunks;
-            const int row = valid + (rem >> 3), c = rem & 7;
-            *reinterpret_cast<uint4 *>(a_s + blk * 8192 + row * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-          }
+          const int chunks = nrows * 8;    // 16-byte chunks per block (rows valid .. valid + nrows - 1)
+          uint8_t *z0 = a_s + valid * 128;
+#pragma unroll
+          for (int blk = 0; blk < NBLK; ++blk)
+            for (int i = lane; i < chunks; i += 32)
+              *reinterpret_cast<uint4 *>(z0 + blk * 8192 + (i >> 3) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
           fence_proxy_async_smem();
         }
         __syncwarp();
