@@ -190,6 +190,10 @@ def kernel_roles(names):
     grouped-K launch of the backward pass is dW2, the second dW1), every other kernel by its own name."""
     roles, gk = [], 0
     for n in names:
+        if "wgrad_kernel" in n:   # the weight gradients' own kernel: dW2, then dW1, like the grouped-K GEMMs
+            roles.append(("dW2" if gk == 0 else "dW1", "backward"))
+            gk += 1
+            continue
         m = _GEMM_ARGS.search(n)
         if m:
             _, group_k, _, b_mn, epi = (int(v) for v in m.groups())
@@ -225,7 +229,9 @@ def source_hash(files) -> str:
 
 # the sources each kernel role is built from (a measured traffic figure holds while they are unchanged)
 def role_sources(role: str):
-    if role.startswith(("gemm", "dH", "dW", "dXp", "router_grad")):
+    if role.startswith("dW"):
+        return ("gemm_tc.cu", "wgrad.cu", "common.cuh")
+    if role.startswith(("gemm", "dH", "dXp", "router_grad")):
         return ("gemm_tc.cu", "common.cuh")
     if role.startswith("router"):
         return ("router.cu", "common.cuh") if "dh" not in role and "split6" not in role and "dwr" not in role \

@@ -76,7 +76,9 @@ enum {
   MOE_DEVERR_NONE = 0,
   MOE_DEVERR_BAD_EXPERT = 1, /* a top-k index outside [0, E) */
   MOE_DEVERR_DUP_EXPERT = 2, /* the same expert twice in one token's top-k */
-  MOE_DEVERR_TIMEOUT = 3     /* a bounded on-chip wait gave up; outputs are invalid */
+  MOE_DEVERR_TIMEOUT = 3,    /* a bounded on-chip wait gave up; outputs are invalid */
+  MOE_DEVERR_GROUP_ROWS = 4  /* moe_backward: an expert's packed rows exceed cfg->capacity (offsets not
+                                from this layer's dispatch); that expert's weight gradients are invalid */
 };
 
 /* Problem description ([Switch] section 現場ではこう使う: num_experts,
@@ -395,6 +397,15 @@ moe_status moe_backward_expert_choice(const moe_config *cfg, const moe_saved_exp
  *   dw1  [E, R1, d]  x dtype out
  *   dw2  [E, d, F]   x dtype out
  * The fixed logit bias gets no gradient.
+ *
+ * bf16 layers with 0 < cfg->capacity <= 192 take the expert weight gradients
+ * from a kernel that keeps each (expert, 128-row tile) unit's rows of dYp /
+ * dA in shared memory across the unit's output tiles; it relies on every
+ * expert's packed rows being at most cfg->capacity (true for offsets from
+ * this layer's dispatch) and records MOE_DEVERR_GROUP_ROWS otherwise.
+ * MOE_WGRAD=gemm in the environment (read at every call) sends them to the
+ * grouped GEMM instead, as do CTA-pair tiles; results agree to fp32
+ * accumulation order.
  */
 moe_status moe_backward(const moe_config *cfg, const moe_saved *saved, const void *dy, void *dx,
                         float *dw_r, void *dw1, void *dw2, void *ws, moe_stream_t stream);

@@ -1183,8 +1183,15 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     }
     if (err != cudaSuccess) return err;
   }
+  // Weight gradients: the unit-resident kernel when the capacity bounds the rows per expert (one CTA per
+  // tile only; MOE_WGRAD=gemm in the environment selects the grouped GEMM below for them as well).
+  const char *wv = getenv("MOE_WGRAD");
+  const bool resident = wgrad_fits(sh) && !pair_grouped_k(sh.d) && !(wv && wv[0] == 'g');
   // dW2_e = dYp_e^T H_e   (grouped over K = rows of e): M = d, N = F
-  {
+  if (resident) {
+    err = launch_wgrad(sh, offsets, dyp, sh.d, h, sh.F, dw2, st, stream);
+    if (err != cudaSuccess) return err;
+  } else {
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.d; a.N = sh.F;
@@ -1211,7 +1218,9 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
     if (err != cudaSuccess) return err;
   }
   // dW1_e = dA_e^T X_e: M = R1, N = d
-  {
+  if (resident) {
+    err = launch_wgrad(sh, offsets, da, sh.R1, x_perm, sh.d, dw1, st, stream);
+  } else {
     Args a{};
     a.offsets = offsets; a.E = sh.E; a.F = sh.F; a.st = st;
     a.M = sh.R1; a.N = sh.d;

@@ -128,6 +128,11 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
                                       const int32_t *offsets, const void *w1, const void *w2, void *h,
                                       const float *gate, void *out, void *y_perm, DeviceStatus *st,
                                       cudaStream_t stream);
+// Expert weight gradients with each (expert, m-tile)'s A rows resident (wgrad.cu), for layers whose
+// capacity bounds the rows per expert (wgrad_fits): dW_e [M, N] = A_e^T B_e, C [E, M, N] bf16.
+bool wgrad_fits(const Shape &sh);
+cudaError_t launch_wgrad(const Shape &sh, const int32_t *offsets, const void *a, int M, const void *b, int N,
+                         void *c, DeviceStatus *st, cudaStream_t stream);
 cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const void *x_perm, const void *w1,
                                const void *w2, const void *pre_act, const void *h, const void *dyp, void *da,
                                void *dxp, void *dw1, void *dw2, DeviceStatus *st, cudaStream_t stream);

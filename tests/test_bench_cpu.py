@@ -100,6 +100,9 @@ def test_kernel_roles_from_demangled_names():
         "router_dwr_sum_kernel", "unpermute_kernel"]
     assert [c for _, c in roles] == ["router"] * 3 + ["dispatch"] * 2 + ["gemm"] * 2 + ["combine"] + ["backward"] * 11
     assert b.kernel_roles([gemm.format("0, 0, 0, 0, 6")]) == [("gemm2_combine", "gemm")]
+    wg = "moe::wg::wgrad_kernel(CUtensorMap_st, CUtensorMap_st, CUtensorMap_st, moe::wg::Args)"
+    assert b.kernel_roles([gemm.format("0, 0, 0, 1, 4"), wg, gemm.format("0, 0, 0, 1, 0"), wg]) == [
+        ("dH", "backward"), ("dW2", "backward"), ("dXp", "backward"), ("dW1", "backward")]
 
 
 def test_oracle_sample_of_the_large_layer_keeps_every_per_expert_shape():

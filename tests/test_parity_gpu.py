@@ -222,17 +222,27 @@ PAIR_CASES = {
                                 cf=(5, 4), renormalize=True, backward=True),
     "dropless-small": SMALL["dropless-small"],
     "gshard-small": SMALL["gshard-small"],
+    # capacity 192 (the most rows the unit-resident weight-gradient kernel takes: three K steps), skewed so
+    # that the first experts are full, later ones partial and the last ones likely empty
+    "wgrad-edge": syn.Workload("wgrad-edge", T=3072, d=256, E=16, k=1, F=256, act="relu", dtype="bf16", cf=(1, 1),
+                               zipf_s=1.5, router_std=1 / 16, backward=True),
+    "large-small": SMALL["large-small"],
 }
 
 
-@pytest.mark.parametrize("mode", ["1", "0", "dynamic"])
+@pytest.mark.parametrize("mode", ["1", "0", "dynamic", "wgrad-gemm"])
 @pytest.mark.parametrize("name", list(PAIR_CASES))
 def test_gemm_tile_modes(name, mode, monkeypatch):
     """Every expert GEMM forced onto CTA-pair tiles (MOE_GEMM_PAIR=1), onto
     one CTA per tile in the fixed order (0), or one CTA per tile handed out by
     the workspace's tile counter (MOE_GEMM_SCHED=dynamic), forward and
     backward, against the oracle; twice in a row for the counter, which every
-    launch must leave at zero."""
+    launch must leave at zero. With one CTA per tile, layers whose capacity
+    is at most 192 rows take their weight gradients from the unit-resident
+    kernel; MOE_WGRAD=gemm (wgrad-gemm) sends them to the grouped GEMM."""
+    if mode == "wgrad-gemm":
+        monkeypatch.setenv("MOE_WGRAD", "gemm")
+        mode = "0"
     if mode == "dynamic":
         monkeypatch.setenv("MOE_GEMM_PAIR", "0")
         monkeypatch.setenv("MOE_GEMM_SCHED", "dynamic")
