@@ -18,7 +18,7 @@
 // K index zero), and in B as well after the last rows of all groups, where the
 // packed buffers hold whatever an earlier call left.
 //
-//   warp 0: TMA loads (A of a unit into one of two buffers, B per K step);
+//   warp 0: TMA loads (A of a unit once its buffer is free, B per K step);
 //   warp 1: TMEM (two 128 x 256 fp32 accumulators) and the tcgen05 MMAs;
 //   warps 2-9: drain an accumulator (two warps per TMEM lane quarter, one per
 //           column half), round to bf16, stage 32 rows x 64 columns in
@@ -38,21 +38,36 @@ constexpr int MAX_ROWS = KSTEPS * BK;          // rows per group this kernel tak
 constexpr int A_STEP = BM * BK * 2;            // 16 KB: two 64-column boxes
 constexpr int A_BUF = KSTEPS * A_STEP;         // 48 KB
 constexpr int B_STEP = BN * BK * 2;            // 32 KB: four 64-column boxes
-constexpr int NSTB = 3;                        // B ring stages
+// Buffer counts (measured on the large layer's backward pass, one box, CUDA
+// events: 1 A buffer + 4 B stages 10.02-10.04 ms; 2 + 3: 10.20-10.37 ms;
+// 1 + 3 with two staging buffers per warp: 10.48-10.51 ms; 2 + 2 with two:
+// 11.30 ms; the grouped GEMM: 11.03-11.06 ms).
+#ifndef MOE_WG_A_BUFS
+#define MOE_WG_A_BUFS 1
+#endif
+#ifndef MOE_WG_B_STAGES
+#define MOE_WG_B_STAGES 4
+#endif
+#ifndef MOE_WG_STG_BUFS
+#define MOE_WG_STG_BUFS 1
+#endif
+constexpr int A_BUFS = MOE_WG_A_BUFS;           // units' A buffers (two: the next unit's A loads under this one's MMAs)
+constexpr int NSTB = MOE_WG_B_STAGES;          // B ring stages
+constexpr int STG_BUFS = MOE_WG_STG_BUFS;      // staging buffers per epilogue warp
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr int STG = 4096;                      // staging bytes per epilogue warp
 constexpr int TMEM_COLS = 512;
 
 struct __align__(8) Smem {
-  uint64_t a_full[2], a_empty[2];
+  uint64_t a_full[A_BUFS], a_empty[A_BUFS];
   uint64_t full[NSTB], empty[NSTB];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
 };
-constexpr size_t SMEM_BYTES = 1024 + 2 * A_BUF + NSTB * B_STEP + EPI_WARPS * STG + sizeof(Smem);
+constexpr size_t SMEM_BYTES = 1024 + A_BUFS * A_BUF + NSTB * B_STEP + EPI_WARPS * STG_BUFS * STG + sizeof(Smem);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Args {
@@ -92,10 +107,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t *base = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  uint8_t *abuf = base;                                   // [2][KSTEPS][A_STEP]
-  uint8_t *bring = abuf + 2 * A_BUF;                      // [NSTB][B_STEP]
-  uint8_t *stage_out = bring + NSTB * B_STEP;             // [EPI_WARPS][STG]
-  Smem &s = *reinterpret_cast<Smem *>(stage_out + EPI_WARPS * STG);
+  uint8_t *abuf = base;                                   // [A_BUFS][KSTEPS][A_STEP]
+  uint8_t *bring = abuf + A_BUFS * A_BUF;                 // [NSTB][B_STEP]
+  uint8_t *stage_out = bring + NSTB * B_STEP;             // [EPI_WARPS][STG_BUFS][STG]
+  Smem &s = *reinterpret_cast<Smem *>(stage_out + EPI_WARPS * STG_BUFS * STG);
   volatile int *abort_flag = &s.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
@@ -107,12 +122,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s.a_full[i], 1);
-      mbar_init(&s.a_empty[i], 1);
-      mbar_init(&s.acc_full[i], 1);
-      mbar_init(&s.acc_empty[i], EPI_WARPS);
-    }
+    for (int i = 0; i < A_BUFS; ++i) { mbar_init(&s.a_full[i], 1); mbar_init(&s.a_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&s.acc_full[i], 1); mbar_init(&s.acc_empty[i], EPI_WARPS); }
     for (int i = 0; i < NSTB; ++i) { mbar_init(&s.full[i], 1); mbar_init(&s.empty[i], 1); }
     mbar_init(&s.drain, 1);
     s.abort_flag = 0;
@@ -162,12 +173,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (++stage == NSTB) { stage = 0; ph ^= 1; }
           }
         }
-        if (++ab == 2) { ab = 0; aph ^= 1; }
+        if (++ab == A_BUFS) { ab = 0; aph ^= 1; }
       }
       if (*abort_flag) {   // let every copy in flight land before the CTA can leave
         for (int i = 0; i < NSTB; ++i)
           if (issued & (1u << i)) drain_wait(&s.full[i], (par >> i) & 1);
-        for (int i = 0; i < 2; ++i)
+        for (int i = 0; i < A_BUFS; ++i)
           if (a_issued & (1u << i)) drain_wait(&s.a_full[i], (a_par >> i) & 1);
       }
     }
@@ -230,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!ok) break;
       if (lane == 0) tc_commit(&s.a_empty[ab]);        // A is free once this unit's MMAs have completed
       __syncwarp();
-      if (++ab == 2) { ab = 0; aph ^= 1; }
+      if (++ab == A_BUFS) { ab = 0; aph ^= 1; }
     }
     if (*abort_flag) {
       if (lane == 0) tc_commit(&s.drain);
@@ -241,7 +252,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;            // TMEM lane quarter: rows 32 q .. 32 q + 31
     const int half = (warp - 2) >> 2;  // column half of the tile
-    uint8_t *stg = stage_out + (warp - 2) * STG;
+    uint8_t *stg = stage_out + (warp - 2) * STG_BUFS * STG;
+    int sbuf = 0;   // the staging buffer of this warp's next store
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
@@ -280,17 +292,23 @@ __global__ void __launch_bounds__(THREADS, 1)
             x[i] = __uint_as_float(xr[cu][i]);
             x[32 + i] = __uint_as_float(xr[cu + 1][i]);
           }
-          if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
+          // the store that last read this buffer has left it (with two buffers: the one before the previous)
+          if (lane == 0) {
+            if (STG_BUFS == 2) bulk_wait_read_1();
+            else bulk_wait_read_all();
+          }
           __syncwarp();
-          uint8_t *rowp = stg + lane * 128;
+          uint8_t *sb = stg + sbuf * STG;
+          uint8_t *rowp = sb + lane * 128;
 #pragma unroll
           for (int j = 0; j < 8; ++j) Vec16<bf16>::store(rowp + ((j ^ (lane & 7)) << 4), x + 8 * j);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_3d(&tmC, stg, col, r0, e);   // rows past M and columns past N are clipped
+            tma_store_3d(&tmC, sb, col, r0, e);   // rows past M and columns past N are clipped
             bulk_commit();
           }
+          if (++sbuf == STG_BUFS) sbuf = 0;
         }
       }
     }
