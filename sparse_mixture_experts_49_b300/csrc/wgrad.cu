@@ -9,20 +9,22 @@
 // (section この記事のポイント).
 //
 // With at most 192 rows per group (three 64-deep K steps) the A rows of one
-// (expert, 128-row m-tile) unit fit in shared memory (48 KB). Each CTA takes
-// whole units (unit u, u + grid, ...): it loads the unit's A rows once, keeps
-// them while its MMAs run over every 256-column n-tile of the unit, and
-// streams only B through the ring, so a 128 x 256 output tile loads 64 KB of
-// operands instead of 96 KB. The rows past the group's end in its last K step
+// (expert, two 128-row m-tiles) unit fit in shared memory (96 KB). Each CTA
+// takes whole units (unit u, u + grid, ...): it loads the unit's A rows once,
+// keeps them while its MMAs run over every 128-column n-tile of the unit, and
+// streams only B through the ring; each 16 KB K step of B feeds the MMAs of
+// both m-tiles (four 128 x 128 fp32 accumulators: two per m-tile, double-
+// buffered), so 256 x 128 of output loads 16 KB of B per K step instead of
+// the grouped GEMM's 96 KB of A and B per 128 x 256. The rows past the group's end in its last K step
 // are zeroed once per unit in A (a zero row of A makes every product over that
 // K index zero), and in B as well after the last rows of all groups, where the
 // packed buffers hold whatever an earlier call left.
 //
 //   warp 0: TMA loads (A of a unit once its buffer is free, B per K step);
-//   warp 1: TMEM (two 128 x 256 fp32 accumulators) and the tcgen05 MMAs;
-//   warps 2-9: drain an accumulator (two warps per TMEM lane quarter, one per
-//           column half), round to bf16, stage 32 rows x 64 columns in
-//           128-byte swizzled shared memory and write them by TMA tile store.
+//   warp 1: TMEM (512 columns of fp32 accumulators) and the tcgen05 MMAs;
+//   warps 2-9: drain the accumulators (per TMEM lane quarter, one warp per
+//           m-tile), round to bf16, stage 32 rows x 64 columns in 128-byte
+//           swizzled shared memory and write them by TMA tile store.
 // Every wait is bounded (the same limit and abort handling as the grouped
 // GEMM).
 #include "common.cuh"
@@ -32,12 +34,20 @@
 namespace moe {
 namespace wg {
 
-constexpr int BM = 128, BN = 256, BK = 64;
+// Two m-tiles per unit: the large layer's backward pass 9.71-9.86 ms against
+// 10.17-10.20 ms with one (one box, CUDA events, same bits).
+#ifndef MOE_WG_MH
+#define MOE_WG_MH 2
+#endif
+constexpr int BM = 128, BK = 64;
+constexpr int MH = MOE_WG_MH;                  // m-tiles of 128 rows per unit, each with its accumulators
+constexpr int TN = 256 / MH;                   // output columns per n-tile (TMEM: 2 buffers x MH x TN = 512)
+constexpr int NBB = TN / 64;                   // 64-column B boxes per K step
 constexpr int KSTEPS = 3;                      // K steps a resident unit may have
 constexpr int MAX_ROWS = KSTEPS * BK;          // rows per group this kernel takes
-constexpr int A_STEP = BM * BK * 2;            // 16 KB: two 64-column boxes
-constexpr int A_BUF = KSTEPS * A_STEP;         // 48 KB
-constexpr int B_STEP = BN * BK * 2;            // 32 KB: four 64-column boxes
+constexpr int A_STEP = BM * BK * 2;            // 16 KB per m-tile: two 64-column boxes
+constexpr int A_BUF = MH * KSTEPS * A_STEP;    // a unit's A rows
+constexpr int B_STEP = TN * BK * 2;            // one K step of an n-tile's B
 // Buffer counts (measured on the large layer's backward pass, one box, CUDA
 // events: 1 A buffer + 4 B stages 10.02-10.04 ms; 2 + 3: 10.20-10.37 ms;
 // 1 + 3 with two staging buffers per warp: 10.48-10.51 ms; 2 + 2 with two:
@@ -46,7 +56,7 @@ constexpr int B_STEP = BN * BK * 2;            // 32 KB: four 64-column boxes
 #define MOE_WG_A_BUFS 1
 #endif
 #ifndef MOE_WG_B_STAGES
-#define MOE_WG_B_STAGES 4
+#define MOE_WG_B_STAGES (MH == 1 ? 4 : 6)
 #endif
 #ifndef MOE_WG_STG_BUFS
 #define MOE_WG_STG_BUFS 1
@@ -113,8 +123,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   Smem &s = *reinterpret_cast<Smem *>(stage_out + EPI_WARPS * STG_BUFS * STG);
   volatile int *abort_flag = &s.abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + BN - 1) / BN;
-  const int n_units = p.E * m_tiles;
+  const int m_tiles = (p.M + BM - 1) / BM, n_tiles = (p.N + TN - 1) / TN;
+  const int m_units = (m_tiles + MH - 1) / MH;    // units per expert (MH m-tiles each)
+  const int n_units = p.E * m_units;
   auto off = [&](int i) -> int { return __ldg(p.offsets + i); };
   auto nt0_error = [](int mt) { return mt == 0; };   // one report per group
 
@@ -147,17 +158,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t a_issued = 0, a_par = 0, issued = 0, par = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const int e = u / m_tiles, mt = u - e * m_tiles;
+        const int e = u / m_units, mp = u - e * m_units;
         const int r0 = off(e), rows = off(e + 1) - r0;
         const int nk = unit_steps(rows);
-        if (rows > MAX_ROWS && nt0_error(mt)) record_error(p.st, MOE_DEVERR_GROUP_ROWS, e);
+        if (rows > MAX_ROWS && nt0_error(mp)) record_error(p.st, MOE_DEVERR_GROUP_ROWS, e);
         if (!mbar_wait_bounded(&s.a_empty[ab], aph ^ 1, abort_flag, p.st)) break;
-        mbar_arrive_expect_tx(&s.a_full[ab], (uint32_t)(nk * A_STEP));
+        mbar_arrive_expect_tx(&s.a_full[ab], (uint32_t)(MH * nk * A_STEP));
         uint8_t *a_s = abuf + ab * A_BUF;
-        for (int ks = 0; ks < nk; ++ks)
+        for (int h = 0; h < MH; ++h)   // (an m-tile past M reads the tensor map's zero fill)
+          for (int ks = 0; ks < nk; ++ks)
 #pragma unroll
-          for (int j = 0; j < 2; ++j)
-            tma_load_2d(a_s + ks * A_STEP + j * 8192, &tmA, &s.a_full[ab], mt * BM + 64 * j, r0 + ks * BK, pol);
+            for (int j = 0; j < 2; ++j)
+              tma_load_2d(a_s + (h * KSTEPS + ks) * A_STEP + j * 8192, &tmA, &s.a_full[ab],
+                          (mp * MH + h) * BM + 64 * j, r0 + ks * BK, pol);
         a_issued |= 1u << ab;
         a_par = (a_par & ~(1u << ab)) | (aph << ab);
         for (int nt = 0; ok && nt < n_tiles; ++nt) {
@@ -166,8 +179,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive_expect_tx(&s.full[stage], B_STEP);
             uint8_t *b_s = bring + stage * B_STEP;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(b_s + j * 8192, &tmB, &s.full[stage], nt * BN + 64 * j, r0 + ks * BK, pol);
+            for (int j = 0; j < NBB; ++j)
+              tma_load_2d(b_s + j * 8192, &tmB, &s.full[stage], nt * TN + 64 * j, r0 + ks * BK, pol);
             issued |= 1u << stage;
             par = (par & ~(1u << stage)) | (ph << stage);
             if (++stage == NSTB) { stage = 0; ph ^= 1; }
@@ -185,12 +198,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, 1, 1);
+    constexpr uint32_t IDESC = idesc_bf16_f32(BM, TN, 1, 1);
     int ab = 0, stage = 0, acc = 0;
     uint32_t aph = 0, ph = 0, acc_ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const int e = u / m_tiles;
+      const int e = u / m_units;
       const int r0 = off(e), rows = off(e + 1) - r0;
       const int nk = unit_steps(rows);
       const int valid = rows - (nk - 1) * BK;          // rows in the last K step (more if clamped: no padding)
@@ -200,7 +213,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait_bounded(&s.a_full[ab], aph, abort_flag, p.st)) break;
       uint8_t *a_s = abuf + ab * A_BUF;
       if (pad > 0) {
-        zero_rows(a_s + (nk - 1) * A_STEP, 2, valid, pad, lane);
+        for (int h = 0; h < MH; ++h) zero_rows(a_s + (h * KSTEPS + nk - 1) * A_STEP, 2, valid, pad, lane);
         fence_proxy_async_smem();
       }
       __syncwarp();
@@ -208,25 +221,29 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int nt = 0; nt < n_tiles; ++nt) {
         if (!mbar_wait_bounded(&s.acc_empty[acc], acc_ph ^ 1, abort_flag, p.st)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * MH * TN);   // m-half h: + h TN
         for (int ks = 0; ks < nk; ++ks) {
           if (!mbar_wait_bounded(&s.full[stage], ph, abort_flag, p.st)) { ok = false; break; }
           uint8_t *b_s = bring + stage * B_STEP;
           const bool last = ks == nk - 1;
           if (last && tail && pad > 0) {
-            zero_rows(b_s, 4, valid, pad, lane);
+            zero_rows(b_s, NBB, valid, pad, lane);
             fence_proxy_async_smem();
           }
           __syncwarp();
           tc_fence_after();
           if (lane == 0) {
-            const uint32_t a0 = smem_u32(a_s + ks * A_STEP), b0 = smem_u32(b_s);
+            const uint32_t b0 = smem_u32(b_s);
             const int nkk = last ? nkk_last : BK / 16;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              if (kk >= nkk) break;
-              tc_mma_bf16(d_tmem, smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
-                          smem_desc_sw128(b0 + kk * 2048, 8192, 1024), IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+            for (int h = 0; h < MH; ++h) {
+              const uint32_t a0 = smem_u32(a_s + (h * KSTEPS + ks) * A_STEP);
+#pragma unroll
+              for (int kk = 0; kk < BK / 16; ++kk) {
+                if (kk >= nkk) break;
+                tc_mma_bf16(d_tmem + (uint32_t)(h * TN), smem_desc_sw128(a0 + kk * 2048, 8192, 1024),
+                            smem_desc_sw128(b0 + kk * 2048, 8192, 1024), IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+              }
             }
             tc_commit(&s.empty[stage]);
           }
@@ -251,24 +268,26 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------------------------------------------------------- epilogue (warps 2..9)
     const int q = warp & 3;            // TMEM lane quarter: rows 32 q .. 32 q + 31
-    const int half = (warp - 2) >> 2;  // column half of the tile
+    const int half = (warp - 2) >> 2;  // one m-tile: the tile's column half; two: the m-half (all TN columns)
+    const int hm = MH == 2 ? half : 0, hc = MH == 2 ? 0 : half;
     uint8_t *stg = stage_out + (warp - 2) * STG_BUFS * STG;
     int sbuf = 0;   // the staging buffer of this warp's next store
     int acc = 0;
     uint32_t acc_ph = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const int e = u / m_tiles, mt = u - e * m_tiles;
+      const int e = u / m_units, mt = (u - e * m_units) * MH + hm;
       const bool zero = off(e + 1) == off(e);
       const int r0 = mt * BM + q * 32;   // first output row of this warp's slice
+      const bool out_rows = r0 < p.M;    // (the second m-tile of the last unit may lie past M)
       for (int nt = 0; nt < n_tiles; ++nt) {
         if (!mbar_wait_bounded(&s.acc_full[acc], acc_ph, abort_flag, p.st)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+        const uint32_t t_row = tmem + (uint32_t)((acc * MH + hm) * TN) + ((uint32_t)(q * 32) << 16);
         uint32_t xr[4][32];
         if (!zero) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32_issue(t_row + (4 * half + c) * 32, xr[c]);
+          for (int c = 0; c < 4; ++c) tmem_ld32_issue(t_row + (4 * hc + c) * 32, xr[c]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_wait32(xr[c]);
         } else {
@@ -284,8 +303,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (++acc == 2) { acc = 0; acc_ph ^= 1; }
 #pragma unroll
         for (int cu = 0; cu < 4; cu += 2) {
-          const int col = nt * BN + (4 * half + cu) * 32;
-          if (col >= p.N) continue;
+          const int col = nt * TN + (4 * hc + cu) * 32;
+          if (col >= p.N || !out_rows) continue;
           float x[64];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -345,7 +364,7 @@ cudaError_t launch_wgrad(const Shape &sh, const int32_t *offsets, const void *a,
   p.N = N;
   p.C = static_cast<bf16 *>(c);
   p.st = st;
-  const int units = sh.E * ((M + wg::BM - 1) / wg::BM);
+  const int units = sh.E * ((M + wg::MH * wg::BM - 1) / (wg::MH * wg::BM));
   int g = sm_count();
   if (g > units) g = units;
   return launch_kernel(wg::wgrad_kernel, dim3(g > 0 ? g : 1), dim3(wg::THREADS), wg::SMEM_BYTES, stream, ma, mb,

@@ -227,6 +227,10 @@ PAIR_CASES = {
     "wgrad-edge": syn.Workload("wgrad-edge", T=3072, d=256, E=16, k=1, F=256, act="relu", dtype="bf16", cf=(1, 1),
                                zipf_s=1.5, router_std=1 / 16, backward=True),
     "large-small": SMALL["large-small"],
+    # three m-tiles for dW2 (d = 384: the weight-gradient kernel's units cover two, the last one runs past M)
+    # and partial 128-column n-tiles (F = 320)
+    "wgrad-odd": syn.Workload("wgrad-odd", T=1024, d=384, E=16, k=2, F=320, act="relu", dtype="bf16", cf=(5, 4),
+                              router_std=1 / np.sqrt(384), backward=True),
 }
 
 
