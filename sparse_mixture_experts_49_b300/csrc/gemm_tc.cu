@@ -50,11 +50,8 @@ constexpr int TMEM_COLS = 512;         // two 128 x 256 fp32 accumulators
 constexpr int THREADS = 320;         // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int MAX_E = 256;
 // TMA ring: four 48 KB stages (one CTA per tile), six 32 KB stages (pair
-// tiles); one stage less for the SwiGLU backward, whose epilogue buffers the
-// saved activations (8 KB per warp).
-template <int PAIR, int EPI> constexpr int n_stages() {
-  return PAIR ? (EPI == EPI_SWIGLU_BWD ? 4 : 6) : (EPI == EPI_SWIGLU_BWD ? 3 : 4);
-}
+// tiles).
+template <int PAIR, int EPI> constexpr int n_stages() { return PAIR ? 6 : 4; }
 template <int PAIR> constexpr int b_bytes() { return (PAIR ? BN / 2 : BN) * BK * 2; }
 template <int PAIR> constexpr int stage_bytes() { return A_BYTES + b_bytes<PAIR>(); }
 
@@ -89,11 +86,9 @@ template <int EPI> constexpr bool tma_store_epi() { return EPI == EPI_STORE || E
 template <int EPI> constexpr bool staged_epi() {
   return tma_store_epi<EPI>() || EPI == EPI_SWIGLU || EPI == EPI_RELU || EPI == EPI_SWIGLU_BWD;
 }
-// Staging bytes per epilogue warp: one 4 KB buffer, two for the SwiGLU
-// backward (G and U in, dG and dU out).
-template <int EPI> constexpr int staging_per_warp() {
-  return staged_epi<EPI>() ? (EPI == EPI_SWIGLU_BWD ? 2 : 1) * STAGE_OUT_BYTES : 0;
-}
+// Staging bytes per epilogue warp: one 4 KB buffer (the SwiGLU backward
+// splits it into two 2 KB halves: G and U in, dG and dU out).
+template <int EPI> constexpr int staging_per_warp() { return staged_epi<EPI>() ? STAGE_OUT_BYTES : 0; }
 template <int PAIR, int GROUP_K, int EPI> constexpr size_t smem_bytes() {
   return 1024 /*align slack*/ + (size_t)n_stages<PAIR, EPI>() * stage_bytes<PAIR>() +
          (size_t)EPI_WARPS * staging_per_warp<EPI>() + sizeof(SmemT<GROUP_K != 0, n_stages<PAIR, EPI>()>);
@@ -717,61 +712,59 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         } else if (EPI == EPI_SWIGLU_BWD && mrow0 + q * 32 + 32 <= rows_e) {
-          // SwiGLU backward, whole 32-row slice, per 64-column group: the
-          // slice's saved G and U are read with coalesced 16-byte loads (8
-          // lanes per 128-byte row piece, all 16 loads of a lane in flight
-          // together) into this warp's two 4 KB buffers (128-byte swizzled
-          // rows). Each lane then takes its row's G and U from them, forms
-          // dG = dH U silu'(G) and dU = dH silu(G) in place, and the two
-          // buffers go out as TMA tile stores into dA = [dG | dU].
+          // SwiGLU backward, whole 32-row slice, per 32-column group: the
+          // slice's saved G and U are read with coalesced 16-byte loads (4
+          // lanes per 64-byte row piece, all 8 loads of a lane in flight
+          // together: 4 of G, 4 of U) into this warp's two 2 KB halves (64-byte rows, 16-byte
+          // units permuted by bits 7-8 of the address, as the 64-byte-swizzle
+          // maps write them). Each lane then takes its row's G and U from
+          // them, forms dG = dH U silu'(G) and dU = dH silu(G) in place, and
+          // the two halves go out as TMA tile stores into dA = [dG | dU].
           uint8_t *bg = stage_out + (warp - 2) * SPW;  // G, then dG
-          uint8_t *bu = bg + STAGE_OUT_BYTES;          // U, then dU
+          uint8_t *bu = bg + STAGE_OUT_BYTES / 2;      // U, then dU
           const int64_t rbase = (int64_t)off(e) + mrow0 + q * 32;
-          const int piece = lane & 7;
+          const int piece = lane & 3;
 #pragma unroll 1
-          for (int gi = 0; gi < 2; ++gi) {
-            const int col0 = nt * BN + half * 128 + gi * 64;
+          for (int gi = 0; gi < 4; ++gi) {
+            const int col0 = nt * BN + half * 128 + gi * 32;
             if (col0 >= p.N) break;
-            if (lane == 0) bulk_wait_read_all();  // the previous group's stores have left the buffers
+            if (lane == 0) bulk_wait_read_all();  // the previous group's stores have left the halves
             __syncwarp();
             {
-              uint4 lg[8], lu[8];
+              uint4 lg[4], lu[4];
               const bool in_f = col0 + piece * 8 < p.F;   // columns past F: zeros (stores clip there)
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int rr = 4 * i + (lane >> 3);
+              for (int i = 0; i < 4; ++i) {
+                const int rr = 8 * i + (lane >> 2);      // rows 0..31 of the slice
                 const bf16 *src = p.aux + (rbase + rr) * p.ldaux + col0 + piece * 8;
                 lg[i] = in_f ? *reinterpret_cast<const uint4 *>(src) : make_uint4(0u, 0u, 0u, 0u);
                 lu[i] = in_f ? *reinterpret_cast<const uint4 *>(src + p.F) : make_uint4(0u, 0u, 0u, 0u);
               }
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int rr = 4 * i + (lane >> 3);
-                const int o = rr * 128 + ((piece ^ (rr & 7)) << 4);
+              for (int i = 0; i < 4; ++i) {
+                const int rr = 8 * i + (lane >> 2);
+                const int o = rr * 64 + ((piece ^ ((rr >> 1) & 3)) << 4);
                 *reinterpret_cast<uint4 *>(bg + o) = lg[i];
                 *reinterpret_cast<uint4 *>(bu + o) = lu[i];
               }
             }
             __syncwarp();
+            tmem_ld32(t_row + (half * 4 + gi) * 32, v);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              tmem_ld32(t_row + (half * 4 + gi * 2 + c) * 32, v);
+            for (int i = 0; i < 4; ++i) {
+              const int o = lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4);
+              float gg[8], uu[8], dgv[8], duv[8];
+              Vec16<bf16>::load(bg + o, gg);
+              Vec16<bf16>::load(bu + o, uu);
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const int o = lane * 128 + (((c * 4 + i) ^ (lane & 7)) << 4);
-                float gg[8], uu[8], dgv[8], duv[8];
-                Vec16<bf16>::load(bg + o, gg);
-                Vec16<bf16>::load(bu + o, uu);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  const float sg = 1.0f / (1.0f + expf(-gg[j]));
-                  const float dh = v[8 * i + j];
-                  duv[j] = dh * gg[j] * sg;                                      // dU = dH * silu(G)
-                  dgv[j] = dh * uu[j] * (sg * (1.0f + gg[j] * (1.0f - sg)));     // dG = dH * U * silu'(G)
-                }
-                Vec16<bf16>::store(bg + o, dgv);
-                Vec16<bf16>::store(bu + o, duv);
+              for (int j = 0; j < 8; ++j) {
+                const float sg = 1.0f / (1.0f + expf(-gg[j]));
+                const float dh = v[8 * i + j];
+                duv[j] = dh * gg[j] * sg;                                      // dU = dH * silu(G)
+                dgv[j] = dh * uu[j] * (sg * (1.0f + gg[j] * (1.0f - sg)));     // dG = dH * U * silu'(G)
               }
+              Vec16<bf16>::store(bg + o, dgv);
+              Vec16<bf16>::store(bu + o, duv);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -1170,11 +1163,11 @@ cudaError_t tc_expert_backward(const Shape &sh, const int32_t *offsets, const vo
       return cudaErrorInvalidValue;
     if (swiglu) {
       a.aux = (const bf16 *)pre_act; a.ldaux = 2 * (int64_t)sh.F;
-      // dA [rows, 2F] = [dG | dU]: one map per F-wide half, 64-column x 32-row store boxes
+      // dA [rows, 2F] = [dG | dU]: one map per F-wide half, 32-column x 32-row store boxes (64-byte swizzle)
       CUtensorMap mc, md;
       const uint64_t stride = 2 * (uint64_t)sh.F * 2;
-      if (!make_map_2d_strided(&mc, da, sh.F, rows, stride, 64, 32) ||
-          !make_map_2d_strided(&md, static_cast<bf16 *>(da) + sh.F, sh.F, rows, stride, 64, 32))
+      if (!make_map_2d_strided_sw64(&mc, da, sh.F, rows, stride, 32, 32) ||
+          !make_map_2d_strided_sw64(&md, static_cast<bf16 *>(da) + sh.F, sh.F, rows, stride, 32, 32))
         return cudaErrorInvalidValue;
       err = launch<0, 0, 1, EPI_SWIGLU_BWD>(pair, ma, mb, mc, md, a, stream);
     } else {

@@ -32,9 +32,10 @@ EncodeTiledFn get_encoder() {
 
 // Tiled map over a row-major tensor of `rank` dims (dims[0] contiguous),
 // rows of dims[0] * elem bytes unless row_stride_bytes says otherwise; the
-// box is box0 x box1 (x 1), 128-byte swizzle.
+// box is box0 x box1 (x 1), 128-byte swizzle unless asked otherwise.
 static bool encode(CUtensorMap *m, const void *ptr, bool f32, int rank, const uint64_t *dims,
-                   uint64_t row_stride_bytes, uint32_t box0, uint32_t box1) {
+                   uint64_t row_stride_bytes, uint32_t box0, uint32_t box1,
+                   CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn enc = get_encoder();
   if (!enc) return false;
   const uint64_t elem = f32 ? 4 : 2;
@@ -45,7 +46,7 @@ static bool encode(CUtensorMap *m, const void *ptr, bool f32, int rank, const ui
   st[0] = row_stride_bytes ? row_stride_bytes : dims[0] * elem;
   if (rank == 3) st[1] = st[0] * dims[1];
   return enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
-             const_cast<void *>(ptr), d, st, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             const_cast<void *>(ptr), d, st, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -59,6 +60,12 @@ bool make_map_2d_strided(CUtensorMap *m, const void *ptr, uint64_t inner, uint64
                          uint32_t box_inner, uint32_t box_outer) {
   const uint64_t dims[2] = {inner, outer};
   return encode(m, ptr, false, 2, dims, row_stride_bytes, box_inner, box_outer);
+}
+
+bool make_map_2d_strided_sw64(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer,
+                              uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const uint64_t dims[2] = {inner, outer};
+  return encode(m, ptr, false, 2, dims, row_stride_bytes, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 bool make_map_3d(CUtensorMap *m, const void *ptr, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
