@@ -116,6 +116,7 @@ struct Args {
   const float *gate;       // EPI_COMBINE: gate of each token (top-1)
   int residual;            // EPI_COMBINE: out = x + g y (1) or g y (0)
   unsigned int *sched;     // {next tile, finished CTAs}, zero at launch: dynamic tile order (null: static)
+  int tail_split;          // grouped-M: cut the tiles of a small last wave into column windows (1) or not (0)
   DeviceStatus *st;
 };
 
@@ -288,6 +289,36 @@ __global__ void __launch_bounds__(THREADS, 1)
   // queue. A CTA whose producer has fetched past the end counts itself
   // finished; the last one resets both counters for the next launch.
   const bool dyn = !PAIR && p.sched != nullptr;
+  // Tail split (grouped-M, one CTA per tile, fixed order; not the SwiGLU
+  // forward, whose tile pairs gate and up columns): when a launch has fewer
+  // than four waves of tiles and its last partial wave holds at most half as
+  // many tiles as there are CTAs, each tile of that wave is cut along N into
+  // 2 (or, at most a quarter, 4) column windows of 128 (64) columns, so that
+  // more CTAs share the wave. A window's MMAs write its columns of the
+  // accumulator (N = window width) and the epilogue stores only those; the
+  // other work units are whole tiles. (With many waves the last one weighs
+  // little, and a window re-reads its tile's whole A rows.)
+  int tail = 0, split = 1;
+  if (!GROUP_K && !PAIR && !SWIGLU_FWD && !dyn && p.tail_split && total_tiles < 4 * units) {
+    tail = total_tiles % units;
+    if (tail > 0 && 2 * tail <= units) split = 4 * tail <= units ? 4 : 2;
+    else tail = 0;
+  }
+  const int total_units = total_tiles + (split - 1) * tail;
+  // work unit -> (tile, first column of the window inside the tile, window width)
+  auto unit_of = [&](int w, int &tile, int &c_off, int &width) {
+    const int nfull = total_tiles - tail;
+    if (w < nfull) {
+      tile = w;
+      c_off = 0;
+      width = BN;
+    } else {
+      const int j = w - nfull;
+      tile = nfull + j / split;
+      width = BN / split;
+      c_off = (j - (j / split) * split) * width;
+    }
+  };
   struct TileIter {
     int next, q;
     uint32_t ph;
@@ -297,7 +328,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (!dyn) {
       const int t = it.next;
       it.next += units;
-      return t < total_tiles ? t : -1;
+      return t < total_units ? t : -1;
     }
     if (!mbar_wait_bounded(&s.tq_full[it.q], it.ph, abort_flag, p.st)) return -2;
     const int t = *reinterpret_cast<volatile int *>(&s.tile_q[it.q]);
@@ -342,11 +373,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       } else {
         tile = it.next;
         it.next += units;
-        if (tile >= total_tiles) break;
+        if (tile >= total_units) break;
       }
-      int e, mt, nt;
+      int e, mt, nt, c_off, width;
+      unit_of(tile, tile, c_off, width);
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
+      // bytes of one stage: A, and B for the window (K-major B: 128-row boxes; MN-major: 64-column boxes)
+      const uint32_t stage_tx = width == BN ? (uint32_t)(DIRECT ? 2 * SB : SB)
+                                            : (uint32_t)(A_BYTES + (B_MN ? (width / 64) * 8192 : 16384));
       for (int ks = 0; ks < nk; ++ks) {
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st) ? 1 : 0;
@@ -355,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint8_t *a_s = tiles + (size_t)stage * SB;
         uint8_t *b_s = a_s + A_BYTES;
         // DIRECT: the even CTA expects both halves' bytes; the odd CTA only loads
-        if (lane == 0 && !(DIRECT && crank)) mbar_arrive_expect_tx(&s.full[stage], DIRECT ? 2 * SB : SB);
+        if (lane == 0 && !(DIRECT && crank)) mbar_arrive_expect_tx(&s.full[stage], stage_tx);
         __syncwarp();
         const int k0 = ks * BK;
         if (lane == 0) {
@@ -375,17 +410,17 @@ __global__ void __launch_bounds__(THREADS, 1)
               // B rows of the tile: 128 per CTA of a pair, 256 (two boxes) otherwise
               int r0, r1;
               if (SWIGLU_FWD) { r0 = nt * 128; r1 = p.F + nt * 128; }
-              else { r0 = nt * BN; r1 = nt * BN + 128; }
+              else { r0 = nt * BN + c_off; r1 = nt * BN + 128; }
               if (PAIR) {
                 ld3(b_s, &tmB, k0, crank ? r1 : r0, e, pol_b);
               } else {
-                ld3(b_s, &tmB, k0, r0, e, pol_b);
-                ld3(b_s + 16384, &tmB, k0, r1, e, pol_b);
+                ld3(b_s, &tmB, k0, r0, e, pol_b);   // (a narrower window: its first rows of this box)
+                if (width == BN) ld3(b_s + 16384, &tmB, k0, r1, e, pol_b);
               }
             } else {
-              const int c0 = nt * BN + (PAIR ? crank * 128 : 0);
-#pragma unroll
-              for (int j = 0; j < (PAIR ? 2 : 4); ++j) ld3(b_s + j * 8192, &tmB, c0 + 64 * j, k0, e, pol_b);
+              const int c0 = nt * BN + (PAIR ? crank * 128 : c_off);
+              const int nb = PAIR ? 2 : width / 64;
+              for (int j = 0; j < nb; ++j) ld3(b_s + j * 8192, &tmB, c0 + 64 * j, k0, e, pol_b);
             }
           } else {
             const int r0 = off(e) + k0;
@@ -418,6 +453,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp == 1 && crank == 0) {
     // ---------------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC = idesc_bf16_f32(TM, BN, A_MN, B_MN);
+    constexpr uint32_t IDESC_128 = idesc_bf16_f32(TM, 128, A_MN, B_MN);   // tail windows
+    constexpr uint32_t IDESC_64 = idesc_bf16_f32(TM, 64, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
@@ -425,14 +462,16 @@ __global__ void __launch_bounds__(THREADS, 1)
     bool ok = true;
     TileIter it{unit0, 0, 0};
     while (ok) {
-      const int tile = consumer_next(it);
+      int tile = consumer_next(it);
       if (tile < 0) { ok = tile == -1; break; }
-      int e, mt, nt;
+      int e, mt, nt, c_off, width;
+      unit_of(tile, tile, c_off, width);
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
+      const uint32_t idesc = width == BN ? IDESC : (width == 128 ? IDESC_128 : IDESC_64);
       if (!mbar_wait_bounded<PAIR != 0>(&s.acc_empty[acc], acc_phase ^ 1, abort_flag, p.st)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+      const uint32_t d_tmem = tmem + (uint32_t)(acc * BN + c_off);   // a window: its columns of the accumulator
       for (int ks = 0; ks < nk; ++ks) {
         if (!mbar_wait_bounded(&s.full[stage], phase, abort_flag, p.st)) { ok = false; break; }
         uint8_t *a_s = tiles + (size_t)stage * SB;
@@ -454,7 +493,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t bd = B_MN ? smem_desc_sw128(b0 + kk * 2048, 8192, 1024)
                                      : smem_desc_sw128(b0 + kk * 32, 16, 1024);
             if (PAIR) tc_mma_bf16_pair(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
-            else tc_mma_bf16(d_tmem, ad, bd, IDESC, (ks > 0 || kk > 0) ? 1u : 0u);
+            else tc_mma_bf16(d_tmem, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           }
           if (PAIR) tc_commit_pair_mc(&s.empty[stage], 0x3);
           else tc_commit(&s.empty[stage]);
@@ -516,10 +555,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t acc_phase = 0;
     TileIter it{unit0, 0, 0};
     while (true) {
-      const int tile = consumer_next(it);
+      int tile = consumer_next(it);
       if (tile < 0) break;
-      int e, mt, nt;
+      int e, mt, nt, c_off, width;
+      unit_of(tile, tile, c_off, width);
       decode(tile, e, mt, nt);
+      // output columns of this unit: [cs, ce) (the whole tile, or a tail window)
+      const int cs = nt * BN + c_off, ce = cs + width;
       if (!mbar_wait_bounded<PAIR != 0>(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
       tc_fence_after();
       const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
@@ -571,7 +613,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int cu = 0; cu < 4; cu += CPB) {
           const int c = 4 * half + cu;
           const int col = nt * BN + c * 32;
-          if (nvalid == 0 || col >= p.N) continue;
+          if (nvalid == 0 || col >= p.N || col < cs || col >= ce) continue;
           float x[32 * CPB];
 #pragma unroll
           for (int u = 0; u < CPB; ++u)
@@ -694,6 +736,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int gi = 0; gi < 2; ++gi) {
             const int col0 = nt * BN + half * 128 + gi * 64;
             if (col0 >= p.N) break;
+            if (col0 < cs || col0 >= ce) continue;
             if (lane == 0) bulk_wait_read_all();  // the previous store has left the buffer
             __syncwarp();
 #pragma unroll 1
@@ -728,6 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int gi = 0; gi < 4; ++gi) {
             const int col0 = nt * BN + half * 128 + gi * 32;
             if (col0 >= p.N) break;
+            if (col0 < cs || col0 >= ce) continue;
             if (lane == 0) bulk_wait_read_all();  // the previous group's stores have left the halves
             __syncwarp();
             {
@@ -812,7 +856,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int g = 0; g < G; ++g) {
               const int col = nt * BN + (c0 + g) * 32;
               tmem_ld32(t_row + (c0 + g) * 32, v);
-              if (!valid || col >= p.N) continue;
+              if (!valid || col >= p.N || col < cs || col >= ce) continue;
               if (EPI == EPI_RELU) {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) v[i] = fmaxf(v[i], 0.0f);
@@ -943,6 +987,12 @@ static int grid_size() {
 // layer's GEMMs are held back by their last partial wave of tiles, not by
 // uneven tile costs), and the short weight-gradient tiles of the large layer
 // slower by the queue handshake, so the fixed stride is the default.
+// Tail windows of the last partial wave (grouped-M, fixed order): on unless
+// MOE_GEMM_TAIL=0 in the environment (read at every call).
+static int tail_split_enabled() {
+  const char *v = getenv("MOE_GEMM_TAIL");
+  return (v && v[0] == '0') ? 0 : 1;
+}
 static unsigned int *tile_counters(DeviceStatus *st) {
   const char *v = getenv("MOE_GEMM_SCHED");
   if (!(v && v[0] == 'd')) return nullptr;
@@ -963,6 +1013,7 @@ static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &m
   const int g = grid_size<0, GROUP_K, A_MN, B_MN, EPI>();
   if (g <= 0) return cudaErrorInvalidConfiguration;
   args.sched = tile_counters(a.st);
+  args.tail_split = tail_split_enabled();
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
                        smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, md, me, args);
 }
@@ -992,6 +1043,7 @@ static cudaError_t launch_single(const CUtensorMap &ma, const CUtensorMap &mb, c
   if (g <= 0) return cudaErrorInvalidConfiguration;
   Args args = a;
   args.sched = tile_counters(a.st);
+  args.tail_split = tail_split_enabled();
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
                        smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, mc, mc, args);
 }

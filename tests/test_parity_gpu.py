@@ -267,6 +267,29 @@ def test_gemm_tile_modes(name, mode, monkeypatch):
     _check_full(w, res, inp, f, b)
 
 
+@pytest.mark.parametrize("name", ["gshard-small", "large-small", "wgrad-odd", "pair-swiglu"])
+def test_gemm_tail_windows(name, monkeypatch):
+    """The last partial wave of grouped-M tiles cut into 128- or 64-column windows (the default) against whole
+    tiles (MOE_GEMM_TAIL=0): every output and gradient bit for bit the same (a window's MMAs accumulate each
+    output element over the same K steps in the same order), and both against the oracle. At these sizes
+    every tile is in the last wave, so each GEMM runs on windows: ReLU and SwiGLU-backward staged epilogues,
+    the plain TMA-store epilogue with K-major and MN-major weights, and the row-by-row path of group ends."""
+    w = PAIR_CASES[name]
+    inp = syn.make_inputs(w, dy=True)
+    monkeypatch.setenv("MOE_GEMM_PAIR", "0")
+    runs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("MOE_GEMM_TAIL", mode)
+        runs[mode] = run_gpu(w, inp, backward=True)
+    monkeypatch.delenv("MOE_GEMM_TAIL")
+    for key in ("out", "h", "y_perm", "dx", "dw_r", "dw1", "dw2"):
+        if runs["1"][key] is None:
+            continue
+        assert np.array_equal(np.asarray(runs["1"][key]), np.asarray(runs["0"][key])), key
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, runs["1"], inp, f, b)
+
+
 @pytest.mark.parametrize("mode", ["1", "0"])
 def test_fused_top1_tile_modes(mode, monkeypatch):
     """moe_forward's combine epilogue (top-1) on both tile modes, groups of ~1000 rows."""
