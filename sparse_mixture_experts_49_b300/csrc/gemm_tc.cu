@@ -116,6 +116,7 @@ struct Args {
   const float *gate;       // EPI_COMBINE: gate of each token (top-1)
   int residual;            // EPI_COMBINE: out = x + g y (1) or g y (0)
   unsigned int *sched;     // {next tile, finished CTAs}, zero at launch: dynamic tile order (null: static)
+  int m64;                 // grouped-M: M = 64 MMAs for m-tiles with at most 64 rows (1) or full tiles (0)
   int tail_split;          // grouped-M: cut the tiles of a small last wave into column windows (1) or not (0)
   DeviceStatus *st;
 };
@@ -249,6 +250,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       nt = local / m_tiles;
       mt = local - nt * m_tiles;
     }
+  };
+  // Short tiles (grouped-M, one CTA per tile): an m-tile holding at most 64 of
+  // its group's rows runs M = 64 MMAs, which write tile row 16 q + i to TMEM
+  // lane 32 q + i (i < 16) of lane quarter q.
+  auto short_tile = [&](int e, int mt) -> bool {
+    if (GROUP_K || PAIR || !p.m64) return false;
+    const int rem = off(e + 1) - off(e) - mt * BM;
+    return rem > 0 && rem <= 64;
   };
   auto k_steps = [&](int e) -> int {
     return GROUP_K ? (off(e + 1) - off(e) + BK - 1) / BK : (p.K + BK - 1) / BK;
@@ -468,7 +477,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       unit_of(tile, tile, c_off, width);
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
-      const uint32_t idesc = width == BN ? IDESC : (width == 128 ? IDESC_128 : IDESC_64);
+      const bool m64 = short_tile(e, mt);
+      uint32_t idesc = width == BN ? IDESC : (width == 128 ? IDESC_128 : IDESC_64);
+      if (m64) idesc = (idesc & ~(0x1Fu << 24)) | ((uint32_t)(64 >> 4) << 24);   // M = 64
       if (!mbar_wait_bounded<PAIR != 0>(&s.acc_empty[acc], acc_phase ^ 1, abort_flag, p.st)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem + (uint32_t)(acc * BN + c_off);   // a window: its columns of the accumulator
@@ -547,7 +558,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Two warps per TMEM lane quarter: warp w reads lanes 32 (w % 4) .. + 31
     // (its rows) and the column half (w - 2) / 4 of the tile.
     const int q = warp & 3;            // TMEM lane quarter this warp may access
-    const int r = q * 32 + lane;       // row inside this CTA's 128 rows of the tile
     const int half = (warp - 2) >> 2;  // column half of the tile
     // the accumulator's release goes to the MMA issuer's CTA (rank 0 of a pair)
     const uint32_t acc_empty0 = PAIR ? mapa_shared(smem_u32(&s.acc_empty[0]), 0) : 0u;
@@ -562,6 +572,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       decode(tile, e, mt, nt);
       // output columns of this unit: [cs, ce) (the whole tile, or a tail window)
       const int cs = nt * BN + c_off, ce = cs + width;
+      // this lane's row of the tile and the warp's slice (32 rows; a short tile: 16 rows in lanes 0-15)
+      const bool m64 = short_tile(e, mt);
+      const int r = m64 ? (lane < 16 ? 16 * q + lane : 1 << 20) : q * 32 + lane;
+      const int slice0 = m64 ? 16 * q : 32 * q, slice_n = m64 ? 16 : 32;
       if (!mbar_wait_bounded<PAIR != 0>(&s.acc_full[acc], acc_phase, abort_flag, p.st)) break;
       tc_fence_after();
       const uint32_t t_row = tmem + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
@@ -588,8 +602,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int r0;
         const bool zero = GROUP_K && off(e + 1) == off(e);
         if (!GROUP_K) {
-          const int lo = mrow0 + q * 32;
-          nvalid = min(32, max(0, off(e + 1) - off(e) - lo));
+          const int lo = mrow0 + slice0;
+          nvalid = min(slice_n, max(0, off(e + 1) - off(e) - lo));
           r0 = off(e) + lo;
         } else {
           r0 = mrow0 + q * 32;
@@ -664,8 +678,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           // next group's rows are never touched. Accumulator columns: G at
           // [c 32, + 32), U at 128 + [c 32, + 32) for the warp's chunks c.
           const int col0 = nt * 128 + half * 64;
-          const int lo = mrow0 + q * 32;
-          const int nvalid = min(32, max(0, rows_e - lo));
+          const int lo = mrow0 + slice0;
+          const int nvalid = min(slice_n, max(0, rows_e - lo));
           if (nvalid == 32 && col0 < p.N) {
             uint8_t *stg = stage_out + (warp - 2) * SPW;
             uint8_t *rowp = stg + lane * 128;
@@ -725,7 +739,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               }
             }
           }
-        } else if (EPI == EPI_RELU && mrow0 + q * 32 + 32 <= rows_e) {
+        } else if (EPI == EPI_RELU && !m64 && mrow0 + q * 32 + 32 <= rows_e) {
           // ReLU forward, whole 32-row slice: per 64-column group, h =
           // relu(acc) staged in 128-byte swizzled rows and written with one
           // TMA tile store.
@@ -754,7 +768,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               bulk_commit();
             }
           }
-        } else if (EPI == EPI_SWIGLU_BWD && mrow0 + q * 32 + 32 <= rows_e) {
+        } else if (EPI == EPI_SWIGLU_BWD && !m64 && mrow0 + q * 32 + 32 <= rows_e) {
           // SwiGLU backward, whole 32-row slice, per 32-column group: the
           // slice's saved G and U are read with coalesced 16-byte loads (4
           // lanes per 64-byte row piece, all 8 loads of a lane in flight
@@ -993,6 +1007,12 @@ static int tail_split_enabled() {
   const char *v = getenv("MOE_GEMM_TAIL");
   return (v && v[0] == '0') ? 0 : 1;
 }
+// M = 64 MMAs for grouped-M m-tiles with at most 64 rows: on unless
+// MOE_GEMM_M64=0 in the environment (read at every call).
+static int m64_enabled() {
+  const char *v = getenv("MOE_GEMM_M64");
+  return (v && v[0] == '0') ? 0 : 1;
+}
 static unsigned int *tile_counters(DeviceStatus *st) {
   const char *v = getenv("MOE_GEMM_SCHED");
   if (!(v && v[0] == 'd')) return nullptr;
@@ -1014,6 +1034,7 @@ static cudaError_t launch(bool pair, const CUtensorMap &ma, const CUtensorMap &m
   if (g <= 0) return cudaErrorInvalidConfiguration;
   args.sched = tile_counters(a.st);
   args.tail_split = tail_split_enabled();
+  args.m64 = m64_enabled();
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
                        smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, md, me, args);
 }
@@ -1044,6 +1065,7 @@ static cudaError_t launch_single(const CUtensorMap &ma, const CUtensorMap &mb, c
   Args args = a;
   args.sched = tile_counters(a.st);
   args.tail_split = tail_split_enabled();
+  args.m64 = m64_enabled();
   return launch_kernel(grouped_gemm_kernel<0, GROUP_K, A_MN, B_MN, EPI>, dim3(g), dim3(THREADS),
                        smem_bytes<0, GROUP_K, EPI>(), stream, ma, mb, mc, mc, mc, args);
 }

@@ -290,6 +290,27 @@ def test_gemm_tail_windows(name, monkeypatch):
     _check_full(w, runs["1"], inp, f, b)
 
 
+@pytest.mark.parametrize("name", ["gshard-small", "large-small", "wgrad-odd", "pair-swiglu", "dropless-small"])
+def test_gemm_short_tiles(name, monkeypatch):
+    """m-tiles that hold at most 64 of their group's rows on M = 64 MMAs (the default; rows 16 q + i in TMEM lane
+    32 q + i, stored row by row) against full 128-row tiles (MOE_GEMM_M64=0): every output and gradient bit for
+    bit the same, and both against the oracle (forward and backward, every grouped-M epilogue)."""
+    w = PAIR_CASES[name]
+    inp = syn.make_inputs(w, dy=True)
+    monkeypatch.setenv("MOE_GEMM_PAIR", "0")
+    runs = {}
+    for mode in ("1", "0"):
+        monkeypatch.setenv("MOE_GEMM_M64", mode)
+        runs[mode] = run_gpu(w, inp, backward=True)
+    monkeypatch.delenv("MOE_GEMM_M64")
+    for key in ("out", "h", "y_perm", "dx", "dw_r", "dw1", "dw2"):
+        if runs["1"][key] is None:
+            continue
+        assert np.array_equal(np.asarray(runs["1"][key]), np.asarray(runs["0"][key])), key
+    f, b = _ref_all(w, inp, True)
+    _check_full(w, runs["1"], inp, f, b)
+
+
 @pytest.mark.parametrize("mode", ["1", "0"])
 def test_fused_top1_tile_modes(mode, monkeypatch):
     """moe_forward's combine epilogue (top-1) on both tile modes, groups of ~1000 rows."""
