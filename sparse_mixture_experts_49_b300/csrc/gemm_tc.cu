@@ -388,9 +388,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       unit_of(tile, tile, c_off, width);
       decode(tile, e, mt, nt);
       const int nk = k_steps(e);
-      // bytes of one stage: A, and B for the window (K-major B: 128-row boxes; MN-major: 64-column boxes)
-      const uint32_t stage_tx = width == BN ? (uint32_t)(DIRECT ? 2 * SB : SB)
-                                            : (uint32_t)(A_BYTES + (B_MN ? (width / 64) * 8192 : 16384));
+      // bytes of one stage: A, and B for the window (K-major B: 128-row boxes; MN-major: 64-column boxes).
+      // With K-major B, A comes in 64-row boxes and a short tile loads one; with MN-major B (already four
+      // boxes a stage) in one 128-row box (measured: the extra box slowed dH by 5%).
+      constexpr bool A64 = !GROUP_K && !B_MN;
+      const bool a_half = A64 && short_tile(e, mt);
+      const uint32_t stage_tx = (width == BN ? (uint32_t)(DIRECT ? 2 * SB : SB)
+                                             : (uint32_t)(A_BYTES + (B_MN ? (width / 64) * 8192 : 16384))) -
+                                (a_half ? (uint32_t)(A_BYTES / 2) : 0u);
       for (int ks = 0; ks < nk; ++ks) {
         int got = 1;
         if (lane == 0) got = mbar_wait_bounded(&s.empty[stage], phase ^ 1, abort_flag, p.st) ? 1 : 0;
@@ -415,6 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             };
             const int row0 = off(e) + mt * TM + half_row;
             ld2(a_s, &tmA, k0, row0, pol_a);
+            if (A64 && !a_half) ld2(a_s + 8192, &tmA, k0, row0 + 64, pol_a);   // A64: the second 64-row box
             if (!B_MN) {
               // B rows of the tile: 128 per CTA of a pair, 256 (two boxes) otherwise
               int r0, r1;
@@ -1129,7 +1135,7 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   a.st = st;
   a.b_once = b_once;
   // GEMM 1 (+ activation): A = x_perm [rows, d], B = W1 [E, R1, d]
-  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
+  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 64) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
     return cudaErrorInvalidValue;
   a.N = sh.F;
   a.K = sh.d;
@@ -1140,7 +1146,7 @@ cudaError_t tc_expert_forward(const Shape &sh, const void *x_perm, const int32_t
   cudaError_t err = gemm1_act(sh, pair, ma, mb, a, rows, stream);
   if (err != cudaSuccess) return err;
   // GEMM 2: A = h [rows, F], B = W2 [E, d, F]
-  if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
+  if (!make_map_2d(&ma, h, sh.F, rows, 64, 64) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
     return cudaErrorInvalidValue;
   Args b{};
   b.offsets = offsets;
@@ -1187,7 +1193,7 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   a.st = st;
   a.b_once = b_once;
   // GEMM 1 (+ activation): A = x_perm [rows, d], B = W1 [E, R1, d]
-  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 128) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
+  if (!make_map_2d(&ma, x_perm, sh.d, rows, 64, 64) || !make_map_3d(&mb, w1, sh.d, sh.R1, sh.E, 64, 128))
     return cudaErrorInvalidValue;
   a.N = sh.F;
   a.K = sh.d;
@@ -1196,7 +1202,7 @@ cudaError_t tc_expert_forward_combine(const Shape &sh, const void *x, const void
   cudaError_t err = gemm1_act(sh, pair, ma, mb, a, rows, stream);
   if (err != cudaSuccess) return err;
   // GEMM 2 + combine: A = h [rows, F], B = W2 [E, d, F]
-  if (!make_map_2d(&ma, h, sh.F, rows, 64, 128) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
+  if (!make_map_2d(&ma, h, sh.F, rows, 64, 64) || !make_map_3d(&mb, w2, sh.F, sh.d, sh.E, 64, 128))
     return cudaErrorInvalidValue;
   Args b{};
   b.offsets = offsets;
