@@ -261,12 +261,17 @@ moe_status moe_dispatch_noalloc(const moe_config *cfg, const void *x, const int3
  * Rows past expert_offsets[E] are not written.
  *
  * bf16 layers run on tcgen05 tiles of 128 rows, one CTA each, in a fixed
- * order (CTA u takes tiles u, u + grid, ...). Two environment variables,
- * read at every call, change that for this call and for moe_forward /
- * moe_backward: MOE_GEMM_PAIR=1 runs CTA-pair tiles (two CTAs of a cluster
- * share an MMA of 256 rows); MOE_GEMM_SCHED=dynamic hands the one-CTA tiles
- * out from a counter in the workspace as CTAs free up. Results agree to
- * fp32 accumulation order.
+ * order (CTA u takes tiles u, u + grid, ...). An m-tile that holds at most
+ * 64 of its expert's rows runs 64-row MMAs, and when a launch has fewer
+ * than four waves of tiles, the tiles of a last wave that fills at most half
+ * of the CTAs are cut into 128- or 64-column windows; both give the same
+ * bits as whole tiles. Environment variables, read at every call, change
+ * this for this call and for moe_forward / moe_backward: MOE_GEMM_PAIR=1
+ * runs CTA-pair tiles (two CTAs of a cluster share an MMA of 256 rows);
+ * MOE_GEMM_SCHED=dynamic hands the one-CTA tiles out from a counter in the
+ * workspace as CTAs free up; MOE_GEMM_M64=0 keeps short m-tiles at 128 rows;
+ * MOE_GEMM_TAIL=0 keeps last-wave tiles whole. Results agree to fp32
+ * accumulation order.
  */
 moe_status moe_expert_gemm(const moe_config *cfg, const void *x_perm,
                            const int32_t *expert_offsets, const void *w1, const void *w2,
